@@ -1,0 +1,77 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module is shared by the CUDA path's tests and benchmark and by the
+float64 oracle's tests.  It holds no attention arithmetic: it only draws
+random numbers, rounds them to the storage dtype, and names the workloads.
+
+Recipe (the pages fix no generator): ``torch.Generator('cpu')`` seeded with
+the workload's seed; Q, then K, then V, each drawn as float32 ``randn`` of
+shape [B, H, N, d]; Q multiplied by ``q_std``; all three rounded to the
+workload dtype (round-to-nearest-even, torch's ``.to``).  Both sides of a
+parity test see exactly these rounded values (the oracle upcasts them to
+float64).
+"""
+import math
+
+import torch
+
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+# The five synthetic workloads: shape, storage dtype, mask and Q spread.  All
+# use scale = 1/sqrt(d).  Seeds are 1000 + position in this list.
+WORKLOADS = [
+    dict(name="b1_h1_n256_d64_fp16", B=1, H=1, N=256, d=64, dtype="fp16",
+         causal=False, q_std=1.0),
+    dict(name="b1_h16_n4096_d128_bf16", B=1, H=16, N=4096, d=128, dtype="bf16",
+         causal=False, q_std=1.0),
+    dict(name="b4_h32_n8192_d128_bf16_causal", B=4, H=32, N=8192, d=128,
+         dtype="bf16", causal=True, q_std=1.0),
+    dict(name="b1_h8_n32768_d64_fp16_causal_qstd4", B=1, H=8, N=32768, d=64,
+         dtype="fp16", causal=True, q_std=4.0),
+    dict(name="b16_h16_n1024_d64_bf16", B=16, H=16, N=1024, d=64, dtype="bf16",
+         causal=False, q_std=1.0),
+]
+for _i, _w in enumerate(WORKLOADS):
+    _w["seed"] = 1000 + _i
+    _w["scale"] = 1.0 / math.sqrt(_w["d"])
+
+
+def workload(name):
+    """The workload dict with this name (or index)."""
+    if isinstance(name, int):
+        return dict(WORKLOADS[name])
+    for w in WORKLOADS:
+        if w["name"] == name:
+            return dict(w)
+    raise KeyError(name)
+
+
+def make_qkv(B, H, N, d, dtype="bf16", q_std=1.0, seed=0):
+    """Q, K, V as CPU tensors [B, H, N, d] of the storage dtype.
+
+    Draw order is Q, K, V from one generator, so a given seed always yields
+    the same three tensors whatever is done with them afterwards.
+    """
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    if q_std != 1.0:
+        q.mul_(q_std)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    t = DTYPES[dtype]
+    return q.to(t), k.to(t), v.to(t)
+
+
+def make_workload_qkv(w):
+    """Q, K, V for a workload dict from ``WORKLOADS``."""
+    return make_qkv(w["B"], w["H"], w["N"], w["d"], w["dtype"], w["q_std"],
+                    w["seed"])
+
+
+def sample_rows(N, count, seed, include=()):
+    """Sorted distinct row indices in [0, N): ``include`` plus ``count`` drawn."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    extra = torch.randint(0, max(N, 1), (count,), generator=g).tolist() if N else []
+    rows = sorted({int(r) for r in list(include) + extra if 0 <= int(r) < N})
+    return rows
