@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Forward-attention benchmark on GB300: TFLOP/s and the fraction of the
+dense BF16 tensor-core peak.
+
+One step = one exact-attention forward pass (one ``fa_fwd`` launch) over one
+synthetic workload already resident in device memory.  FLOPs per step follow
+the usual convention 4*B*H*N^2*d (two matmuls of 2*N^2*d each), halved for
+causal masking.
+
+Default workload: B=1, H=16, N=4096, d=128, bf16, unmasked, seeded inputs.
+``--workload`` selects another of the five synthetic workloads.
+
+Printed (rank 0, one JSON line): value (whole job TFLOP/s), ms_per_step,
+``roofline`` (achieved vs the measured bf16 peak; DRAM traffic from the last
+ncu capture when the kernel sources still match it), ``cpu_baseline`` (the
+float64 oracle timed on the host cores on a bounded sample of rows), ``e2e``
+(same metric through the public call with pinned host buffers, copies in the
+timed region), ``clocks`` (nvidia-smi samples during the timed region) and
+``gpu_launches``.
+
+``--impl reference`` times the float64 oracle on the host cores instead
+(rank 0 only), on bounded samples of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+forward pass has no exchange step); value = all ranks' FLOPs / the slowest
+rank's time.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "b1_h16_n4096_d128_bf16"
+METRIC = "attention fwd TFLOP/s (causal halved) and % of GB300 dense BF16 tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- accounting
+
+def step_flops(w):
+    f = 4.0 * w["B"] * w["H"] * w["N"] * w["N"] * w["d"]
+    return f / 2 if w["causal"] else f
+
+
+def io_bytes(w):
+    elems = w["B"] * w["H"] * w["N"] * w["d"]
+    return dict(h2d=3 * elems * 2, d2h=elems * 2 + w["B"] * w["H"] * w["N"] * 4)
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; a stored ncu traffic figure is only valid for it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_tiled_attention_14_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "fa.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload):
+    """DRAM bytes per launch from profiles/traffic.json, if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        data = json.load(open(path))
+    except (OSError, ValueError):
+        return None, "no profiles/traffic.json"
+    entry = data.get("workloads", {}).get(workload)
+    if not entry:
+        return None, "no ncu capture for this workload"
+    if entry.get("kernel_hash") != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return entry.get("dram_bytes_per_launch"), entry.get("note")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        data = json.load(open(path))
+        return float(data["bf16_tflops"]), float(data.get("bf16_tflops_sustained") or 0), "measured"
+    except (OSError, ValueError, KeyError, TypeError):
+        return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (host-stamped) while the benchmark runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NAMES = [None, None, None, "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.error = None
+        self.proc = None
+        self.thread = None
+        self.device_index = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        bus = self._bus_id()
+        if bus:
+            cmd += ["-i", bus]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError as e:
+            self.error = f"nvidia-smi unavailable: {e}"
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _bus_id(self):
+        try:
+            props = torch.cuda.get_device_properties(self.device_index)
+            return "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except Exception:  # older torch: fall back to nvidia-smi's default (all GPUs)
+            return None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1, fallback_window=None):
+        def pick(a, b):
+            return [s for t, s in self.samples if a <= t <= b]
+        window = "timed"
+        rows = pick(t0, t1)
+        if len(rows) < 3 and fallback_window:
+            rows, window = pick(*fallback_window), "warmup+timed"
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(rows),
+               "window": window}
+        if self.error:
+            out["error"] = self.error
+        if not rows:
+            return out
+        try:
+            sm = [float(r[0]) for r in rows]
+            out["sm_mhz"] = statistics.median(sm)
+            out["sm_max_mhz"] = max(float(r[1]) for r in rows)
+            out["power_w_max"] = max(float(r[2]) for r in rows if r[2] not in ("[N/A]", ""))
+        except ValueError:
+            pass
+        reasons = set()
+        for r in rows:
+            for i, name in enumerate(self.NAMES):
+                if name and r[i].lower() == "active":
+                    reasons.add(name)
+        out["reasons"] = sorted(reasons)
+        return out
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x, world, device=None):
+    """Largest value of x over all ranks (x itself when running alone)."""
+    if world == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, q, k, v, budget_s, seed=0, max_rows=None):
+    """Time the float64 oracle on seeded rows of head (0, 0) for about budget_s.
+
+    Returns (TFLOP/s, seconds, rows, cores, description).  The FLOPs of a row
+    are 4*d per visible key (its share of the two matmuls), which sums to the
+    workload's convention over all rows.
+    """
+    import numpy as np
+
+    import oracle
+    lib = oracle.load()
+    N, d = w["N"], w["d"]
+    kh, vh = k[0, 0].double().numpy(), v[0, 0].double().numpy()
+    g = np.random.default_rng(seed)
+
+    def run(nrows):
+        rows = np.sort(g.integers(0, N, size=nrows))
+        qr = q[0, 0][torch.from_numpy(rows)].double().numpy()
+        t0 = time.perf_counter()
+        oracle.attention_rows(qr, rows, kh, vh, causal=w["causal"], scale=w["scale"], lib=lib)
+        dt = time.perf_counter() - t0
+        vis = (rows + 1).sum() if w["causal"] else nrows * N
+        return dt, 4.0 * d * float(vis)
+
+    cores = oracle.num_threads(lib)
+    probe = max(cores * 4, 16)
+    dt, fl = run(probe)
+    rows = probe
+    if dt < budget_s:
+        rows = int(min(probe * budget_s / max(dt, 1e-6), max_rows or 10 ** 9))
+        rows = max(rows, probe)
+        dt, fl = run(rows)
+    desc = (f"{rows} seeded random query rows of head (0,0) of {w['name']} "
+            f"({rows / (w['B'] * w['H'] * N):.2e} of all rows), float64, {cores} threads")
+    return fl / dt / 1e12, dt, rows, cores, desc
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = seeded_inputs.make_workload_qkv(w)
+    total = args.steps + args.warmup
+    per_step = max(0.2, min(10.0, args.reference_seconds / max(total, 1)))
+    import oracle
+    oracle.load()
+    vals = []
+    for i in range(total):
+        tf, dt, rows, cores, desc = oracle_sample(w, q, k, v, per_step, seed=i)
+        if i >= args.warmup:
+            vals.append((tf, dt))
+    value = statistics.median(tf for tf, _ in vals)
+    ms = statistics.median(dt for _, dt in vals) * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
+                   "causal": w["causal"], "storage_dtype": w["dtype"], "seed": w["seed"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import exact_tiled_attention_14_gb300 as fa
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+
+    q, k, v = seeded_inputs.make_workload_qkv(w)
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    per_replica = io_bytes(w)["h2d"] + io_bytes(w)["d2h"]
+    replicas = 1 if per_replica > 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_replica)) + 1
+    bufs = []
+    for _ in range(replicas):
+        dq, dk, dv = (t.to(device) for t in (q, k, v))
+        o = torch.empty_like(dq)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+        bufs.append((dq, dk, dv, o, lse))
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        dq, dk, dv, o, lse = bufs[i % replicas]
+        rc = fa.fa_fwd(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"],
+                       fa.dtype_code(dq.dtype), stream)
+        if rc:
+            raise fa.FaError(rc)
+
+    sampler = ClockSampler(local).start()
+    t_warm = time.time()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    code, word = fa.fa_status(stream)
+    if code:
+        raise fa.FaError(code, f"warmup status {word:#x}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    t1 = time.time()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    kern_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    code, word = fa.fa_status(stream)
+    if code:
+        raise fa.FaError(code, f"timed status {word:#x}")
+    total_ms = max_over_ranks(total_ms, world, device)
+    kern_ms_max = max_over_ranks(kern_ms, world, device)
+
+    # ---- end to end: pinned host inputs -> device -> fa_fwd -> host outputs
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dq, dk, dv, o, lse = bufs[0]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.attention_forward(dq, dk, dv, causal=w["causal"], scale=w["scale"], out=o, lse=lse,
+                             stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1, fallback_window=(t_warm, t1))
+
+    if rank != 0:
+        return 0
+    flops = step_flops(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (kern_ms_max * 1e-3) / 1e12
+    peak, peak_sustained, peak_src = measured_peaks()
+    traffic, traffic_note = stored_traffic(w["name"])
+    io = io_bytes(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d,
+                   "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": (f"{replicas} rotating input replicas "
+                          f"({replicas * per_replica / 2**20:.0f} MiB > L2)")
+                   if replicas > 1 else "inputs larger than L2"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
+                     "kernel_ms": kern_ms_max, "flops_per_launch": flops,
+                     "traffic": traffic,
+                     "traffic_note": traffic_note,
+                     "compulsory_bytes": io["h2d"] + io["d2h"]},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "gpu": torch.cuda.get_device_name(device),
+    }
+    if not args.no_cpu_baseline:
+        tf, dt, rows, cores, desc = oracle_sample(w, q, k, v, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(json.dumps(line) + "\n")
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of: " + ", ".join(x["name"] for x in seeded_inputs.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = seeded_inputs.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

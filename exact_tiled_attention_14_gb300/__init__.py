@@ -1,0 +1,169 @@
+"""Exact tiled attention forward for GB300 (sm_103a): Python binding.
+
+This module only marshals arguments to the C ABI in ``include/fa.h``
+(``fa_fwd``, ``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``,
+``fa_work_tiles``, ``fa_version``), under the same names.  Every step of
+the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
+there is no CPU or PyTorch fallback.  When the library has not been built,
+every call raises.
+
+``attention_forward`` is the convenience call a user makes: it allocates O
+and LSE with PyTorch (device memory is PyTorch's job here) and calls
+``fa_fwd`` on the current CUDA stream.
+"""
+import ctypes
+import math
+import os
+
+from .build import LIB_PATH, build  # noqa: F401
+
+FA_BF16 = 0
+FA_FP16 = 1
+
+FA_OK = 0
+FA_ERR_NULLPTR = 1
+FA_ERR_SHAPE = 2
+FA_ERR_UNSUPPORTED_D = 3
+FA_ERR_DTYPE = 4
+FA_ERR_ALIGN = 5
+FA_ERR_SCALE = 6
+FA_ERR_DEVICE = 7
+FA_ERR_TENSORMAP = 8
+FA_ERR_LAUNCH = 9
+FA_ERR_TIMEOUT = 10
+FA_ERR_CUDA = 11
+
+# Functions the C ABI exports (checked against include/fa.h by the tests).
+EXPORTS = ("fa_fwd", "fa_strerror", "fa_status", "fa_set_watchdog_ns", "fa_work_tiles",
+           "fa_version")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    """A non-zero return code of the C ABI."""
+
+    def __init__(self, code, where="fa_fwd"):
+        self.code = int(code)
+        super().__init__(f"{where}: {fa_strerror(self.code)} (code {self.code})")
+
+
+def load_library(path=None):
+    """Load ``libfa.so`` (raises if it has not been built)."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library not built: {p} is missing "
+            "(run exact_tiled_attention_14_gb300.build.build())")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_strerror.argtypes = [i]
+    lib.fa_strerror.restype = ctypes.c_char_p
+    lib.fa_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_status.restype = i
+    lib.fa_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_watchdog_ns.restype = None
+    lib.fa_work_tiles.argtypes = [i, i, ctypes.POINTER(ctypes.c_longlong)]
+    lib.fa_work_tiles.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _addr(x):
+    """Device address of a tensor, or an int / None passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None):
+    """Raw C call; tensors or integer addresses; returns the C return code."""
+    lib = load_library()
+    return lib.fa_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                      int(N), int(d), int(bool(causal)), float(scale), int(dtype),
+                      _stream(stream))
+
+
+def fa_strerror(code):
+    return load_library().fa_strerror(int(code)).decode()
+
+
+def fa_status(stream=None):
+    """(code, raw status word) after synchronising ``stream``."""
+    detail = ctypes.c_uint(0)
+    code = load_library().fa_status(_stream(stream), ctypes.byref(detail))
+    return code, detail.value
+
+
+def fa_set_watchdog_ns(ns):
+    load_library().fa_set_watchdog_ns(int(ns))
+
+
+def fa_work_tiles(N, causal):
+    out = ctypes.c_longlong(0)
+    code = load_library().fa_work_tiles(int(N), int(bool(causal)), ctypes.byref(out))
+    if code:
+        raise FaError(code, "fa_work_tiles")
+    return out.value
+
+
+def fa_version():
+    return load_library().fa_version()
+
+
+def dtype_code(torch_dtype):
+    import torch
+    if torch_dtype == torch.bfloat16:
+        return FA_BF16
+    if torch_dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"unsupported dtype {torch_dtype}; use bfloat16 or float16")
+
+
+def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """O, LSE = exact attention of CUDA tensors q, k, v [B, H, N, d].
+
+    O has the input dtype; LSE is float32 [B, H, N] (natural log).  ``scale``
+    defaults to 1/sqrt(d).  Runs on ``stream`` (default: current stream).
+    """
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d] of one shape")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = dtype_code(q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd(q, k, v, out, lse, B, H, N, d, causal, scale, code, stream)
+    if rc != FA_OK:
+        raise FaError(rc)
+    return out, lse

@@ -1,0 +1,184 @@
+// fa_api.cu — the C ABI declared in include/fa.h: argument checks, TMA
+// descriptors, per-device setup and the launch of the forward kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.cuh"
+
+namespace {
+
+// Device status word written by the kernels' bounded waits (bit 0 = a wait
+// ran out, bits 8..15 = where).  One per device; read and cleared by fa_status.
+__device__ unsigned int g_fa_status = 0;
+
+constexpr unsigned long long kDefaultWatchdogNs = 2000000000ull;
+std::atomic<unsigned long long> g_watchdog_ns{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool supported = false;
+  unsigned int* status = nullptr;
+  int err = FA_ERR_DEVICE;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+bool g_dev_ready[kMaxDevices] = {};
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, queried once with that device current.
+const DeviceInfo* device_info(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo info;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+      info.supported = (major == 10 && minor == 3);
+      void* addr = nullptr;
+      if (info.supported && cudaGetSymbolAddress(&addr, g_fa_status) == cudaSuccess) {
+        info.status = static_cast<unsigned int*>(addr);
+        info.err = FA_OK;
+      }
+    }
+    g_dev[dev] = info;
+    g_dev_ready[dev] = true;
+  }
+  return &g_dev[dev];
+}
+
+// 3-D view [BH, N, d] of a contiguous [B, H, N, d] tensor; boxes of 128 rows x
+// 64 columns (128 bytes), 128-byte swizzle, zero fill past N.
+bool make_tmap(CUtensorMap* m, const void* ptr, int BH, int N, int d, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa::kBM), 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(ptr), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULLPTR: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "bad shape (negative size, d <= 0, or sizes overflow)";
+    case FA_ERR_UNSUPPORTED_D: return "head width d must be 64 or 128";
+    case FA_ERR_DTYPE: return "dtype must be FA_BF16 or FA_FP16";
+    case FA_ERR_ALIGN: return "q/k/v/o must be 16-byte aligned and lse 4-byte aligned";
+    case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 GPU";
+    case FA_ERR_TENSORMAP: return "TMA descriptor creation failed";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_TIMEOUT: return "a bounded wait in a kernel ran out (watchdog)";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown error code";
+  }
+}
+
+void fa_set_watchdog_ns(unsigned long long ns) { g_watchdog_ns.store(ns); }
+
+int fa_work_tiles(int N, int causal, long long* pairs) {
+  if (!pairs) return FA_ERR_NULLPTR;
+  if (N < 0) return FA_ERR_SHAPE;
+  const long long n = (static_cast<long long>(N) + fa::kBN - 1) / fa::kBN;
+  *pairs = causal ? n * (n + 1) / 2 : n * n;
+  return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_qblk = (static_cast<long long>(N) + 2 * fa::kBM - 1) / (2 * fa::kBM);
+  if (bh > INT_MAX || bh * n_qblk > INT_MAX) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0 || N == 0) return FA_OK;  // nothing to write
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::FwdParams p;
+  if (!make_tmap(&p.tm_q, q, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_k, k, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_v, v, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_o, o, static_cast<int>(bh), N, d, bf16))
+    return FA_ERR_TENSORMAP;
+  p.lse = lse;
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_ns = wd ? wd : kDefaultWatchdogNs;
+  p.BH = static_cast<int>(bh);
+  p.N = N;
+  p.n_qblk = static_cast<int>(n_qblk);
+  p.n_kv = (N + fa::kBN - 1) / fa::kBN;
+  p.num_units = static_cast<int>(bh * n_qblk);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
+
+  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(p, grid, bf16, causal != 0, stream)
+                                  : fa::launch_fwd_d128(p, grid, bf16, causal != 0, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_status(cudaStream_t stream, unsigned int* detail) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fa_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (detail) *detail = word;
+  return word ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,495 @@
+// fa_fwd_kernel.cuh — exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes ("FlashAttention: The Matrix You Never Have to Write
+// Down", section "From softmax to attention: rescale the output too"): for
+// each query row, key/value tiles stream past a resident query tile; the
+// kernel keeps a running maximum m, a running exp-sum l and an unnormalised
+// output accumulator O, rescales l and O by exp(m_old - m_new) when a tile
+// raises the maximum, and divides O by l once after the last tile (section
+// "Build it"; the deferred division).  LSE = m + ln l is written per row.
+//
+// Rescaling is lazy: the reference maximum is only moved when a tile's
+// maximum exceeds it by more than kTau in log2 units (a factor of 2^8);
+// otherwise the tile is accumulated against the stale reference.  Because l
+// and O always share one reference, the final O / l and m + ln l are exact
+// for any threshold (section "What it doesn't solve", the FA4 paragraph on
+// deferring the correction while tracking it).
+//
+// Causal runs skip key tiles that lie wholly in a query tile's future and
+// mask only the diagonal tile (section "Causal masking: half the score tiles
+// disappear").
+//
+// Structure of one CTA (persistent; one CTA per SM):
+//   warps 0-3  softmax warpgroup 0  -> query tile 0 of the unit (TMEM lanes 0-127)
+//   warps 4-7  softmax warpgroup 1  -> query tile 1 of the unit
+//   warp  8    MMA issuer (one thread): S = Q K^T and O += P V on tcgen05
+//   warp  9    TMA producer (one thread): Q tiles and a ring of K/V tiles
+// A work unit is (batch*head, block of 256 query rows) = two 128-row query
+// tiles.  TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (d fp32
+// columns each); P (16-bit) overwrites the first 64 columns of its S.
+//
+// MMA issue order per key tile j (the two tiles ping-pong so one tile's
+// softmax runs while the tensor core works on the other tile):
+//   prologue: S0_0, S1_0
+//   step j  : PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// so S_w_{j+1} completing implies PV_w_j completed, which is what lets the
+// softmax warpgroup rescale O_w in place before it releases P_w_{j+1}.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;              // query rows per tile = TMEM lanes
+constexpr int kBN = 128;              // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kTau = 8.0f;          // lazy-rescale threshold, log2 units
+constexpr float kLn2 = 0.693147180559945309f;
+
+// Sites recorded in the status word when a wait runs out.
+enum WaitSite : uint32_t {
+  kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFull = 4, kSitePFull = 5,
+  kSiteOFree = 6, kSiteSFull = 7, kSiteODone = 8
+};
+
+struct FwdParams {
+  CUtensorMap tm_q;  // [BH, N, d] boxes of 128 rows x 64 columns, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_o;
+  float* lse;              // [BH, N]
+  unsigned int* status;    // device status word
+  unsigned long long watchdog_ns;
+  int BH;                  // batch * heads
+  int N;                   // sequence length
+  int n_qblk;              // ceil(N / 256): units per head
+  int n_kv;                // ceil(N / 128): key tiles per head
+  int num_units;           // BH * n_qblk
+  float scale_log2;        // scale * log2(e)
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kChunks = D / 64;             // 128-byte swizzle columns per row
+  static constexpr int kTile = kBM * D * 2;          // one 128 x D tile of 16-bit values
+  static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 128 bytes
+  static constexpr int kStages = (D == 128) ? 3 : 6; // K/V ring depth
+  static constexpr int kQ = 0;                       // two query tiles
+  static constexpr int kKV = kQ + 2 * kTile;         // ring of K or V tiles
+  static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles
+  static constexpr int kBar = kO + 2 * kTile;
+  // barrier indices
+  static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
+                       bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
+                       bOFree = bODone + 2, bFinal = bOFree + 2, kNumBars = bFinal + 1;
+  static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base address, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// TMEM column of S / O for query tile w.
+template <int D>
+__device__ __forceinline__ uint32_t s_col(int w) { return w ? 128u : 0u; }
+template <int D>
+__device__ __forceinline__ uint32_t o_col(int w) { return 256u + (w ? D : 0); }
+
+struct Unit {
+  int bh, mblk, n0, n1;
+};
+
+// Static persistent schedule: units are ordered heaviest first (for causal,
+// the last query blocks of every head first) and dealt to CTAs in a snake
+// (boustrophedon) order, round by round.  Deterministic, so every role of a
+// CTA walks the same list without communicating.
+__device__ __forceinline__ int unit_at(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
+template <bool kCausal>
+__device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
+  Unit u;
+  const int level = s / p.BH;
+  u.bh = s - level * p.BH;
+  u.mblk = p.n_qblk - 1 - level;
+  const int t0 = 2 * u.mblk;
+  if (kCausal) {
+    u.n0 = min(t0 + 1, p.n_kv);
+    u.n1 = min(t0 + 2, p.n_kv);
+  } else {
+    u.n0 = p.n_kv;
+    u.n1 = p.n_kv;
+  }
+  if ((t0 + 1) * kBM >= p.N) u.n1 = 0;  // second query tile lies wholly past N
+  return u;
+}
+
+template <int D, bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw_base);  // generic pointer to the aligned base
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sgen + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
+
+  // ---------------------------------------------------------------- setup
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_base_ptr), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x == kLoadWarp * 32) {
+    *abort_flag = 0;
+    ptx::mbar_init(bar(L::bQFull), 1);
+    ptx::mbar_init(bar(L::bQEmpty), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::bKvFull + s), 1);
+      ptx::mbar_init(bar(L::bKvEmpty + s), 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      ptx::mbar_init(bar(L::bSFull + w), 1);
+      ptx::mbar_init(bar(L::bPFull + w), 128);
+      ptx::mbar_init(bar(L::bODone + w), 1);
+      ptx::mbar_init(bar(L::bOFree + w), 128);
+    }
+    ptx::mbar_init(bar(L::bFinal), 1);
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+    ptx::prefetch_tmap(&p.tm_q);
+    ptx::prefetch_tmap(&p.tm_k);
+    ptx::prefetch_tmap(&p.tm_v);
+    ptx::prefetch_tmap(&p.tm_o);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_ptr;
+  const ptx::Watchdog wd{p.watchdog_ns, abort_flag, p.status};
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == kLoadWarp) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      uint32_t loads = 0;       // K/V tiles issued (ring position)
+      uint32_t q_issued = 0;    // units whose Q load was issued
+      uint32_t k_units = 0;     // units walked
+      bool alive = true;
+      for (int r = 0;; ++r) {
+        const int s = unit_at(r, cta, grid);
+        if (s >= p.num_units) break;
+        const Unit u = decode_unit<kCausal>(s, p);
+        const int nkv = max(u.n0, u.n1);
+        if (k_units > 0)
+          alive = ptx::wait_bounded(bar(L::bQEmpty), (k_units - 1) & 1, wd, kSiteQEmpty) && alive;
+        if (alive) {
+          const int ntile = u.n1 > 0 ? 2 : 1;
+          ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * L::kTile);
+          for (int w = 0; w < ntile; ++w)
+            for (int c = 0; c < L::kChunks; ++c)
+              ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
+                               bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
+          q_issued = k_units + 1;
+        }
+        for (int j = 0; j < nkv; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
+            if (use > 0)
+              alive = ptx::wait_bounded(bar(L::bKvEmpty + slot), (use - 1) & 1, wd, kSiteKvEmpty) &&
+                      alive;
+            if (alive) {
+              ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), L::kTile);
+              const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
+              for (int c = 0; c < L::kChunks; ++c)
+                ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
+                                 bar(L::bKvFull + slot), c * 64, j * kBN, u.bh);
+              ++loads;
+            }
+          }
+        }
+        ++k_units;
+      }
+      // Drain: make sure every issued copy has landed before the CTA can exit.
+      const uint64_t drain = 100000000ull;
+      const uint32_t first = loads > (uint32_t)L::kStages ? loads - L::kStages : 0;
+      for (uint32_t l = first; l < loads; ++l)
+        ptx::wait_drain(bar(L::bKvFull + l % L::kStages), (l / L::kStages) & 1, drain);
+      if (q_issued > 0) ptx::wait_drain(bar(L::bQFull), (q_issued - 1) & 1, drain);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr int fmt = kBf16 ? 1 : 0;
+      constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
+      constexpr uint32_t idesc_o = ptx::idesc_f16(kBM, D, fmt, 1);    // P (TMEM) x V (MN-major)
+      uint32_t loads = 0;          // K/V tiles consumed (ring position)
+      uint32_t k_units = 0;        // units walked
+      uint32_t ucnt[2] = {0, 0};   // units in which query tile w was active
+      uint32_t pcnt[2] = {0, 0};   // P tiles consumed per query tile
+      bool alive = true;
+      bool issued_any = false;
+
+      // S_w = Q_w K^T over the head width, 16 columns per instruction.  Both
+      // operands are K-major with a 128-byte swizzle: a K step of 16 columns
+      // moves 32 bytes inside a swizzle row, every 64 columns is a new chunk.
+      auto issue_s = [&](int w, uint32_t kslot) {
+        const uint32_t qa = sbase + L::kQ + w * L::kTile;
+        const uint32_t ka = sbase + L::kKV + kslot * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(tmem_base + s_col<D>(w), ptx::smem_desc_sw128(qa + off, 16, 1024),
+                      ptx::smem_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+        }
+      };
+      // O_w (+)= P_w V over 128 keys, 16 keys per instruction.  P comes from
+      // TMEM (two 16-bit values per column); V is MN-major (d contiguous):
+      // 8-key groups are 1024 bytes apart, 64-column chunks kChunkBytes apart.
+      auto issue_pv = [&](int w, uint32_t vslot, bool acc) {
+        const uint32_t va = sbase + L::kKV + vslot * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(tmem_base + o_col<D>(w), tmem_base + s_col<D>(w) + kk * 8,
+                      ptx::smem_desc_sw128(va + kk * 2048, L::kChunkBytes, 1024), idesc_o,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      auto next_full = [&]() -> uint32_t {
+        const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
+        alive = ptx::wait_bounded(bar(L::bKvFull + slot), use & 1, wd, kSiteKvFull) && alive;
+        ++loads;
+        return slot;
+      };
+      auto pv_step = [&](int w, int j, int n, uint32_t vslot) {
+        if (j >= n) return;
+        if (j == 0 && ucnt[w] > 0)  // O_w of the previous unit must have been read out
+          alive = ptx::wait_bounded(bar(L::bOFree + w), (ucnt[w] - 1) & 1, wd, kSiteOFree) && alive;
+        alive = ptx::wait_bounded(bar(L::bPFull + w), pcnt[w] & 1, wd, kSitePFull) && alive;
+        ++pcnt[w];
+        ptx::tc_fence_after();
+        if (alive) {
+          issue_pv(w, vslot, j > 0);
+          if (j == n - 1) ptx::mma_commit(bar(L::bODone + w));
+        }
+      };
+
+      for (int r = 0;; ++r) {
+        const int s = unit_at(r, cta, grid);
+        if (s >= p.num_units) break;
+        const Unit u = decode_unit<kCausal>(s, p);
+        const int nkv = max(u.n0, u.n1);
+        alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
+        ptx::tc_fence_after();
+
+        uint32_t kslot = next_full();
+        if (alive) {
+          if (u.n0 > 0) { issue_s(0, kslot); ptx::mma_commit(bar(L::bSFull + 0)); }
+          if (u.n1 > 0) { issue_s(1, kslot); ptx::mma_commit(bar(L::bSFull + 1)); }
+          ptx::mma_commit(bar(L::bKvEmpty + kslot));
+          if (nkv == 1) ptx::mma_commit(bar(L::bQEmpty));
+          issued_any = true;
+        }
+        for (int j = 0; j < nkv; ++j) {
+          const uint32_t vslot = next_full();
+          const bool more = j + 1 < nkv;
+          pv_step(0, j, u.n0, vslot);                       // PV0_j
+          if (more) kslot = next_full();
+          if (alive && more && j + 1 < u.n0) {              // S0_{j+1}
+            issue_s(0, kslot);
+            ptx::mma_commit(bar(L::bSFull + 0));
+          }
+          pv_step(1, j, u.n1, vslot);                       // PV1_j
+          if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
+          if (alive && more && j + 1 < u.n1) {              // S1_{j+1}
+            issue_s(1, kslot);
+            ptx::mma_commit(bar(L::bSFull + 1));
+          }
+          if (alive && more) {
+            ptx::mma_commit(bar(L::bKvEmpty + kslot));
+            if (j + 2 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
+          }
+        }
+        if (u.n0 > 0) ++ucnt[0];
+        if (u.n1 > 0) ++ucnt[1];
+        ++k_units;
+      }
+      // Drain: every MMA issued by this thread has completed before TMEM is freed.
+      if (issued_any) {
+        ptx::mma_commit(bar(L::bFinal));
+        ptx::wait_drain(bar(L::bFinal), 0, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ softmax + epilogue
+    const int w = warp >> 2;                 // query tile of the unit
+    const int t = threadIdx.x & 127;         // row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + s_col<D>(w);
+    const uint32_t tO = tmem_base + lane_off + o_col<D>(w);
+    const uint32_t stage = sbase + L::kO + w * L::kTile;
+    const float c = p.scale_log2;
+    uint32_t scnt = 0, ucnt = 0;
+
+    for (int r = 0;; ++r) {
+      const int s = unit_at(r, cta, grid);
+      if (s >= p.num_units) break;
+      const Unit u = decode_unit<kCausal>(s, p);
+      const int n = w ? u.n1 : u.n0;
+      if (n == 0) continue;
+      const int tile = 2 * u.mblk + w;
+      const int row = tile * kBM + t;
+
+      float m_ref = -INFINITY;  // reference maximum of the raw scores q.k
+      float neg_m = 0.f;        // -m_ref * c (0 while m_ref is -inf)
+      float l = 0.f;            // running sum of 2^(s*c + neg_m)
+      for (int j = 0; j < n; ++j) {
+        ptx::wait_bounded(bar(L::bSFull + w), scnt & 1, wd, kSiteSFull);
+        ++scnt;
+        __syncwarp();
+        ptx::tc_fence_after();
+        uint32_t sr[kBN];
+#pragma unroll
+        for (int q4 = 0; q4 < kBN / 32; ++q4) ptx::tmem_ld32(tS + q4 * 32, sr + q4 * 32);
+        ptx::tmem_wait_ld();
+        float sv[kBN];
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(sr[i]);
+
+        // mask: keys past N, and on the diagonal tile keys after this row
+        const int rem = p.N - j * kBN;
+        const bool diag = kCausal && j == tile;
+        if (diag || rem < kBN) {
+          int lim = rem < kBN ? rem : kBN;
+          if (diag) lim = min(lim, t + 1);
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i >= lim) sv[i] = -INFINITY;
+        }
+
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kBN; i += 8) {
+          a0 = ptx::max3(a0, sv[i + 0], sv[i + 1]);
+          a1 = ptx::max3(a1, sv[i + 2], sv[i + 3]);
+          a2 = ptx::max3(a2, sv[i + 4], sv[i + 5]);
+          a3 = ptx::max3(a3, sv[i + 6], sv[i + 7]);
+        }
+        const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+
+        // lazy rescale: move the reference only when the tile max exceeds it
+        // by more than kTau (always on the first finite tile; never for -inf)
+        const bool grow = (mx - m_ref) * c > kTau;
+        float alpha = 1.f;
+        if (grow) {
+          const float nm = -mx * c;
+          alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(nm - neg_m);
+          l *= alpha;
+          m_ref = mx;
+          neg_m = nm;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // PV_w_{j-1} is complete (it was issued before S_w_j), and PV_w_j
+          // cannot start before this warpgroup arrives on p_full below.
+#pragma unroll 1
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t orr[32];
+            ptx::tmem_ld32(tO + q4 * 32, orr);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            ptx::tmem_st32(tO + q4 * 32, orr);
+          }
+        }
+
+        // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int i = 0; i < kBN / 2; i += 2) {
+          const float p0 = ptx::ex2(fmaf(sv[2 * i + 0], c, neg_m));
+          const float p1 = ptx::ex2(fmaf(sv[2 * i + 1], c, neg_m));
+          const float p2 = ptx::ex2(fmaf(sv[2 * i + 2], c, neg_m));
+          const float p3 = ptx::ex2(fmaf(sv[2 * i + 3], c, neg_m));
+          l0 += p0;
+          l1 += p1;
+          l2 += p2;
+          l3 += p3;
+          pk[i] = ptx::pack2<kBf16>(p0, p1);
+          pk[i + 1] = ptx::pack2<kBf16>(p2, p3);
+        }
+        l += (l0 + l1) + (l2 + l3);
+        ptx::tmem_st32(tS, pk);
+        ptx::tmem_st32(tS + 32, pk + 32);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bPFull + w));
+      }
+
+      // ---- epilogue: O / l -> 16-bit staging tile -> TMA store; LSE per row
+      ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
+      ++ucnt;
+      __syncwarp();
+      ptx::tc_fence_after();
+      if (t == 0) ptx::bulk_wait_group_read0();   // staging tile free again
+      ptx::named_bar_sync(1 + w, 128);
+      const float inv_l = 1.0f / l;
+#pragma unroll 1
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t orr[32];
+        ptx::tmem_ld32(tO + q4 * 32, orr);
+        ptx::tmem_wait_ld();
+        const int chunk = q4 >> 1;
+#pragma unroll
+        for (int pc4 = 0; pc4 < 4; ++pc4) {
+          const int pc = (q4 & 1) * 4 + pc4;   // 16-byte piece within the 128-byte row
+          uint32_t v4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v4[e] = ptx::pack2<kBf16>(__uint_as_float(orr[pc4 * 8 + 2 * e]) * inv_l,
+                                      __uint_as_float(orr[pc4 * 8 + 2 * e + 1]) * inv_l);
+          const uint32_t addr =
+              stage + chunk * L::kChunkBytes + t * 128 + ((pc ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4[0]),
+                       "r"(v4[1]), "r"(v4[2]), "r"(v4[3])
+                       : "memory");
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(1 + w, 128);
+      if (t == 0) {
+        for (int ch = 0; ch < L::kChunks; ++ch)
+          ptx::tma_store_3d(&p.tm_o, stage + ch * L::kChunkBytes, ch * 64, tile * kBM, u.bh);
+        ptx::bulk_commit_group();
+      }
+      if (row < p.N)
+        p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
+    }
+    if (t == 0) ptx::bulk_wait_group0();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace fa

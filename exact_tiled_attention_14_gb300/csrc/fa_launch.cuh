@@ -1,0 +1,36 @@
+// fa_launch.cuh — host-side launch of one compiled variant of the forward kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+// Launch fa_fwd_kernel<D, kBf16, kCausal> with `grid` persistent CTAs.
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};  // devices on which the smem limit was raised
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load() & bit)) {
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, kBf16, kCausal>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  fa_fwd_kernel<D, kBf16, kCausal><<<grid, kThreads, Smem<D>::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_d64(const FwdParams& p, int grid, bool bf16, bool causal,
+                           cudaStream_t stream);
+cudaError_t launch_fwd_d128(const FwdParams& p, int grid, bool bf16, bool causal,
+                            cudaStream_t stream);
+
+}  // namespace fa

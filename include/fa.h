@@ -1,0 +1,123 @@
+/*
+ * fa.h — C ABI of the exact, tiled attention forward pass for GB300 (sm_103a).
+ *
+ * The operation is exact attention, O = softmax(Q K^T * scale) V, with the
+ * per-row log-sum-exp LSE kept for a backward pass ("FlashAttention: The
+ * Matrix You Never Have to Write Down", section "What attention computes, in
+ * one page" for the function, section "From softmax to attention: rescale
+ * the output too" for the online recurrence the kernels run, section "Build
+ * it" for the outputs O and L).  The N x N score or probability matrix is
+ * never written to memory ("Why FlashAttention Can Avoid a Square Attention
+ * Array Without Making Attention Linear", section "Tiles need a shared
+ * softmax normalization").
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are dense, contiguous, row-major, on the CURRENT CUDA device:
+ *      q, k, v, o : [B, H, N, d] in the storage dtype (bf16 or fp16);
+ *      lse        : [B, H, N] float32, natural log of the scaled scores.
+ *  - The caller owns every buffer.  The library allocates no device memory:
+ *    no workspace and no N x N buffer.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  A
+ *    non-zero return means nothing was launched.
+ *  - Causal masking is upper-left aligned: query i sees keys j <= i (section
+ *    "Build it", note on non-square causal alignment); with equal query and
+ *    key lengths this is also the bottom-right convention.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage dtype of q, k, v and o. */
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/* Return codes.  They mirror the pages' raise-on-bad-input contract (section
+ * "Build it", the input checks; section "Check it", the failing cases). */
+enum {
+  FA_OK = 0,
+  FA_ERR_NULLPTR = 1,        /* a required pointer is NULL                     */
+  FA_ERR_SHAPE = 2,          /* B, H or N negative, d <= 0, or sizes overflow  */
+  FA_ERR_UNSUPPORTED_D = 3,  /* d is not 64 or 128                             */
+  FA_ERR_DTYPE = 4,          /* dtype is not FA_BF16 / FA_FP16                 */
+  FA_ERR_ALIGN = 5,          /* q/k/v/o not 16-byte aligned, lse not 4-byte    */
+  FA_ERR_SCALE = 6,          /* scale not finite and > 0                       */
+  FA_ERR_DEVICE = 7,         /* current device is not a compute 10.3 GPU       */
+  FA_ERR_TENSORMAP = 8,      /* the driver refused a TMA descriptor            */
+  FA_ERR_LAUNCH = 9,         /* the launch itself failed (CUDA error)          */
+  FA_ERR_TIMEOUT = 10,       /* a kernel's bounded wait ran out (fa_status)    */
+  FA_ERR_CUDA = 11           /* a CUDA runtime call failed (fa_status)         */
+};
+
+/*
+ * fa_fwd — exact attention forward.
+ *
+ *   q, k, v : device pointers, [B, H, N, d], dtype `dtype`, 16-byte aligned.
+ *   o       : device pointer, [B, H, N, d], dtype `dtype`, 16-byte aligned;
+ *             O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) v_j, rounded to
+ *             nearest-even in the storage dtype.
+ *   lse     : device pointer, [B, H, N] float32, 4-byte aligned;
+ *             LSE[b,h,i] = ln sum_j exp(scale * q_i . k_j).
+ *   B, H, N : batch, heads, sequence length (queries = keys = N).  Any N >= 0;
+ *             a ragged last tile is masked.  B*H*N == 0 writes nothing and
+ *             returns FA_OK without touching the pointers.
+ *   d       : head width, 64 or 128.
+ *   causal  : nonzero for the causal mask (key j visible to query i iff j <= i).
+ *   scale   : multiplier of q.k, finite and > 0 (usually 1/sqrt(d)).
+ *   dtype   : FA_BF16 or FA_FP16 (q, k, v, o share it).
+ *   stream  : CUDA stream the kernel is enqueued on.
+ *
+ * Errors: FA_ERR_SHAPE, FA_ERR_UNSUPPORTED_D, FA_ERR_DTYPE, FA_ERR_SCALE are
+ * checked first, then the empty case, then FA_ERR_NULLPTR, FA_ERR_ALIGN,
+ * FA_ERR_DEVICE, FA_ERR_TENSORMAP, FA_ERR_LAUNCH.  Errors that happen on the
+ * device after the launch are reported by fa_status().
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int N, int d, int causal, float scale, int dtype,
+           cudaStream_t stream);
+
+/* Human-readable name of a return code (static string, never NULL). */
+const char *fa_strerror(int code);
+
+/*
+ * fa_status — device-side error state of kernels launched so far.
+ *
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Every wait inside the kernels is bounded by a
+ * watchdog; when one runs out the kernel records it there, finishes without
+ * hanging (its outputs are then undefined) and this call returns
+ * FA_ERR_TIMEOUT.  Returns FA_OK when no kernel reported a problem, FA_ERR_CUDA
+ * if the synchronisation or the read failed.  `detail` (may be NULL) receives
+ * the raw status word (bit 0: timeout; bits 8..15: id of the first wait that
+ * ran out).
+ */
+int fa_status(cudaStream_t stream, unsigned int *detail);
+
+/*
+ * fa_set_watchdog_ns — budget of every bounded wait in kernels launched after
+ * this call, in nanoseconds (default 2e9 = 2 s).  0 restores the default.
+ * Host-side setting shared by all threads of the process.
+ */
+void fa_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * fa_work_tiles — host-side count of the (query tile, key tile) pairs the
+ * forward kernel computes for one head with 128-row tiles: n^2 unmasked, or
+ * n(n+1)/2 causal with n = ceil(N/128) (section "Causal masking: half the
+ * score tiles disappear": whole future tiles are skipped, diagonal tiles are
+ * masked).  Writes the count to *pairs.  Returns FA_ERR_SHAPE for N < 0,
+ * FA_ERR_NULLPTR for a NULL `pairs`.
+ */
+int fa_work_tiles(int N, int causal, long long *pairs);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The shared library must load and export every function ``include/fa.h``
+declares; argument errors must come back as return codes before any device
+work; and the causal tile schedule must match the counts the pages print.
+No test here launches a kernel.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_tiled_attention_14_gb300 as fa
+from oracle_pins import read_golden  # noqa: F401  (golden helpers live there)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIB_PATH):
+        fa.build()
+    return fa.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_lists_the_binding_names():
+    assert header_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_header_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(fa_\w+)$", out, flags=re.M))
+    for name in header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_library_has_no_oracle_or_torch_dependency():
+    out = subprocess.run(["nm", "-D", fa.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    assert "oracle_" not in out
+    ldd = subprocess.run(["ldd", fa.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in ldd and "liboracle" not in ldd
+
+
+def test_strerror_covers_codes(lib):
+    for code in range(0, 12):
+        s = fa.fa_strerror(code)
+        assert s and s != "unknown error code"
+    assert fa.fa_strerror(999) == "unknown error code"
+    assert fa.fa_version() >= 100
+
+
+def test_work_tiles_match_printed_table(lib):
+    """Causal tiles computed: 36 of 64 at 1024 and 528 of 1024 at 4096 (block 128)."""
+    rows = [line.split() for line in open(os.path.join(ROOT, "tests", "golden", "causal_tiles.txt"))
+            if line.strip() and not line.startswith("#")]
+    assert rows
+    for ctx, block, computed, total, skipped in rows:
+        assert int(block) == 128
+        assert fa.fa_work_tiles(int(ctx), True) == int(computed)
+        assert fa.fa_work_tiles(int(ctx), False) == int(total)
+        assert round(100 * (1 - int(computed) / int(total))) == int(skipped)
+    assert fa.fa_work_tiles(0, True) == 0
+    assert fa.fa_work_tiles(129, True) == 3 and fa.fa_work_tiles(129, False) == 4
+    with pytest.raises(fa.FaError):
+        fa.fa_work_tiles(-1, False)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced (errors are returned first)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(B=-1), fa.FA_ERR_SHAPE),
+    (dict(N=-5), fa.FA_ERR_SHAPE),
+    (dict(d=0), fa.FA_ERR_SHAPE),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_SHAPE),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED_D),
+    (dict(dtype=7), fa.FA_ERR_DTYPE),
+    (dict(scale=0.0), fa.FA_ERR_SCALE),
+    (dict(scale=-1.0), fa.FA_ERR_SCALE),
+    (dict(scale=float("nan")), fa.FA_ERR_SCALE),
+    (dict(scale=float("inf")), fa.FA_ERR_SCALE),
+    (dict(q=None), fa.FA_ERR_NULLPTR),
+    (dict(lse=None), fa.FA_ERR_NULLPTR),
+    (dict(k=FAKE + 8), fa.FA_ERR_ALIGN),
+    (dict(o=FAKE + 2), fa.FA_ERR_ALIGN),
+    (dict(lse=FAKE + 2), fa.FA_ERR_ALIGN),
+    (dict(N=0, q=None, k=None, v=None, o=None, lse=None), fa.FA_OK),
+    (dict(B=0), fa.FA_OK),
+    (dict(H=0, q=None), fa.FA_OK),
+])
+def test_argument_errors(lib, args, code):
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=300, d=128, causal=0,
+                scale=0.125, dtype=fa.FA_BF16)
+    call.update(args)
+    assert fa.fa_fwd(**call) == code
+
+
+def test_no_gpu_fails_loudly(lib):
+    """Without a usable sm_103 device a valid call is refused, never computed on the CPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 0, 0.125, fa.FA_FP16)
+    assert rc == fa.FA_ERR_DEVICE
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.attention_forward(q, q, q)
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(RuntimeError):
+        fa.load_library(str(tmp_path / "libfa.so"))
+
+
+def test_binding_dtype_contract():
+    import torch
+    assert fa.dtype_code(torch.bfloat16) == fa.FA_BF16
+    assert fa.dtype_code(torch.float16) == fa.FA_FP16
+    with pytest.raises(TypeError):
+        fa.dtype_code(torch.float32)
+    a = torch.zeros(1, 1, 4, 64, dtype=torch.float16)
+    b = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fa.attention_forward(a, b, a)
+    with pytest.raises(ValueError):
+        fa.attention_forward(a[0], a[0], a[0])
+    _ = ctypes  # keep the import used
