@@ -100,51 +100,104 @@ def measured_peaks():
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (host-stamped) while the benchmark runs."""
+    """SM clock, power and clock-event reasons sampled while the benchmark runs.
 
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
-              "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
-    NAMES = [None, None, None, "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-             "sw_power_cap"]
+    Polls NVML (read-only queries through ctypes) every ~2 ms in a thread;
+    falls back to ``nvidia-smi -lms 20`` when NVML cannot be opened.
+    """
+
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.sw_power_cap",
+                  "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown"]
 
     def __init__(self, device_index):
-        self.samples = []
+        self.samples = []        # (host time, sm_mhz, max_mhz, power_w, reason names)
         self.error = None
-        self.proc = None
-        self.thread = None
+        self.source = None
         self.device_index = device_index
+        self._stop = threading.Event()
+        self.thread = None
+        self.proc = None
+
+    # -- NVML
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        ok = False
+        try:
+            props = torch.cuda.get_device_properties(self.device_index)
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(handle)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            count = ctypes.c_uint(0)
+            lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+            if count.value != 1:
+                raise OSError("cannot identify the GPU in NVML")
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) != 0:
+                raise OSError("nvmlDeviceGetHandleByIndex failed")
+        return lib, handle
+
+    def _nvml_loop(self, lib, handle):
+        import ctypes
+        clk, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            t = time.time()
+            if lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0:
+                lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))
+                p = lib.nvmlDeviceGetPowerUsage(handle, ctypes.byref(pw))
+                get_reasons(handle, ctypes.byref(rs))
+                names = [n for bit, n in self.REASONS.items() if rs.value & bit]
+                self.samples.append((t, float(clk.value), float(mx.value),
+                                     pw.value / 1000.0 if p == 0 else None, names))
+            time.sleep(0.002)
+
+    # -- nvidia-smi fallback
+    def _smi_loop(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.SMI_FIELDS):
+                continue
+            try:
+                names = [n for n, v in zip(["sw_power_cap", "hw_slowdown", "sw_thermal_slowdown",
+                                            "hw_thermal_slowdown"], parts[3:])
+                         if v.lower() == "active"]
+                pw = float(parts[2]) if parts[2] not in ("[N/A]", "") else None
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), pw, names))
+            except ValueError:
+                pass
 
     def start(self):
-        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-               "-lms", "20"]
-        bus = self._bus_id()
-        if bus:
-            cmd += ["-i", bus]
         try:
-            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                                         text=True)
+            lib, handle = self._nvml_open()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(lib, handle), daemon=True)
         except OSError as e:
-            self.error = f"nvidia-smi unavailable: {e}"
-            return self
-        self.thread = threading.Thread(target=self._read, daemon=True)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = f"nvidia-smi ({e})"
+                self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+            except OSError as e2:
+                self.error = f"no clock source: {e}; {e2}"
+                return self
         self.thread.start()
         return self
 
-    def _bus_id(self):
-        try:
-            props = torch.cuda.get_device_properties(self.device_index)
-            return "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
-        except Exception:  # older torch: fall back to nvidia-smi's default (all GPUs)
-            return None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) == len(self.FIELDS):
-                self.samples.append((time.time(), parts))
-
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -156,30 +209,24 @@ class ClockSampler:
 
     def summary(self, t0, t1, fallback_window=None):
         def pick(a, b):
-            return [s for t, s in self.samples if a <= t <= b]
+            return [x for x in self.samples if a <= x[0] <= b]
         window = "timed"
         rows = pick(t0, t1)
         if len(rows) < 3 and fallback_window:
             rows, window = pick(*fallback_window), "warmup+timed"
         out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(rows),
-               "window": window}
+               "window": window, "source": self.source}
         if self.error:
             out["error"] = self.error
         if not rows:
             return out
-        try:
-            sm = [float(r[0]) for r in rows]
-            out["sm_mhz"] = statistics.median(sm)
-            out["sm_max_mhz"] = max(float(r[1]) for r in rows)
-            out["power_w_max"] = max(float(r[2]) for r in rows if r[2] not in ("[N/A]", ""))
-        except ValueError:
-            pass
-        reasons = set()
-        for r in rows:
-            for i, name in enumerate(self.NAMES):
-                if name and r[i].lower() == "active":
-                    reasons.add(name)
-        out["reasons"] = sorted(reasons)
+        out["sm_mhz"] = statistics.median(r[1] for r in rows)
+        out["sm_min_mhz"] = min(r[1] for r in rows)
+        out["sm_max_mhz"] = max(r[2] for r in rows)
+        pws = [r[3] for r in rows if r[3] is not None]
+        if pws:
+            out["power_w_max"] = max(pws)
+        out["reasons"] = sorted({n for r in rows for n in r[4]})
         return out
 
 
@@ -216,41 +263,32 @@ def barrier(world, device=None):
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(w, q, k, v, budget_s, seed=0, max_rows=None):
-    """Time the float64 oracle on seeded rows of head (0, 0) for about budget_s.
+def oracle_sample(w, q, k, v, budget_s, start_head=0):
+    """Time the float64 oracle on whole heads of the workload for about budget_s.
 
-    Returns (TFLOP/s, seconds, rows, cores, description).  The FLOPs of a row
-    are 4*d per visible key (its share of the two matmuls), which sums to the
-    workload's convention over all rows.
+    Heads are taken in order from ``start_head`` (wrapping) until the budget
+    is spent or every head is done.  Every head does the same work, so the
+    throughput of whole heads is the throughput of the workload.  Returns
+    (TFLOP/s, seconds, heads, cores, description).
     """
-    import numpy as np
-
     import oracle
     lib = oracle.load()
-    N, d = w["N"], w["d"]
-    kh, vh = k[0, 0].double().numpy(), v[0, 0].double().numpy()
-    g = np.random.default_rng(seed)
-
-    def run(nrows):
-        rows = np.sort(g.integers(0, N, size=nrows))
-        qr = q[0, 0][torch.from_numpy(rows)].double().numpy()
-        t0 = time.perf_counter()
-        oracle.attention_rows(qr, rows, kh, vh, causal=w["causal"], scale=w["scale"], lib=lib)
-        dt = time.perf_counter() - t0
-        vis = (rows + 1).sum() if w["causal"] else nrows * N
-        return dt, 4.0 * d * float(vis)
-
+    B, H = w["B"], w["H"]
+    nheads = B * H
     cores = oracle.num_threads(lib)
-    probe = max(cores * 4, 16)
-    dt, fl = run(probe)
-    rows = probe
-    if dt < budget_s:
-        rows = int(min(probe * budget_s / max(dt, 1e-6), max_rows or 10 ** 9))
-        rows = max(rows, probe)
-        dt, fl = run(rows)
-    desc = (f"{rows} seeded random query rows of head (0,0) of {w['name']} "
-            f"({rows / (w['B'] * w['H'] * N):.2e} of all rows), float64, {cores} threads")
-    return fl / dt / 1e12, dt, rows, cores, desc
+    done, spent = 0, 0.0
+    while done < nheads and (done == 0 or spent < budget_s):
+        hb = (start_head + done) % nheads
+        b, h = divmod(hb, H)
+        qh, kh, vh = (t[b, h].double().numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.attention(qh, kh, vh, causal=w["causal"], scale=w["scale"], lib=lib)
+        spent += time.perf_counter() - t0
+        done += 1
+    flops = step_flops(w) * done / nheads
+    desc = (f"{done} of {nheads} whole heads of {w['name']} (float64, {cores} threads); "
+            "every head does the same work")
+    return flops / spent / 1e12, spent, done, cores, desc
 
 
 # ---------------------------------------------------------------- arms
@@ -266,7 +304,7 @@ def run_reference(args, w):
     oracle.load()
     vals = []
     for i in range(total):
-        tf, dt, rows, cores, desc = oracle_sample(w, q, k, v, per_step, seed=i)
+        tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, per_step, start_head=i)
         if i >= args.warmup:
             vals.append((tf, dt))
     value = statistics.median(tf for tf, _ in vals)
@@ -298,6 +336,7 @@ def run_ours(args, w):
     init_dist(world, "nccl")
     fa.load_library()
 
+    sampler = ClockSampler(local).start()
     q, k, v = seeded_inputs.make_workload_qkv(w)
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     per_replica = io_bytes(w)["h2d"] + io_bytes(w)["d2h"]
@@ -317,7 +356,6 @@ def run_ours(args, w):
         if rc:
             raise fa.FaError(rc)
 
-    sampler = ClockSampler(local).start()
     t_warm = time.time()
     for i in range(args.warmup):
         step(i)
@@ -410,7 +448,7 @@ def run_ours(args, w):
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
-        tf, dt, rows, cores, desc = oracle_sample(w, q, k, v, args.cpu_seconds)
+        tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     print(json.dumps(line), flush=True)
@@ -428,6 +466,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="one of: " + ", ".join(x["name"] for x in seeded_inputs.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B of the workload (smaller profiling captures)")
+    ap.add_argument("--heads", type=int, default=None, help="override H of the workload")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
@@ -437,6 +478,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = seeded_inputs.workload(args.workload)
+    if args.batch is not None or args.heads is not None:
+        w["B"] = args.batch if args.batch is not None else w["B"]
+        w["H"] = args.heads if args.heads is not None else w["H"]
+        w["name"] = f"{w['name']}@B{w['B']}H{w['H']}"
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -152,6 +152,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
       !make_tmap(&p.tm_v, v, static_cast<int>(bh), N, d, bf16) ||
       !make_tmap(&p.tm_o, o, static_cast<int>(bh), N, d, bf16))
     return FA_ERR_TENSORMAP;
+  p.o = o;
   p.lse = lse;
   p.status = info->status;
   const unsigned long long wd = g_watchdog_ns.load();

@@ -63,6 +63,7 @@ struct FwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_o;
+  void* o;                 // [BH, N, d] (direct-store epilogue)
   float* lse;              // [BH, N]
   unsigned int* status;    // device status word
   unsigned long long watchdog_ns;
@@ -74,16 +75,21 @@ struct FwdParams {
   float scale_log2;        // scale * log2(e)
 };
 
+// Shared-memory plan.  At d = 128 the two output staging tiles would cost two
+// K/V ring stages (the ring then cannot cover L2 latency), so O is written
+// straight from registers; at d = 64 there is room for both, and O goes out
+// through a staging tile and a TMA store.
 template <int D>
 struct Smem {
   static constexpr int kChunks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kTile = kBM * D * 2;          // one 128 x D tile of 16-bit values
   static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 128 bytes
-  static constexpr int kStages = (D == 128) ? 3 : 6; // K/V ring depth
+  static constexpr bool kTmaStore = (D == 64);       // epilogue through smem + TMA store
+  static constexpr int kStages = (D == 128) ? 5 : 8; // K/V ring depth
   static constexpr int kQ = 0;                       // two query tiles
   static constexpr int kKV = kQ + 2 * kTile;         // ring of K or V tiles
-  static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles
-  static constexpr int kBar = kO + 2 * kTile;
+  static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles (if any)
+  static constexpr int kBar = kO + (kTmaStore ? 2 * kTile : 0);
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
                        bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
@@ -192,20 +198,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s >= p.num_units) break;
         const Unit u = decode_unit<kCausal>(s, p);
         const int nkv = max(u.n0, u.n1);
-        if (k_units > 0)
-          alive = ptx::wait_bounded(bar(L::bQEmpty), (k_units - 1) & 1, wd, kSiteQEmpty) && alive;
-        if (alive) {
-          const int ntile = u.n1 > 0 ? 2 : 1;
-          ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * L::kTile);
-          for (int w = 0; w < ntile; ++w)
-            for (int c = 0; c < L::kChunks; ++c)
-              ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
-                               bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
-          q_issued = k_units + 1;
-        }
+        // Q of this unit may only overwrite the buffer once the previous
+        // unit's last S MMA has read it; the first K tile does not wait for
+        // that, so it is requested first.
+        auto load_q = [&]() {
+          if (k_units > 0)
+            alive = ptx::wait_bounded(bar(L::bQEmpty), (k_units - 1) & 1, wd, kSiteQEmpty) && alive;
+          if (alive) {
+            const int ntile = u.n1 > 0 ? 2 : 1;
+            ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * L::kTile);
+            for (int w = 0; w < ntile; ++w)
+              for (int c = 0; c < L::kChunks; ++c)
+                ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
+                                 bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
+            q_issued = k_units + 1;
+          }
+        };
         for (int j = 0; j < nkv; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
+            if (j == 0 && kv == 1) load_q();
             const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
             if (use > 0)
               alive = ptx::wait_bounded(bar(L::bKvEmpty + slot), (use - 1) & 1, wd, kSiteKvEmpty) &&
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + s_col<D>(w);
     const uint32_t tO = tmem_base + lane_off + o_col<D>(w);
-    const uint32_t stage = sbase + L::kO + w * L::kTile;
+    const uint32_t stage = sbase + L::kO + w * L::kTile;   // used when kTmaStore
     const float c = p.scale_log2;
     uint32_t scnt = 0, ucnt = 0;
 
@@ -415,23 +427,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
-        // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM.
+        // The exponent argument and the row sum use two-lane fp32 instructions.
+        const uint64_t c2 = ptx::f2_pack(c, c);
+        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+        uint64_t acc0 = ptx::f2_pack(0.f, 0.f), acc1 = acc0;
         uint32_t pk[kBN / 2];
 #pragma unroll
         for (int i = 0; i < kBN / 2; i += 2) {
-          const float p0 = ptx::ex2(fmaf(sv[2 * i + 0], c, neg_m));
-          const float p1 = ptx::ex2(fmaf(sv[2 * i + 1], c, neg_m));
-          const float p2 = ptx::ex2(fmaf(sv[2 * i + 2], c, neg_m));
-          const float p3 = ptx::ex2(fmaf(sv[2 * i + 3], c, neg_m));
-          l0 += p0;
-          l1 += p1;
-          l2 += p2;
-          l3 += p3;
+          float x0, x1, x2, x3;
+          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(sv[2 * i + 0], sv[2 * i + 1]), c2, nm2), x0, x1);
+          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(sv[2 * i + 2], sv[2 * i + 3]), c2, nm2), x2, x3);
+          const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+          acc0 = ptx::fadd2(acc0, ptx::f2_pack(p0, p1));
+          acc1 = ptx::fadd2(acc1, ptx::f2_pack(p2, p3));
           pk[i] = ptx::pack2<kBf16>(p0, p1);
           pk[i + 1] = ptx::pack2<kBf16>(p2, p3);
         }
-        l += (l0 + l1) + (l2 + l3);
+        {
+          float a, b, cc, dd;
+          ptx::f2_unpack(acc0, a, b);
+          ptx::f2_unpack(acc1, cc, dd);
+          l += (a + b) + (cc + dd);
+        }
         ptx::tmem_st32(tS, pk);
         ptx::tmem_st32(tS + 32, pk + 32);
         ptx::tmem_wait_st();
@@ -439,48 +457,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(L::bPFull + w));
       }
 
-      // ---- epilogue: O / l -> 16-bit staging tile -> TMA store; LSE per row
+      // ---- epilogue: O / l in the storage dtype, and LSE = m + ln l per row
       ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
       ++ucnt;
       __syncwarp();
       ptx::tc_fence_after();
-      if (t == 0) ptx::bulk_wait_group_read0();   // staging tile free again
-      ptx::named_bar_sync(1 + w, 128);
       const float inv_l = 1.0f / l;
+      if constexpr (L::kTmaStore) {
+        // through a swizzled staging tile and a TMA store (rows past N clipped)
+        if (t == 0) ptx::bulk_wait_group_read0();   // staging tile free again
+        ptx::named_bar_sync(1 + w, 128);
 #pragma unroll 1
-      for (int q4 = 0; q4 < D / 32; ++q4) {
-        uint32_t orr[32];
-        ptx::tmem_ld32(tO + q4 * 32, orr);
-        ptx::tmem_wait_ld();
-        const int chunk = q4 >> 1;
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t orr[32];
+          ptx::tmem_ld32(tO + q4 * 32, orr);
+          ptx::tmem_wait_ld();
+          const int chunk = q4 >> 1;
 #pragma unroll
-        for (int pc4 = 0; pc4 < 4; ++pc4) {
-          const int pc = (q4 & 1) * 4 + pc4;   // 16-byte piece within the 128-byte row
-          uint32_t v4[4];
+          for (int pc4 = 0; pc4 < 4; ++pc4) {
+            const int pc = (q4 & 1) * 4 + pc4;   // 16-byte piece within the 128-byte row
+            uint32_t v4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            v4[e] = ptx::pack2<kBf16>(__uint_as_float(orr[pc4 * 8 + 2 * e]) * inv_l,
-                                      __uint_as_float(orr[pc4 * 8 + 2 * e + 1]) * inv_l);
-          const uint32_t addr =
-              stage + chunk * L::kChunkBytes + t * 128 + ((pc ^ (t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4[0]),
-                       "r"(v4[1]), "r"(v4[2]), "r"(v4[3])
-                       : "memory");
+            for (int e = 0; e < 4; ++e)
+              v4[e] = ptx::pack2<kBf16>(__uint_as_float(orr[pc4 * 8 + 2 * e]) * inv_l,
+                                        __uint_as_float(orr[pc4 * 8 + 2 * e + 1]) * inv_l);
+            const uint32_t addr =
+                stage + chunk * L::kChunkBytes + t * 128 + ((pc ^ (t & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v4[0]),
+                         "r"(v4[1]), "r"(v4[2]), "r"(v4[3])
+                         : "memory");
+          }
         }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(1 + w, 128);
-      if (t == 0) {
-        for (int ch = 0; ch < L::kChunks; ++ch)
-          ptx::tma_store_3d(&p.tm_o, stage + ch * L::kChunkBytes, ch * 64, tile * kBM, u.bh);
-        ptx::bulk_commit_group();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(1 + w, 128);
+        if (t == 0) {
+          for (int ch = 0; ch < L::kChunks; ++ch)
+            ptx::tma_store_3d(&p.tm_o, stage + ch * L::kChunkBytes, ch * 64, tile * kBM, u.bh);
+          ptx::bulk_commit_group();
+        }
+      } else {
+        // straight from registers: each thread writes its own row
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
+                                               (static_cast<size_t>(u.bh) * p.N + row) * (D * 2));
+#pragma unroll 1
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t orr[32];
+          ptx::tmem_ld32(tO + q4 * 32, orr);
+          ptx::tmem_wait_ld();
+          const uint64_t il2 = ptx::f2_pack(inv_l, inv_l);
+          uint32_t pk16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a, b;
+            ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(__uint_as_float(orr[2 * e]),
+                                                   __uint_as_float(orr[2 * e + 1])), il2), a, b);
+            pk16[e] = ptx::pack2<kBf16>(a, b);
+          }
+          if (row < p.N) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[q4 * 4 + v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2],
+                                            pk16[4 * v + 3]);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
       }
       if (row < p.N)
         p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
     }
-    if (t == 0) ptx::bulk_wait_group0();
+    if constexpr (L::kTmaStore) {
+      if (t == 0) ptx::bulk_wait_group0();
+    }
   }
 
   // ---------------------------------------------------------------- teardown
