@@ -30,16 +30,23 @@ def nvcc():
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build(verbose=False, ptxas_info=False, extra_flags=()):
-    """Compile and link; returns the path of the shared library."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose=False, ptxas_info=False, extra_flags=(), build_dir=None):
+    """Compile and link; returns the path of the shared library.
+
+    ``extra_flags`` are added to every nvcc compile (e.g. ``-DFA_TRACE`` for
+    the event-trace build); ``build_dir`` puts objects and ``libfa.so``
+    somewhere other than ``_build/``.
+    """
+    bdir = build_dir or BUILD_DIR
+    lib_path = os.path.join(bdir, "libfa.so")
+    os.makedirs(bdir, exist_ok=True)
     flags = list(NVCC_FLAGS) + list(extra_flags)
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [nvcc(), *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
@@ -55,13 +62,13 @@ def build(verbose=False, ptxas_info=False, extra_flags=()):
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     link = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     if verbose:
         print(" ".join(link), flush=True)
     subprocess.run(link, check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

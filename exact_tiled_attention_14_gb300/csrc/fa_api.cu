@@ -21,6 +21,7 @@ __device__ unsigned int g_fa_status = 0;
 
 constexpr unsigned long long kDefaultWatchdogNs = 2000000000ull;
 std::atomic<unsigned long long> g_watchdog_ns{0};
+std::atomic<unsigned long long*> g_trace{nullptr};  // FA_TRACE builds only
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -115,7 +116,21 @@ const char* fa_strerror(int code) {
   }
 }
 
-void fa_set_watchdog_ns(unsigned long long ns) { g_watchdog_ns.store(ns); }
+void fa_set_watchdog_ns(unsigned long long ns) {
+  const unsigned long long kMaxNs = 1000000000000ull;  // 1000 s keeps the cycle count in range
+  g_watchdog_ns.store(ns > kMaxNs ? kMaxNs : ns);
+}
+
+#ifdef FA_TRACE
+// Trace builds only (not part of the ABI in fa.h): device buffer that
+// kernels launched afterwards record events into, or NULL to stop.  It must
+// hold grid * 4 * kTraceCap * 16 bytes.
+int fa_debug_set_trace(void* buf) {
+  g_trace.store(static_cast<unsigned long long*>(buf));
+  return FA_OK;
+}
+int fa_debug_trace_cap(void) { return fa::kTraceCap; }
+#endif
 
 int fa_work_tiles(int N, int causal, long long* pairs) {
   if (!pairs) return FA_ERR_NULLPTR;
@@ -154,9 +169,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return FA_ERR_TENSORMAP;
   p.o = o;
   p.lse = lse;
+  p.trace = g_trace.load();
   p.status = info->status;
+  // The kernels count the budget in SM cycles; converting at the highest SM
+  // clock of the part (2.1 GHz) makes the real-time budget at least the one
+  // asked for, whatever clock the GPU runs at.
   const unsigned long long wd = g_watchdog_ns.load();
-  p.watchdog_ns = wd ? wd : kDefaultWatchdogNs;
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
   p.BH = static_cast<int>(bh);
   p.N = N;
   p.n_qblk = static_cast<int>(n_qblk);

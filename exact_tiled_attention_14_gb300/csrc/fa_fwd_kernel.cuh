@@ -24,6 +24,8 @@
 //   warps 4-7  softmax warpgroup 1  -> query tile 1 of the unit
 //   warp  8    MMA issuer (one thread): S = Q K^T and O += P V on tcgen05
 //   warp  9    TMA producer (one thread): Q tiles and a ring of K/V tiles
+//   warps 10-11 idle (they complete the third warpgroup, which lets the
+//              issue warps give their registers to the softmax warpgroups)
 // A work unit is (batch*head, block of 256 query rows) = two 128-row query
 // tiles.  TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (d fp32
 // columns each); P (16-bit) overwrites the first 64 columns of its S.
@@ -45,9 +47,16 @@ namespace fa {
 
 constexpr int kBM = 128;              // query rows per tile = TMEM lanes
 constexpr int kBN = 128;              // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;         // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+// Registers per thread after the split: the launch gives every thread 168
+// (64512 per CTA); the issue warpgroup drops to 88 so the two softmax
+// warpgroups can hold a whole 128-column score row plus its packed P.
+// 2 * 128 * kSoftmaxRegs + 128 * kIssueRegs must not exceed 168 * 384.
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kIssueRegs = 88;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kIssueRegs <= 168 * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTau = 8.0f;          // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.693147180559945309f;
@@ -66,14 +75,41 @@ struct FwdParams {
   void* o;                 // [BH, N, d] (direct-store epilogue)
   float* lse;              // [BH, N]
   unsigned int* status;    // device status word
-  unsigned long long watchdog_ns;
+  unsigned long long watchdog_cycles;  // budget of one bounded wait, SM cycles
   int BH;                  // batch * heads
   int N;                   // sequence length
   int n_qblk;              // ceil(N / 256): units per head
   int n_kv;                // ceil(N / 128): key tiles per head
   int num_units;           // BH * n_qblk
   float scale_log2;        // scale * log2(e)
+  unsigned long long* trace;  // event trace buffer (only read in FA_TRACE builds)
 };
+
+// ---------------------------------------------------------------- tracing
+// Builds compiled with -DFA_TRACE record timestamped events of each role of
+// each CTA (SM clock, clock64) into p.trace: kTraceCap events of two 64-bit
+// words (time, event << 32 | argument) per (CTA, role).  Roles: 0/1 softmax
+// warpgroups (their first thread), 2 MMA issuer, 3 TMA producer.  Normal
+// builds compile every trace point away.
+constexpr int kTraceCap = 4096;
+enum TraceEvent : uint32_t {
+  kEvSReady = 1, kEvPArrive = 2, kEvRescale = 3, kEvEpiStart = 4, kEvEpiEnd = 5,
+  kEvUnit = 10, kEvPvIssue = 11, kEvSIssue = 12, kEvKvWaited = 13, kEvPWaited = 14,
+  kEvLoadK = 20, kEvLoadV = 21, kEvLoadQ = 22
+};
+__device__ __forceinline__ void trace_event(const FwdParams& p, int role, uint32_t& cnt,
+                                            uint32_t ev, uint32_t arg) {
+#ifdef FA_TRACE
+  if (p.trace != nullptr && cnt < static_cast<uint32_t>(kTraceCap)) {
+    const size_t i = (static_cast<size_t>(blockIdx.x) * 4 + role) * kTraceCap + cnt;
+    p.trace[2 * i] = clock64();
+    p.trace[2 * i + 1] = (static_cast<unsigned long long>(ev) << 32) | arg;
+  }
+  ++cnt;
+#else
+  (void)p; (void)role; (void)cnt; (void)ev; (void)arg;
+#endif
+}
 
 // Shared-memory plan.  At d = 128 the two output staging tiles would cost two
 // K/V ring stages (the ring then cannot cover L2 latency), so O is written
@@ -182,13 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_base_ptr;
-  const ptx::Watchdog wd{p.watchdog_ns, abort_flag, p.status};
+  const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
   const int grid = gridDim.x;
   const int cta = blockIdx.x;
-
+  // Each role's code sits inside the branch that set its register budget.
+  if (warp >= 8) {
+  ptx::setmaxnreg_dec<kIssueRegs>();
   if (warp == kLoadWarp) {
     // ============================================================ TMA producer
     if (lane == 0) {
+      uint32_t tr = 0;          // trace events recorded
       uint32_t loads = 0;       // K/V tiles issued (ring position)
       uint32_t q_issued = 0;    // units whose Q load was issued
       uint32_t k_units = 0;     // units walked
@@ -212,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
                                  bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
             q_issued = k_units + 1;
+            trace_event(p, 3, tr, kEvLoadQ, k_units);
           }
         };
         for (int j = 0; j < nkv; ++j) {
@@ -228,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < L::kChunks; ++c)
                 ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
                                  bar(L::bKvFull + slot), c * 64, j * kBN, u.bh);
+              trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
               ++loads;
             }
           }
@@ -235,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++k_units;
       }
       // Drain: make sure every issued copy has landed before the CTA can exit.
-      const uint64_t drain = 100000000ull;
+      const unsigned long long drain = 200000000ull;   // cycles (~0.1 s)
       const uint32_t first = loads > (uint32_t)L::kStages ? loads - L::kStages : 0;
       for (uint32_t l = first; l < loads; ++l)
         ptx::wait_drain(bar(L::bKvFull + l % L::kStages), (l / L::kStages) & 1, drain);
@@ -244,58 +285,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
+    // One thread issues every tcgen05 instruction.  The issue loop has to
+    // keep up with the tensor core (an M128 x N128 x K16 MMA lasts ~64
+    // cycles), so descriptors are precomputed: per MMA only the 32-bit
+    // address word changes, by a compile-time offset.
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
       constexpr uint32_t idesc_o = ptx::idesc_f16(kBM, D, fmt, 1);    // P (TMEM) x V (MN-major)
-      uint32_t loads = 0;          // K/V tiles consumed (ring position)
-      uint32_t k_units = 0;        // units walked
-      uint32_t ucnt[2] = {0, 0};   // units in which query tile w was active
-      uint32_t pcnt[2] = {0, 0};   // P tiles consumed per query tile
-      bool alive = true;
-      bool issued_any = false;
+      // Address words of the shared-memory descriptors (start >> 4 | LBO >> 4 << 16).
+      const uint32_t q_lo0 = ptx::desc_lo(sbase + L::kQ, 16);
+      const uint32_t q_lo1 = ptx::desc_lo(sbase + L::kQ + L::kTile, 16);
+      const uint32_t k_lo0 = ptx::desc_lo(sbase + L::kKV, 16);
+      const uint32_t v_lo0 = ptx::desc_lo(sbase + L::kKV, L::kChunkBytes);
+      constexpr uint32_t kSlotLo = L::kTile >> 4;
+      const uint32_t tS0 = tmem_base + s_col<D>(0), tS1 = tmem_base + s_col<D>(1);
+      const uint32_t tO0 = tmem_base + o_col<D>(0), tO1 = tmem_base + o_col<D>(1);
 
-      // S_w = Q_w K^T over the head width, 16 columns per instruction.  Both
-      // operands are K-major with a 128-byte swizzle: a K step of 16 columns
-      // moves 32 bytes inside a swizzle row, every 64 columns is a new chunk.
-      auto issue_s = [&](int w, uint32_t kslot) {
-        const uint32_t qa = sbase + L::kQ + w * L::kTile;
-        const uint32_t ka = sbase + L::kKV + kslot * L::kTile;
+      // S = Q_w K^T over the head width: K-major operands, 128-byte swizzle;
+      // a K step of 16 columns moves 32 bytes inside a swizzle row, and every
+      // 64 columns start a new chunk.
+      auto issue_s = [&](uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(tmem_base + s_col<D>(w), ptx::smem_desc_sw128(qa + off, 16, 1024),
-                      ptx::smem_desc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+          const uint32_t off = static_cast<uint32_t>((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+          ptx::mma_ss(d_tmem, ptx::desc_sw128(q_lo + off), ptx::desc_sw128(k_lo + off), idesc_s,
+                      kk > 0);
         }
       };
-      // O_w (+)= P_w V over 128 keys, 16 keys per instruction.  P comes from
-      // TMEM (two 16-bit values per column); V is MN-major (d contiguous):
-      // 8-key groups are 1024 bytes apart, 64-column chunks kChunkBytes apart.
-      auto issue_pv = [&](int w, uint32_t vslot, bool acc) {
-        const uint32_t va = sbase + L::kKV + vslot * L::kTile;
+      // O_w (+)= P_w V over 128 keys: P from TMEM (two 16-bit values per
+      // column, 8 columns per 16 keys); V MN-major (d contiguous): 8-key
+      // groups 1024 bytes apart (SBO), 64-column chunks kChunkBytes apart (LBO).
+      auto issue_pv = [&](uint32_t o_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t acc) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts(tmem_base + o_col<D>(w), tmem_base + s_col<D>(w) + kk * 8,
-                      ptx::smem_desc_sw128(va + kk * 2048, L::kChunkBytes, 1024), idesc_o,
-                      (acc || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(o_tmem, p_tmem + kk * 8, ptx::desc_sw128(v_lo + kk * (2048 >> 4)), idesc_o,
+                      kk > 0 ? 1u : acc);
       };
+
+      uint32_t tr = 0;                 // trace events recorded
+      uint32_t slot = 0, phase = 0;    // K/V ring position
+      uint32_t loads = 0;              // K/V tiles consumed (trace argument)
+      uint32_t k_units = 0;            // units walked
+      uint32_t ucnt0 = 0, ucnt1 = 0;   // units in which query tile 0 / 1 was active
+      uint32_t pph0 = 0, pph1 = 0;     // p_full phase parity of tile 0 / 1
+      bool alive = true;
+      bool issued_any = false;
       auto next_full = [&]() -> uint32_t {
-        const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
-        alive = ptx::wait_bounded(bar(L::bKvFull + slot), use & 1, wd, kSiteKvFull) && alive;
+        alive = ptx::wait_bounded(bar(L::bKvFull + slot), phase, wd, kSiteKvFull) && alive;
+        trace_event(p, 2, tr, kEvKvWaited, loads);
         ++loads;
-        return slot;
-      };
-      auto pv_step = [&](int w, int j, int n, uint32_t vslot) {
-        if (j >= n) return;
-        if (j == 0 && ucnt[w] > 0)  // O_w of the previous unit must have been read out
-          alive = ptx::wait_bounded(bar(L::bOFree + w), (ucnt[w] - 1) & 1, wd, kSiteOFree) && alive;
-        alive = ptx::wait_bounded(bar(L::bPFull + w), pcnt[w] & 1, wd, kSitePFull) && alive;
-        ++pcnt[w];
-        ptx::tc_fence_after();
-        if (alive) {
-          issue_pv(w, vslot, j > 0);
-          if (j == n - 1) ptx::mma_commit(bar(L::bODone + w));
-        }
+        const uint32_t got = slot;
+        if (++slot == static_cast<uint32_t>(L::kStages)) { slot = 0; phase ^= 1u; }
+        return got;
       };
 
       for (int r = 0;; ++r) {
@@ -305,28 +347,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nkv = max(u.n0, u.n1);
         alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
         ptx::tc_fence_after();
+        trace_event(p, 2, tr, kEvUnit, k_units);
 
         uint32_t kslot = next_full();
         if (alive) {
-          if (u.n0 > 0) { issue_s(0, kslot); ptx::mma_commit(bar(L::bSFull + 0)); }
-          if (u.n1 > 0) { issue_s(1, kslot); ptx::mma_commit(bar(L::bSFull + 1)); }
+          if (u.n0 > 0) {
+            issue_s(tS0, q_lo0, k_lo0 + kslot * kSlotLo);
+            ptx::mma_commit(bar(L::bSFull + 0));
+          }
+          if (u.n1 > 0) {
+            issue_s(tS1, q_lo1, k_lo0 + kslot * kSlotLo);
+            ptx::mma_commit(bar(L::bSFull + 1));
+          }
           ptx::mma_commit(bar(L::bKvEmpty + kslot));
           if (nkv == 1) ptx::mma_commit(bar(L::bQEmpty));
           issued_any = true;
         }
         for (int j = 0; j < nkv; ++j) {
           const uint32_t vslot = next_full();
+          const uint32_t v_lo = v_lo0 + vslot * kSlotLo;
           const bool more = j + 1 < nkv;
-          pv_step(0, j, u.n0, vslot);                       // PV0_j
+          // ---- PV0_j
+          if (j < u.n0) {
+            if (j == 0 && ucnt0 > 0)   // O0 of the previous unit must have been read out
+              alive = ptx::wait_bounded(bar(L::bOFree + 0), (ucnt0 - 1) & 1, wd, kSiteOFree) && alive;
+            alive = ptx::wait_bounded(bar(L::bPFull + 0), pph0, wd, kSitePFull) && alive;
+            pph0 ^= 1u;
+            ptx::tc_fence_after();
+            if (alive) {
+              trace_event(p, 2, tr, kEvPvIssue, j);
+              issue_pv(tO0, tS0, v_lo, j > 0 ? 1u : 0u);
+              if (j == u.n0 - 1) ptx::mma_commit(bar(L::bODone + 0));
+            }
+          }
           if (more) kslot = next_full();
-          if (alive && more && j + 1 < u.n0) {              // S0_{j+1}
-            issue_s(0, kslot);
+          // ---- S0_{j+1}
+          if (alive && more && j + 1 < u.n0) {
+            trace_event(p, 2, tr, kEvSIssue, j + 1);
+            issue_s(tS0, q_lo0, k_lo0 + kslot * kSlotLo);
             ptx::mma_commit(bar(L::bSFull + 0));
           }
-          pv_step(1, j, u.n1, vslot);                       // PV1_j
+          // ---- PV1_j
+          if (j < u.n1) {
+            if (j == 0 && ucnt1 > 0)
+              alive = ptx::wait_bounded(bar(L::bOFree + 1), (ucnt1 - 1) & 1, wd, kSiteOFree) && alive;
+            alive = ptx::wait_bounded(bar(L::bPFull + 1), pph1, wd, kSitePFull) && alive;
+            pph1 ^= 1u;
+            ptx::tc_fence_after();
+            if (alive) {
+              trace_event(p, 2, tr, kEvPvIssue, (1u << 16) | j);
+              issue_pv(tO1, tS1, v_lo, j > 0 ? 1u : 0u);
+              if (j == u.n1 - 1) ptx::mma_commit(bar(L::bODone + 1));
+            }
+          }
           if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
-          if (alive && more && j + 1 < u.n1) {              // S1_{j+1}
-            issue_s(1, kslot);
+          // ---- S1_{j+1}
+          if (alive && more && j + 1 < u.n1) {
+            trace_event(p, 2, tr, kEvSIssue, (1u << 16) | (j + 1));
+            issue_s(tS1, q_lo1, k_lo0 + kslot * kSlotLo);
             ptx::mma_commit(bar(L::bSFull + 1));
           }
           if (alive && more) {
@@ -334,18 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 2 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
           }
         }
-        if (u.n0 > 0) ++ucnt[0];
-        if (u.n1 > 0) ++ucnt[1];
+        if (u.n0 > 0) ++ucnt0;
+        if (u.n1 > 0) ++ucnt1;
         ++k_units;
       }
       // Drain: every MMA issued by this thread has completed before TMEM is freed.
       if (issued_any) {
         ptx::mma_commit(bar(L::bFinal));
-        ptx::wait_drain(bar(L::bFinal), 0, 100000000ull);
+        ptx::wait_drain(bar(L::bFinal), 0, 200000000ull);
       }
     }
     __syncwarp();
+  }
   } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
     // ============================================================ softmax + epilogue
     const int w = warp >> 2;                 // query tile of the unit
     const int t = threadIdx.x & 127;         // row within the tile = TMEM lane
@@ -355,6 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = sbase + L::kO + w * L::kTile;   // used when kTmaStore
     const float c = p.scale_log2;
     uint32_t scnt = 0, ucnt = 0;
+    uint32_t tr = 0;                          // trace events recorded (thread t == 0)
+    const bool tracer = (t == 0);
 
     for (int r = 0;; ++r) {
       const int s = unit_at(r, cta, grid);
@@ -371,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j) {
         ptx::wait_bounded(bar(L::bSFull + w), scnt & 1, wd, kSiteSFull);
         ++scnt;
+        if (tracer) trace_event(p, w, tr, kEvSReady, j);
         __syncwarp();
         ptx::tc_fence_after();
         uint32_t sr[kBN];
@@ -414,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           neg_m = nm;
         }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          if (tracer) trace_event(p, w, tr, kEvRescale, j);
           // PV_w_{j-1} is complete (it was issued before S_w_j), and PV_w_j
           // cannot start before this warpgroup arrives on p_full below.
 #pragma unroll 1
@@ -455,11 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + w));
+        if (tracer) trace_event(p, w, tr, kEvPArrive, j);
       }
 
       // ---- epilogue: O / l in the storage dtype, and LSE = m + ln l per row
       ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
       ++ucnt;
+      if (tracer) trace_event(p, w, tr, kEvEpiStart, ucnt - 1);
       __syncwarp();
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -527,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row < p.N)
         p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
+      if (tracer) trace_event(p, w, tr, kEvEpiEnd, ucnt - 1);
     }
     if constexpr (L::kTmaStore) {
       if (t == 0) ptx::bulk_wait_group0();

@@ -50,24 +50,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Shared state of the bounded waits of one CTA.
 struct Watchdog {
-  unsigned long long budget_ns;  // per wait
-  volatile int* abort_flag;      // shared memory; nonzero once any wait ran out
-  unsigned int* status;          // device status word (bit 0 timeout, bits 8..15 site)
+  unsigned long long budget_cycles;  // per wait, in SM clock cycles
+  volatile int* abort_flag;          // shared memory; nonzero once any wait ran out
+  unsigned int* status;              // device status word (bit 0 timeout, bits 8..15 site)
 };
 
 // Wait until the phase with `parity` of the barrier has completed.  Returns
 // false, without waiting further, once the CTA is aborting; sets the abort
-// flag and the status word when this wait itself exceeds the budget.
+// flag and the status word when this wait itself exceeds the budget.  The
+// budget is counted with the SM cycle counter, read only every 64 polls, so
+// an ordinary wait costs nothing beyond the polls themselves.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd,
                                              uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort_flag) return false;
-    if (globaltimer() - t0 > wd.budget_ns) {
+    if (static_cast<unsigned long long>(clock64() - t0) > wd.budget_cycles) {
       *wd.abort_flag = 1;
       atomicCAS(wd.status, 0u, 1u | ((site & 0xffu) << 8));
       atomicOr(wd.status, 1u);
@@ -77,10 +79,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 }
 
 // Wait used while draining at teardown: ignores the abort flag, own budget.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
-  const uint64_t t0 = globaltimer();
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long budget_cycles) {
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > budget_ns) return false;
+    if (static_cast<unsigned long long>(clock64() - t0) > budget_cycles) return false;
   return true;
 }
 
@@ -90,6 +93,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute it).  The counts must be multiples of 8 in [24, 256].
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ---------------------------------------------------------------- TMA
@@ -236,6 +250,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   d |= 1ull << 46;
   d |= 2ull << 61;
   return d;
+}
+
+// The same descriptor split into its two 32-bit words: the low word holds
+// the start address and the leading-dimension offset, the high word the
+// stride-dimension offset (1024 bytes: eight 128-byte rows), the version and
+// the swizzle mode, which are the same for every operand here.
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
+  return ((addr >> 4) & 0x3FFFu) | ((lbo >> 4) << 16);
+}
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t lo) {
+  return (static_cast<uint64_t>(kDescHiSw128) << 32) | lo;
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator.
