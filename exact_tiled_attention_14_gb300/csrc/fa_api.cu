@@ -121,8 +121,8 @@ void fa_set_watchdog_ns(unsigned long long ns) {
   g_watchdog_ns.store(ns > kMaxNs ? kMaxNs : ns);
 }
 
-#ifdef FA_TRACE
-// Trace builds only (not part of the ABI in fa.h): device buffer that
+#if defined(FA_TRACE) || defined(FA_PROFILE)
+// Trace / profile builds only (not part of the ABI in fa.h): device buffer that
 // kernels launched afterwards record events into, or NULL to stop.  It must
 // hold grid * 4 * kTraceCap * 16 bytes.
 int fa_debug_set_trace(void* buf) {
@@ -130,6 +130,7 @@ int fa_debug_set_trace(void* buf) {
   return FA_OK;
 }
 int fa_debug_trace_cap(void) { return fa::kTraceCap; }
+int fa_debug_prof_slots(void) { return fa::kProfSlots; }
 #endif
 
 int fa_work_tiles(int N, int causal, long long* pairs) {

@@ -16,6 +16,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ long long clk64() {
+  long long t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+  return t;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -63,13 +69,13 @@ struct Watchdog {
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd,
                                              uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
+  const long long t0 = clk64();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort_flag) return false;
-    if (static_cast<unsigned long long>(clock64() - t0) > wd.budget_cycles) {
+    if (static_cast<unsigned long long>(clk64() - t0) > wd.budget_cycles) {
       *wd.abort_flag = 1;
       atomicCAS(wd.status, 0u, 1u | ((site & 0xffu) << 8));
       atomicOr(wd.status, 1u);
@@ -81,9 +87,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 // Wait used while draining at teardown: ignores the abort flag, own budget.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
                                            unsigned long long budget_cycles) {
-  const long long t0 = clock64();
+  const long long t0 = clk64();
   while (!mbar_try_wait(bar, parity))
-    if (static_cast<unsigned long long>(clock64() - t0) > budget_cycles) return false;
+    if (static_cast<unsigned long long>(clk64() - t0) > budget_cycles) return false;
   return true;
 }
 
