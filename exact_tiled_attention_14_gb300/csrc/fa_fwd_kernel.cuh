@@ -97,12 +97,44 @@ enum TraceEvent : uint32_t {
   kEvUnit = 10, kEvPvIssue = 11, kEvSIssue = 12, kEvKvWaited = 13, kEvPWaited = 14,
   kEvLoadK = 20, kEvLoadV = 21, kEvLoadQ = 22
 };
+// Builds compiled with -DFA_PROFILE instead accumulate, per role, the SM
+// cycles spent in each wait and work phase, and write the totals once at the
+// end (kProfSlots 32-bit counters per role per CTA, into p.trace).
+constexpr int kProfSlots = 16;
+struct Prof {
+#ifdef FA_PROFILE
+  uint32_t acc[kProfSlots];
+  long long t_mark;
+  __device__ __forceinline__ Prof() : t_mark(ptx::clk64()) {
+#pragma unroll
+    for (int i = 0; i < kProfSlots; ++i) acc[i] = 0;
+  }
+  // Charge the cycles since the previous mark to counter i.
+  __device__ __forceinline__ void lap(int i) {
+    const long long t = ptx::clk64();
+    acc[i] += static_cast<uint32_t>(t - t_mark);
+    t_mark = t;
+  }
+  __device__ __forceinline__ void count(int i) { acc[i] += 1; }
+  __device__ __forceinline__ void flush(const FwdParams& p, int role) {
+    if (p.trace == nullptr) return;
+    unsigned long long* dst = p.trace + (static_cast<size_t>(blockIdx.x) * 4 + role) * kProfSlots;
+#pragma unroll
+    for (int i = 0; i < kProfSlots; ++i) dst[i] = acc[i];
+  }
+#else
+  __device__ __forceinline__ void lap(int) {}
+  __device__ __forceinline__ void count(int) {}
+  __device__ __forceinline__ void flush(const FwdParams&, int) {}
+#endif
+};
+
 __device__ __forceinline__ void trace_event(const FwdParams& p, int role, uint32_t& cnt,
                                             uint32_t ev, uint32_t arg) {
 #ifdef FA_TRACE
   if (p.trace != nullptr && cnt < static_cast<uint32_t>(kTraceCap)) {
     const size_t i = (static_cast<size_t>(blockIdx.x) * 4 + role) * kTraceCap + cnt;
-    p.trace[2 * i] = clock64();
+    p.trace[2 * i] = ptx::clk64();
     p.trace[2 * i + 1] = (static_cast<unsigned long long>(ev) << 32) | arg;
   }
   ++cnt;
@@ -324,6 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       uint32_t tr = 0;                 // trace events recorded
+      Prof pf;                         // FA_PROFILE: 0 kv wait, 1 p wait, 2 q wait, 3 o_free wait,
+                                       // 4 S issue, 5 PV issue, 6 other, 7 groups issued
       uint32_t slot = 0, phase = 0;    // K/V ring position
       uint32_t loads = 0;              // K/V tiles consumed (trace argument)
       uint32_t k_units = 0;            // units walked
@@ -332,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool alive = true;
       bool issued_any = false;
       auto next_full = [&]() -> uint32_t {
+        pf.lap(6);
         alive = ptx::wait_bounded(bar(L::bKvFull + slot), phase, wd, kSiteKvFull) && alive;
+        pf.lap(0);
         trace_event(p, 2, tr, kEvKvWaited, loads);
         ++loads;
         const uint32_t got = slot;
@@ -345,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s >= p.num_units) break;
         const Unit u = decode_unit<kCausal>(s, p);
         const int nkv = max(u.n0, u.n1);
+        pf.lap(6);
         alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
+        pf.lap(2);
         ptx::tc_fence_after();
         trace_event(p, 2, tr, kEvUnit, k_units);
 
@@ -369,14 +407,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = j + 1 < nkv;
           // ---- PV0_j
           if (j < u.n0) {
+            pf.lap(6);
             if (j == 0 && ucnt0 > 0)   // O0 of the previous unit must have been read out
               alive = ptx::wait_bounded(bar(L::bOFree + 0), (ucnt0 - 1) & 1, wd, kSiteOFree) && alive;
+            pf.lap(3);
             alive = ptx::wait_bounded(bar(L::bPFull + 0), pph0, wd, kSitePFull) && alive;
+            pf.lap(1);
             pph0 ^= 1u;
             ptx::tc_fence_after();
             if (alive) {
               trace_event(p, 2, tr, kEvPvIssue, j);
               issue_pv(tO0, tS0, v_lo, j > 0 ? 1u : 0u);
+              pf.lap(5);
+              pf.count(7);
               if (j == u.n0 - 1) ptx::mma_commit(bar(L::bODone + 0));
             }
           }
@@ -384,19 +427,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           // ---- S0_{j+1}
           if (alive && more && j + 1 < u.n0) {
             trace_event(p, 2, tr, kEvSIssue, j + 1);
+            pf.lap(6);
             issue_s(tS0, q_lo0, k_lo0 + kslot * kSlotLo);
+            pf.lap(4);
+            pf.count(7);
             ptx::mma_commit(bar(L::bSFull + 0));
           }
           // ---- PV1_j
           if (j < u.n1) {
+            pf.lap(6);
             if (j == 0 && ucnt1 > 0)
               alive = ptx::wait_bounded(bar(L::bOFree + 1), (ucnt1 - 1) & 1, wd, kSiteOFree) && alive;
+            pf.lap(3);
             alive = ptx::wait_bounded(bar(L::bPFull + 1), pph1, wd, kSitePFull) && alive;
+            pf.lap(1);
             pph1 ^= 1u;
             ptx::tc_fence_after();
             if (alive) {
               trace_event(p, 2, tr, kEvPvIssue, (1u << 16) | j);
               issue_pv(tO1, tS1, v_lo, j > 0 ? 1u : 0u);
+              pf.lap(5);
+              pf.count(7);
               if (j == u.n1 - 1) ptx::mma_commit(bar(L::bODone + 1));
             }
           }
@@ -404,7 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // ---- S1_{j+1}
           if (alive && more && j + 1 < u.n1) {
             trace_event(p, 2, tr, kEvSIssue, (1u << 16) | (j + 1));
+            pf.lap(6);
             issue_s(tS1, q_lo1, k_lo0 + kslot * kSlotLo);
+            pf.lap(4);
+            pf.count(7);
             ptx::mma_commit(bar(L::bSFull + 1));
           }
           if (alive && more) {
@@ -416,6 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n1 > 0) ++ucnt1;
         ++k_units;
       }
+      pf.lap(6);
+      pf.flush(p, 2);
       // Drain: every MMA issued by this thread has completed before TMEM is freed.
       if (issued_any) {
         ptx::mma_commit(bar(L::bFinal));
@@ -437,6 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t scnt = 0, ucnt = 0;
     uint32_t tr = 0;                          // trace events recorded (thread t == 0)
     const bool tracer = (t == 0);
+    Prof pf;   // FA_PROFILE: 0 s wait, 1 load S, 2 max + rescale, 3 exp/sum/pack, 4 store P + arrive,
+               // 5 o_done wait, 6 epilogue, 7 other, 8 tiles, 9 rescales
 
     for (int r = 0;; ++r) {
       const int s = unit_at(r, cta, grid);
@@ -451,7 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float neg_m = 0.f;        // -m_ref * c (0 while m_ref is -inf)
       float l = 0.f;            // running sum of 2^(s*c + neg_m)
       for (int j = 0; j < n; ++j) {
+        pf.lap(7);
         ptx::wait_bounded(bar(L::bSFull + w), scnt & 1, wd, kSiteSFull);
+        pf.lap(0);
+        pf.count(8);
         ++scnt;
         if (tracer) trace_event(p, w, tr, kEvSReady, j);
         __syncwarp();
@@ -463,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[kBN];
 #pragma unroll
         for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(sr[i]);
+        pf.lap(1);
 
         // mask: keys past N, and on the diagonal tile keys after this row
         const int rem = p.N - j * kBN;
@@ -498,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           if (tracer) trace_event(p, w, tr, kEvRescale, j);
+          pf.count(9);
           // PV_w_{j-1} is complete (it was issued before S_w_j), and PV_w_j
           // cannot start before this warpgroup arrives on p_full below.
 #pragma unroll 1
@@ -511,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
+        pf.lap(2);
         // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM.
         // The exponent argument and the row sum use two-lane fp32 instructions.
         const uint64_t c2 = ptx::f2_pack(c, c);
@@ -534,16 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::f2_unpack(acc1, cc, dd);
           l += (a + b) + (cc + dd);
         }
+        pf.lap(3);
         ptx::tmem_st32(tS, pk);
         ptx::tmem_st32(tS + 32, pk + 32);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + w));
+        pf.lap(4);
         if (tracer) trace_event(p, w, tr, kEvPArrive, j);
       }
 
       // ---- epilogue: O / l in the storage dtype, and LSE = m + ln l per row
+      pf.lap(7);
       ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
+      pf.lap(5);
       ++ucnt;
       if (tracer) trace_event(p, w, tr, kEvEpiStart, ucnt - 1);
       __syncwarp();
@@ -614,7 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row < p.N)
         p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
       if (tracer) trace_event(p, w, tr, kEvEpiEnd, ucnt - 1);
+      pf.lap(6);
     }
+    pf.lap(7);
+    if (tracer) pf.flush(p, w);
     if constexpr (L::kTmaStore) {
       if (t == 0) ptx::bulk_wait_group0();
     }
