@@ -182,6 +182,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.n_qblk = static_cast<int>(n_qblk);
   p.n_kv = (N + fa::kBN - 1) / fa::kBN;
   p.num_units = static_cast<int>(bh * n_qblk);
+  // Head-by-head unit order when the K and V of all heads would take more
+  // than half of L2 (so concurrent units re-read K/V from L2, not HBM).
+  const long long kv_bytes = bh * 2ll * N * d * 2ll;
+  p.head_major = kv_bytes > (64ll << 20) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int grid = p.num_units < info->sms ? p.num_units : info->sms;
 

@@ -81,6 +81,7 @@ struct FwdParams {
   int n_qblk;              // ceil(N / 256): units per head
   int n_kv;                // ceil(N / 128): key tiles per head
   int num_units;           // BH * n_qblk
+  int head_major;          // unit order: 1 = head by head, 0 = level by level (see unit_at)
   float scale_log2;        // scale * log2(e)
   unsigned long long* trace;  // event trace buffer (only read in FA_TRACE builds)
 };
@@ -178,10 +179,15 @@ struct Unit {
   int bh, mblk, n0, n1;
 };
 
-// Static persistent schedule: units are ordered heaviest first (for causal,
-// the last query blocks of every head first) and dealt to CTAs in a snake
-// (boustrophedon) order, round by round.  Deterministic, so every role of a
-// CTA walks the same list without communicating.
+// Static persistent schedule, deterministic so every role of a CTA walks the
+// same list without communicating.  Units are dealt to CTAs in a snake
+// (boustrophedon) order, round by round, from one of two orderings:
+//  - level by level (head_major = 0): the heaviest query block of every
+//    head first (for causal, the last blocks), which balances best;
+//  - head by head (head_major = 1): all query blocks of a head, heaviest
+//    first, then the next head.  Units in flight then share a few heads'
+//    K/V, which stay in L2; the host picks this when the K/V of all heads
+//    would not fit in L2 (at the price of a few percent of balance).
 __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
@@ -189,9 +195,14 @@ __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
 template <bool kCausal>
 __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   Unit u;
-  const int level = s / p.BH;
-  u.bh = s - level * p.BH;
-  u.mblk = p.n_qblk - 1 - level;
+  if (p.head_major) {
+    u.bh = s / p.n_qblk;
+    u.mblk = p.n_qblk - 1 - (s - u.bh * p.n_qblk);
+  } else {
+    const int level = s / p.BH;
+    u.bh = s - level * p.BH;
+    u.mblk = p.n_qblk - 1 - level;
+  }
   const int t0 = 2 * u.mblk;
   if (kCausal) {
     u.n0 = min(t0 + 1, p.n_kv);
