@@ -351,11 +351,19 @@ def run_ours(args, w):
         lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
         bufs.append((dq, dk, dv, o, lse))
     stream = torch.cuda.current_stream(device)
+    # Balancing workspace of fa_fwd_ws (allocated once, outside the timed
+    # region); None when this shape leaves no partial last round.
+    ws = fa.make_workspace(B, H, N, d, w["causal"], device=device) if args.split else None
+    ws_bytes = 0 if ws is None else ws.numel()
 
     def step(i):
         dq, dk, dv, o, lse = bufs[i % replicas]
-        rc = fa.fa_fwd(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"],
-                       fa.dtype_code(dq.dtype), stream)
+        if ws is None:
+            rc = fa.fa_fwd(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"],
+                           fa.dtype_code(dq.dtype), stream)
+        else:
+            rc = fa.fa_fwd_ws(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"],
+                              fa.dtype_code(dq.dtype), ws, ws_bytes, stream)
         if rc:
             raise fa.FaError(rc)
 
@@ -399,7 +407,7 @@ def run_ours(args, w):
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         fa.attention_forward(dq, dk, dv, causal=w["causal"], scale=w["scale"], out=o, lse=lse,
-                             stream=stream)
+                             stream=stream, workspace=ws)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -433,6 +441,9 @@ def run_ours(args, w):
         "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "entry": "fa_fwd_ws" if ws is not None else "fa_fwd",
+                   "tail": (f"last-round units split along keys (workspace {ws_bytes / 2**20:.1f} MiB)"
+                            if ws is not None else "whole units only"),
                    "l2": (f"{replicas} rotating input replicas "
                           f"({replicas * per_replica / 2**20:.0f} MiB"
                           f"{' > L2' if replicas * per_replica > L2_BYTES else ', < L2: launch-bound size'})")
@@ -477,6 +488,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split", action="store_true",
+                    help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -1,15 +1,17 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``,
-``fa_work_tiles``, ``fa_version``), under the same names.  Every step of
+(``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_strerror``,
+``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``, ``fa_version``),
+under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
 every call raises.
 
 ``attention_forward`` is the convenience call a user makes: it allocates O
-and LSE with PyTorch (device memory is PyTorch's job here) and calls
-``fa_fwd`` on the current CUDA stream.
+and LSE (and, when asked, the balancing workspace) with PyTorch — device
+memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
+current CUDA stream.
 """
 import ctypes
 import math
@@ -32,10 +34,11 @@ FA_ERR_TENSORMAP = 8
 FA_ERR_LAUNCH = 9
 FA_ERR_TIMEOUT = 10
 FA_ERR_CUDA = 11
+FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_strerror", "fa_status", "fa_set_watchdog_ns", "fa_work_tiles",
-           "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_strerror", "fa_status",
+           "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
 
 _lib = None
 
@@ -62,6 +65,10 @@ def load_library(path=None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_ws.restype = i
+    lib.fa_fwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_fwd_workspace_size.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -102,6 +109,34 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None):
                       _stream(stream))
 
 
+def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, workspace_bytes,
+              stream=None):
+    """Raw C call with a balancing workspace; returns the C return code."""
+    lib = load_library()
+    return lib.fa_fwd_ws(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                         int(N), int(d), int(bool(causal)), float(scale), int(dtype),
+                         _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_workspace_size(B, H, N, d, causal):
+    """Workspace bytes fa_fwd_ws needs for this shape on the current device."""
+    out = ctypes.c_size_t(0)
+    code = load_library().fa_fwd_workspace_size(int(B), int(H), int(N), int(d),
+                                                int(bool(causal)), ctypes.byref(out))
+    if code:
+        raise FaError(code, "fa_fwd_workspace_size")
+    return out.value
+
+
+def make_workspace(B, H, N, d, causal, device=None):
+    """A device workspace (uint8 tensor) sized for fa_fwd_ws, or None if none is needed."""
+    import torch
+    n = fa_fwd_workspace_size(B, H, N, d, causal)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
 def fa_strerror(code):
     return load_library().fa_strerror(int(code)).decode()
 
@@ -138,11 +173,15 @@ def dtype_code(torch_dtype):
     raise TypeError(f"unsupported dtype {torch_dtype}; use bfloat16 or float16")
 
 
-def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None,
+                      workspace=None):
     """O, LSE = exact attention of CUDA tensors q, k, v [B, H, N, d].
 
     O has the input dtype; LSE is float32 [B, H, N] (natural log).  ``scale``
     defaults to 1/sqrt(d).  Runs on ``stream`` (default: current stream).
+    ``workspace``: None runs ``fa_fwd``; a uint8 CUDA tensor (see
+    ``make_workspace``) or ``"auto"`` (allocate one) runs ``fa_fwd_ws``, which
+    balances the last round of work across the SMs.
     """
     import torch
     if not (q.dtype == k.dtype == v.dtype):
@@ -163,7 +202,16 @@ def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, str
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_fwd(q, k, v, out, lse, B, H, N, d, causal, scale, code, stream)
+    if workspace is None:
+        rc = fa_fwd(q, k, v, out, lse, B, H, N, d, causal, scale, code, stream)
+    else:
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be None, 'auto' or a CUDA tensor")
+            workspace = make_workspace(B, H, N, d, causal, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        rc = fa_fwd_ws(q, k, v, out, lse, B, H, N, d, causal, scale, code, workspace, ws_bytes,
+                       stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse

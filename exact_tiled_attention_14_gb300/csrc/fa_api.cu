@@ -96,7 +96,7 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int BH, int N, int d, bool bf16)
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 const char* fa_strerror(int code) {
   switch (code) {
@@ -112,6 +112,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_LAUNCH: return "kernel launch failed";
     case FA_ERR_TIMEOUT: return "a bounded wait in a kernel ran out (watchdog)";
     case FA_ERR_CUDA: return "CUDA runtime error";
+    case FA_ERR_WORKSPACE: return "workspace smaller than fa_fwd_workspace_size reports";
     default: return "unknown error code";
   }
 }
@@ -141,8 +142,48 @@ int fa_work_tiles(int N, int causal, long long* pairs) {
   return FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Size of one split schedule: units, persistent grid, tail.
+struct SplitPlan {
+  long long units = 0;
+  int grid = 0;
+  int full_rounds = 0;
+  int tail_units = 0;
+  bool split = false;
+  size_t counter_bytes = 0;   // 2 * tail_units ints, rounded up to 256 bytes
+  size_t slot_bytes = 0;      // one workspace slot
+  size_t bytes = 0;           // whole workspace (0 when the tail is not split)
+};
+
+// The tail is split when the call is unmasked, the units do not fill whole
+// rounds of the persistent grid, and there is more than one key tile to
+// split.  `sms` is the device's SM count.
+SplitPlan plan_split(long long bh, int N, int d, int causal, int sms) {
+  SplitPlan sp;
+  const long long n_qblk = (static_cast<long long>(N) + 2 * fa::kBM - 1) / (2 * fa::kBM);
+  const int n_kv = (N + fa::kBN - 1) / fa::kBN;
+  sp.units = bh * n_qblk;
+  sp.grid = static_cast<int>(sp.units < sms ? sp.units : sms);
+  if (sp.grid <= 0) return sp;
+  sp.full_rounds = static_cast<int>(sp.units / sp.grid);
+  sp.tail_units = static_cast<int>(sp.units - static_cast<long long>(sp.full_rounds) * sp.grid);
+  sp.split = !causal && sp.tail_units > 0 && n_kv >= 2;
+  if (sp.split) {
+    sp.counter_bytes = ((2 * static_cast<size_t>(sp.tail_units) * sizeof(int)) + 255) / 256 * 256;
+    const int slot_floats = (d == 64) ? fa::kSlotFloats<64>() : fa::kSlotFloats<128>();
+    sp.slot_bytes = static_cast<size_t>(slot_floats) * sizeof(float);
+    sp.bytes = sp.counter_bytes + 2 * static_cast<size_t>(sp.grid) * sp.slot_bytes;
+  }
+  return sp;
+}
+
+// Shared by fa_fwd (no workspace) and fa_fwd_ws.
+int launch_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, int causal, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_qblk = (static_cast<long long>(N) + 2 * fa::kBM - 1) / (2 * fa::kBM);
@@ -160,6 +201,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const DeviceInfo* info = device_info(&dev);
   if (!info || !info->supported) return FA_ERR_DEVICE;
   if (info->err != FA_OK) return info->err;
+
+  SplitPlan sp = plan_split(bh, N, d, causal, info->sms);
+  if (workspace != nullptr && sp.split) {
+    if (workspace_bytes < sp.bytes) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  } else {
+    sp.split = false;   // no workspace (fa_fwd), or nothing to split
+  }
 
   const bool bf16 = dtype == FA_BF16;
   fa::FwdParams p;
@@ -187,11 +236,48 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const long long kv_bytes = bh * 2ll * N * d * 2ll;
   p.head_major = kv_bytes > (64ll << 20) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
+  p.split = sp.split ? 1 : 0;
+  p.full_rounds = sp.full_rounds;
+  p.tail_units = sp.split ? sp.tail_units : 0;
+  p.ws_count = sp.split ? static_cast<int*>(workspace) : nullptr;
+  p.ws_part = sp.split ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.counter_bytes)
+                       : nullptr;
+  if (sp.split && cudaMemsetAsync(workspace, 0, sp.counter_bytes, stream) != cudaSuccess)
+    return FA_ERR_LAUNCH;
 
-  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(p, grid, bf16, causal != 0, stream)
-                                  : fa::launch_fwd_d128(p, grid, bf16, causal != 0, stream);
+  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(p, sp.grid, bf16, causal != 0, stream)
+                                  : fa::launch_fwd_d128(p, sp.grid, bf16, causal != 0, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+  return launch_forward(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, 0, stream);
+}
+
+int fa_fwd_workspace_size(int B, int H, int N, int d, int causal, size_t* bytes) {
+  if (!bytes) return FA_ERR_NULLPTR;
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  *bytes = 0;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0 || N == 0) return FA_OK;
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  *bytes = plan_split(bh, N, d, causal, info->sms).bytes;
+  return FA_OK;
+}
+
+int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+              int d, int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+              cudaStream_t stream) {
+  return launch_forward(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream);
 }
 
 int fa_status(cudaStream_t stream, unsigned int* detail) {

@@ -82,6 +82,15 @@ struct FwdParams {
   int n_kv;                // ceil(N / 128): key tiles per head
   int num_units;           // BH * n_qblk
   int head_major;          // unit order: 1 = head by head, 0 = level by level (see unit_at)
+  // Split tail (unmasked only, see next_piece): after full_rounds rounds of
+  // whole units, the last tail_units units are cut along the key axis so
+  // every CTA gets the same number of key tiles.  Partial results go to
+  // ws_part; ws_count counts, per (tail unit, query tile), pieces finished.
+  int split;               // 0: whole units only
+  int full_rounds;
+  int tail_units;
+  float* ws_part;          // 2 * grid slots of kSlotFloats(D) floats
+  int* ws_count;           // 2 * tail_units counters, zero at launch
   float scale_log2;        // scale * log2(e)
   unsigned long long* trace;  // event trace buffer (only read in FA_TRACE builds)
 };
@@ -163,7 +172,7 @@ struct Smem {
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
                        bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
                        bOFree = bODone + 2, bFinal = bOFree + 2, kNumBars = bFinal + 1;
-  static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base address, abort flag
+  static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base, abort flag, 2 merge flags
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024
   static_assert(kAlloc <= 232448, "shared memory budget");
@@ -178,6 +187,19 @@ __device__ __forceinline__ uint32_t o_col(int w) { return 256u + (w ? D : 0); }
 struct Unit {
   int bh, mblk, n0, n1;
 };
+
+// A piece of work: key tiles [kb, kb + n_w) of query tile w of one unit.
+// tail >= 0 marks a partial piece of tail unit `tail` whose results go to
+// workspace slot `slot` and are merged by whichever piece finishes last.
+struct Piece {
+  int bh, mblk, kb, n0, n1, tail, slot;
+};
+
+// Floats of one workspace slot: unnormalised O of both query tiles stored
+// column by column (element (col, row) of tile w at (w*D + col)*128 + row,
+// so a warp's rows are contiguous), then (-m*c, l) per row.
+template <int D>
+__host__ __device__ constexpr int kSlotFloats() { return 2 * kBM * (D + 2); }
 
 // Static persistent schedule, deterministic so every role of a CTA walks the
 // same list without communicating.  Units are dealt to CTAs in a snake
@@ -215,7 +237,89 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   return u;
 }
 
-template <int D, bool kBf16, bool kCausal>
+// Per-CTA walk over its pieces.  Whole units first (round by round as
+// above); with a split tail, CTA c then takes tail key tiles
+// [c*W/grid, (c+1)*W/grid) of the W = tail_units * n_kv tail key tiles, in
+// unit order, so every CTA does the same number of key tiles and at most two
+// pieces of the tail.
+struct Cursor {
+  int r;                 // next round of whole units
+  long long pos, end;    // tail key tiles left to this CTA
+  int first_t;           // tail unit of this CTA's first tail piece
+};
+__device__ __forceinline__ long long tail_start(const FwdParams& p, int c, int grid) {
+  return static_cast<long long>(p.tail_units) * p.n_kv * c / grid;
+}
+template <bool kSplit>
+__device__ __forceinline__ void cursor_init(const FwdParams& p, int cta, int grid, Cursor& cu) {
+  cu.r = 0;
+  cu.pos = kSplit ? tail_start(p, cta, grid) : 0;
+  cu.end = kSplit ? tail_start(p, cta + 1, grid) : 0;
+  cu.first_t = kSplit ? static_cast<int>(cu.pos / p.n_kv) : 0;
+}
+template <bool kCausal, bool kSplit>
+__device__ __forceinline__ bool next_piece(const FwdParams& p, int cta, int grid, Cursor& cu,
+                                           Piece& pc) {
+  if (!kSplit || cu.r < p.full_rounds) {
+    const int s = unit_at(cu.r, cta, grid);
+    if (!kSplit && s >= p.num_units) return false;
+    ++cu.r;
+    const Unit u = decode_unit<kCausal>(s, p);
+    pc.bh = u.bh; pc.mblk = u.mblk; pc.kb = 0; pc.n0 = u.n0; pc.n1 = u.n1;
+    pc.tail = -1; pc.slot = 0;
+    return true;
+  }
+  if (cu.pos >= cu.end) return false;
+  const int t = static_cast<int>(cu.pos / p.n_kv);
+  const long long ubeg = static_cast<long long>(t) * p.n_kv;
+  const int kb = static_cast<int>(cu.pos - ubeg);
+  const int ke = static_cast<int>((cu.end < ubeg + p.n_kv ? cu.end : ubeg + p.n_kv) - ubeg);
+  cu.pos = ubeg + ke;
+  const Unit u = decode_unit<kCausal>(p.full_rounds * grid + t, p);
+  pc.bh = u.bh; pc.mblk = u.mblk; pc.kb = kb;
+  pc.n0 = ke - kb;
+  pc.n1 = u.n1 > 0 ? ke - kb : 0;
+  pc.tail = (kb == 0 && ke == p.n_kv) ? -1 : t;
+  pc.slot = 2 * cta + (t == cu.first_t ? 0 : 1);
+  return true;
+}
+
+// Walks the CTAs holding pieces of one tail unit, in CTA order, without a
+// division per step: CTA c's tail range starts at c*q + floor(c*r/grid)
+// with q = W / grid, r = W mod grid (W = tail_units * n_kv), so consecutive
+// starts differ by q or q + 1.  Each CTA holds at most one piece of a unit.
+struct TailWalk {
+  int c;            // current CTA
+  long long st;     // its tail range start
+  int frac;         // c * r mod grid
+  long long q;
+  int r, grid;
+  __device__ __forceinline__ void init(const FwdParams& p, int grid_, int t) {
+    grid = grid_;
+    const long long W = static_cast<long long>(p.tail_units) * p.n_kv;
+    q = W / grid;
+    r = static_cast<int>(W - q * grid);
+    const long long ua = static_cast<long long>(t) * p.n_kv;
+    // first CTA whose range starts at or before ua (its range then covers ua)
+    long long c0 = ((ua + 1) * grid + W - 1) / W - 1;
+    c = static_cast<int>(c0 < 0 ? 0 : (c0 > grid - 1 ? grid - 1 : c0));
+    st = static_cast<long long>(c) * q + (static_cast<long long>(c) * r) / grid;
+    frac = static_cast<int>((static_cast<long long>(c) * r) % grid);
+  }
+  __device__ __forceinline__ long long next_start() const {
+    return st + q + ((frac + r >= grid) ? 1 : 0);
+  }
+  __device__ __forceinline__ void step() {
+    st += q;
+    frac += r;
+    if (frac >= grid) { ++st; frac -= grid; }
+    ++c;
+  }
+};
+
+// kSplit: compile the split-tail path (unmasked calls with a workspace only);
+// the other variants carry none of its code.
+template <int D, bool kBf16, bool kCausal, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
@@ -229,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sgen + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 8);  // [2]
 
   // ---------------------------------------------------------------- setup
   if (warp == kMmaWarp) {
@@ -273,15 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tr = 0;          // trace events recorded
       uint32_t loads = 0;       // K/V tiles issued (ring position)
       uint32_t q_issued = 0;    // units whose Q load was issued
-      uint32_t k_units = 0;     // units walked
+      uint32_t k_units = 0;     // pieces walked
       bool alive = true;
-      for (int r = 0;; ++r) {
-        const int s = unit_at(r, cta, grid);
-        if (s >= p.num_units) break;
-        const Unit u = decode_unit<kCausal>(s, p);
+      Cursor cu;
+      cursor_init<kSplit>(p, cta, grid, cu);
+      Piece u;
+      while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
         const int nkv = max(u.n0, u.n1);
-        // Q of this unit may only overwrite the buffer once the previous
-        // unit's last S MMA has read it; the first K tile does not wait for
+        // Q of this piece may only overwrite the buffer once the previous
+        // piece's last S MMA has read it; the first K tile does not wait for
         // that, so it is requested first.
         auto load_q = [&]() {
           if (k_units > 0)
@@ -310,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
               for (int c = 0; c < L::kChunks; ++c)
                 ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
-                                 bar(L::bKvFull + slot), c * 64, j * kBN, u.bh);
+                                 bar(L::bKvFull + slot), c * 64, (u.kb + j) * kBN, u.bh);
               trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
               ++loads;
             }
@@ -387,10 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return got;
       };
 
-      for (int r = 0;; ++r) {
-        const int s = unit_at(r, cta, grid);
-        if (s >= p.num_units) break;
-        const Unit u = decode_unit<kCausal>(s, p);
+      Cursor cu;
+      cursor_init<kSplit>(p, cta, grid, cu);
+      Piece u;
+      while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
         const int nkv = max(u.n0, u.n1);
         pf.lap(6);
         alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
@@ -507,10 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Prof pf;   // FA_PROFILE: 0 s wait, 1 load S, 2 max + rescale, 3 exp/sum/pack, 4 store P + arrive,
                // 5 o_done wait, 6 epilogue, 7 other, 8 tiles, 9 rescales
 
-    for (int r = 0;; ++r) {
-      const int s = unit_at(r, cta, grid);
-      if (s >= p.num_units) break;
-      const Unit u = decode_unit<kCausal>(s, p);
+    Cursor cu;
+    cursor_init<kSplit>(p, cta, grid, cu);
+    Piece u;
+    while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
       const int n = w ? u.n1 : u.n0;
       if (n == 0) continue;
       const int tile = 2 * u.mblk + w;
@@ -538,8 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pf.lap(1);
 
         // mask: keys past N, and on the diagonal tile keys after this row
-        const int rem = p.N - j * kBN;
-        const bool diag = kCausal && j == tile;
+        const int kj = u.kb + j;                 // key tile index
+        const int rem = p.N - kj * kBN;
+        const bool diag = kCausal && kj == tile;
         if (diag || rem < kBN) {
           int lim = rem < kBN ? rem : kBN;
           if (diag) lim = min(lim, t + 1);
@@ -628,7 +734,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
-      if constexpr (L::kTmaStore) {
+      if (kSplit && u.tail >= 0) {
+        // Partial piece of a split unit: unnormalised O rows and (-m*c, l)
+        // go to this piece's workspace slot; the piece that finishes last
+        // (counted per tail unit and query tile) merges all of them with
+        // the combining identity: with m* the largest m, each piece is
+        // scaled by 2^((m_p - m*) c), l = sum of scaled l_p, O = sum of
+        // scaled O_p / l, LSE = m* + ln l.
+        pf.lap(6);
+        float* slot = p.ws_part + static_cast<size_t>(u.slot) * kSlotFloats<D>();
+        float* so = slot + static_cast<size_t>(w) * D * kBM + t;
+#pragma unroll 1
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t orr[32];
+          ptx::tmem_ld32(tO + q4 * 32, orr);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) so[(q4 * 32 + e) * kBM] = __uint_as_float(orr[e]);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
+        reinterpret_cast<float2*>(slot + 2 * kBM * D)[w * kBM + t] = make_float2(neg_m, l);
+        pf.lap(10);
+        __threadfence();
+        pf.lap(11);
+        ptx::named_bar_sync(1 + w, 128);
+        const long long ua = static_cast<long long>(u.tail) * p.n_kv, ub = ua + p.n_kv;
+        int npieces = 0;
+        {
+          TailWalk tw;
+          tw.init(p, grid, u.tail);
+          for (; tw.c < grid && tw.st < ub; tw.step()) {
+            const long long en = tw.next_start();
+            if (tw.st < en && en > ua) ++npieces;
+          }
+        }
+        if (t == 0) {
+          const int done = atomicAdd(p.ws_count + 2 * u.tail + w, 1);
+          merge_flag[w] = (done == npieces - 1) ? 1 : 0;
+        }
+        ptx::named_bar_sync(1 + w, 128);
+        pf.lap(12);
+        if (merge_flag[w]) {
+          __threadfence();
+          pf.count(14);
+          // One pass over the pieces with the online rescale: a running
+          // reference nm_run = -m*c, running l and an O row accumulator.
+          float nm_run = INFINITY, l_run = 0.f;
+          float acc[D];
+#pragma unroll
+          for (int e = 0; e < D; ++e) acc[e] = 0.f;
+          TailWalk tw;
+          tw.init(p, grid, u.tail);
+          for (; tw.c < grid && tw.st < ub; tw.step()) {
+            const long long en = tw.next_start();
+            if (!(tw.st < en && en > ua)) continue;          // no piece of this unit
+            const int first_t = static_cast<int>(tw.st / p.n_kv);
+            const float* sp = p.ws_part +
+                              static_cast<size_t>(2 * tw.c + (u.tail == first_t ? 0 : 1)) * kSlotFloats<D>();
+            const float2 ml = reinterpret_cast<const float2*>(sp + 2 * kBM * D)[w * kBM + t];
+            if (!(ml.y > 0.f)) continue;
+            float f = 1.f;
+            if (ml.x < nm_run) {                              // larger maximum: move the reference
+              const float a = (nm_run == INFINITY) ? 0.f : ptx::ex2(ml.x - nm_run);
+#pragma unroll
+              for (int e = 0; e < D; ++e) acc[e] *= a;
+              l_run *= a;
+              nm_run = ml.x;
+            } else {
+              f = ptx::ex2(nm_run - ml.x);
+            }
+            l_run += f * ml.y;
+            const float* src = sp + static_cast<size_t>(w) * D * kBM + t;
+#pragma unroll
+            for (int e = 0; e < D; ++e) acc[e] += f * src[e * kBM];
+          }
+          const float inv_lt = 1.0f / l_run;
+          if (row < p.N) {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
+                                                   (static_cast<size_t>(u.bh) * p.N + row) * (D * 2));
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v)
+              orow[v] = make_uint4(ptx::pack2<kBf16>(acc[8 * v] * inv_lt, acc[8 * v + 1] * inv_lt),
+                                   ptx::pack2<kBf16>(acc[8 * v + 2] * inv_lt, acc[8 * v + 3] * inv_lt),
+                                   ptx::pack2<kBf16>(acc[8 * v + 4] * inv_lt, acc[8 * v + 5] * inv_lt),
+                                   ptx::pack2<kBf16>(acc[8 * v + 6] * inv_lt, acc[8 * v + 7] * inv_lt));
+            p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l_run) - nm_run) * kLn2;
+          }
+          if (t == 0) p.ws_count[2 * u.tail + w] = 0;   // ready for the next call
+          pf.lap(13);
+        }
+        pf.count(15);
+      } else if constexpr (L::kTmaStore) {
         // through a swizzled staging tile and a TMA store (rows past N clipped)
         if (t == 0) ptx::bulk_wait_group_read0();   // staging tile free again
         ptx::named_bar_sync(1 + w, 128);
@@ -690,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
       }
-      if (row < p.N)
+      if ((!kSplit || u.tail < 0) && row < p.N)
         p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
       if (tracer) trace_event(p, w, tr, kEvEpiEnd, ucnt - 1);
       pf.lap(6);

@@ -10,8 +10,8 @@
 
 namespace fa {
 
-// Launch fa_fwd_kernel<D, kBf16, kCausal> with `grid` persistent CTAs.
-template <int D, bool kBf16, bool kCausal>
+// Launch fa_fwd_kernel<D, kBf16, kCausal, kSplit> with `grid` persistent CTAs.
+template <int D, bool kBf16, bool kCausal, bool kSplit>
 cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};  // devices on which the smem limit was raised
   int dev = 0;
@@ -19,12 +19,12 @@ cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel<D, kBf16, kCausal>,
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, kBf16, kCausal, kSplit>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kAlloc);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  fa_fwd_kernel<D, kBf16, kCausal><<<grid, kThreads, Smem<D>::kAlloc, stream>>>(p);
+  fa_fwd_kernel<D, kBf16, kCausal, kSplit><<<grid, kThreads, Smem<D>::kAlloc, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -15,8 +15,9 @@
  *  - Tensors are dense, contiguous, row-major, on the CURRENT CUDA device:
  *      q, k, v, o : [B, H, N, d] in the storage dtype (bf16 or fp16);
  *      lse        : [B, H, N] float32, natural log of the scaled scores.
- *  - The caller owns every buffer.  The library allocates no device memory:
- *    no workspace and no N x N buffer.
+ *  - The caller owns every buffer.  The library allocates no device memory
+ *    and never builds an N x N buffer; fa_fwd_ws takes a caller-provided
+ *    workspace of O(SMs * 128 * d) floats for balancing, not an N x N one.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  A
  *    non-zero return means nothing was launched.
  *  - Causal masking is upper-left aligned: query i sees keys j <= i (section
@@ -26,6 +27,7 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -49,7 +51,8 @@ enum {
   FA_ERR_TENSORMAP = 8,      /* the driver refused a TMA descriptor            */
   FA_ERR_LAUNCH = 9,         /* the launch itself failed (CUDA error)          */
   FA_ERR_TIMEOUT = 10,       /* a kernel's bounded wait ran out (fa_status)    */
-  FA_ERR_CUDA = 11           /* a CUDA runtime call failed (fa_status)         */
+  FA_ERR_CUDA = 11,          /* a CUDA runtime call failed (fa_status)         */
+  FA_ERR_WORKSPACE = 12      /* workspace smaller than fa_fwd_workspace_size   */
 };
 
 /*
@@ -78,6 +81,41 @@ enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int N, int d, int causal, float scale, int dtype,
            cudaStream_t stream);
+
+/*
+ * fa_fwd_ws — fa_fwd with a caller-provided workspace used to balance the
+ * last round of work across all SMs.
+ *
+ * The persistent kernel deals whole (batch*head, 256-row query block) units
+ * to the SMs; when the units do not fill whole rounds, the last units are
+ * cut along the key axis so every SM does the same number of key tiles, and
+ * the partial results of a cut unit (unnormalised O, running max m and sum
+ * l per row, kept in the workspace) are combined by the identity the online
+ * softmax rests on: rescale every part to the largest m, add, divide once
+ * ("FlashAttention: The Matrix You Never Have to Write Down", section "What
+ * it doesn't solve", on splitting the key axis across workers and combining
+ * partial results).  Results equal fa_fwd's up to rounding order.
+ *
+ *   workspace, workspace_bytes : device buffer, 256-byte aligned, at least
+ *       the size fa_fwd_workspace_size reports for the same shape on the
+ *       current device.  Owned by the caller; its contents need no
+ *       initialisation and are not meaningful after the call.  Calls that
+ *       share one workspace must not overlap on the GPU (use one workspace
+ *       per stream).  NULL (or a shape that needs none) runs fa_fwd.
+ *   Other arguments, errors and asynchrony as fa_fwd; FA_ERR_WORKSPACE when
+ *   the workspace is too small, FA_ERR_ALIGN when it is misaligned.
+ * Causal calls, and calls whose units fill whole rounds, use no workspace.
+ */
+int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int H, int N, int d, int causal, float scale, int dtype,
+              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_fwd_workspace_size — bytes of workspace fa_fwd_ws needs for this shape
+ * on the current device (0 when it would not split anything).  Returns
+ * FA_ERR_NULLPTR, FA_ERR_SHAPE, FA_ERR_UNSUPPORTED_D or FA_ERR_DEVICE.
+ */
+int fa_fwd_workspace_size(int B, int H, int N, int d, int causal, size_t *bytes);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *fa_strerror(int code);

@@ -54,7 +54,7 @@ def test_library_has_no_oracle_or_torch_dependency():
 
 
 def test_strerror_covers_codes(lib):
-    for code in range(0, 12):
+    for code in range(0, 13):
         s = fa.fa_strerror(code)
         assert s and s != "unknown error code"
     assert fa.fa_strerror(999) == "unknown error code"
@@ -118,6 +118,20 @@ def test_no_gpu_fails_loudly(lib):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         fa.attention_forward(q, q, q)
+
+
+def test_workspace_size_host_errors(lib):
+    import ctypes as C
+    out = C.c_size_t(7)
+    assert lib.fa_fwd_workspace_size(1, 1, 256, 64, 0, None) == fa.FA_ERR_NULLPTR
+    assert lib.fa_fwd_workspace_size(-1, 1, 256, 64, 0, C.byref(out)) == fa.FA_ERR_SHAPE
+    assert lib.fa_fwd_workspace_size(1, 1, 256, 80, 0, C.byref(out)) == fa.FA_ERR_UNSUPPORTED_D
+    assert lib.fa_fwd_workspace_size(0, 1, 256, 64, 0, C.byref(out)) == fa.FA_OK and out.value == 0
+    # fa_fwd_ws validates like fa_fwd before touching the device
+    assert fa.fa_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 300, 96, 0, 0.1, fa.FA_BF16,
+                        None, 0) == fa.FA_ERR_UNSUPPORTED_D
+    assert fa.fa_fwd_ws(None, FAKE, FAKE, FAKE, FAKE, 1, 1, 300, 64, 0, 0.1, fa.FA_BF16,
+                        None, 0) == fa.FA_ERR_NULLPTR
 
 
 def test_missing_library_raises(tmp_path):
