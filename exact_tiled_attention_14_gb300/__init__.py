@@ -1,8 +1,9 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_strerror``,
-``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``, ``fa_version``),
+(``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``,
+``fa_version``),
 under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
@@ -37,8 +38,8 @@ FA_ERR_CUDA = 11
 FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_strerror", "fa_status",
-           "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_strerror",
+           "fa_status", "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
 
 _lib = None
 
@@ -69,6 +70,8 @@ def load_library(path=None):
     lib.fa_fwd_ws.restype = i
     lib.fa_fwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_fwd_workspace_size.restype = i
+    lib.fa_fwd_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_static.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -116,6 +119,14 @@ def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, work
     return lib.fa_fwd_ws(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
                          int(N), int(d), int(bool(causal)), float(scale), int(dtype),
                          _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_fwd_static(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None):
+    """Raw C call of the entry point that allocates nothing (library-held scratch)."""
+    lib = load_library()
+    return lib.fa_fwd_static(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                             int(N), int(d), int(bool(causal)), float(scale), int(dtype),
+                             _stream(stream))
 
 
 def fa_fwd_workspace_size(B, H, N, d, causal):

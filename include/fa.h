@@ -117,6 +117,32 @@ int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse,
  */
 int fa_fwd_workspace_size(int B, int H, int N, int d, int causal, size_t *bytes);
 
+/*
+ * fa_fwd_static — fa_fwd_ws for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart; this is an integration convenience.  Some
+ * callers only ever see raw device pointers and have no allocator of their
+ * own to get a workspace from (a plugin or launch hook inside a host
+ * framework that owns all device memory), and some must not call cudaMalloc
+ * on their path at all (it can synchronise the whole device, which a
+ * latency-bound loop cannot afford).  This entry point allocates nothing: it
+ * runs fa_fwd_ws with a 40 MiB scratch array that the library keeps on every
+ * GPU it is loaded on, from load until the process exits.
+ *
+ *   Arguments, results and errors as fa_fwd_ws, without the workspace.
+ *   FA_ERR_WORKSPACE when the shape needs more than the 40 MiB array holds
+ *   (no supported shape does on a GPU with up to 152 SMs).
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and leaves its last contents
+ *   in it (the counters that must start at zero are cleared by each call):
+ *   calls that overlap on the GPU — other streams, other host threads —
+ *   race on it and must be serialised by the caller.
+ */
+int fa_fwd_static(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int N, int d, int causal, float scale, int dtype,
+                  cudaStream_t stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char *fa_strerror(int code);
 
