@@ -22,20 +22,27 @@
 // Structure of one CTA (persistent; one CTA per SM):
 //   warps 0-3  softmax warpgroup 0  -> query tile 0 of the unit (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1  -> query tile 1 of the unit
-//   warp  8    MMA issuer (one thread): S = Q K^T and O += P V on tcgen05
+//   warp  8    MMA issuer (one thread): S = Q K^T, and at d = 128 also O += P V
 //   warp  9    TMA producer (one thread): Q tiles and a ring of K/V tiles
-//   warps 10-11 idle (they complete the third warpgroup, which lets the
-//              issue warps give their registers to the softmax warpgroups)
+//   warp  10   at d = 64, second MMA issuer (one thread): O += P V
+//   warps 10-11 otherwise idle (they complete the third warpgroup, which lets
+//              the issue warps give their registers to the softmax warpgroups)
 // A work unit is (batch*head, block of 256 query rows) = two 128-row query
 // tiles.  TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (d fp32
-// columns each); P (16-bit) overwrites the first 64 columns of its S.
+// columns each).  P (16-bit) overwrites the first 64 columns of its S at
+// d = 128; at d = 64 it has 64 columns of its own (see OwnP).
 //
 // MMA issue order per key tile j (the two tiles ping-pong so one tile's
 // softmax runs while the tensor core works on the other tile):
 //   prologue: S0_0, S1_0
-//   step j  : PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
-// so S_w_{j+1} completing implies PV_w_j completed, which is what lets the
-// softmax warpgroup rescale O_w in place before it releases P_w_{j+1}.
+//   d = 128 : PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+//             so S_w_{j+1} completing implies PV_w_j completed, which is what
+//             lets the softmax warpgroup rescale O_w in place before it
+//             releases P_w_{j+1};
+//   d = 64  : S0_{j+1}, S1_{j+1}, PV0_j, PV1_j
+//             S_w_{j+1} only waits for the softmax to have read S_w_j, and
+//             the softmax waits for PV_w_{j-1} before it writes P_w_j or
+//             rescales O_w.
 #pragma once
 
 #include <cuda.h>
@@ -50,6 +57,7 @@ constexpr int kBN = 128;              // keys per K/V tile
 constexpr int kThreads = 384;         // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr int kPvWarp = 10;           // second MMA issuer (own-P layout only)
 // Registers per thread after the split: the launch gives every thread 168
 // (64512 per CTA); the issue warpgroup drops to 88 so the two softmax
 // warpgroups can hold a whole 128-column score row plus its packed P.
@@ -64,7 +72,7 @@ constexpr float kLn2 = 0.693147180559945309f;
 // Sites recorded in the status word when a wait runs out.
 enum WaitSite : uint32_t {
   kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFull = 4, kSitePFull = 5,
-  kSiteOFree = 6, kSiteSFull = 7, kSiteODone = 8
+  kSiteOFree = 6, kSiteSFull = 7, kSiteODone = 8, kSiteSFree = 9, kSitePvDone = 10
 };
 
 struct FwdParams {
@@ -110,7 +118,7 @@ enum TraceEvent : uint32_t {
 // Builds compiled with -DFA_PROFILE instead accumulate, per role, the SM
 // cycles spent in each wait and work phase, and write the totals once at the
 // end (kProfSlots 32-bit counters per role per CTA, into p.trace).
-constexpr int kProfSlots = 16;
+constexpr int kProfSlots = 20;
 struct Prof {
 #ifdef FA_PROFILE
   uint32_t acc[kProfSlots];
@@ -171,7 +179,8 @@ struct Smem {
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
                        bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
-                       bOFree = bODone + 2, bFinal = bOFree + 2, kNumBars = bFinal + 1;
+                       bOFree = bODone + 2, bSFree = bOFree + 2, bPvDone = bSFree + 2,
+                       bFinal = bPvDone + 2, bFinalPv = bFinal + 1, kNumBars = bFinalPv + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base, abort flag, 2 merge flags
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024
@@ -183,6 +192,22 @@ template <int D>
 __device__ __forceinline__ uint32_t s_col(int w) { return w ? 128u : 0u; }
 template <int D>
 __device__ __forceinline__ uint32_t o_col(int w) { return 256u + (w ? D : 0); }
+
+// Where P lives.  At d = 128, S0, S1, O0 and O1 fill all 512 TMEM columns,
+// so P overwrites the first 64 columns of its S; the next S of that query
+// tile then has to wait until the P.V product has read P.  At d = 64 the
+// last 128 columns are free and each query tile gets a P buffer of its own
+// (64 columns: 128 16-bit values per row).  The next S can then be computed
+// as soon as the softmax has read the current S into registers, which takes
+// the tensor-core work of the next tile off the softmax's critical path.
+template <int D>
+struct OwnP {
+  static constexpr bool kOn = (2 * 128 + 2 * D + 2 * 64) <= static_cast<int>(kTmemCols);
+};
+template <int D>
+__device__ __forceinline__ uint32_t p_col(int w) {
+  return OwnP<D>::kOn ? 256u + 2u * D + (w ? 64u : 0u) : s_col<D>(w);
+}
 
 struct Unit {
   int bh, mblk, n0, n1;
@@ -353,8 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(L::bPFull + w), 128);
       ptx::mbar_init(bar(L::bODone + w), 1);
       ptx::mbar_init(bar(L::bOFree + w), 128);
+      ptx::mbar_init(bar(L::bSFree + w), 128);
+      ptx::mbar_init(bar(L::bPvDone + w), 1);
     }
     ptx::mbar_init(bar(L::bFinal), 1);
+    ptx::mbar_init(bar(L::bFinalPv), 1);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
     ptx::prefetch_tmap(&p.tm_q);
@@ -402,23 +430,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             trace_event(p, 3, tr, kEvLoadQ, k_units);
           }
         };
+        auto load_kv = [&](int kv, int j) {
+          const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
+          if (use > 0)
+            alive = ptx::wait_bounded(bar(L::bKvEmpty + slot), (use - 1) & 1, wd, kSiteKvEmpty) &&
+                    alive;
+          if (alive) {
+            ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), L::kTile);
+            const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
+            for (int c = 0; c < L::kChunks; ++c)
+              ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
+                               bar(L::bKvFull + slot), c * 64, (u.kb + j) * kBN, u.bh);
+            trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
+            ++loads;
+          }
+        };
+        // The ring is filled in the order the MMA issuer consumes it:
+        // K0 V0 K1 V1 ... when P overwrites S (S_{j+1} follows P_j V_j), and
+        // K0 K1 V0 K2 V1 ... with a P buffer of its own (S_{j+1} goes first).
+        load_kv(0, 0);
+        load_q();
         for (int j = 0; j < nkv; ++j) {
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
-            if (j == 0 && kv == 1) load_q();
-            const uint32_t slot = loads % L::kStages, use = loads / L::kStages;
-            if (use > 0)
-              alive = ptx::wait_bounded(bar(L::bKvEmpty + slot), (use - 1) & 1, wd, kSiteKvEmpty) &&
-                      alive;
-            if (alive) {
-              ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), L::kTile);
-              const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
-              for (int c = 0; c < L::kChunks; ++c)
-                ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
-                                 bar(L::bKvFull + slot), c * 64, (u.kb + j) * kBN, u.bh);
-              trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
-              ++loads;
-            }
+          if (OwnP<D>::kOn) {
+            if (j + 1 < nkv) load_kv(0, j + 1);
+            load_kv(1, j);
+          } else {
+            load_kv(1, j);
+            if (j + 1 < nkv) load_kv(0, j + 1);
           }
         }
         ++k_units;
@@ -431,12 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q_issued > 0) ptx::wait_drain(bar(L::bQFull), (q_issued - 1) & 1, drain);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ============================================================ MMA issuer
-    // One thread issues every tcgen05 instruction.  The issue loop has to
-    // keep up with the tensor core (an M128 x N128 x K16 MMA lasts ~64
-    // cycles), so descriptors are precomputed: per MMA only the 32-bit
-    // address word changes, by a compile-time offset.
+  } else if (warp == kMmaWarp || (OwnP<D>::kOn && warp == kPvWarp)) {
+    // ============================================================ MMA issuers
+    // The issue loop has to keep up with the tensor core (an M128 x N128 x
+    // K16 MMA lasts ~64 cycles), so descriptors are precomputed: per MMA only
+    // the 32-bit address word changes, by a compile-time offset.
+    // When P overwrites S, one thread (warp 8) issues every tcgen05
+    // instruction, in an order that carries the S/P dependence.  With its own
+    // P the two products are independent and each gets an issuing thread:
+    // warp 8 the S = Q K^T products, warp 10 the O += P V products.  Any wait
+    // on a barrier stalls the waiting thread until the tensor core has taken
+    // every MMA it queued before, which leaves the pipe idle meanwhile; with
+    // two issuers one thread's waits overlap the other's queued work.
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
@@ -495,6 +539,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor cu;
       cursor_init<kSplit>(p, cta, grid, cu);
       Piece u;
+      if constexpr (OwnP<D>::kOn) {
+        // With a P buffer per query tile, S_w_{j+1} waits only until the
+        // softmax has read S_w_j, and P_w_j V_j only for P_w_j.
+        const uint32_t tP0 = tmem_base + p_col<D>(0), tP1 = tmem_base + p_col<D>(1);
+        uint32_t sc0 = 0, sc1 = 0;     // S issued into S0 / S1 so far
+        auto issue_s_own = [&](int w, uint32_t kslot_) {
+          uint32_t& sc = w ? sc1 : sc0;
+          pf.lap(6);
+          if (sc > 0)   // the softmax has read the previous S of this tile
+            alive = ptx::wait_bounded(bar(L::bSFree + w), (sc - 1) & 1, wd, kSiteSFree) && alive;
+          pf.lap(16);
+          ptx::tc_fence_after();
+          if (alive) {
+            issue_s(w ? tS1 : tS0, w ? q_lo1 : q_lo0, k_lo0 + kslot_ * kSlotLo);
+            ptx::mma_commit(bar(L::bSFull + w));
+          }
+          ++sc;
+          pf.lap(4);
+          pf.count(7);
+        };
+        auto issue_pv_own = [&](int w, int j, uint32_t v_lo) {
+          uint32_t& pph = w ? pph1 : pph0;
+          const uint32_t ucnt = w ? ucnt1 : ucnt0;
+          pf.lap(6);
+          if (j == 0 && ucnt > 0)   // O_w of the previous piece must have been read out
+            alive = ptx::wait_bounded(bar(L::bOFree + w), (ucnt - 1) & 1, wd, kSiteOFree) && alive;
+          pf.lap(3);
+          alive = ptx::wait_bounded(bar(L::bPFull + w), pph, wd, kSitePFull) && alive;
+          pf.lap(1);
+          pph ^= 1u;
+          ptx::tc_fence_after();
+          if (alive) {
+            issue_pv(w ? tO1 : tO0, w ? tP1 : tP0, v_lo, j > 0 ? 1u : 0u);
+            ptx::mma_commit(bar(L::bPvDone + w));
+          }
+          pf.lap(5);
+          pf.count(7);
+        };
+        // The producer fills the ring with K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2}
+        // V_{n-1} for a piece of n key tiles: 2n loads from ring position
+        // `base`; each issuer waits only for the tiles it reads.
+        auto ring_wait = [&](uint32_t pos) -> uint32_t {
+          const uint32_t sl = pos % L::kStages;
+          pf.lap(6);
+          alive = ptx::wait_bounded(bar(L::bKvFull + sl), (pos / L::kStages) & 1, wd, kSiteKvFull) &&
+                  alive;
+          pf.lap(0);
+          ptx::tc_fence_after();
+          return sl;
+        };
+        uint32_t base = 0;
+        if (warp == kMmaWarp) {
+          // S = Q K^T for both query tiles, one key tile ahead of the softmax
+          while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+            const int nkv = max(u.n0, u.n1);
+            pf.lap(6);
+            alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
+            pf.lap(2);
+            ptx::tc_fence_after();
+            for (int j = 0; j < nkv; ++j) {
+              const uint32_t kslot = ring_wait(base + (j == 0 ? 0u : 2u * j - 1u));
+              if (j < u.n0) issue_s_own(0, kslot);
+              if (j < u.n1) issue_s_own(1, kslot);
+              if (alive) {
+                ptx::mma_commit(bar(L::bKvEmpty + kslot));
+                if (j + 1 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
+              }
+              issued_any = true;
+            }
+            base += 2u * nkv;
+            ++k_units;
+          }
+        } else {
+          // O += P V for both query tiles, as soon as the softmax has written P
+          while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+            const int nkv = max(u.n0, u.n1);
+            for (int j = 0; j < nkv; ++j) {
+              const uint32_t vslot =
+                  ring_wait(base + (j + 1 < nkv ? 2u * j + 2u : 2u * nkv - 1u));
+              const uint32_t v_lo = v_lo0 + vslot * kSlotLo;
+              if (j < u.n0) issue_pv_own(0, j, v_lo);
+              if (j < u.n1) issue_pv_own(1, j, v_lo);
+              if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
+              issued_any = true;
+            }
+            if (u.n0 > 0) ++ucnt0;
+            if (u.n1 > 0) ++ucnt1;
+            base += 2u * nkv;
+          }
+        }
+      } else
       while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
         const int nkv = max(u.n0, u.n1);
         pf.lap(6);
@@ -587,11 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++k_units;
       }
       pf.lap(6);
-      pf.flush(p, 2);
+      const bool pv_thread = OwnP<D>::kOn && warp == kPvWarp;
+      pf.flush(p, pv_thread ? 3 : 2);
       // Drain: every MMA issued by this thread has completed before TMEM is freed.
       if (issued_any) {
-        ptx::mma_commit(bar(L::bFinal));
-        ptx::wait_drain(bar(L::bFinal), 0, 200000000ull);
+        const uint32_t fb = bar(pv_thread ? L::bFinalPv : L::bFinal);
+        ptx::mma_commit(fb);
+        ptx::wait_drain(fb, 0, 200000000ull);
       }
     }
     __syncwarp();
@@ -604,9 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + s_col<D>(w);
     const uint32_t tO = tmem_base + lane_off + o_col<D>(w);
+    const uint32_t tP = tmem_base + lane_off + p_col<D>(w);
     const uint32_t stage = sbase + L::kO + w * L::kTile;   // used when kTmaStore
     const float c = p.scale_log2;
     uint32_t scnt = 0, ucnt = 0;
+    uint32_t pvcnt = 0;                       // P.V products of this tile waited for (own P)
     uint32_t tr = 0;                          // trace events recorded (thread t == 0)
     const bool tracer = (t == 0);
     Prof pf;   // FA_PROFILE: 0 s wait, 1 load S, 2 max + rescale, 3 exp/sum/pack, 4 store P + arrive,
@@ -640,6 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[kBN];
 #pragma unroll
         for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(sr[i]);
+        if constexpr (OwnP<D>::kOn) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bSFree + w));   // S_w may be overwritten now
+        }
         pf.lap(1);
 
         // mask: keys past N, and on the diagonal tile keys after this row
@@ -675,11 +818,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
           neg_m = nm;
         }
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, grow);
+        // O_w *= alpha.  PV_w_{j-1} must be complete (when P overwrites S it
+        // was issued before S_w_j; with its own P the caller waits for it),
+        // and PV_w_j cannot start before this warpgroup arrives on p_full.
+        auto rescale_o = [&]() {
           if (tracer) trace_event(p, w, tr, kEvRescale, j);
           pf.count(9);
-          // PV_w_{j-1} is complete (it was issued before S_w_j), and PV_w_j
-          // cannot start before this warpgroup arrives on p_full below.
 #pragma unroll 1
           for (int q4 = 0; q4 < D / 32; ++q4) {
             uint32_t orr[32];
@@ -689,7 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             ptx::tmem_st32(tO + q4 * 32, orr);
           }
-        }
+        };
+        if (!OwnP<D>::kOn && rescale) rescale_o();
 
         pf.lap(2);
         // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM.
@@ -716,8 +862,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += (a + b) + (cc + dd);
         }
         pf.lap(3);
-        ptx::tmem_st32(tS, pk);
-        ptx::tmem_st32(tS + 32, pk + 32);
+        if constexpr (OwnP<D>::kOn) {
+          // P_w and O_w are still in use by PV_w_{j-1} until it completes.
+          if (j > 0) {
+            pf.lap(3);
+            ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
+            ++pvcnt;
+            pf.lap(16);
+            __syncwarp();
+            ptx::tc_fence_after();
+          }
+          if (rescale) rescale_o();
+        }
+        ptx::tmem_st32(tP, pk);
+        ptx::tmem_st32(tP + 32, pk + 32);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + w));
@@ -727,7 +885,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- epilogue: O / l in the storage dtype, and LSE = m + ln l per row
       pf.lap(7);
-      ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
+      if constexpr (OwnP<D>::kOn) {
+        ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);   // last PV_w
+        ++pvcnt;
+      } else {
+        ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
+      }
       pf.lap(5);
       ++ucnt;
       if (tracer) trace_event(p, w, tr, kEvEpiStart, ucnt - 1);
