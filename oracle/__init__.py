@@ -6,10 +6,13 @@ never import, link or call it, and it imports nothing from them.
 
 * ``attention`` / ``attention_rows`` — the plain definition (scores, row max,
   exp-sum, V blend, logsumexp) in C, ``attn_oracle.c``.
+* ``attention_grad`` / ``grad_query_rows`` / ``grad_key_rows`` — the
+  gradients of that definition with respect to Q, K and V (chain rule through
+  the softmax) in C, ``attn_grad_oracle.c``.
 * ``online_model`` — the block-wise online recurrence in numpy, the second
   derivation the C code is pinned against.
 
-``build()`` compiles ``attn_oracle.c`` with gcc (OpenMP over rows) into
+``build()`` compiles both C files with gcc (OpenMP over rows) into
 ``oracle/_build/liboracle.so``; the first call to ``attention`` builds it if
 it is missing.
 """
@@ -24,16 +27,19 @@ from . import online_model  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_GRAD_SRC = os.path.join(_HERE, "attn_grad_oracle.c")
+SOURCES = (_SRC, _GRAD_SRC)
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lib = None
 
 
-def compile_oracle(src=_SRC, out=_LIB_PATH, extra_flags=()):
-    """Compile an oracle source file into a shared library; returns the path."""
+def compile_oracle(src=SOURCES, out=_LIB_PATH, extra_flags=()):
+    """Compile oracle source file(s) into a shared library; returns the path."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
+    srcs = [src] if isinstance(src, (str, os.PathLike)) else list(src)
     cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c99", *extra_flags,
-           src, "-o", out + ".tmp", "-lm"]
+           *srcs, "-o", out + ".tmp", "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(out + ".tmp", out)
     return out
@@ -59,6 +65,17 @@ def _bind(path):
     lib.oracle_attention.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    if hasattr(lib, "oracle_attention_grad"):   # a forward-only build has none
+        i32, f64 = ctypes.c_int, ctypes.c_double
+        lib.oracle_attention_grad.argtypes = [i64, i64, i64, i64, i64, p, p, p, p, i32, f64,
+                                              p, p, p]
+        lib.oracle_attention_grad.restype = i32
+        lib.oracle_grad_query_rows.argtypes = [i64, i64, i64, p, p, i64, p, p, p, i32, f64,
+                                               p, p, p]
+        lib.oracle_grad_query_rows.restype = i32
+        lib.oracle_grad_key_rows.argtypes = [i64, i64, i64, p, p, p, p, i64, p, p, p, i32,
+                                             f64, p, p]
+        lib.oracle_grad_key_rows.restype = i32
     return lib
 
 
@@ -68,8 +85,8 @@ def load(path=None):
     if path is not None:
         return _bind(path)
     if _lib is None:
-        if not os.path.exists(_LIB_PATH) or (
-                os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        if not os.path.exists(_LIB_PATH) or any(
+                os.path.getmtime(_LIB_PATH) < os.path.getmtime(f) for f in SOURCES):
             compile_oracle()
         _lib = _bind(_LIB_PATH)
     return _lib
@@ -140,3 +157,83 @@ def attention_rows(q_rows, q_pos, k, v, causal=False, scale=None, lib=None):
 def num_threads(lib=None):
     """OpenMP threads the oracle runs rows on."""
     return int((lib or load()).oracle_num_threads())
+
+
+def attention_grad(q, k, v, dout, causal=False, scale=None, lib=None):
+    """Gradients of exact attention over the last two axes, in float64.
+
+    q [..., Tq, d], k [..., Tk, d], v [..., Tk, dv], dout [..., Tq, dv] ->
+    (dq, dk, dv) of the scalar sum(dout * O), O = attention(q, k, v).
+    Query i and key j sit at positions i and j (upper-left causal).
+    """
+    lib = lib or load()
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    lead = q.shape[:-2]
+    if k.shape[:-2] != lead or v.shape[:-2] != lead or g.shape[:-2] != lead:
+        raise ValueError("leading axes differ")
+    tq, d = q.shape[-2:]
+    tk, dv = v.shape[-2:]
+    if k.shape[-1] != d or k.shape[-2] != tk or g.shape[-2:] != (tq, dv):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bh = int(np.prod(lead)) if lead else 1
+    dq, dk, dvv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    rc = lib.oracle_attention_grad(bh, tq, tk, d, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   int(bool(causal)), float(scale), _ptr(dq), _ptr(dk),
+                                   _ptr(dvv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_grad failed ({rc})")
+    return dq, dk, dvv
+
+
+def grad_query_rows(q_rows, dout_rows, q_pos, k, v, causal=False, scale=None, lib=None):
+    """dQ of selected query rows of ONE head, with each row's lse and D.
+
+    q_rows [R, d], dout_rows [R, dv], positions q_pos [R]; k [Tk, d],
+    v [Tk, dv] -> (dq [R, d], lse [R], delta [R]).
+    """
+    lib = lib or load()
+    q_rows, g, k, v = _f64(q_rows), _f64(dout_rows), _f64(k), _f64(v)
+    pos = np.ascontiguousarray(np.asarray(q_pos, dtype=np.int64))
+    r, d = q_rows.shape
+    tk, dv = v.shape
+    if pos.shape != (r,) or k.shape != (tk, d) or g.shape != (r, dv):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, lse, delta = np.zeros((r, d)), np.zeros(r), np.zeros(r)
+    rc = lib.oracle_grad_query_rows(tk, d, dv, _ptr(k), _ptr(v), r, _ptr(q_rows), _ptr(g),
+                                    _ptr(pos), int(bool(causal)), float(scale), _ptr(dq),
+                                    _ptr(lse), _ptr(delta))
+    if rc != 0:
+        raise RuntimeError(f"oracle_grad_query_rows failed ({rc})")
+    return dq, lse, delta
+
+
+def grad_key_rows(k_rows, v_rows, k_pos, q, dout, lse, delta, causal=False, scale=None,
+                  lib=None):
+    """dK, dV of selected key rows of ONE head.
+
+    k_rows [R, d], v_rows [R, dv], positions k_pos [R]; all queries of the
+    head q [Tq, d], dout [Tq, dv] with their lse [Tq] and delta [Tq] (from
+    ``grad_query_rows`` over every query) -> (dk [R, d], dv [R, dv]).
+    """
+    lib = lib or load()
+    k_rows, v_rows, q, g = _f64(k_rows), _f64(v_rows), _f64(q), _f64(dout)
+    lse, delta = _f64(lse), _f64(delta)
+    pos = np.ascontiguousarray(np.asarray(k_pos, dtype=np.int64))
+    r, d = k_rows.shape
+    tq, dv = g.shape
+    if pos.shape != (r,) or v_rows.shape != (r, dv) or q.shape != (tq, d) or \
+            lse.shape != (tq,) or delta.shape != (tq,):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dk, dvv = np.zeros((r, d)), np.zeros((r, dv))
+    rc = lib.oracle_grad_key_rows(tq, d, dv, _ptr(q), _ptr(g), _ptr(lse), _ptr(delta), r,
+                                  _ptr(k_rows), _ptr(v_rows), _ptr(pos), int(bool(causal)),
+                                  float(scale), _ptr(dk), _ptr(dvv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_grad_key_rows failed ({rc})")
+    return dk, dvv
