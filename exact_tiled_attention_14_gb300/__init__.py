@@ -2,8 +2,8 @@
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
 (``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
-``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``,
-``fa_version``),
+``fa_bwd``, ``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``,
+``fa_work_tiles``, ``fa_version``),
 under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
@@ -12,7 +12,8 @@ every call raises.
 ``attention_forward`` is the convenience call a user makes: it allocates O
 and LSE (and, when asked, the balancing workspace) with PyTorch — device
 memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
-current CUDA stream.
+current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
+(dQ, dK, dV and the D scratch).
 """
 import ctypes
 import math
@@ -38,8 +39,8 @@ FA_ERR_CUDA = 11
 FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_strerror",
-           "fa_status", "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+           "fa_strerror", "fa_status", "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
 
 _lib = None
 
@@ -72,6 +73,8 @@ def load_library(path=None):
     lib.fa_fwd_workspace_size.restype = i
     lib.fa_fwd_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_static.restype = i
+    lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
+    lib.fa_bwd.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -127,6 +130,15 @@ def fa_fwd_static(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None
     return lib.fa_fwd_static(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
                              int(N), int(d), int(bool(causal)), float(scale), int(dtype),
                              _stream(stream))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
+           stream=None):
+    """Raw C call of the backward pass; tensors or integer addresses; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout), _addr(dq),
+                      _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(N), int(d),
+                      int(bool(causal)), float(scale), int(dtype), _stream(stream))
 
 
 def fa_fwd_workspace_size(B, H, N, d, causal):
@@ -226,3 +238,34 @@ def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, str
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=None):
+    """dQ, dK, dV of sum(dout * O) for O, LSE = attention_forward(q, k, v).
+
+    All tensors are CUDA [B, H, N, d] of one 16-bit dtype except lse (float32
+    [B, H, N]).  Allocates dq, dk, dv and the float32 D scratch with PyTorch
+    and calls ``fa_bwd`` on ``stream`` (default: current stream).
+    """
+    import torch
+    ts = (q, k, v, o, dout)
+    if any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, o, dout must all be [B, H, N, d] of one shape")
+    if lse.dtype != torch.float32 or lse.shape != q.shape[:3]:
+        raise ValueError("lse must be float32 [B, H, N]")
+    if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = dtype_code(q.dtype)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, code, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv

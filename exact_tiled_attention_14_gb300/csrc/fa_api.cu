@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_launch.cuh"
 #include "fa_launch.cuh"
 
 namespace {
@@ -96,7 +97,7 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int BH, int N, int d, bool bf16)
 
 extern "C" {
 
-int fa_version(void) { return 101; }
+int fa_version(void) { return 102; }
 
 const char* fa_strerror(int code) {
   switch (code) {
@@ -278,6 +279,56 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, 
               cudaStream_t stream) {
   return launch_forward(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace,
                         workspace_bytes, stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int N,
+           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_tiles = (static_cast<long long>(N) + fa::kBwdTile - 1) / fa::kBwdTile;
+  if (bh > INT_MAX || bh * n_tiles > INT_MAX) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0 || N == 0) return FA_OK;  // nothing to write
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta) return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta);
+  if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::BwdParams p;
+  if (!make_tmap(&p.tm_q, q, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_k, k, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_v, v, static_cast<int>(bh), N, d, bf16) ||
+      !make_tmap(&p.tm_do, dout, static_cast<int>(bh), N, d, bf16))
+    return FA_ERR_TENSORMAP;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
+  p.BH = static_cast<int>(bh);
+  p.N = N;
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e =
+      (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
+                : fa::launch_bwd_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_status(cudaStream_t stream, unsigned int* detail) {

@@ -1,0 +1,62 @@
+// fa_bwd_launch.cuh — host-side launches of the backward kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "fa_bwd_kernel.cuh"
+
+namespace fa {
+
+// Raise the dynamic shared-memory limit of `fn` once per device.
+template <typename Fn>
+cudaError_t bwd_smem_attr(Fn fn, std::atomic<uint64_t>& done, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done.load() & bit)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit);
+  }
+  return cudaSuccess;
+}
+
+// D = rowsum(dO * O), then dK/dV (one CTA per key tile), then dQ (one CTA per
+// query tile), all on `stream`.  `o`, `dout` are [BH, N, D] in the storage dtype.
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* dout, float* delta,
+                               int sms, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.BH) * p.N;
+  const long long threads = rows * (D / 8);
+  long long blocks = (threads + 255) / 256;
+  const long long cap = 8ll * sms;
+  if (blocks > cap) blocks = cap;
+  fa_bwd_delta_kernel<D, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  static std::atomic<uint64_t> done_kv{0}, done_q{0};
+  constexpr int kAlloc = BwdSmem<D>::kAlloc;
+  e = bwd_smem_attr(fa_bwd_dkdv_kernel<D, kBf16, kCausal>, done_kv, kAlloc);
+  if (e != cudaSuccess) return e;
+  e = bwd_smem_attr(fa_bwd_dq_kernel<D, kBf16, kCausal>, done_q, kAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = p.BH * p.n_tiles;
+  fa_bwd_dkdv_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAlloc, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fa_bwd_dq_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
+                           bool bf16, bool causal, int sms, cudaStream_t stream);
+cudaError_t launch_bwd_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
+                            bool bf16, bool causal, int sms, cudaStream_t stream);
+
+}  // namespace fa

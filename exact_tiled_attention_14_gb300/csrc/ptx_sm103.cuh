@@ -228,6 +228,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 // registers -> 32 consecutive 32-bit TMEM columns of this thread's lane.
+// 32 lanes x 16 columns of 32 bits from 16 registers per thread (this warp's lanes).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -330,6 +339,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// The two 16-bit values of a packed pair (low half first) as floats.
+template <bool kBf16>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+  if constexpr (kBf16) {
+    lo = __uint_as_float(v << 16);
+    hi = __uint_as_float(v & 0xffff0000u);
+  } else {
+    unsigned short a = static_cast<unsigned short>(v & 0xffffu);
+    unsigned short b = static_cast<unsigned short>(v >> 16);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(a));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(b));
+  }
 }
 
 }  // namespace ptx

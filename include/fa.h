@@ -143,6 +143,39 @@ int fa_fwd_static(const void *q, const void *k, const void *v, void *o, float *l
                   int B, int H, int N, int d, int causal, float scale, int dtype,
                   cudaStream_t stream);
 
+/*
+ * fa_bwd — gradients of exact attention: dQ, dK, dV of sum(dO * O) for the
+ * O that fa_fwd computes from the same q, k, v, causal and scale.
+ *
+ * The pages describe the backward pass as keeping Q, K, V, the output O and
+ * the per-row statistics L, and rebuilding the score and probability tiles
+ * from them rather than storing the N x N matrices ("FlashAttention: The
+ * Matrix You Never Have to Write Down", section "The forward pass is only
+ * half of it"; "Why FlashAttention Can Avoid a Square Attention Array
+ * Without Making Attention Linear", section "Backward can recreate tiles
+ * instead of retaining the square").  With P = exp(scale q.k - LSE) and
+ * D = rowsum(dO * O): dV = P^T dO, dS = P * (dO V^T - D), dQ = scale dS K,
+ * dK = scale dS^T Q.  No N x N buffer is allocated or written.
+ *
+ *   q, k, v, o : device pointers, [B, H, N, d], dtype `dtype`, 16-byte
+ *                aligned; o is the fa_fwd output for q, k, v.
+ *   lse        : device pointer, [B, H, N] float32, the fa_fwd LSE.
+ *   dout       : device pointer, [B, H, N, d], dtype `dtype`: dLoss/dO.
+ *   dq, dk, dv : device pointers, [B, H, N, d], dtype `dtype`, 16-byte
+ *                aligned, written (rounded to nearest-even).
+ *   delta      : device pointer, [B, H, N] float32, 4-byte aligned, owned
+ *                by the caller: written with D = rowsum(dO * O) and read
+ *                back by the gradient kernels (scratch for the caller).
+ *   B, H, N, d, causal, scale, dtype, stream : as fa_fwd.
+ * Errors and asynchrony as fa_fwd (FA_ERR_NULLPTR for any of the ten
+ * pointers).  Results are deterministic: every gradient row is written by
+ * one CTA, without atomics.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, float *delta,
+           int B, int H, int N, int d, int causal, float scale, int dtype,
+           cudaStream_t stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char *fa_strerror(int code);
 

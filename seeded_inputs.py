@@ -63,6 +63,14 @@ def make_qkv(B, H, N, d, dtype="bf16", q_std=1.0, seed=0):
     return q.to(t), k.to(t), v.to(t)
 
 
+def make_dout(B, H, N, d, dtype="bf16", seed=0):
+    """An upstream gradient dO [B, H, N, d] (N(0,1), rounded to the storage
+    dtype) from its own generator, seeded 500000 + seed so it never repeats
+    the Q, K, V draws of the same seed."""
+    g = torch.Generator("cpu").manual_seed(500000 + int(seed))
+    return torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(DTYPES[dtype])
+
+
 def make_workload_qkv(w):
     """Q, K, V for a workload dict from ``WORKLOADS``."""
     return make_qkv(w["B"], w["H"], w["N"], w["d"], w["dtype"], w["q_std"],

@@ -152,3 +152,19 @@ def test_binding_dtype_contract():
     with pytest.raises(ValueError):
         fa.attention_forward(a[0], a[0], a[0])
     _ = ctypes  # keep the import used
+
+
+def test_bwd_host_errors(lib):
+    """fa_bwd checks its arguments before any device work, in fa_fwd's order."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                delta=FAKE, B=1, H=2, N=300, d=128, causal=1, scale=0.125, dtype=fa.FA_BF16)
+    cases = [(dict(B=-1), fa.FA_ERR_SHAPE), (dict(d=80), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dtype=3), fa.FA_ERR_DTYPE), (dict(scale=-2.0), fa.FA_ERR_SCALE),
+             (dict(N=0, q=None), fa.FA_OK), (dict(dout=None), fa.FA_ERR_NULLPTR),
+             (dict(delta=None), fa.FA_ERR_NULLPTR), (dict(dv=FAKE + 4), fa.FA_ERR_ALIGN),
+             (dict(delta=FAKE + 2), fa.FA_ERR_ALIGN)]
+    for args, code in cases:
+        assert fa.fa_bwd(**{**call, **args}) == code, args
+    import torch
+    if not torch.cuda.is_available():
+        assert fa.fa_bwd(**call) == fa.FA_ERR_DEVICE
