@@ -21,6 +21,10 @@ timed region), ``clocks`` (nvidia-smi samples during the timed region) and
 ``--impl reference`` times the float64 oracle on the host cores instead
 (rank 0 only), on bounded samples of the same workload.
 
+``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
+call (three kernels) with the forward's O and LSE and a seeded dO resident
+on the device; FLOPs are 2.5x the forward's (five matmuls against two).
+
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 forward pass has no exchange step); value = all ranks' FLOPs / the slowest
 rank's time.
@@ -46,6 +50,8 @@ import seeded_inputs  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_WORKLOAD = "b1_h16_n4096_d128_bf16"
 METRIC = "attention fwd TFLOP/s (causal halved) and % of GB300 dense BF16 tensor peak"
+METRIC_BWD = ("attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved) and % of GB300 "
+              "dense BF16 tensor peak")
 FALLBACK_PEAK_TFLOPS = 1900.0
 
 
@@ -54,6 +60,18 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 def step_flops(w):
     f = 4.0 * w["B"] * w["H"] * w["N"] * w["N"] * w["d"]
     return f / 2 if w["causal"] else f
+
+
+def step_flops_bwd(w):
+    """Backward FLOPs by the usual convention: five N^2 d matmuls (dV, dP, dQ, dK
+    and the recomputed S) against the forward's two, i.e. 2.5x the forward."""
+    return 2.5 * step_flops(w)
+
+
+def io_bytes_bwd(w):
+    elems = w["B"] * w["H"] * w["N"] * w["d"]
+    rows = w["B"] * w["H"] * w["N"]
+    return dict(h2d=5 * elems * 2 + rows * 4, d2h=3 * elems * 2)
 
 
 def io_bytes(w):
@@ -291,6 +309,29 @@ def oracle_sample(w, q, k, v, budget_s, start_head=0):
     return flops / spent / 1e12, spent, done, cores, desc
 
 
+def oracle_grad_sample(w, q, k, v, dout, budget_s, start_head=0):
+    """Time the float64 gradient oracle on whole heads for about budget_s
+    (the backward counterpart of ``oracle_sample``)."""
+    import oracle
+    lib = oracle.load()
+    B, H = w["B"], w["H"]
+    nheads = B * H
+    cores = oracle.num_threads(lib)
+    done, spent = 0, 0.0
+    while done < nheads and (done == 0 or spent < budget_s):
+        hb = (start_head + done) % nheads
+        b, h = divmod(hb, H)
+        qh, kh, vh, gh = (t[b, h].double().numpy() for t in (q, k, v, dout))
+        t0 = time.perf_counter()
+        oracle.attention_grad(qh, kh, vh, gh, causal=w["causal"], scale=w["scale"], lib=lib)
+        spent += time.perf_counter() - t0
+        done += 1
+    flops = step_flops_bwd(w) * done / nheads
+    desc = (f"gradients of {done} of {nheads} whole heads of {w['name']} (float64, {cores} "
+            "threads); every head does the same work")
+    return flops / spent / 1e12, spent, done, cores, desc
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(args, w):
@@ -303,14 +344,20 @@ def run_reference(args, w):
     import oracle
     oracle.load()
     vals = []
+    bwd = args.pass_ == "bwd"
+    dout = seeded_inputs.make_dout(w["B"], w["H"], w["N"], w["d"], w["dtype"], seed=w["seed"]) \
+        if bwd else None
     for i in range(total):
-        tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, per_step, start_head=i)
+        if bwd:
+            tf, dt, heads, cores, desc = oracle_grad_sample(w, q, k, v, dout, per_step, start_head=i)
+        else:
+            tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, per_step, start_head=i)
         if i >= args.warmup:
             vals.append((tf, dt))
     value = statistics.median(tf for tf, _ in vals)
     ms = statistics.median(dt for _, dt in vals) * 1e3
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s",
         "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
@@ -473,6 +520,140 @@ def run_ours(args, w):
     return 0
 
 
+def run_ours_bwd(args, w):
+    """The backward pass: one step = one fa_bwd call (three kernels) on
+    inputs, the forward's O and LSE, and dO resident in device memory."""
+    import exact_tiled_attention_14_gb300 as fa
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+
+    sampler = ClockSampler(local).start()
+    q, k, v = seeded_inputs.make_workload_qkv(w)
+    dout = seeded_inputs.make_dout(w["B"], w["H"], w["N"], w["d"], w["dtype"], seed=w["seed"])
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    io = io_bytes_bwd(w)
+    per_replica = io["h2d"] + io["d2h"] + B * H * N * 4
+    replicas = 1 if per_replica > 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_replica)) + 1
+    replicas = min(replicas, 64)
+    stream = torch.cuda.current_stream(device)
+    code = fa.dtype_code(q.dtype)
+    bufs = []
+    for _ in range(replicas):
+        dq_, dk_, dv_, do_ = (t.to(device) for t in (q, k, v, dout))
+        o, lse = fa.attention_forward(dq_, dk_, dv_, causal=w["causal"], scale=w["scale"],
+                                      stream=stream)
+        gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+        delta = torch.empty((B, H, N), dtype=torch.float32, device=device)
+        bufs.append((dq_, dk_, dv_, o, lse, do_, gq, gk, gv, delta))
+
+    def step(i):
+        rc = fa.fa_bwd(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], code, stream)
+        if rc:
+            raise fa.FaError(rc, "fa_bwd")
+
+    t_warm = time.time()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"warmup status {word:#x}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    t1 = time.time()
+    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
+    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
+                             world, device)
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"timed status {word:#x}")
+
+    # end to end: pinned host q, k, v, o, lse, dO in; dQ, dK, dV out
+    hosts = [t.pin_memory() for t in (q, k, v)]
+    dq_, dk_, dv_, o, lse, do_ = bufs[0][:6]
+    ho, hl = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    hdo = dout.pin_memory()
+    outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        for dst, src in zip((dq_, dk_, dv_, o, lse, do_), hosts + [ho, hl, hdo]):
+            dst.copy_(src, non_blocking=True)
+        grads = fa.attention_backward(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
+                                      scale=w["scale"], stream=stream)
+        for dst, src in zip(outs, grads):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1, fallback_window=(t_warm, t1))
+
+    if rank != 0:
+        return 0
+    flops = step_flops_bwd(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak, peak_sustained, peak_src = measured_peaks()
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "pass": "backward", "B": B, "H": H, "N": N, "d": d,
+                   "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "entry": "fa_bwd",
+                   "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
+                          if replicas > 1 else "inputs larger than L2")},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
+                     "kernel_ms": kern_ms, "flops_per_launch": flops,
+                     "scope": "one fa_bwd call: D, dK/dV and dQ kernels together",
+                     "traffic": None, "traffic_note": "no ncu DRAM capture of the backward yet"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+        "gpu": torch.cuda.get_device_name(device),
+    }
+    if not args.no_cpu_baseline:
+        tf, dt, heads, cores, desc = oracle_grad_sample(w, q, k, v, dout, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(json.dumps(line) + "\n")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,6 +672,8 @@ def main(argv=None):
     ap.add_argument("--split", action="store_true",
                     help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward pass (default) or the backward pass (fa_bwd)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -501,6 +684,8 @@ def main(argv=None):
         w["name"] = f"{w['name']}@B{w['B']}H{w['H']}"
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 
