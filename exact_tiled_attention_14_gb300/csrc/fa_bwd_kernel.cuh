@@ -26,11 +26,12 @@
 // and the result is deterministic; the price is that S and dP are formed
 // twice (seven tile GEMMs per (i, j) instead of five).
 //
-// CTA layout (both tensor-core kernels): warps 0-3 are the element-wise
-// warpgroup, thread t owning TMEM lane t (a key row in dkdv, a query row in
-// dq); warp 4 issues the tcgen05 MMAs from one thread; warp 5 issues the TMA
-// loads from one thread.  TMEM: S (or S^T) in columns 0-127, dP (dP^T) in
-// 128-255, the fp32 accumulators from 256.  The 16-bit P^T and dS^T (dS)
+// CTA layout (both tensor-core kernels): warps 0-7 do the element-wise
+// work, warp w on TMEM lanes 32*(w%4) .. +31 (key rows in dkdv, query rows
+// in dq) and on column half w/4 of each 128-column tile, so a row's 128
+// scores are shared by two threads; warp 8 issues the tcgen05 MMAs from one
+// thread; warp 9 issues the TMA loads from one thread.  TMEM: S (or S^T) in
+// columns 0-127, dP (dP^T) in 128-255, the fp32 accumulators from 256.  The 16-bit P^T and dS^T (dS)
 // overwrite the first 64 columns of S^T and dP^T (S) once those are read.
 #pragma once
 
@@ -41,9 +42,10 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdMmaWarp = 4;
-constexpr int kBwdLoadWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdEwThreads = 256;       // element-wise warps 0-7
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
 constexpr int kBwdTile = 128;            // rows of a query or key tile = TMEM lanes
 constexpr uint32_t kBwdTmemCols = 512;
 
@@ -154,16 +156,16 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
                 kk > 0 ? 1u : acc);
 }
 
-// Write one row of a TMEM accumulator (D fp32 columns), times `mul`, to
-// global memory in the storage dtype (rows past N are skipped).
-template <int D, bool kBf16>
-__device__ __forceinline__ void store_acc_row(uint32_t t_acc, float mul, void* base, long long row,
-                                              bool in_range) {
-  uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * (D * 2));
+// Write columns [c0, c0 + NC) of one row of a TMEM accumulator (fp32), times
+// `mul`, to global memory in the storage dtype (rows past N are skipped).
+template <int D, int NC, bool kBf16>
+__device__ __forceinline__ void store_acc_cols(uint32_t t_acc, int c0, float mul, void* base,
+                                               long long row, bool in_range) {
+  uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * (D * 2) + c0 * 2);
 #pragma unroll 1
-  for (int q4 = 0; q4 < D / 32; ++q4) {
+  for (int q4 = 0; q4 < NC / 32; ++q4) {
     uint32_t r[32];
-    ptx::tmem_ld32(t_acc + q4 * 32, r);
+    ptx::tmem_ld32(t_acc + c0 + q4 * 32, r);
     ptx::tmem_wait_ld();
     uint32_t pk[16];
 #pragma unroll
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int i0 = kCausal ? kt : 0;           // query tiles i >= kt see this key tile
   const int nq = p.n_tiles - i0;
 
-  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, 128);
+  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, kBwdEwThreads);
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
@@ -313,8 +315,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ element-wise
-    const int t = threadIdx.x;                            // key row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int t = quarter * 32 + lane;                    // key row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + kColS, tDp = tmem_base + lane_off + kColDp;
     const long long key = static_cast<long long>(kt) * kBwdTile + t;
     const float c = p.scale_log2;
@@ -326,24 +329,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // LSE (in log2 units) and D of the 128 queries of tile i; a query past
       // N gets LSE = +inf, so its P is 0.
       float* lv = vec + (it & 1) * 256;
-      const int qrow = i * kBwdTile + t;
-      lv[t] = qrow < p.N ? lse_h[qrow] * 1.4426950408889634f : INFINITY;
-      lv[128 + t] = qrow < p.N ? del_h[qrow] : 0.f;
-      ptx::named_bar_sync(1, 128);
+      if (half == 0) {
+        const int qrow = i * kBwdTile + t;
+        lv[t] = qrow < p.N ? lse_h[qrow] * 1.4426950408889634f : INFINITY;
+        lv[128 + t] = qrow < p.N ? del_h[qrow] : 0.f;
+      }
+      ptx::named_bar_sync(1, kBwdEwThreads);
       ptx::wait_bounded(bar(L::bSFull), it & 1, wd, kSiteBwdSFull);
       __syncwarp();
       ptx::tc_fence_after();
+      // this thread's 64 query columns of S^T and dP^T, 32 at a time
       const bool diag = kCausal && i == kt;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32], dpr[32];
-        ptx::tmem_ld32(tS + ch * 32, sr);
-        ptx::tmem_ld32(tDp + ch * 32, dpr);
+        ptx::tmem_ld32(tS + half * 64 + ch * 32, sr);
+        ptx::tmem_ld32(tDp + half * 64 + ch * 32, dpr);
         ptx::tmem_wait_ld();
-        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int qc = ch * 32 + e;                     // query column within the tile
+          const int qc = half * 64 + ch * 32 + e;         // query column within the tile
           float p0 = ptx::ex2(fmaf(__uint_as_float(sr[e]), c, -lv[qc]));
           float p1 = ptx::ex2(fmaf(__uint_as_float(sr[e + 1]), c, -lv[qc + 1]));
           if (diag) {                                     // key after the query: masked
@@ -352,23 +358,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const float d0 = p0 * (__uint_as_float(dpr[e]) - lv[128 + qc]);
           const float d1 = p1 * (__uint_as_float(dpr[e + 1]) - lv[128 + qc + 1]);
-          pk[e / 2] = ptx::pack2<kBf16>(p0, p1);
-          dk[e / 2] = ptx::pack2<kBf16>(d0, d1);
+          pk[ch * 16 + e / 2] = ptx::pack2<kBf16>(p0, p1);
+          dk[ch * 16 + e / 2] = ptx::pack2<kBf16>(d0, d1);
         }
-        ptx::tmem_st16(tS + ch * 16, pk);
-        ptx::tmem_st16(tDp + ch * 16, dk);
       }
+      // P^T and dS^T go to the first 64 columns of S^T and dP^T, which the
+      // other half's warps read: every load is done before any store.
+      ptx::named_bar_sync(2, kBwdEwThreads);
+      ptx::tmem_st16(tS + half * 32, pk);
+      ptx::tmem_st16(tS + half * 32 + 16, pk + 16);
+      ptx::tmem_st16(tDp + half * 32, dk);
+      ptx::tmem_st16(tDp + half * 32 + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bPFull));
     }
-    // dV_j and dK_j = scale * (dS^T Q) rows to global memory
+    // dV_j rows (warps 0-3) and dK_j = scale * (dS^T Q) rows (warps 4-7)
     ptx::wait_bounded(bar(L::bDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
     const long long row = static_cast<long long>(bh) * p.N + key;
-    store_acc_row<D, kBf16>(tmem_base + lane_off + kColAcc, 1.f, p.dv, row, key < p.N);
-    store_acc_row<D, kBf16>(tmem_base + lane_off + kColAcc + D, p.scale, p.dk, row, key < p.N);
+    if (half == 0)
+      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, 1.f, p.dv, row, key < p.N);
+    else
+      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
+                                  key < p.N);
   }
 
   ptx::tc_fence_before();
@@ -399,7 +413,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
   const int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
 
-  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, 128);
+  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, kBwdEwThreads);
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
@@ -441,8 +455,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ element-wise
-    const int t = threadIdx.x;                            // query row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int t = quarter * 32 + lane;                    // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + kColS, tDp = tmem_base + lane_off + kColDp;
     const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
     const bool q_in = qrow < p.N;
@@ -457,33 +472,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // keys past N, and on the diagonal tile keys after this query, are masked
       int lim = p.N - j * kBwdTile;
       if (kCausal && j == qt) lim = min(lim, t + 1);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      uint32_t dk[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32], dpr[32];
-        ptx::tmem_ld32(tS + ch * 32, sr);
-        ptx::tmem_ld32(tDp + ch * 32, dpr);
+        ptx::tmem_ld32(tS + half * 64 + ch * 32, sr);
+        ptx::tmem_ld32(tDp + half * 64 + ch * 32, dpr);
         ptx::tmem_wait_ld();
-        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int kc = ch * 32 + e;                     // key column within the tile
+          const int kc = half * 64 + ch * 32 + e;         // key column within the tile
           float p0 = ptx::ex2(fmaf(__uint_as_float(sr[e]), c, -lse2));
           float p1 = ptx::ex2(fmaf(__uint_as_float(sr[e + 1]), c, -lse2));
           if (kc >= lim) p0 = 0.f;
           if (kc + 1 >= lim) p1 = 0.f;
-          dk[e / 2] = ptx::pack2<kBf16>(p0 * (__uint_as_float(dpr[e]) - dl),
-                                        p1 * (__uint_as_float(dpr[e + 1]) - dl));
+          dk[ch * 16 + e / 2] = ptx::pack2<kBf16>(p0 * (__uint_as_float(dpr[e]) - dl),
+                                                  p1 * (__uint_as_float(dpr[e + 1]) - dl));
         }
-        ptx::tmem_st16(tS + ch * 16, dk);
       }
+      // dS goes to the first 64 columns of S, which the other half's warps
+      // read: every load is done before any store.
+      ptx::named_bar_sync(1, kBwdEwThreads);
+      ptx::tmem_st16(tS + half * 32, dk);
+      ptx::tmem_st16(tS + half * 32 + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bPFull));
     }
+    // dQ = scale * (dS K): each half of the warps writes half of the columns
     ptx::wait_bounded(bar(L::bDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
-    store_acc_row<D, kBf16>(tmem_base + lane_off + kColAcc, p.scale, p.dq, grow, q_in);
+    store_acc_cols<D, D / 2, kBf16>(tmem_base + lane_off + kColAcc, half * (D / 2), p.scale, p.dq,
+                                    grow, q_in);
   }
 
   ptx::tc_fence_before();
