@@ -2,8 +2,8 @@
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
 (``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
-``fa_bwd``, ``fa_strerror``, ``fa_status``, ``fa_set_watchdog_ns``,
-``fa_work_tiles``, ``fa_version``),
+``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
+``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``, ``fa_version``),
 under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
@@ -13,7 +13,7 @@ every call raises.
 and LSE (and, when asked, the balancing workspace) with PyTorch — device
 memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
 current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
-(dQ, dK, dV and the D scratch).
+(dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``.
 """
 import ctypes
 import math
@@ -40,7 +40,8 @@ FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
-           "fa_strerror", "fa_status", "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
+           "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
+           "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
 
 _lib = None
 
@@ -75,6 +76,10 @@ def load_library(path=None):
     lib.fa_fwd_static.restype = i
     lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_decode.restype = i
+    lib.fa_decode_workspace_size.argtypes = [i] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_decode_workspace_size.restype = i
     lib.fa_strerror.argtypes = [i]
     lib.fa_strerror.restype = ctypes.c_char_p
     lib.fa_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -139,6 +144,25 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, 
     return lib.fa_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout), _addr(dq),
                       _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(N), int(d),
                       int(bool(causal)), float(scale), int(dtype), _stream(stream))
+
+
+def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+              workspace_bytes, stream=None):
+    """Raw C call of split-KV decoding; tensors or integer addresses; returns the code."""
+    lib = load_library()
+    return lib.fa_decode(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                         int(Nq), int(Nk), int(d), int(bool(causal)), float(scale), int(dtype),
+                         _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_decode_workspace_size(B, H, Nq, Nk, d):
+    """Workspace bytes fa_decode needs for this shape on the current device."""
+    out = ctypes.c_size_t(0)
+    code = load_library().fa_decode_workspace_size(int(B), int(H), int(Nq), int(Nk), int(d),
+                                                   ctypes.byref(out))
+    if code:
+        raise FaError(code, "fa_decode_workspace_size")
+    return out.value
 
 
 def fa_fwd_workspace_size(B, H, N, d, causal):
@@ -269,3 +293,42 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=N
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def attention_decode(q, k, v, causal=False, scale=None, out=None, lse=None, workspace=None,
+                     stream=None):
+    """O, LSE of a few queries q [B, H, Nq, d] (Nq <= 16) against a cache
+    k, v [B, H, Nk, d] with the key axis split across the GPU (``fa_decode``).
+
+    ``causal``: query i sits at position Nk - Nq + i.  ``workspace``: a uint8
+    CUDA tensor of at least ``fa_decode_workspace_size`` bytes, or None to
+    allocate one.
+    """
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if not all(t.is_cuda and t.is_contiguous() for t in (q, k, v)):
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = dtype_code(q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = fa_decode_workspace_size(B, H, Nq, Nk, d)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = fa_decode(q, k, v, out, lse, B, H, Nq, Nk, d, causal, scale, code, workspace, ws_bytes,
+                   stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_decode")
+    return out, lse

@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_bwd_launch.cuh"
+#include "fa_decode_kernel.cuh"
 #include "fa_launch.cuh"
 
 namespace {
@@ -97,7 +98,7 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int BH, int N, int d, bool bf16)
 
 extern "C" {
 
-int fa_version(void) { return 102; }
+int fa_version(void) { return 103; }
 
 const char* fa_strerror(int code) {
   switch (code) {
@@ -328,6 +329,112 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   const cudaError_t e =
       (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
                 : fa::launch_bwd_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"
+
+namespace fa {
+cudaError_t launch_decode(const DecodeParams& p, void* o, float* lse, int d, bool bf16,
+                          cudaStream_t stream);
+}
+
+namespace {
+
+// Split of the key axis for fa_decode: enough CTAs for about two per SM.
+struct DecodePlan {
+  int splits = 0;
+  int tiles_per_split = 0;
+  size_t o_bytes = 0;     // partial outputs
+  size_t bytes = 0;       // whole workspace (partial outputs, then (m, l) pairs)
+};
+
+DecodePlan plan_decode(long long bh, int Nq, int Nk, int d, int sms) {
+  DecodePlan dp;
+  const int tiles = (Nk + fa::kDecTile - 1) / fa::kDecTile;
+  if (tiles == 0 || bh == 0) return dp;
+  long long want = (2ll * sms + bh - 1) / bh;
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  dp.tiles_per_split = static_cast<int>((tiles + want - 1) / want);
+  dp.splits = (tiles + dp.tiles_per_split - 1) / dp.tiles_per_split;
+  const size_t parts = static_cast<size_t>(bh) * dp.splits * Nq;
+  dp.o_bytes = (parts * d * sizeof(float) + 255) / 256 * 256;
+  dp.bytes = dp.o_bytes + (parts * 2 * sizeof(float) + 255) / 256 * 256;
+  return dp;
+}
+
+int decode_checks(int B, int H, int Nq, int Nk, int d, long long* bh) {
+  if (B < 0 || H < 0 || Nk < 0 || d <= 0) return FA_ERR_SHAPE;
+  if (Nq < 1 || Nq > fa::kDecMaxQ) return FA_ERR_SHAPE;
+  *bh = static_cast<long long>(B) * H;
+  if (*bh * Nq > INT_MAX || *bh * ((static_cast<long long>(Nk) + 127) / 128) > INT_MAX)
+    return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, size_t* bytes) {
+  if (!bytes) return FA_ERR_NULLPTR;
+  long long bh = 0;
+  const int rc = decode_checks(B, H, Nq, Nk, d, &bh);
+  if (rc != FA_OK) return rc;
+  *bytes = 0;
+  if (bh == 0 || Nk == 0) return FA_OK;
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  *bytes = plan_decode(bh, Nq, Nk, d, info->sms).bytes;
+  return FA_OK;
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, int causal, float scale, int dtype, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream) {
+  long long bh = 0;
+  const int rc = decode_checks(B, H, Nq, Nk, d, &bh);
+  if (rc != FA_OK) return rc;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0) return FA_OK;  // nothing to write
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+  const DecodePlan dp = plan_decode(bh, Nq, Nk, d, info->sms);
+  if (dp.bytes > 0) {
+    if (!workspace || workspace_bytes < dp.bytes) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  }
+  const bool bf16 = dtype == FA_BF16;
+  fa::DecodeParams p;
+  if (Nk > 0 && (!make_tmap(&p.tm_k, k, static_cast<int>(bh), Nk, d, bf16) ||
+                 !make_tmap(&p.tm_v, v, static_cast<int>(bh), Nk, d, bf16)))
+    return FA_ERR_TENSORMAP;
+  p.q = q;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = dp.bytes ? reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + dp.o_bytes)
+                       : nullptr;
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
+  p.BH = static_cast<int>(bh);
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.splits = dp.splits;
+  p.tiles_per_split = dp.tiles_per_split;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = fa::launch_decode(p, o, lse, d, bf16, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

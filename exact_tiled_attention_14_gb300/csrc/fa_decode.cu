@@ -1,0 +1,48 @@
+// fa_decode.cu — launches of the split-KV decoding kernels (both head widths).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "fa_decode_kernel.cuh"
+
+namespace fa {
+
+namespace {
+
+template <int D, bool kBf16>
+cudaError_t launch_decode_variant(const DecodeParams& p, void* o, float* lse, cudaStream_t stream) {
+  if (p.splits > 0) {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done.load() & bit)) {
+      e = cudaFuncSetAttribute(fa_decode_partial_kernel<D, kBf16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, DecSmem<D>::kAlloc);
+      if (e != cudaSuccess) return e;
+      done.fetch_or(bit);
+    }
+    fa_decode_partial_kernel<D, kBf16>
+        <<<p.BH * p.splits, kDecThreads, DecSmem<D>::kAlloc, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  fa_decode_combine_kernel<D, kBf16><<<p.BH * p.Nq, D, 0, stream>>>(p.part_o, p.part_ml, o, lse,
+                                                                    p.splits, p.Nq);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, void* o, float* lse, int d, bool bf16,
+                          cudaStream_t stream) {
+  if (d == 64)
+    return bf16 ? launch_decode_variant<64, true>(p, o, lse, stream)
+                : launch_decode_variant<64, false>(p, o, lse, stream);
+  return bf16 ? launch_decode_variant<128, true>(p, o, lse, stream)
+              : launch_decode_variant<128, false>(p, o, lse, stream);
+}
+
+}  // namespace fa

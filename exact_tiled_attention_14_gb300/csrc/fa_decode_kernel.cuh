@@ -1,0 +1,315 @@
+// fa_decode_kernel.cuh — split-KV attention for a few queries against a long
+// key/value cache (decoding), on the CUDA cores.
+//
+// With Nq <= 16 queries per head there is no square score matrix to avoid;
+// the work is bound by reading K and V from HBM, and a head alone cannot keep
+// every SM busy.  So the key axis is split across CTAs, each CTA streams its
+// key range tile by tile through shared memory (TMA, 128 keys per tile) and
+// keeps, per query, the online softmax state of its range: a running
+// maximum m, a running sum l and an unnormalised output.  A second kernel
+// combines the parts with the same rescale identity the online softmax
+// rests on — scale every part to the largest m, add, divide once ("FlashAttention:
+// The Matrix You Never Have to Write Down", section "What it doesn't solve":
+// decoding reads one query against a cached history, and Flash-Decoding
+// splits the key axis across parallel workers and combines partial results).
+//
+// Causal masking uses the decoding convention: query i of Nq sits at
+// position Nk - Nq + i, after the cached keys, and sees keys j <= that
+// position (first page, section "Build it", note on non-square causal
+// alignment: incremental decoding offsets the query positions by the cache
+// length).
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx_sm103.cuh"
+
+namespace fa {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecTile = 128;       // keys per tile
+constexpr int kDecMaxQ = 16;        // queries per head
+enum DecWaitSite : uint32_t { kSiteDecFull = 30 };
+
+struct DecodeParams {
+  CUtensorMap tm_k;     // [BH, Nk, d], boxes of 128 rows x 64 columns, 128-byte swizzle
+  CUtensorMap tm_v;
+  const void* q;        // [BH, Nq, d]
+  float* part_o;        // [BH, splits, Nq, d] unnormalised partial outputs
+  float2* part_ml;      // [BH, splits, Nq] (m in log2 units, l) of each part
+  unsigned int* status;
+  unsigned long long watchdog_cycles;
+  int BH;
+  int Nq;
+  int Nk;
+  int splits;           // CTAs per head
+  int tiles_per_split;  // key tiles of one split (the last may have fewer)
+  int causal;
+  float scale_log2;     // scale * log2(e)
+};
+
+template <int D>
+struct DecSmem {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kDecTile * D * 2;        // one K or V tile
+  static constexpr int kChunkBytes = kDecTile * 128;
+  static constexpr int kStages = (D == 128) ? 3 : 5;
+  static constexpr int kRing = 0;                         // [stage][K, V]
+  static constexpr int kQ = kRing + kStages * 2 * kTile;  // fp32 [16][D]
+  static constexpr int kS = kQ + kDecMaxQ * D * 4;        // fp32 scores [2 halves][16][128], then P [16][128]
+  static constexpr int kAlpha = kS + 2 * kDecMaxQ * kDecTile * 4;   // fp32 [16]
+  static constexpr int kRed = kAlpha + kDecMaxQ * 4;      // fp32 [256 threads][8] for the final reduction
+  static constexpr int kBar = kRed + kDecThreads * 8 * 4;
+  static constexpr int kMisc = kBar + 8 * kStages;        // abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// 8 consecutive values of row r, 16-byte piece j (of D/8) of a tile stored as
+// 64-column chunks with the 128-byte swizzle.
+template <int D, bool kBf16>
+__device__ __forceinline__ void load8(const uint8_t* tile, int r, int j, float* out) {
+  const int chunk = j >> 3, pc = j & 7;
+  const uint4 v = *reinterpret_cast<const uint4*>(tile + chunk * (kDecTile * 128) + r * 128 +
+                                                  ((pc ^ (r & 7)) << 4));
+  ptx::unpack2<kBf16>(v.x, out[0], out[1]);
+  ptx::unpack2<kBf16>(v.y, out[2], out[3]);
+  ptx::unpack2<kBf16>(v.z, out[4], out[5]);
+  ptx::unpack2<kBf16>(v.w, out[6], out[7]);
+}
+
+// One CTA per (split, batch*head): the online softmax over keys
+// [split * tiles_per_split * 128, ...) for every query of the head.
+//   phase A  scores: thread (key r, half h) dots its 64 (d = 128) or 32
+//            (d = 64) columns of K_r with every query; halves summed in phase B.
+//   phase B  softmax: warp w owns queries w and w + 8: tile maximum, new
+//            reference, rescale factor alpha, P = 2^(s*c - m), row sum.
+//   phase C  P V: thread (query, 8-column piece, key group) accumulates over
+//            the keys of its group; groups are summed once at the end.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    fa_decode_partial_kernel(const __grid_constant__ DecodeParams p) {
+  using L = DecSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw_base);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc);
+  const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % p.splits, bh = blockIdx.x / p.splits;
+  const int Nq = p.Nq;
+  const int n_tiles_all = (p.Nk + kDecTile - 1) / kDecTile;
+  const int t0 = split * p.tiles_per_split;
+  const int nt = max(0, min(p.tiles_per_split, n_tiles_all - t0));
+  float* q_s = reinterpret_cast<float*>(sgen + L::kQ);
+  float* s_s = reinterpret_cast<float*>(sgen + L::kS);
+  float* alpha_s = reinterpret_cast<float*>(sgen + L::kAlpha);
+  const float c = p.scale_log2;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < L::kStages; ++s) ptx::mbar_init(bar(s), 1);
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  // queries of this head, as fp32
+  {
+    const uint16_t* qg = static_cast<const uint16_t*>(p.q) + static_cast<size_t>(bh) * Nq * D;
+    for (int i = tid; i < Nq * D / 2; i += kDecThreads) {
+      float a, b;
+      ptx::unpack2<kBf16>(reinterpret_cast<const uint32_t*>(qg)[i], a, b);
+      q_s[2 * i] = a;
+      q_s[2 * i + 1] = b;
+    }
+  }
+  __syncthreads();
+  auto issue = [&](int it) {   // TMA loads of tile t0 + it into slot it % kStages
+    const int slot = it % L::kStages;
+    const uint32_t dst = sbase + L::kRing + slot * 2 * L::kTile;
+    ptx::mbar_arrive_expect_tx(bar(slot), 2 * L::kTile);
+    for (int ch = 0; ch < L::kChunks; ++ch) {
+      ptx::tma_load_3d(dst + ch * L::kChunkBytes, &p.tm_k, bar(slot), ch * 64, (t0 + it) * kDecTile, bh);
+      ptx::tma_load_3d(dst + L::kTile + ch * L::kChunkBytes, &p.tm_v, bar(slot), ch * 64,
+                       (t0 + it) * kDecTile, bh);
+    }
+  };
+  int issued = 0;   // tiles whose loads thread 0 has issued
+  if (tid == 0)
+    for (; issued < nt && issued < L::kStages; ++issued) issue(issued);
+
+  // phase-C work split: 8-column piece, query, key group
+  constexpr int kPieces = D / 8;
+  int groups = kDecThreads / (kPieces * Nq);   // key groups per query (power of two below)
+  groups = groups >= 16 ? 16 : groups >= 8 ? 8 : groups >= 4 ? 4 : groups >= 2 ? 2 : 1;
+  const int piece = tid % kPieces;
+  const int qc = (tid / kPieces) / groups;     // query of this thread in phase C
+  const int kg = (tid / kPieces) % groups;     // key group
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  // softmax state of queries w and w + 8 (held by every lane of warp w)
+  float m2[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  // phase-A mapping: key row r, column half h
+  const int r = tid & 127, h = tid >> 7;
+  constexpr int kMyPieces = kPieces / 2;
+  bool alive = true;
+  for (int it = 0; it < nt; ++it) {
+    const int slot = it % L::kStages;
+    alive = ptx::wait_bounded(bar(slot), (it / L::kStages) & 1, wd, kSiteDecFull) && alive;
+    const uint8_t* kt = sgen + L::kRing + slot * 2 * L::kTile;
+    const uint8_t* vt = kt + L::kTile;
+    const int key0 = (t0 + it) * kDecTile;
+    // ---- phase A: partial dots of key r with every query over my columns
+    {
+      float sacc[kDecMaxQ];
+#pragma unroll
+      for (int q = 0; q < kDecMaxQ; ++q) sacc[q] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kMyPieces; ++jj) {
+        const int j = h * kMyPieces + jj;
+        float kv[8];
+        load8<D, kBf16>(kt, r, j, kv);
+#pragma unroll
+        for (int q = 0; q < kDecMaxQ; ++q) {
+          if (q < Nq) {
+            const float4 a = *reinterpret_cast<const float4*>(q_s + q * D + j * 8);
+            const float4 b = *reinterpret_cast<const float4*>(q_s + q * D + j * 8 + 4);
+            sacc[q] = fmaf(a.x, kv[0], fmaf(a.y, kv[1], fmaf(a.z, kv[2], fmaf(a.w, kv[3],
+                      fmaf(b.x, kv[4], fmaf(b.y, kv[5], fmaf(b.z, kv[6], fmaf(b.w, kv[7], sacc[q]))))))));
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kDecMaxQ; ++q)
+        if (q < Nq) s_s[(h * kDecMaxQ + q) * kDecTile + r] = sacc[q];
+    }
+    __syncthreads();
+    // ---- phase B: online softmax per query (warp w: queries w, w + 8)
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int q = warp + 8 * k2;
+      if (q < Nq) {
+        const long long pos = static_cast<long long>(p.Nk) - Nq + q;   // causal: last keys visible
+        float sv[4];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kr = lane + 32 * e;
+          const long long key = key0 + kr;
+          float s = s_s[q * kDecTile + kr] + s_s[(kDecMaxQ + q) * kDecTile + kr];
+          const bool vis = key < p.Nk && (!p.causal || key <= pos);
+          sv[e] = vis ? s * c : -INFINITY;
+          tmax = fmaxf(tmax, sv[e]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        const float mnew = fmaxf(m2[k2], tmax);
+        // no visible key yet: keep the reference at 0 so -inf - (-inf) never occurs
+        const float ref = (mnew == -INFINITY) ? 0.f : mnew;
+        const float alpha = (m2[k2] == -INFINITY) ? 0.f : ptx::ex2(m2[k2] - ref);
+        float lsum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pv = ptx::ex2(sv[e] - ref);
+          s_s[q * kDecTile + lane + 32 * e] = pv;   // P over the first score half
+          lsum += pv;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        l[k2] = l[k2] * alpha + lsum;
+        m2[k2] = mnew;
+        if (lane == 0) alpha_s[q] = alpha;
+      }
+    }
+    __syncthreads();
+    // ---- phase C: O(q, piece) = alpha * O + sum over my key group of P V
+    if (qc < Nq) {
+      const float a = alpha_s[qc];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= a;
+      const float* prow = s_s + qc * kDecTile;
+#pragma unroll 4
+      for (int kr = kg; kr < kDecTile; kr += groups) {
+        const float pv = prow[kr];
+        float vv[8];
+        load8<D, kBf16>(vt, kr, piece, vv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pv, vv[e], acc[e]);
+      }
+    }
+    __syncthreads();   // the slot and the score buffer are free again
+    if (tid == 0 && alive && it + L::kStages < nt) issue(issued++);
+  }
+  // After an aborted wait, loads may still be in flight: let them land
+  // before the CTA exits (bounded).
+  if (tid == 0 && !alive)
+    for (int it = 0; it < issued; ++it)
+      ptx::wait_drain(bar(it % L::kStages), (it / L::kStages) & 1, 200000000ull);
+
+  // ---- sum the key groups and write this part: unnormalised O, (m, l)
+  float* red = reinterpret_cast<float*>(sgen + L::kRed);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[tid * 8 + e] = acc[e];
+  __syncthreads();
+  const size_t part = (static_cast<size_t>(bh) * p.splits + split) * Nq;
+  if (qc < Nq && kg == 0) {
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
+    for (int g = 0; g < groups; ++g) {
+      const int src = (qc * groups + g) * kPieces + piece;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] += red[src * 8 + e];
+    }
+    float4* dst = reinterpret_cast<float4*>(p.part_o + (part + qc) * D + piece * 8);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < 2; ++k2) {
+    const int q = warp + 8 * k2;
+    if (q < Nq && lane == 0) p.part_ml[part + q] = make_float2(m2[k2], l[k2]);
+  }
+}
+
+// One block of D threads per (batch*head, query): combine the parts, thread
+// c owning output column c.  Parts with no visible key (l = 0) are skipped;
+// a query with none at all gets O = 0 and LSE = -inf.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(D) fa_decode_combine_kernel(const float* __restrict__ part_o,
+                                                              const float2* __restrict__ part_ml,
+                                                              void* o, float* lse, int splits,
+                                                              int Nq) {
+  const int c = threadIdx.x;
+  const int q = blockIdx.x % Nq, bh = blockIdx.x / Nq;
+  float m = -INFINITY, lt = 0.f, acc = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t part = (static_cast<size_t>(bh) * splits + s) * Nq + q;
+    const float2 ml = part_ml[part];
+    if (!(ml.y > 0.f)) continue;
+    const float ov = part_o[part * D + c];
+    if (ml.x > m) {           // larger maximum: move the reference
+      const float a = (m == -INFINITY) ? 0.f : ptx::ex2(m - ml.x);
+      acc = acc * a + ov;
+      lt = lt * a + ml.y;
+      m = ml.x;
+    } else {
+      const float f = ptx::ex2(ml.x - m);
+      acc += f * ov;
+      lt += f * ml.y;
+    }
+  }
+  const size_t row = static_cast<size_t>(bh) * Nq + q;
+  const float out = lt > 0.f ? acc / lt : 0.f;
+  const uint32_t pk = ptx::pack2<kBf16>(out, 0.f);   // the value in the low half
+  static_cast<uint16_t*>(o)[row * D + c] = static_cast<uint16_t>(pk & 0xffffu);
+  if (c == 0) lse[row] = lt > 0.f ? (m + ptx::lg2(lt)) * 0.693147180559945309f : -INFINITY;
+}
+
+}  // namespace fa

@@ -176,6 +176,51 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            int B, int H, int N, int d, int causal, float scale, int dtype,
            cudaStream_t stream);
 
+/*
+ * fa_decode — attention of a few new queries against a long key/value cache
+ * (decoding), with the key axis split across the GPU.
+ *
+ * With one (or a few) queries against N cached keys there is no square
+ * score matrix to avoid; the call is bound by reading K and V and by finding
+ * parallelism, so the key axis is split across many CTAs, each keeping the
+ * online-softmax state (m, l, unnormalised O) of its key range, and the
+ * parts are combined with the rescale identity: each part scaled to the
+ * largest m, summed, divided once ("FlashAttention: The Matrix You Never
+ * Have to Write Down", section "What it doesn't solve", on decoding and on
+ * Flash-Decoding splitting the key axis and combining partial results).
+ *
+ *   q        : device pointer, [B, H, Nq, d], 1 <= Nq <= 16, 16-byte aligned.
+ *   k, v     : device pointers, [B, H, Nk, d], the cache, 16-byte aligned
+ *              (may be NULL when Nk == 0).
+ *   o        : device pointer, [B, H, Nq, d], written in the storage dtype.
+ *   lse      : device pointer, [B, H, Nq] float32, natural-log LSE.
+ *   causal   : nonzero: query i sits at position Nk - Nq + i, after the
+ *              cached keys, and sees keys j <= that position (the decoding
+ *              convention: query positions offset by the cache length;
+ *              section "Build it", note on non-square causal alignment).
+ *   workspace, workspace_bytes : device buffer, 256-byte aligned, at least
+ *              fa_decode_workspace_size bytes (partial results), owned by
+ *              the caller; contents need no initialisation.  Calls sharing
+ *              one workspace must not overlap on the GPU.
+ *   scale, dtype, stream : as fa_fwd.
+ * Nk == 0 writes O = 0 and LSE = -inf (the pages' empty-key policy), and so
+ * does a causal query whose position is negative (Nq > Nk).
+ * Errors: FA_ERR_SHAPE (also for Nq outside 1..16), FA_ERR_UNSUPPORTED_D,
+ * FA_ERR_DTYPE, FA_ERR_SCALE, then B*H == 0 returns FA_OK, then
+ * FA_ERR_NULLPTR, FA_ERR_ALIGN, FA_ERR_DEVICE, FA_ERR_WORKSPACE,
+ * FA_ERR_TENSORMAP, FA_ERR_LAUNCH.
+ */
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int H, int Nq, int Nk, int d, int causal, float scale, int dtype,
+              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_decode_workspace_size — bytes of workspace fa_decode needs for this
+ * shape on the current device (0 when Nk == 0 or B*H == 0).  Returns
+ * FA_ERR_NULLPTR, FA_ERR_SHAPE, FA_ERR_UNSUPPORTED_D or FA_ERR_DEVICE.
+ */
+int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, size_t *bytes);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char *fa_strerror(int code);
 

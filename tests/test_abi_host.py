@@ -168,3 +168,20 @@ def test_bwd_host_errors(lib):
     import torch
     if not torch.cuda.is_available():
         assert fa.fa_bwd(**call) == fa.FA_ERR_DEVICE
+
+
+def test_decode_host_errors(lib):
+    """fa_decode checks shapes (1 <= Nq <= 16), width, dtype, scale, pointers."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=2, H=4, Nq=1, Nk=5000, d=128,
+                causal=0, scale=0.1, dtype=fa.FA_BF16, workspace=FAKE * 16, workspace_bytes=1 << 30)
+    cases = [(dict(Nq=0), fa.FA_ERR_SHAPE), (dict(Nq=17), fa.FA_ERR_SHAPE),
+             (dict(Nk=-1), fa.FA_ERR_SHAPE), (dict(d=32), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dtype=9), fa.FA_ERR_DTYPE), (dict(scale=float("nan")), fa.FA_ERR_SCALE),
+             (dict(B=0, q=None), fa.FA_OK), (dict(o=None), fa.FA_ERR_NULLPTR),
+             (dict(k=None), fa.FA_ERR_NULLPTR), (dict(v=FAKE + 8), fa.FA_ERR_ALIGN)]
+    for args, code in cases:
+        assert fa.fa_decode(**{**call, **args}) == code, args
+    import ctypes as C
+    out = C.c_size_t(5)
+    assert lib.fa_decode_workspace_size(1, 1, 17, 10, 64, C.byref(out)) == fa.FA_ERR_SHAPE
+    assert lib.fa_decode_workspace_size(1, 1, 4, 0, 64, C.byref(out)) == fa.FA_OK and out.value == 0
