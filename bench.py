@@ -21,6 +21,9 @@ timed region), ``clocks`` (nvidia-smi samples during the timed region) and
 ``--impl reference`` times the float64 oracle on the host cores instead
 (rank 0 only), on bounded samples of the same workload.
 
+``--pass decode`` times split-KV decoding (``fa_decode``) on a decoding
+workload (GB/s of K/V read against the measured HBM copy bandwidth).
+
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
 call (three kernels) with the forward's O and LSE and a seeded dO resident
 on the device; FLOPs are 2.5x the forward's (five matmuls against two).
@@ -50,6 +53,7 @@ import seeded_inputs  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_WORKLOAD = "b1_h16_n4096_d128_bf16"
 METRIC = "attention fwd TFLOP/s (causal halved) and % of GB300 dense BF16 tensor peak"
+METRIC_DEC = "attention decode (split-KV) K/V read GB/s and % of GB300 HBM copy bandwidth"
 METRIC_BWD = ("attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved) and % of GB300 "
               "dense BF16 tensor peak")
 FALLBACK_PEAK_TFLOPS = 1900.0
@@ -654,6 +658,138 @@ def run_ours_bwd(args, w):
     return 0
 
 
+def run_ours_decode(args, w):
+    """Split-KV decoding: one step = one fa_decode call (partial and combine
+    kernels) of the workload's queries against its cache, resident in device
+    memory.  HBM-bound: the metric is the K/V bytes read per second."""
+    import exact_tiled_attention_14_gb300 as fa
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+    sampler = ClockSampler(local).start()
+    B, H, Nq, Nk, d = w["B"], w["H"], w["Nq"], w["Nk"], w["d"]
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, w["dtype"], seed=w["seed"])
+    kv_bytes = 2 * B * H * Nk * d * 2
+    io = dict(h2d=B * H * Nq * d * 2 + kv_bytes, d2h=B * H * Nq * (d * 2 + 4))
+    per_replica = io["h2d"] + io["d2h"]
+    replicas = 1 if per_replica > 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_replica)) + 1
+    replicas = min(replicas, 64)
+    stream = torch.cuda.current_stream(device)
+    code = fa.dtype_code(q.dtype)
+    ws_bytes = fa.fa_decode_workspace_size(B, H, Nq, Nk, d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    bufs = []
+    for _ in range(replicas):
+        dq_, dk_, dv_ = (t.to(device) for t in (q, k, v))
+        bufs.append((dq_, dk_, dv_, torch.empty_like(dq_),
+                     torch.empty((B, H, Nq), dtype=torch.float32, device=device)))
+
+    def step(i):
+        dq_, dk_, dv_, o, lse = bufs[i % replicas]
+        rc = fa.fa_decode(dq_, dk_, dv_, o, lse, B, H, Nq, Nk, d, w["causal"], w["scale"], code,
+                          ws, ws_bytes, stream)
+        if rc:
+            raise fa.FaError(rc, "fa_decode")
+
+    t_warm = time.time()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"warmup status {word:#x}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    t1 = time.time()
+    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
+    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
+                             world, device)
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"timed status {word:#x}")
+
+    # end to end: pinned host q and cache in, o and lse out
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    dq_, dk_, dv_, o, lse = bufs[0]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        fa.attention_decode(dq_, dk_, dv_, causal=w["causal"], scale=w["scale"], out=o, lse=lse,
+                            workspace=ws, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1, fallback_window=(t_warm, t1))
+    if rank != 0:
+        return 0
+    gbs = lambda ms: world * kv_bytes / (ms * 1e-3) / 1e9   # noqa: E731
+    peak, src = measured_hbm()
+    line = {
+        "metric": METRIC_DEC, "value": world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "pass": "decode", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
+                   "d": d, "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
+                   "entry": "fa_decode", "parallelism": "single GPU" if world == 1 else f"replicas x{world}",
+                   "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
+                          if replicas > 1 else "cache larger than L2")},
+        "roofline": {"bound": "hbm", "achieved": gbs(kern_ms), "peak": peak, "unit": "GB/s",
+                     "frac": gbs(kern_ms) / peak, "peak_source": src, "kernel_ms": kern_ms,
+                     "bytes_per_launch": kv_bytes,
+                     "scope": "one fa_decode call: split-KV partial and combine kernels",
+                     "traffic": None, "traffic_note": "no ncu DRAM capture of the decode kernels yet"},
+        "e2e": {"value": gbs(e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
+                "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "gpu": torch.cuda.get_device_name(device),
+    }
+    print(json.dumps(line), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(json.dumps(line) + "\n")
+    return 0
+
+
+def measured_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["hbm_gbs"]), "measured HBM copy"
+    except (OSError, ValueError, KeyError, TypeError):
+        return 6800.0, "fallback"
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -672,11 +808,25 @@ def main(argv=None):
     ap.add_argument("--split", action="store_true",
                     help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="time the forward pass (default) or the backward pass (fa_bwd)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode"], default="fwd",
+                    help="time the forward pass (default), the backward pass (fa_bwd) or "
+                         "split-KV decoding (fa_decode; --workload names a decoding workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.pass_ == "decode":
+        name = args.workload if args.workload != DEFAULT_WORKLOAD else \
+            seeded_inputs.DECODE_WORKLOADS[-1]["name"]
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the decoding pass has no reference arm; the oracle checks it in tests"}))
+            return 0
+        wd = seeded_inputs.decode_workload(name)
+        if args.batch is not None or args.heads is not None:
+            wd["B"] = args.batch if args.batch is not None else wd["B"]
+            wd["H"] = args.heads if args.heads is not None else wd["H"]
+            wd["name"] = f"{wd['name']}@B{wd['B']}H{wd['H']}"
+        return run_ours_decode(args, wd)
     w = seeded_inputs.workload(args.workload)
     if args.batch is not None or args.heads is not None:
         w["B"] = args.batch if args.batch is not None else w["B"]

@@ -10,23 +10,34 @@ namespace fa {
 
 namespace {
 
+template <int D, int NQ, bool kBf16>
+cudaError_t launch_partial(const DecodeParams& p, cudaStream_t stream) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done.load() & bit)) {
+    e = cudaFuncSetAttribute(fa_decode_partial_kernel<D, NQ, kBf16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, DecSmem<D, NQ>::kAlloc);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit);
+  }
+  fa_decode_partial_kernel<D, NQ, kBf16>
+      <<<p.BH * p.splits, kDecThreads, DecSmem<D, NQ>::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// The partial kernel compiled for the smallest query-slot count >= Nq.
 template <int D, bool kBf16>
 cudaError_t launch_decode_variant(const DecodeParams& p, void* o, float* lse, cudaStream_t stream) {
   if (p.splits > 0) {
-    static std::atomic<uint64_t> done{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(done.load() & bit)) {
-      e = cudaFuncSetAttribute(fa_decode_partial_kernel<D, kBf16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, DecSmem<D>::kAlloc);
-      if (e != cudaSuccess) return e;
-      done.fetch_or(bit);
-    }
-    fa_decode_partial_kernel<D, kBf16>
-        <<<p.BH * p.splits, kDecThreads, DecSmem<D>::kAlloc, stream>>>(p);
-    e = cudaGetLastError();
+    cudaError_t e;
+    if (p.Nq <= 1) e = launch_partial<D, 1, kBf16>(p, stream);
+    else if (p.Nq <= 2) e = launch_partial<D, 2, kBf16>(p, stream);
+    else if (p.Nq <= 4) e = launch_partial<D, 4, kBf16>(p, stream);
+    else if (p.Nq <= 8) e = launch_partial<D, 8, kBf16>(p, stream);
+    else e = launch_partial<D, 16, kBf16>(p, stream);
     if (e != cudaSuccess) return e;
   }
   fa_decode_combine_kernel<D, kBf16><<<p.BH * p.Nq, D, 0, stream>>>(p.part_o, p.part_ml, o, lse,

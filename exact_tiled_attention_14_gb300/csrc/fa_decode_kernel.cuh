@@ -27,7 +27,7 @@
 
 namespace fa {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 512;
 constexpr int kDecTile = 128;       // keys per tile
 constexpr int kDecMaxQ = 16;        // queries per head
 enum DecWaitSite : uint32_t { kSiteDecFull = 30 };
@@ -49,27 +49,28 @@ struct DecodeParams {
   float scale_log2;     // scale * log2(e)
 };
 
-template <int D>
+// NQ: query slots compiled in (1, 2, 4, 8 or 16 >= Nq; the extra slots idle).
+template <int D, int NQ>
 struct DecSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kDecTile * D * 2;        // one K or V tile
   static constexpr int kChunkBytes = kDecTile * 128;
-  static constexpr int kStages = (D == 128) ? 3 : 5;
-  static constexpr int kRing = 0;                         // [stage][K, V]
-  static constexpr int kQ = kRing + kStages * 2 * kTile;  // fp32 [16][D]
-  static constexpr int kS = kQ + kDecMaxQ * D * 4;        // fp32 scores [2 halves][16][128], then P [16][128]
-  static constexpr int kAlpha = kS + 2 * kDecMaxQ * kDecTile * 4;   // fp32 [16]
-  static constexpr int kRed = kAlpha + kDecMaxQ * 4;      // fp32 [256 threads][8] for the final reduction
-  static constexpr int kBar = kRed + kDecThreads * 8 * 4;
+  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static constexpr int kRing = 0;                         // [stage][K, V]; reused for the final sum
+  static constexpr int kQ = kRing + kStages * 2 * kTile;  // fp32 [NQ][D]
+  static constexpr int kS = kQ + NQ * D * 4;              // fp32 scores, then P: [NQ][128]
+  static constexpr int kAlpha = kS + NQ * kDecTile * 4;   // fp32 [NQ]
+  static constexpr int kBar = (kAlpha + NQ * 4 + 15) / 16 * 16;
   static constexpr int kMisc = kBar + 8 * kStages;        // abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget");
+  static_assert(kDecThreads * 8 * 4 <= kStages * 2 * kTile, "final sum fits in the ring");
 };
 
 // 8 consecutive values of row r, 16-byte piece j (of D/8) of a tile stored as
 // 64-column chunks with the 128-byte swizzle.
-template <int D, bool kBf16>
+template <bool kBf16>
 __device__ __forceinline__ void load8(const uint8_t* tile, int r, int j, float* out) {
   const int chunk = j >> 3, pc = j & 7;
   const uint4 v = *reinterpret_cast<const uint4*>(tile + chunk * (kDecTile * 128) + r * 128 +
@@ -82,16 +83,17 @@ __device__ __forceinline__ void load8(const uint8_t* tile, int r, int j, float* 
 
 // One CTA per (split, batch*head): the online softmax over keys
 // [split * tiles_per_split * 128, ...) for every query of the head.
-//   phase A  scores: thread (key r, half h) dots its 64 (d = 128) or 32
-//            (d = 64) columns of K_r with every query; halves summed in phase B.
-//   phase B  softmax: warp w owns queries w and w + 8: tile maximum, new
-//            reference, rescale factor alpha, P = 2^(s*c - m), row sum.
+//   phase A  scores: four consecutive threads share key r, each dotting a
+//            quarter of its columns with every query (two-lane fp32 FMAs),
+//            summed with two shuffles.
+//   phase B  softmax: warp w owns query w: tile maximum, new reference,
+//            rescale factor alpha, P = 2^(s*c - m), row sum.
 //   phase C  P V: thread (query, 8-column piece, key group) accumulates over
 //            the keys of its group; groups are summed once at the end.
-template <int D, bool kBf16>
+template <int D, int NQ, bool kBf16>
 __global__ void __launch_bounds__(kDecThreads, 1)
     fa_decode_partial_kernel(const __grid_constant__ DecodeParams p) {
-  using L = DecSmem<D>;
+  using L = DecSmem<D, NQ>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -117,12 +119,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
-  // queries of this head, as fp32
+  // queries of this head, as fp32 (slots past Nq are zero)
   {
-    const uint16_t* qg = static_cast<const uint16_t*>(p.q) + static_cast<size_t>(bh) * Nq * D;
-    for (int i = tid; i < Nq * D / 2; i += kDecThreads) {
-      float a, b;
-      ptx::unpack2<kBf16>(reinterpret_cast<const uint32_t*>(qg)[i], a, b);
+    const uint32_t* qg = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) +
+                                                           static_cast<size_t>(bh) * Nq * D);
+    for (int i = tid; i < NQ * D / 2; i += kDecThreads) {
+      float a = 0.f, b = 0.f;
+      if (i < Nq * D / 2) ptx::unpack2<kBf16>(qg[i], a, b);
       q_s[2 * i] = a;
       q_s[2 * i + 1] = b;
     }
@@ -142,22 +145,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (tid == 0)
     for (; issued < nt && issued < L::kStages; ++issued) issue(issued);
 
-  // phase-C work split: 8-column piece, query, key group
-  constexpr int kPieces = D / 8;
-  int groups = kDecThreads / (kPieces * Nq);   // key groups per query (power of two below)
-  groups = groups >= 16 ? 16 : groups >= 8 ? 8 : groups >= 4 ? 4 : groups >= 2 ? 2 : 1;
+  // phase-A mapping: key row r, column quarter qd
+  const int r = tid >> 2, qd = tid & 3;
+  constexpr int kPieces = D / 8;              // 16-byte pieces per row
+  constexpr int kMyPieces = kPieces / 4;
+  // phase-C mapping: 8-column piece, query, key group
+  constexpr int kGroupsAll = kDecThreads / kPieces;
+  constexpr int kGroups = kGroupsAll / NQ;    // key groups per query
   const int piece = tid % kPieces;
-  const int qc = (tid / kPieces) / groups;     // query of this thread in phase C
-  const int kg = (tid / kPieces) % groups;     // key group
+  const int qc = (tid / kPieces) / kGroups;
+  const int kg = (tid / kPieces) % kGroups;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  // softmax state of queries w and w + 8 (held by every lane of warp w)
-  float m2[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  // softmax state of query `warp` (held by every lane of warp w < NQ)
+  float m2 = -INFINITY, l = 0.f;
 
-  // phase-A mapping: key row r, column half h
-  const int r = tid & 127, h = tid >> 7;
-  constexpr int kMyPieces = kPieces / 2;
   bool alive = true;
   for (int it = 0; it < nt; ++it) {
     const int slot = it % L::kStages;
@@ -165,67 +168,70 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint8_t* kt = sgen + L::kRing + slot * 2 * L::kTile;
     const uint8_t* vt = kt + L::kTile;
     const int key0 = (t0 + it) * kDecTile;
-    // ---- phase A: partial dots of key r with every query over my columns
+    // ---- phase A
     {
-      float sacc[kDecMaxQ];
+      uint64_t sacc[NQ];
 #pragma unroll
-      for (int q = 0; q < kDecMaxQ; ++q) sacc[q] = 0.f;
+      for (int q = 0; q < NQ; ++q) sacc[q] = ptx::f2_pack(0.f, 0.f);
 #pragma unroll
       for (int jj = 0; jj < kMyPieces; ++jj) {
-        const int j = h * kMyPieces + jj;
+        const int j = qd * kMyPieces + jj;
         float kv[8];
-        load8<D, kBf16>(kt, r, j, kv);
+        load8<kBf16>(kt, r, j, kv);
+        const uint64_t k01 = ptx::f2_pack(kv[0], kv[1]), k23 = ptx::f2_pack(kv[2], kv[3]);
+        const uint64_t k45 = ptx::f2_pack(kv[4], kv[5]), k67 = ptx::f2_pack(kv[6], kv[7]);
 #pragma unroll
-        for (int q = 0; q < kDecMaxQ; ++q) {
-          if (q < Nq) {
-            const float4 a = *reinterpret_cast<const float4*>(q_s + q * D + j * 8);
-            const float4 b = *reinterpret_cast<const float4*>(q_s + q * D + j * 8 + 4);
-            sacc[q] = fmaf(a.x, kv[0], fmaf(a.y, kv[1], fmaf(a.z, kv[2], fmaf(a.w, kv[3],
-                      fmaf(b.x, kv[4], fmaf(b.y, kv[5], fmaf(b.z, kv[6], fmaf(b.w, kv[7], sacc[q]))))))));
-          }
+        for (int q = 0; q < NQ; ++q) {
+          const uint64_t* qp = reinterpret_cast<const uint64_t*>(q_s + q * D + j * 8);
+          sacc[q] = ptx::ffma2(k01, qp[0], sacc[q]);
+          sacc[q] = ptx::ffma2(k23, qp[1], sacc[q]);
+          sacc[q] = ptx::ffma2(k45, qp[2], sacc[q]);
+          sacc[q] = ptx::ffma2(k67, qp[3], sacc[q]);
         }
       }
 #pragma unroll
-      for (int q = 0; q < kDecMaxQ; ++q)
-        if (q < Nq) s_s[(h * kDecMaxQ + q) * kDecTile + r] = sacc[q];
+      for (int q = 0; q < NQ; ++q) {
+        float a, b;
+        ptx::f2_unpack(sacc[q], a, b);
+        float sum = a + b;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (qd == 0) s_s[q * kDecTile + r] = sum;
+      }
     }
     __syncthreads();
-    // ---- phase B: online softmax per query (warp w: queries w, w + 8)
+    // ---- phase B: online softmax of query `warp`
+    if (warp < NQ && warp < Nq) {
+      const int q = warp;
+      const long long pos = static_cast<long long>(p.Nk) - Nq + q;   // causal: last keys visible
+      float sv[4];
+      float tmax = -INFINITY;
 #pragma unroll
-    for (int k2 = 0; k2 < 2; ++k2) {
-      const int q = warp + 8 * k2;
-      if (q < Nq) {
-        const long long pos = static_cast<long long>(p.Nk) - Nq + q;   // causal: last keys visible
-        float sv[4];
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kr = lane + 32 * e;
-          const long long key = key0 + kr;
-          float s = s_s[q * kDecTile + kr] + s_s[(kDecMaxQ + q) * kDecTile + kr];
-          const bool vis = key < p.Nk && (!p.causal || key <= pos);
-          sv[e] = vis ? s * c : -INFINITY;
-          tmax = fmaxf(tmax, sv[e]);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-        const float mnew = fmaxf(m2[k2], tmax);
-        // no visible key yet: keep the reference at 0 so -inf - (-inf) never occurs
-        const float ref = (mnew == -INFINITY) ? 0.f : mnew;
-        const float alpha = (m2[k2] == -INFINITY) ? 0.f : ptx::ex2(m2[k2] - ref);
-        float lsum = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pv = ptx::ex2(sv[e] - ref);
-          s_s[q * kDecTile + lane + 32 * e] = pv;   // P over the first score half
-          lsum += pv;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-        l[k2] = l[k2] * alpha + lsum;
-        m2[k2] = mnew;
-        if (lane == 0) alpha_s[q] = alpha;
+      for (int e = 0; e < 4; ++e) {
+        const int kr = lane + 32 * e;
+        const long long key = key0 + kr;
+        const bool vis = key < p.Nk && (!p.causal || key <= pos);
+        sv[e] = vis ? s_s[q * kDecTile + kr] * c : -INFINITY;
+        tmax = fmaxf(tmax, sv[e]);
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+      const float mnew = fmaxf(m2, tmax);
+      // no visible key yet: keep the reference at 0 so -inf - (-inf) never occurs
+      const float ref = (mnew == -INFINITY) ? 0.f : mnew;
+      const float alpha = (m2 == -INFINITY) ? 0.f : ptx::ex2(m2 - ref);
+      float lsum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pv = ptx::ex2(sv[e] - ref);
+        s_s[q * kDecTile + lane + 32 * e] = pv;
+        lsum += pv;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      l = l * alpha + lsum;
+      m2 = mnew;
+      if (lane == 0) alpha_s[q] = alpha;
     }
     __syncthreads();
     // ---- phase C: O(q, piece) = alpha * O + sum over my key group of P V
@@ -234,11 +240,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] *= a;
       const float* prow = s_s + qc * kDecTile;
-#pragma unroll 4
-      for (int kr = kg; kr < kDecTile; kr += groups) {
+#pragma unroll
+      for (int kr = kg; kr < kDecTile; kr += kGroups) {
         const float pv = prow[kr];
         float vv[8];
-        load8<D, kBf16>(vt, kr, piece, vv);
+        load8<kBf16>(vt, kr, piece, vv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(pv, vv[e], acc[e]);
       }
@@ -247,13 +253,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (tid == 0 && alive && it + L::kStages < nt) issue(issued++);
   }
   // After an aborted wait, loads may still be in flight: let them land
-  // before the CTA exits (bounded).
+  // before the ring is reused and the CTA exits (bounded).
   if (tid == 0 && !alive)
     for (int it = 0; it < issued; ++it)
       ptx::wait_drain(bar(it % L::kStages), (it / L::kStages) & 1, 200000000ull);
+  __syncthreads();
 
-  // ---- sum the key groups and write this part: unnormalised O, (m, l)
-  float* red = reinterpret_cast<float*>(sgen + L::kRed);
+  // ---- sum the key groups (in the now idle ring) and write this part
+  float* red = reinterpret_cast<float*>(sgen + L::kRing);
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[tid * 8 + e] = acc[e];
   __syncthreads();
@@ -262,8 +269,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     float o[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = 0.f;
-    for (int g = 0; g < groups; ++g) {
-      const int src = (qc * groups + g) * kPieces + piece;
+    for (int g = 0; g < kGroups; ++g) {
+      const int src = (qc * kGroups + g) * kPieces + piece;
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] += red[src * 8 + e];
     }
@@ -271,11 +278,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     dst[0] = make_float4(o[0], o[1], o[2], o[3]);
     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
   }
-#pragma unroll
-  for (int k2 = 0; k2 < 2; ++k2) {
-    const int q = warp + 8 * k2;
-    if (q < Nq && lane == 0) p.part_ml[part + q] = make_float2(m2[k2], l[k2]);
-  }
+  if (warp < NQ && warp < Nq && lane == 0) p.part_ml[part + warp] = make_float2(m2, l);
 }
 
 // One block of D threads per (batch*head, query): combine the parts, thread

@@ -36,6 +36,29 @@ for _i, _w in enumerate(WORKLOADS):
     _w["scale"] = 1.0 / math.sqrt(_w["d"])
 
 
+# Decoding workloads (split-KV, fa_decode): Nq new queries per head against a
+# cache of Nk keys.  The pages print no decoding configuration; these take
+# the causal long-context workload's cache (B1 H8 N32768 d64 fp16) and a
+# larger batch of heads at d128, one new query each, causal.  Seeds 2000 + i.
+DECODE_WORKLOADS = [
+    dict(name="decode_b1_h8_q1_k32768_d64_fp16", B=1, H=8, Nq=1, Nk=32768, d=64, dtype="fp16",
+         causal=True),
+    dict(name="decode_b8_h32_q1_k32768_d128_bf16", B=8, H=32, Nq=1, Nk=32768, d=128,
+         dtype="bf16", causal=True),
+]
+for _i, _w in enumerate(DECODE_WORKLOADS):
+    _w["seed"] = 2000 + _i
+    _w["scale"] = 1.0 / math.sqrt(_w["d"])
+
+
+def decode_workload(name):
+    """The decoding workload dict with this name."""
+    for w in DECODE_WORKLOADS:
+        if w["name"] == name:
+            return dict(w)
+    raise KeyError(name)
+
+
 def workload(name):
     """The workload dict with this name (or index)."""
     if isinstance(name, int):
