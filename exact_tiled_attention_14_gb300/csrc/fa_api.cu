@@ -341,7 +341,9 @@ cudaError_t launch_decode(const DecodeParams& p, void* o, float* lse, int d, boo
 
 namespace {
 
-// Split of the key axis for fa_decode: enough CTAs for about two per SM.
+// Split of the key axis for fa_decode: up to 16 CTAs per SM (short CTAs
+// even out the last wave), but at least 8 key tiles per CTA (a CTA's fixed
+// cost — query load, pipeline fill, its part of the combine — stays small).
 struct DecodePlan {
   int splits = 0;
   int tiles_per_split = 0;
@@ -353,9 +355,9 @@ DecodePlan plan_decode(long long bh, int Nq, int Nk, int d, int sms) {
   DecodePlan dp;
   const int tiles = (Nk + fa::kDecTile - 1) / fa::kDecTile;
   if (tiles == 0 || bh == 0) return dp;
-  long long want = (2ll * sms + bh - 1) / bh;
+  long long want = (16ll * sms + bh - 1) / bh;
+  if (want > (tiles + 7) / 8) want = (tiles + 7) / 8;
   if (want < 1) want = 1;
-  if (want > tiles) want = tiles;
   dp.tiles_per_split = static_cast<int>((tiles + want - 1) / want);
   dp.splits = (tiles + dp.tiles_per_split - 1) / dp.tiles_per_split;
   const size_t parts = static_cast<size_t>(bh) * dp.splits * Nq;
