@@ -57,10 +57,10 @@ struct DecSmem {
   static constexpr int kChunkBytes = kDecTile * 128;
   static constexpr int kStages = (D == 128) ? 3 : 6;
   static constexpr int kRing = 0;                         // [stage][K, V]; reused for the final sum
-  static constexpr int kQ = kRing + kStages * 2 * kTile;  // fp32 [NQ][D]
-  static constexpr int kS = kQ + NQ * D * 4;              // fp32 scores, then P: [NQ][128]
-  static constexpr int kAlpha = kS + NQ * kDecTile * 4;   // fp32 [NQ]
-  static constexpr int kBar = (kAlpha + NQ * 4 + 15) / 16 * 16;
+  static constexpr int kQRow = D + 16;                    // padded query row, floats (see q_index)
+  static constexpr int kQ = kRing + kStages * 2 * kTile;  // fp32 [NQ][kQRow]
+  static constexpr int kS = kQ + NQ * kQRow * 4;          // fp32 scores [NQ][128]
+  static constexpr int kBar = (kS + NQ * kDecTile * 4 + 15) / 16 * 16;
   static constexpr int kMisc = kBar + 8 * kStages;        // abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -81,15 +81,24 @@ __device__ __forceinline__ void load8(const uint8_t* tile, int r, int j, float* 
   ptx::unpack2<kBf16>(v.w, out[6], out[7]);
 }
 
+// Shared-memory index of column `col` of query q: each quarter of the row
+// is shifted by 16 bytes, so the four threads that share a key (one quarter
+// each) read their query values from different banks.
+template <int D>
+__device__ __forceinline__ int q_index(int q, int col) {
+  return q * (D + 16) + col + (col / (D / 4)) * 4;
+}
+
 // One CTA per (split, batch*head): the online softmax over keys
 // [split * tiles_per_split * 128, ...) for every query of the head.
 //   phase A  scores: four consecutive threads share key r, each dotting a
 //            quarter of its columns with every query (two-lane fp32 FMAs),
 //            summed with two shuffles.
-//   phase B  softmax: warp w owns query w: tile maximum, new reference,
-//            rescale factor alpha, P = 2^(s*c - m), row sum.
-//   phase C  P V: thread (query, 8-column piece, key group) accumulates over
-//            the keys of its group; groups are summed once at the end.
+//   phase B  P V: thread (query, 8-column piece, key group) works for one
+//            query, the same for a whole warp; every warp of a query takes
+//            the tile's maximum and sum itself (new reference, rescale
+//            factor, running sum), then accumulates P V over the keys of its
+//            group.  Groups are summed once at the end.
 template <int D, int NQ, bool kBf16>
 __global__ void __launch_bounds__(kDecThreads, 1)
     fa_decode_partial_kernel(const __grid_constant__ DecodeParams p) {
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc);
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int split = blockIdx.x % p.splits, bh = blockIdx.x / p.splits;
   const int Nq = p.Nq;
   const int n_tiles_all = (p.Nk + kDecTile - 1) / kDecTile;
@@ -110,7 +119,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int nt = max(0, min(p.tiles_per_split, n_tiles_all - t0));
   float* q_s = reinterpret_cast<float*>(sgen + L::kQ);
   float* s_s = reinterpret_cast<float*>(sgen + L::kS);
-  float* alpha_s = reinterpret_cast<float*>(sgen + L::kAlpha);
   const float c = p.scale_log2;
 
   if (tid == 0) {
@@ -126,8 +134,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int i = tid; i < NQ * D / 2; i += kDecThreads) {
       float a = 0.f, b = 0.f;
       if (i < Nq * D / 2) ptx::unpack2<kBf16>(qg[i], a, b);
-      q_s[2 * i] = a;
-      q_s[2 * i + 1] = b;
+      const int q = (2 * i) / D, col = (2 * i) % D;
+      q_s[q_index<D>(q, col)] = a;
+      q_s[q_index<D>(q, col + 1)] = b;
     }
   }
   __syncthreads();
@@ -149,16 +158,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int r = tid >> 2, qd = tid & 3;
   constexpr int kPieces = D / 8;              // 16-byte pieces per row
   constexpr int kMyPieces = kPieces / 4;
-  // phase-C mapping: 8-column piece, query, key group
+  // phase-B mapping: 8-column piece, query, key group
   constexpr int kGroupsAll = kDecThreads / kPieces;
   constexpr int kGroups = kGroupsAll / NQ;    // key groups per query
+  static_assert((kGroups * kPieces) % 32 == 0, "a warp serves one query");
   const int piece = tid % kPieces;
   const int qc = (tid / kPieces) / kGroups;
   const int kg = (tid / kPieces) % kGroups;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  // softmax state of query `warp` (held by every lane of warp w < NQ)
+  // softmax state of query qc (kept alike by every warp serving it)
   float m2 = -INFINITY, l = 0.f;
 
   bool alive = true;
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint64_t k45 = ptx::f2_pack(kv[4], kv[5]), k67 = ptx::f2_pack(kv[6], kv[7]);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          const uint64_t* qp = reinterpret_cast<const uint64_t*>(q_s + q * D + j * 8);
+          const uint64_t* qp = reinterpret_cast<const uint64_t*>(q_s + q_index<D>(q, j * 8));
           sacc[q] = ptx::ffma2(k01, qp[0], sacc[q]);
           sacc[q] = ptx::ffma2(k23, qp[1], sacc[q]);
           sacc[q] = ptx::ffma2(k45, qp[2], sacc[q]);
@@ -200,10 +210,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
     __syncthreads();
-    // ---- phase B: online softmax of query `warp`
-    if (warp < NQ && warp < Nq) {
-      const int q = warp;
-      const long long pos = static_cast<long long>(p.Nk) - Nq + q;   // causal: last keys visible
+    // ---- phase B: this warp's query qc: tile maximum and sum, then P V
+    if (qc < Nq) {
+      const long long pos = static_cast<long long>(p.Nk) - Nq + qc;   // causal: last keys visible
+      const float* srow = s_s + qc * kDecTile;
       float sv[4];
       float tmax = -INFINITY;
 #pragma unroll
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int kr = lane + 32 * e;
         const long long key = key0 + kr;
         const bool vis = key < p.Nk && (!p.causal || key <= pos);
-        sv[e] = vis ? s_s[q * kDecTile + kr] * c : -INFINITY;
+        sv[e] = vis ? srow[kr] * c : -INFINITY;
         tmax = fmaxf(tmax, sv[e]);
       }
 #pragma unroll
@@ -222,27 +232,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const float alpha = (m2 == -INFINITY) ? 0.f : ptx::ex2(m2 - ref);
       float lsum = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = ptx::ex2(sv[e] - ref);
-        s_s[q * kDecTile + lane + 32 * e] = pv;
-        lsum += pv;
-      }
+      for (int e = 0; e < 4; ++e) lsum += ptx::ex2(sv[e] - ref);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
       l = l * alpha + lsum;
       m2 = mnew;
-      if (lane == 0) alpha_s[q] = alpha;
-    }
-    __syncthreads();
-    // ---- phase C: O(q, piece) = alpha * O + sum over my key group of P V
-    if (qc < Nq) {
-      const float a = alpha_s[qc];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] *= a;
-      const float* prow = s_s + qc * kDecTile;
+      for (int e = 0; e < 8; ++e) acc[e] *= alpha;
 #pragma unroll
       for (int kr = kg; kr < kDecTile; kr += kGroups) {
-        const float pv = prow[kr];
+        const long long key = key0 + kr;
+        const bool vis = key < p.Nk && (!p.causal || key <= pos);
+        const float pv = vis ? ptx::ex2(srow[kr] * c - ref) : 0.f;
         float vv[8];
         load8<kBf16>(vt, kr, piece, vv);
 #pragma unroll
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     dst[0] = make_float4(o[0], o[1], o[2], o[3]);
     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
   }
-  if (warp < NQ && warp < Nq && lane == 0) p.part_ml[part + warp] = make_float2(m2, l);
+  if (qc < Nq && kg == 0 && piece == 0) p.part_ml[part + qc] = make_float2(m2, l);
 }
 
 // One block of D threads per (batch*head, query): combine the parts, thread
