@@ -84,15 +84,18 @@ def io_bytes(w):
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources; a stored ncu traffic figure is only valid for it."""
+    """Hash of the sources the forward kernel and its launch are built from; a
+    stored ncu traffic figure is only valid for it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_14_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and "bwd" not in name:   # the forward's sources
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "fa.h"), "rb").read())
+    for name in FORWARD_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
+
+
+FORWARD_SOURCES = ("fa_api.cu", "fa_fwd_d128.cu", "fa_fwd_d64.cu", "fa_fwd_kernel.cuh",
+                   "fa_launch.cuh", "ptx_sm103.cuh")
 
 
 def stored_traffic(workload):

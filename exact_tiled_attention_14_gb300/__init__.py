@@ -3,7 +3,8 @@
 This module only marshals arguments to the C ABI in ``include/fa.h``
 (``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
-``fa_status``, ``fa_set_watchdog_ns``, ``fa_work_tiles``, ``fa_version``),
+``fa_status``, ``fa_set_watchdog_ns``, ``fa_watchdog_selftest``,
+``fa_work_tiles``, ``fa_version``),
 under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
@@ -41,7 +42,7 @@ FA_ERR_WORKSPACE = 12
 # Functions the C ABI exports (checked against include/fa.h by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
-           "fa_set_watchdog_ns", "fa_work_tiles", "fa_version")
+           "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_work_tiles", "fa_version")
 
 _lib = None
 
@@ -86,6 +87,8 @@ def load_library(path=None):
     lib.fa_status.restype = i
     lib.fa_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
     lib.fa_set_watchdog_ns.restype = None
+    lib.fa_watchdog_selftest.argtypes = [ctypes.c_ulonglong, vp]
+    lib.fa_watchdog_selftest.restype = i
     lib.fa_work_tiles.argtypes = [i, i, ctypes.POINTER(ctypes.c_longlong)]
     lib.fa_work_tiles.restype = i
     lib.fa_version.argtypes = []
@@ -197,6 +200,11 @@ def fa_status(stream=None):
 
 def fa_set_watchdog_ns(ns):
     load_library().fa_set_watchdog_ns(int(ns))
+
+
+def fa_watchdog_selftest(budget_ns, stream=None):
+    """Launch the failure-detection self-test (a wait that must run out)."""
+    return load_library().fa_watchdog_selftest(int(budget_ns), _stream(stream))
 
 
 def fa_work_tiles(N, causal):

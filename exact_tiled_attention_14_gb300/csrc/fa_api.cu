@@ -22,6 +22,25 @@ namespace {
 __device__ unsigned int g_fa_status = 0;
 
 constexpr unsigned long long kDefaultWatchdogNs = 2000000000ull;
+
+// Site recorded by the watchdog self-test's wait.
+constexpr unsigned int kSiteSelfTest = 31;
+
+// One thread waits, through the same bounded wait every kernel uses, on a
+// barrier that nothing ever completes; the wait runs out after the budget
+// and records the timeout in the status word, and the kernel returns.
+__global__ void fa_watchdog_selftest_kernel(unsigned long long budget_cycles,
+                                            unsigned int* status) {
+  __shared__ __align__(8) unsigned long long never;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t bar = fa::ptx::smem_u32(&never);
+  fa::ptx::mbar_init(bar, 1);
+  fa::ptx::fence_mbar_init();
+  const fa::ptx::Watchdog wd{budget_cycles, &abort_flag, status};
+  fa::ptx::wait_bounded(bar, 0, wd, kSiteSelfTest);
+}
 std::atomic<unsigned long long> g_watchdog_ns{0};
 std::atomic<unsigned long long*> g_trace{nullptr};  // FA_TRACE builds only
 
@@ -438,6 +457,16 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaError_t e = fa::launch_decode(p, o, lse, d, bf16, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_watchdog_selftest(unsigned long long budget_ns, cudaStream_t stream) {
+  if (budget_ns == 0 || budget_ns > 1000000000ull) return FA_ERR_SHAPE;
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+  fa_watchdog_selftest_kernel<<<1, 32, 0, stream>>>(budget_ns * 21ull / 10ull, info->status);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_status(cudaStream_t stream, unsigned int* detail) {

@@ -246,6 +246,19 @@ int fa_status(cudaStream_t stream, unsigned int *detail);
 void fa_set_watchdog_ns(unsigned long long ns);
 
 /*
+ * fa_watchdog_selftest — failure-detection self-test (the pages have no
+ * counterpart).  Launches on `stream` a one-thread kernel whose bounded
+ * wait, the same routine every kernel of this library waits with, is on a
+ * barrier that nothing ever completes.  The wait runs out after
+ * `budget_ns` nanoseconds (1 .. 1e9) and records a timeout with site 31 in
+ * the status word; fa_status then returns FA_ERR_TIMEOUT.  No fault, trap
+ * or hang is involved, and the context stays usable.
+ * Returns FA_ERR_SHAPE for a budget outside 1 .. 1e9, FA_ERR_DEVICE, or
+ * FA_ERR_LAUNCH.
+ */
+int fa_watchdog_selftest(unsigned long long budget_ns, cudaStream_t stream);
+
+/*
  * fa_work_tiles — host-side count of the (query tile, key tile) pairs the
  * forward kernel computes for one head with 128-row tiles: n^2 unmasked, or
  * n(n+1)/2 causal with n = ceil(N/128) (section "Causal masking: half the

@@ -185,3 +185,11 @@ def test_decode_host_errors(lib):
     out = C.c_size_t(5)
     assert lib.fa_decode_workspace_size(1, 1, 17, 10, 64, C.byref(out)) == fa.FA_ERR_SHAPE
     assert lib.fa_decode_workspace_size(1, 1, 4, 0, 64, C.byref(out)) == fa.FA_OK and out.value == 0
+
+
+def test_watchdog_selftest_host_errors(lib):
+    assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
+    assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
+    import torch
+    if not torch.cuda.is_available():
+        assert fa.fa_watchdog_selftest(1000) == fa.FA_ERR_DEVICE
