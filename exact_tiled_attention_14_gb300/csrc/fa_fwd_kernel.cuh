@@ -29,8 +29,8 @@
 //              the issue warps give their registers to the softmax warpgroups)
 // A work unit is (batch*head, block of 256 query rows) = two 128-row query
 // tiles.  TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (d fp32
-// columns each).  P (16-bit) overwrites the first 64 columns of its S at
-// d = 128; at d = 64 it has 64 columns of its own (see OwnP).
+// columns each).  P (16-bit) has 64 TMEM columns of its own at d = 64 and a
+// shared-memory tile at d = 128 (see OwnP).
 //
 // MMA issue order per key tile j (the two tiles ping-pong so one tile's
 // softmax runs while the tensor core works on the other tile):
@@ -161,6 +161,26 @@ __device__ __forceinline__ void trace_event(const FwdParams& p, int role, uint32
 #endif
 }
 
+// Where P lives.  P gets storage of its own, so the next S of a query tile
+// can be computed as soon as the softmax has read the current S into
+// registers, which takes the tensor-core work of the next tile off the
+// softmax's critical path.  At d = 64 the last 128 TMEM columns are free and
+// each query tile gets a P buffer there (64 columns: 128 16-bit values per
+// row).  At d = 128, S0, S1, O0 and O1 fill all 512 TMEM columns, so P goes
+// to shared memory (one 128 x 128 tile per query tile, laid out like a Q
+// tile) and the P.V product reads both operands from there.  Built with
+// FA_D128_P_IN_S, P instead overwrites the first 64 columns of its S at
+// d = 128, and the next S waits until the P.V product has read P.
+#ifndef FA_D128_P_IN_S
+#define FA_D128_P_IN_S 0
+#endif
+template <int D>
+struct OwnP {
+  static constexpr bool kTmem = (2 * 128 + 2 * D + 2 * 64) <= static_cast<int>(kTmemCols);
+  static constexpr bool kSmem = !kTmem && !FA_D128_P_IN_S;
+  static constexpr bool kOn = kTmem || kSmem;
+};
+
 // Shared-memory plan.  At d = 128 the two output staging tiles would cost two
 // K/V ring stages (the ring then cannot cover L2 latency), so O is written
 // straight from registers; at d = 64 there is room for both, and O goes out
@@ -171,11 +191,14 @@ struct Smem {
   static constexpr int kTile = kBM * D * 2;          // one 128 x D tile of 16-bit values
   static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 128 bytes
   static constexpr bool kTmaStore = (D == 64);       // epilogue through smem + TMA store
-  static constexpr int kStages = (D == 128) ? 5 : 8; // K/V ring depth
+  // K/V ring depth (at d = 128 with P in shared memory the two P tiles take
+  // two of the five stages)
+  static constexpr int kStages = (D == 128) ? (OwnP<D>::kSmem ? 3 : 5) : 8;
   static constexpr int kQ = 0;                       // two query tiles
   static constexpr int kKV = kQ + 2 * kTile;         // ring of K or V tiles
   static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles (if any)
-  static constexpr int kBar = kO + (kTmaStore ? 2 * kTile : 0);
+  static constexpr int kP = kO + (kTmaStore ? 2 * kTile : 0);   // two P tiles (if in smem)
+  static constexpr int kBar = kP + (OwnP<D>::kSmem ? 2 * kBM * kBN * 2 : 0);
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
                        bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
@@ -192,21 +215,10 @@ template <int D>
 __device__ __forceinline__ uint32_t s_col(int w) { return w ? 128u : 0u; }
 template <int D>
 __device__ __forceinline__ uint32_t o_col(int w) { return 256u + (w ? D : 0); }
-
-// Where P lives.  At d = 128, S0, S1, O0 and O1 fill all 512 TMEM columns,
-// so P overwrites the first 64 columns of its S; the next S of that query
-// tile then has to wait until the P.V product has read P.  At d = 64 the
-// last 128 columns are free and each query tile gets a P buffer of its own
-// (64 columns: 128 16-bit values per row).  The next S can then be computed
-// as soon as the softmax has read the current S into registers, which takes
-// the tensor-core work of the next tile off the softmax's critical path.
-template <int D>
-struct OwnP {
-  static constexpr bool kOn = (2 * 128 + 2 * D + 2 * 64) <= static_cast<int>(kTmemCols);
-};
+// TMEM column of P (P in TMEM only).
 template <int D>
 __device__ __forceinline__ uint32_t p_col(int w) {
-  return OwnP<D>::kOn ? 256u + 2u * D + (w ? 64u : 0u) : s_col<D>(w);
+  return OwnP<D>::kTmem ? 256u + 2u * D + (w ? 64u : 0u) : s_col<D>(w);
 }
 
 struct Unit {
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t idesc_o = ptx::idesc_f16(kBM, D, fmt, 1);    // P (TMEM) x V (MN-major)
+      constexpr uint32_t idesc_o = ptx::idesc_f16(kBM, D, fmt, 1);    // P x V (MN-major)
       // Address words of the shared-memory descriptors (start >> 4 | LBO >> 4 << 16).
       const uint32_t q_lo0 = ptx::desc_lo(sbase + L::kQ, 16);
       const uint32_t q_lo1 = ptx::desc_lo(sbase + L::kQ + L::kTile, 16);
@@ -508,11 +520,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_w (+)= P_w V over 128 keys: P from TMEM (two 16-bit values per
       // column, 8 columns per 16 keys); V MN-major (d contiguous): 8-key
       // groups 1024 bytes apart (SBO), 64-column chunks kChunkBytes apart (LBO).
-      auto issue_pv = [&](uint32_t o_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t acc) {
+      // P in shared memory: the A operand is a K-major tile laid out like Q
+      // (128 keys along K in two 64-column chunks), so its K steps advance as
+      // in issue_s.
+      auto issue_pv = [&](uint32_t o_tmem, uint32_t p_addr, uint32_t v_lo, uint32_t acc) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts(o_tmem, p_tmem + kk * 8, ptx::desc_sw128(v_lo + kk * (2048 >> 4)), idesc_o,
-                      kk > 0 ? 1u : acc);
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          if constexpr (OwnP<D>::kSmem) {
+            const uint32_t off = static_cast<uint32_t>((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ss(o_tmem, ptx::desc_sw128(p_addr + off),
+                        ptx::desc_sw128(v_lo + kk * (2048 >> 4)), idesc_o, kk > 0 ? 1u : acc);
+          } else {
+            ptx::mma_ts(o_tmem, p_addr + kk * 8, ptx::desc_sw128(v_lo + kk * (2048 >> 4)), idesc_o,
+                        kk > 0 ? 1u : acc);
+          }
+        }
       };
 
       uint32_t tr = 0;                 // trace events recorded
@@ -542,7 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (OwnP<D>::kOn) {
         // With a P buffer per query tile, S_w_{j+1} waits only until the
         // softmax has read S_w_j, and P_w_j V_j only for P_w_j.
-        const uint32_t tP0 = tmem_base + p_col<D>(0), tP1 = tmem_base + p_col<D>(1);
+        // P_w: TMEM column address, or the address word of its shared-memory descriptor
+        const uint32_t tP0 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP, 16) : tmem_base + p_col<D>(0);
+        const uint32_t tP1 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP + kBM * kBN * 2, 16)
+                                            : tmem_base + p_col<D>(1);
         uint32_t sc0 = 0, sc1 = 0;     // S issued into S0 / S1 so far
         auto issue_s_own = [&](int w, uint32_t kslot_) {
           uint32_t& sc = w ? sc1 : sc0;
@@ -874,9 +899,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (rescale) rescale_o();
         }
-        ptx::tmem_st32(tP, pk);
-        ptx::tmem_st32(tP + 32, pk + 32);
-        ptx::tmem_wait_st();
+        if constexpr (OwnP<D>::kSmem) {
+          // row t of the P_w tile: 16 pieces of 8 keys, 128-byte swizzle
+          uint8_t* prow = sgen + L::kP + w * (kBM * kBN * 2) + t * 128;
+#pragma unroll
+          for (int k = 0; k < kBN / 8; ++k)
+            *reinterpret_cast<uint4*>(prow + (k >> 3) * L::kChunkBytes + (((k & 7) ^ (t & 7)) << 4)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
+        } else {
+          ptx::tmem_st32(tP, pk);
+          ptx::tmem_st32(tP + 32, pk + 32);
+        }
+        ptx::tmem_wait_st();               // P (in TMEM) and a rescaled O are written
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + w));
         pf.lap(4);
