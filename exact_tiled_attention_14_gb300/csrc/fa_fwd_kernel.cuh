@@ -22,27 +22,25 @@
 // Structure of one CTA (persistent; one CTA per SM):
 //   warps 0-3  softmax warpgroup 0  -> query tile 0 of the unit (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1  -> query tile 1 of the unit
-//   warp  8    MMA issuer (one thread): S = Q K^T, and at d = 128 also O += P V
+//   warp  8    MMA issuer (one thread): S = Q K^T
 //   warp  9    TMA producer (one thread): Q tiles and a ring of K/V tiles
-//   warp  10   at d = 64, second MMA issuer (one thread): O += P V
-//   warps 10-11 otherwise idle (they complete the third warpgroup, which lets
-//              the issue warps give their registers to the softmax warpgroups)
+//   warp  10   MMA issuer (one thread): O += P V
+//   warp  11   idle (it completes the third warpgroup, which lets the issue
+//              warps give their registers to the softmax warpgroups)
 // A work unit is (batch*head, block of 256 query rows) = two 128-row query
 // tiles.  TMEM holds S0, S1 (128 fp32 columns each) and O0, O1 (d fp32
 // columns each).  P (16-bit) has 64 TMEM columns of its own at d = 64 and a
 // shared-memory tile at d = 128 (see OwnP).
 //
-// MMA issue order per key tile j (the two tiles ping-pong so one tile's
-// softmax runs while the tensor core works on the other tile):
-//   prologue: S0_0, S1_0
-//   d = 128 : PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
-//             so S_w_{j+1} completing implies PV_w_j completed, which is what
-//             lets the softmax warpgroup rescale O_w in place before it
-//             releases P_w_{j+1};
-//   d = 64  : S0_{j+1}, S1_{j+1}, PV0_j, PV1_j
-//             S_w_{j+1} only waits for the softmax to have read S_w_j, and
-//             the softmax waits for PV_w_{j-1} before it writes P_w_j or
-//             rescales O_w.
+// The two query tiles ping-pong, so one tile's softmax runs while the tensor
+// core works on the other tile.  S_w_{j+1} = Q_w K_{j+1}^T is issued as soon
+// as the softmax has read S_w_j into registers (barrier SFree), one key tile
+// ahead of the softmax; P_w_j V_j as soon as the softmax has written P_w_j.
+// The softmax waits for P_w_{j-1} V_{j-1} (barrier PvDone) before it writes
+// P_w_j or rescales O_w.  The two products have an issuing thread each:
+// a thread that waits on a barrier stalls until the tensor core has taken
+// every MMA it queued before, and with two issuers one thread's waits
+// overlap the other's queued work.
 #pragma once
 
 #include <cuda.h>
@@ -72,7 +70,7 @@ constexpr float kLn2 = 0.693147180559945309f;
 // Sites recorded in the status word when a wait runs out.
 enum WaitSite : uint32_t {
   kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFull = 4, kSitePFull = 5,
-  kSiteOFree = 6, kSiteSFull = 7, kSiteODone = 8, kSiteSFree = 9, kSitePvDone = 10
+  kSiteOFree = 6, kSiteSFull = 7, kSiteSFree = 9, kSitePvDone = 10
 };
 
 struct FwdParams {
@@ -161,24 +159,18 @@ __device__ __forceinline__ void trace_event(const FwdParams& p, int role, uint32
 #endif
 }
 
-// Where P lives.  P gets storage of its own, so the next S of a query tile
+// Where P lives.  P has storage of its own, so the next S of a query tile
 // can be computed as soon as the softmax has read the current S into
 // registers, which takes the tensor-core work of the next tile off the
 // softmax's critical path.  At d = 64 the last 128 TMEM columns are free and
 // each query tile gets a P buffer there (64 columns: 128 16-bit values per
 // row).  At d = 128, S0, S1, O0 and O1 fill all 512 TMEM columns, so P goes
 // to shared memory (one 128 x 128 tile per query tile, laid out like a Q
-// tile) and the P.V product reads both operands from there.  Built with
-// FA_D128_P_IN_S, P instead overwrites the first 64 columns of its S at
-// d = 128, and the next S waits until the P.V product has read P.
-#ifndef FA_D128_P_IN_S
-#define FA_D128_P_IN_S 0
-#endif
+// tile) and the P.V product reads both operands from there.
 template <int D>
 struct OwnP {
   static constexpr bool kTmem = (2 * 128 + 2 * D + 2 * 64) <= static_cast<int>(kTmemCols);
-  static constexpr bool kSmem = !kTmem && !FA_D128_P_IN_S;
-  static constexpr bool kOn = kTmem || kSmem;
+  static constexpr bool kSmem = !kTmem;
 };
 
 // Shared-memory plan.  At d = 128 the two output staging tiles would cost two
@@ -201,8 +193,8 @@ struct Smem {
   static constexpr int kBar = kP + (OwnP<D>::kSmem ? 2 * kBM * kBN * 2 : 0);
   // barrier indices
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
-                       bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bODone = bPFull + 2,
-                       bOFree = bODone + 2, bSFree = bOFree + 2, bPvDone = bSFree + 2,
+                       bSFull = 2 + 2 * kStages, bPFull = bSFull + 2,
+                       bOFree = bPFull + 2, bSFree = bOFree + 2, bPvDone = bSFree + 2,
                        bFinal = bPvDone + 2, bFinalPv = bFinal + 1, kNumBars = bFinalPv + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base, abort flag, 2 merge flags
   static constexpr int kBytes = kMisc + 16;
@@ -215,11 +207,9 @@ template <int D>
 __device__ __forceinline__ uint32_t s_col(int w) { return w ? 128u : 0u; }
 template <int D>
 __device__ __forceinline__ uint32_t o_col(int w) { return 256u + (w ? D : 0); }
-// TMEM column of P (P in TMEM only).
+// TMEM column of P (d = 64, where P is in TMEM).
 template <int D>
-__device__ __forceinline__ uint32_t p_col(int w) {
-  return OwnP<D>::kTmem ? 256u + 2u * D + (w ? 64u : 0u) : s_col<D>(w);
-}
+__device__ __forceinline__ uint32_t p_col(int w) { return 256u + 2u * D + (w ? 64u : 0u); }
 
 struct Unit {
   int bh, mblk, n0, n1;
@@ -388,7 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 2; ++w) {
       ptx::mbar_init(bar(L::bSFull + w), 1);
       ptx::mbar_init(bar(L::bPFull + w), 128);
-      ptx::mbar_init(bar(L::bODone + w), 1);
       ptx::mbar_init(bar(L::bOFree + w), 128);
       ptx::mbar_init(bar(L::bSFree + w), 128);
       ptx::mbar_init(bar(L::bPvDone + w), 1);
@@ -457,19 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++loads;
           }
         };
-        // The ring is filled in the order the MMA issuer consumes it:
-        // K0 V0 K1 V1 ... when P overwrites S (S_{j+1} follows P_j V_j), and
-        // K0 K1 V0 K2 V1 ... with a P buffer of its own (S_{j+1} goes first).
+        // The ring is filled in the order the two MMA issuers need the tiles:
+        // K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2} V_{n-1} (S_{j+1} before P_j V_j).
         load_kv(0, 0);
         load_q();
         for (int j = 0; j < nkv; ++j) {
-          if (OwnP<D>::kOn) {
-            if (j + 1 < nkv) load_kv(0, j + 1);
-            load_kv(1, j);
-          } else {
-            load_kv(1, j);
-            if (j + 1 < nkv) load_kv(0, j + 1);
-          }
+          if (j + 1 < nkv) load_kv(0, j + 1);
+          load_kv(1, j);
         }
         ++k_units;
       }
@@ -481,18 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q_issued > 0) ptx::wait_drain(bar(L::bQFull), (q_issued - 1) & 1, drain);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp || (OwnP<D>::kOn && warp == kPvWarp)) {
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ============================================================ MMA issuers
     // The issue loop has to keep up with the tensor core (an M128 x N128 x
     // K16 MMA lasts ~64 cycles), so descriptors are precomputed: per MMA only
     // the 32-bit address word changes, by a compile-time offset.
-    // When P overwrites S, one thread (warp 8) issues every tcgen05
-    // instruction, in an order that carries the S/P dependence.  With its own
-    // P the two products are independent and each gets an issuing thread:
-    // warp 8 the S = Q K^T products, warp 10 the O += P V products.  Any wait
-    // on a barrier stalls the waiting thread until the tensor core has taken
-    // every MMA it queued before, which leaves the pipe idle meanwhile; with
-    // two issuers one thread's waits overlap the other's queued work.
+    // Warp 8 issues the S = Q K^T products, warp 10 the O += P V products.
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
@@ -537,217 +514,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
-      uint32_t tr = 0;                 // trace events recorded
       Prof pf;                         // FA_PROFILE: 0 kv wait, 1 p wait, 2 q wait, 3 o_free wait,
-                                       // 4 S issue, 5 PV issue, 6 other, 7 groups issued
-      uint32_t slot = 0, phase = 0;    // K/V ring position
-      uint32_t loads = 0;              // K/V tiles consumed (trace argument)
+                                       // 4 S issue, 5 PV issue, 6 other, 7 groups issued,
+                                       // 16 S-free wait
       uint32_t k_units = 0;            // units walked
       uint32_t ucnt0 = 0, ucnt1 = 0;   // units in which query tile 0 / 1 was active
       uint32_t pph0 = 0, pph1 = 0;     // p_full phase parity of tile 0 / 1
       bool alive = true;
       bool issued_any = false;
-      auto next_full = [&]() -> uint32_t {
-        pf.lap(6);
-        alive = ptx::wait_bounded(bar(L::bKvFull + slot), phase, wd, kSiteKvFull) && alive;
-        pf.lap(0);
-        trace_event(p, 2, tr, kEvKvWaited, loads);
-        ++loads;
-        const uint32_t got = slot;
-        if (++slot == static_cast<uint32_t>(L::kStages)) { slot = 0; phase ^= 1u; }
-        return got;
-      };
-
       Cursor cu;
       cursor_init<kSplit>(p, cta, grid, cu);
       Piece u;
-      if constexpr (OwnP<D>::kOn) {
-        // With a P buffer per query tile, S_w_{j+1} waits only until the
-        // softmax has read S_w_j, and P_w_j V_j only for P_w_j.
-        // P_w: TMEM column address, or the address word of its shared-memory descriptor
-        const uint32_t tP0 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP, 16) : tmem_base + p_col<D>(0);
-        const uint32_t tP1 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP + kBM * kBN * 2, 16)
-                                            : tmem_base + p_col<D>(1);
-        uint32_t sc0 = 0, sc1 = 0;     // S issued into S0 / S1 so far
-        auto issue_s_own = [&](int w, uint32_t kslot_) {
-          uint32_t& sc = w ? sc1 : sc0;
-          pf.lap(6);
-          if (sc > 0)   // the softmax has read the previous S of this tile
-            alive = ptx::wait_bounded(bar(L::bSFree + w), (sc - 1) & 1, wd, kSiteSFree) && alive;
-          pf.lap(16);
-          ptx::tc_fence_after();
-          if (alive) {
-            issue_s(w ? tS1 : tS0, w ? q_lo1 : q_lo0, k_lo0 + kslot_ * kSlotLo);
-            ptx::mma_commit(bar(L::bSFull + w));
-          }
-          ++sc;
-          pf.lap(4);
-          pf.count(7);
-        };
-        auto issue_pv_own = [&](int w, int j, uint32_t v_lo) {
-          uint32_t& pph = w ? pph1 : pph0;
-          const uint32_t ucnt = w ? ucnt1 : ucnt0;
-          pf.lap(6);
-          if (j == 0 && ucnt > 0)   // O_w of the previous piece must have been read out
-            alive = ptx::wait_bounded(bar(L::bOFree + w), (ucnt - 1) & 1, wd, kSiteOFree) && alive;
-          pf.lap(3);
-          alive = ptx::wait_bounded(bar(L::bPFull + w), pph, wd, kSitePFull) && alive;
-          pf.lap(1);
-          pph ^= 1u;
-          ptx::tc_fence_after();
-          if (alive) {
-            issue_pv(w ? tO1 : tO0, w ? tP1 : tP0, v_lo, j > 0 ? 1u : 0u);
-            ptx::mma_commit(bar(L::bPvDone + w));
-          }
-          pf.lap(5);
-          pf.count(7);
-        };
-        // The producer fills the ring with K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2}
-        // V_{n-1} for a piece of n key tiles: 2n loads from ring position
-        // `base`; each issuer waits only for the tiles it reads.
-        auto ring_wait = [&](uint32_t pos) -> uint32_t {
-          const uint32_t sl = pos % L::kStages;
-          pf.lap(6);
-          alive = ptx::wait_bounded(bar(L::bKvFull + sl), (pos / L::kStages) & 1, wd, kSiteKvFull) &&
-                  alive;
-          pf.lap(0);
-          ptx::tc_fence_after();
-          return sl;
-        };
-        uint32_t base = 0;
-        if (warp == kMmaWarp) {
-          // S = Q K^T for both query tiles, one key tile ahead of the softmax
-          while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
-            const int nkv = max(u.n0, u.n1);
-            pf.lap(6);
-            alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
-            pf.lap(2);
-            ptx::tc_fence_after();
-            for (int j = 0; j < nkv; ++j) {
-              const uint32_t kslot = ring_wait(base + (j == 0 ? 0u : 2u * j - 1u));
-              if (j < u.n0) issue_s_own(0, kslot);
-              if (j < u.n1) issue_s_own(1, kslot);
-              if (alive) {
-                ptx::mma_commit(bar(L::bKvEmpty + kslot));
-                if (j + 1 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
-              }
-              issued_any = true;
-            }
-            base += 2u * nkv;
-            ++k_units;
-          }
-        } else {
-          // O += P V for both query tiles, as soon as the softmax has written P
-          while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
-            const int nkv = max(u.n0, u.n1);
-            for (int j = 0; j < nkv; ++j) {
-              const uint32_t vslot =
-                  ring_wait(base + (j + 1 < nkv ? 2u * j + 2u : 2u * nkv - 1u));
-              const uint32_t v_lo = v_lo0 + vslot * kSlotLo;
-              if (j < u.n0) issue_pv_own(0, j, v_lo);
-              if (j < u.n1) issue_pv_own(1, j, v_lo);
-              if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
-              issued_any = true;
-            }
-            if (u.n0 > 0) ++ucnt0;
-            if (u.n1 > 0) ++ucnt1;
-            base += 2u * nkv;
-          }
-        }
-      } else
-      while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
-        const int nkv = max(u.n0, u.n1);
+      // With a P buffer per query tile, S_w_{j+1} waits only until the
+      // softmax has read S_w_j, and P_w_j V_j only for P_w_j.
+      // P_w: TMEM column address, or the address word of its shared-memory descriptor
+      const uint32_t tP0 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP, 16) : tmem_base + p_col<D>(0);
+      const uint32_t tP1 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP + kBM * kBN * 2, 16)
+                                          : tmem_base + p_col<D>(1);
+      uint32_t sc0 = 0, sc1 = 0;     // S issued into S0 / S1 so far
+      auto issue_s_own = [&](int w, uint32_t kslot_) {
+        uint32_t& sc = w ? sc1 : sc0;
         pf.lap(6);
-        alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
-        pf.lap(2);
+        if (sc > 0)   // the softmax has read the previous S of this tile
+          alive = ptx::wait_bounded(bar(L::bSFree + w), (sc - 1) & 1, wd, kSiteSFree) && alive;
+        pf.lap(16);
         ptx::tc_fence_after();
-        trace_event(p, 2, tr, kEvUnit, k_units);
-
-        uint32_t kslot = next_full();
         if (alive) {
-          if (u.n0 > 0) {
-            issue_s(tS0, q_lo0, k_lo0 + kslot * kSlotLo);
-            ptx::mma_commit(bar(L::bSFull + 0));
-          }
-          if (u.n1 > 0) {
-            issue_s(tS1, q_lo1, k_lo0 + kslot * kSlotLo);
-            ptx::mma_commit(bar(L::bSFull + 1));
-          }
-          ptx::mma_commit(bar(L::bKvEmpty + kslot));
-          if (nkv == 1) ptx::mma_commit(bar(L::bQEmpty));
-          issued_any = true;
+          issue_s(w ? tS1 : tS0, w ? q_lo1 : q_lo0, k_lo0 + kslot_ * kSlotLo);
+          ptx::mma_commit(bar(L::bSFull + w));
         }
-        for (int j = 0; j < nkv; ++j) {
-          const uint32_t vslot = next_full();
-          const uint32_t v_lo = v_lo0 + vslot * kSlotLo;
-          const bool more = j + 1 < nkv;
-          // ---- PV0_j
-          if (j < u.n0) {
-            pf.lap(6);
-            if (j == 0 && ucnt0 > 0)   // O0 of the previous unit must have been read out
-              alive = ptx::wait_bounded(bar(L::bOFree + 0), (ucnt0 - 1) & 1, wd, kSiteOFree) && alive;
-            pf.lap(3);
-            alive = ptx::wait_bounded(bar(L::bPFull + 0), pph0, wd, kSitePFull) && alive;
-            pf.lap(1);
-            pph0 ^= 1u;
-            ptx::tc_fence_after();
-            if (alive) {
-              trace_event(p, 2, tr, kEvPvIssue, j);
-              issue_pv(tO0, tS0, v_lo, j > 0 ? 1u : 0u);
-              pf.lap(5);
-              pf.count(7);
-              if (j == u.n0 - 1) ptx::mma_commit(bar(L::bODone + 0));
-            }
-          }
-          if (more) kslot = next_full();
-          // ---- S0_{j+1}
-          if (alive && more && j + 1 < u.n0) {
-            trace_event(p, 2, tr, kEvSIssue, j + 1);
-            pf.lap(6);
-            issue_s(tS0, q_lo0, k_lo0 + kslot * kSlotLo);
-            pf.lap(4);
-            pf.count(7);
-            ptx::mma_commit(bar(L::bSFull + 0));
-          }
-          // ---- PV1_j
-          if (j < u.n1) {
-            pf.lap(6);
-            if (j == 0 && ucnt1 > 0)
-              alive = ptx::wait_bounded(bar(L::bOFree + 1), (ucnt1 - 1) & 1, wd, kSiteOFree) && alive;
-            pf.lap(3);
-            alive = ptx::wait_bounded(bar(L::bPFull + 1), pph1, wd, kSitePFull) && alive;
-            pf.lap(1);
-            pph1 ^= 1u;
-            ptx::tc_fence_after();
-            if (alive) {
-              trace_event(p, 2, tr, kEvPvIssue, (1u << 16) | j);
-              issue_pv(tO1, tS1, v_lo, j > 0 ? 1u : 0u);
-              pf.lap(5);
-              pf.count(7);
-              if (j == u.n1 - 1) ptx::mma_commit(bar(L::bODone + 1));
-            }
-          }
-          if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
-          // ---- S1_{j+1}
-          if (alive && more && j + 1 < u.n1) {
-            trace_event(p, 2, tr, kEvSIssue, (1u << 16) | (j + 1));
-            pf.lap(6);
-            issue_s(tS1, q_lo1, k_lo0 + kslot * kSlotLo);
-            pf.lap(4);
-            pf.count(7);
-            ptx::mma_commit(bar(L::bSFull + 1));
-          }
-          if (alive && more) {
-            ptx::mma_commit(bar(L::bKvEmpty + kslot));
-            if (j + 2 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
-          }
+        ++sc;
+        pf.lap(4);
+        pf.count(7);
+      };
+      auto issue_pv_own = [&](int w, int j, uint32_t v_lo) {
+        uint32_t& pph = w ? pph1 : pph0;
+        const uint32_t ucnt = w ? ucnt1 : ucnt0;
+        pf.lap(6);
+        if (j == 0 && ucnt > 0)   // O_w of the previous piece must have been read out
+          alive = ptx::wait_bounded(bar(L::bOFree + w), (ucnt - 1) & 1, wd, kSiteOFree) && alive;
+        pf.lap(3);
+        alive = ptx::wait_bounded(bar(L::bPFull + w), pph, wd, kSitePFull) && alive;
+        pf.lap(1);
+        pph ^= 1u;
+        ptx::tc_fence_after();
+        if (alive) {
+          issue_pv(w ? tO1 : tO0, w ? tP1 : tP0, v_lo, j > 0 ? 1u : 0u);
+          ptx::mma_commit(bar(L::bPvDone + w));
         }
-        if (u.n0 > 0) ++ucnt0;
-        if (u.n1 > 0) ++ucnt1;
-        ++k_units;
+        pf.lap(5);
+        pf.count(7);
+      };
+      // The producer fills the ring with K0 K1 V0 K2 V1 ... K_{n-1} V_{n-2}
+      // V_{n-1} for a piece of n key tiles: 2n loads from ring position
+      // `base`; each issuer waits only for the tiles it reads.
+      auto ring_wait = [&](uint32_t pos) -> uint32_t {
+        const uint32_t sl = pos % L::kStages;
+        pf.lap(6);
+        alive = ptx::wait_bounded(bar(L::bKvFull + sl), (pos / L::kStages) & 1, wd, kSiteKvFull) &&
+                alive;
+        pf.lap(0);
+        ptx::tc_fence_after();
+        return sl;
+      };
+      uint32_t base = 0;
+      if (warp == kMmaWarp) {
+        // S = Q K^T for both query tiles, one key tile ahead of the softmax
+        while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+          const int nkv = max(u.n0, u.n1);
+          pf.lap(6);
+          alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
+          pf.lap(2);
+          ptx::tc_fence_after();
+          for (int j = 0; j < nkv; ++j) {
+            const uint32_t kslot = ring_wait(base + (j == 0 ? 0u : 2u * j - 1u));
+            if (j < u.n0) issue_s_own(0, kslot);
+            if (j < u.n1) issue_s_own(1, kslot);
+            if (alive) {
+              ptx::mma_commit(bar(L::bKvEmpty + kslot));
+              if (j + 1 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
+            }
+            issued_any = true;
+          }
+          base += 2u * nkv;
+          ++k_units;
+        }
+      } else {
+        // O += P V for both query tiles, as soon as the softmax has written P
+        while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+          const int nkv = max(u.n0, u.n1);
+          for (int j = 0; j < nkv; ++j) {
+            const uint32_t vslot =
+                ring_wait(base + (j + 1 < nkv ? 2u * j + 2u : 2u * nkv - 1u));
+            const uint32_t v_lo = v_lo0 + vslot * kSlotLo;
+            if (j < u.n0) issue_pv_own(0, j, v_lo);
+            if (j < u.n1) issue_pv_own(1, j, v_lo);
+            if (alive) ptx::mma_commit(bar(L::bKvEmpty + vslot));
+            issued_any = true;
+          }
+          if (u.n0 > 0) ++ucnt0;
+          if (u.n1 > 0) ++ucnt1;
+          base += 2u * nkv;
+        }
       }
       pf.lap(6);
-      const bool pv_thread = OwnP<D>::kOn && warp == kPvWarp;
+      const bool pv_thread = (warp == kPvWarp);
       pf.flush(p, pv_thread ? 3 : 2);
       // Drain: every MMA issued by this thread has completed before TMEM is freed.
       if (issued_any) {
@@ -770,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = sbase + L::kO + w * L::kTile;   // used when kTmaStore
     const float c = p.scale_log2;
     uint32_t scnt = 0, ucnt = 0;
-    uint32_t pvcnt = 0;                       // P.V products of this tile waited for (own P)
+    uint32_t pvcnt = 0;                       // P.V products of this tile waited for
     uint32_t tr = 0;                          // trace events recorded (thread t == 0)
     const bool tracer = (t == 0);
     Prof pf;   // FA_PROFILE: 0 s wait, 1 load S, 2 max + rescale, 3 exp/sum/pack, 4 store P + arrive,
@@ -804,10 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sv[kBN];
 #pragma unroll
         for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(sr[i]);
-        if constexpr (OwnP<D>::kOn) {
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(L::bSFree + w));   // S_w may be overwritten now
-        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bSFree + w));     // S_w may be overwritten now
         pf.lap(1);
 
         // mask: keys past N, and on the diagonal tile keys after this row
@@ -844,9 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           neg_m = nm;
         }
         const bool rescale = j > 0 && __any_sync(0xffffffffu, grow);
-        // O_w *= alpha.  PV_w_{j-1} must be complete (when P overwrites S it
-        // was issued before S_w_j; with its own P the caller waits for it),
-        // and PV_w_j cannot start before this warpgroup arrives on p_full.
+        // O_w *= alpha.  PV_w_{j-1} must be complete (waited for below) and
+        // PV_w_j cannot start before this warpgroup arrives on p_full.
         auto rescale_o = [&]() {
           if (tracer) trace_event(p, w, tr, kEvRescale, j);
           pf.count(9);
@@ -860,7 +728,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st32(tO + q4 * 32, orr);
           }
         };
-        if (!OwnP<D>::kOn && rescale) rescale_o();
 
         pf.lap(2);
         // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM.
@@ -887,18 +754,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += (a + b) + (cc + dd);
         }
         pf.lap(3);
-        if constexpr (OwnP<D>::kOn) {
-          // P_w and O_w are still in use by PV_w_{j-1} until it completes.
-          if (j > 0) {
-            pf.lap(3);
-            ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
-            ++pvcnt;
-            pf.lap(16);
-            __syncwarp();
-            ptx::tc_fence_after();
-          }
-          if (rescale) rescale_o();
+        // P_w and O_w are still in use by PV_w_{j-1} until it completes.
+        if (j > 0) {
+          pf.lap(3);
+          ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
+          ++pvcnt;
+          pf.lap(16);
+          __syncwarp();
+          ptx::tc_fence_after();
         }
+        if (rescale) rescale_o();
         if constexpr (OwnP<D>::kSmem) {
           // row t of the P_w tile: 16 pieces of 8 keys, 128-byte swizzle
           uint8_t* prow = sgen + L::kP + w * (kBM * kBN * 2) + t * 128;
@@ -920,12 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- epilogue: O / l in the storage dtype, and LSE = m + ln l per row
       pf.lap(7);
-      if constexpr (OwnP<D>::kOn) {
-        ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);   // last PV_w
-        ++pvcnt;
-      } else {
-        ptx::wait_bounded(bar(L::bODone + w), ucnt & 1, wd, kSiteODone);
-      }
+      ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);   // last PV_w
+      ++pvcnt;
       pf.lap(5);
       ++ucnt;
       if (tracer) trace_event(p, w, tr, kEvEpiStart, ucnt - 1);
