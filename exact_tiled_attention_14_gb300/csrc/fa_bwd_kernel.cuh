@@ -15,12 +15,12 @@
 // Three kernels, launched in this order on one stream:
 //   fa_bwd_delta_kernel  D = rowsum(dO * O), memory-bound, one pass over O, dO.
 //   fa_bwd_dkdv_kernel   one CTA per (batch*head, key tile j): K_j, V_j stay in
-//                        shared memory while (Q_i, dO_i) stream past; rebuilds
+//                        shared memory while Q_i and dO_i stream past; rebuilds
 //                        S^T = K_j Q_i^T and dP^T = V_j dO_i^T on the tensor
 //                        core, forms P^T and dS^T in registers, accumulates
 //                        dV_j and dK_j in TMEM.
 //   fa_bwd_dq_kernel     one CTA per (batch*head, query tile i): Q_i, dO_i stay
-//                        while (K_j, V_j) stream past; rebuilds S and dP, forms
+//                        while K_j and V_j stream past; rebuilds S and dP, forms
 //                        dS, accumulates dQ_i in TMEM.
 // Each gradient row is written by exactly one CTA, so there are no atomics
 // and the result is deterministic; the price is that S and dP are formed
@@ -31,8 +31,24 @@
 // in dq) and on column half w/4 of each 128-column tile, so a row's 128
 // scores are shared by two threads; warp 8 issues the tcgen05 MMAs from one
 // thread; warp 9 issues the TMA loads from one thread.  TMEM: S (or S^T) in
-// columns 0-127, dP (dP^T) in 128-255, the fp32 accumulators from 256.  The 16-bit P^T and dS^T (dS)
-// overwrite the first 64 columns of S^T and dP^T (S) once those are read.
+// columns 0-127, dP (dP^T) in 128-255, the fp32 accumulators from 256.  The
+// streamed operands come through two rings: ring A holds the operand the
+// last product of a tile still reads (Q_i in dkdv, K_j in dq), ring B the
+// other one (dO_i, V_j), so B's slots free up earlier.
+//
+// Overlap.  The tensor core is kept busy while the element-wise warps work:
+//   dkdv  the element-wise pass runs in two phases.  Phase 1 turns S^T_i into
+//         P^T_i and writes it, 16-bit, over the S^T columns the same warp has
+//         just read (columns 0-31 and 64-95); phase 2 does the same with
+//         dP^T_i and dS^T_i (columns 128-159 and 192-223).  The MMA thread
+//         issues dV_j += P^T_i dO_i as soon as phase 1 is done, then S^T_{i+1},
+//         then dK_j += dS^T_i Q_i once phase 2 is done, then dP^T_{i+1}: each
+//         product that overwrites a 16-bit operand follows the one that reads
+//         it in the thread's order.  Phase 1 of tile i+1 runs while the
+//         tensor core works on dK_j and dP^T_{i+1}.
+//   dq    dS goes to TMEM columns of its own (two buffers after dQ), so
+//         S_{j+1} and dP_{j+1} are issued as soon as the element-wise warps
+//         have read S_j and dP_j, and dQ_i += dS_j K_j when dS_j is written.
 #pragma once
 
 #include <cuda.h>
@@ -52,7 +68,8 @@ constexpr uint32_t kBwdTmemCols = 512;
 // Sites recorded in the status word when a wait of a backward kernel runs out.
 enum BwdWaitSite : uint32_t {
   kSiteBwdEmpty = 20, kSiteBwdRes = 21, kSiteBwdFull = 22, kSiteBwdSFull = 23,
-  kSiteBwdPFull = 24, kSiteBwdDone = 25
+  kSiteBwdPFull = 24, kSiteBwdDone = 25, kSiteBwdDpFull = 26, kSiteBwdDsReady = 27,
+  kSiteBwdDsFree = 28, kSiteBwdSFree = 29
 };
 
 struct BwdParams {
@@ -74,25 +91,37 @@ struct BwdParams {
   float scale_log2;    // scale * log2(e)
 };
 
-// Shared memory of the two tensor-core kernels: a resident pair of tiles (K_j,
-// V_j or Q_i, dO_i), a ring of streamed pairs, the per-query LSE and D of the
-// current query tile (dkdv only, double-buffered), and the barriers.
-template <int D>
+// Shared memory of the two tensor-core kernels: the resident pair of tiles
+// (K_j, V_j or Q_i, dO_i), ring A and ring B of streamed tiles, kVecBytes of
+// per-query vectors (dkdv: -LSE in log2 units and D of the current query
+// tile), the ring barriers and eight kernel-specific barriers.
+template <int D, int kVecBytes>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kBwdTile * D * 2;
   static constexpr int kChunkBytes = kBwdTile * 128;
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStagesA = (D == 128) ? 3 : 6;
+  static constexpr int kStagesB = (D == 128) ? 2 : 4;
   static constexpr int kRes = 0;
-  static constexpr int kRing = kRes + 2 * kTile;
-  static constexpr int kVec = kRing + kStages * 2 * kTile;   // [2 buffers][2 vectors][128] floats
-  static constexpr int kBar = kVec + 2 * 2 * kBwdTile * 4;
-  static constexpr int bFull = 0, bEmpty = kStages, bRes = 2 * kStages, bSFull = bRes + 1,
-                       bPFull = bSFull + 1, bDone = bPFull + 1, kNumBars = bDone + 1;
+  static constexpr int kRingA = kRes + 2 * kTile;
+  static constexpr int kRingB = kRingA + kStagesA * kTile;
+  static constexpr int kVec = kRingB + kStagesB * kTile;
+  static constexpr int kBar = kVec + kVecBytes;
+  static constexpr int bFullA = 0, bEmptyA = kStagesA, bFullB = 2 * kStagesA,
+                       bEmptyB = bFullB + kStagesB, bRes = bEmptyB + kStagesB, bX = bRes + 1,
+                       kNumBars = bX + 8;
   static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+// Kernel-specific barriers (offsets from bX).
+struct DkdvBars {
+  static constexpr int kSFull = 0, kDpFull = 1, kPReady = 2, kDsReady = 3, kDone = 4;
+};
+struct DqBars {
+  static constexpr int kSFull = 0, kSFree = 1, kPFull = 2, kDsFree = 4, kDone = 6;   // PFull, DsFree: 2 each
 };
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
@@ -134,8 +163,8 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const uint4* __restri
 // TMEM columns.
 constexpr uint32_t kColS = 0, kColDp = 128, kColAcc = 256;
 
-// Issue A (K-major, resident) x B^T (K-major) over the head width into d_tmem:
-// M = N = 128, K = D in steps of 16 columns.
+// Issue A (K-major, shared memory) x B^T (K-major) over the head width into
+// d_tmem: M = N = 128, K = D in steps of 16 columns.
 template <int D, int Chunk>
 __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                              uint32_t idesc) {
@@ -147,13 +176,18 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_lo, uin
 }
 
 // Issue A (16-bit, in TMEM, 128 rows x 128 along K) x B (MN-major tile of 128
-// rows along K, D columns) into d_tmem (N = D).
+// rows along K, D columns) into d_tmem (N = D).  kSplitA: A's 64 packed
+// columns sit in two blocks of 32 at a_tmem and a_tmem + 64 (a 16-bit tile
+// written over the fp32 columns each half of the warps read).
+template <bool kSplitA>
 __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                              uint32_t idesc, uint32_t acc) {
 #pragma unroll
-  for (int kk = 0; kk < kBwdTile / 16; ++kk)
-    ptx::mma_ts(d_tmem, a_tmem + kk * 8, ptx::desc_sw128(b_lo + kk * (2048 >> 4)), idesc,
+  for (int kk = 0; kk < kBwdTile / 16; ++kk) {
+    const uint32_t acol = kSplitA ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
+    ptx::mma_ts(d_tmem, a_tmem + acol, ptx::desc_sw128(b_lo + kk * (2048 >> 4)), idesc,
                 kk > 0 ? 1u : acc);
+  }
 }
 
 // Write columns [c0, c0 + NC) of one row of a TMEM accumulator (fp32), times
@@ -180,11 +214,11 @@ __device__ __forceinline__ void store_acc_cols(uint32_t t_acc, int c0, float mul
 }
 
 // Shared setup of the two tensor-core kernels: TMEM allocation by the MMA
-// warp, barrier initialisation by the load thread.
-template <int D>
+// warp; the ring barriers and, through `init_x(bar)`, the kernel's own
+// barriers initialised by the load thread.
+template <class L, class InitX>
 __device__ __forceinline__ uint32_t bwd_setup(uint32_t sbase, uint8_t* sgen, int warp,
-                                              uint32_t pfull_count) {
-  using L = BwdSmem<D>;
+                                              InitX init_x) {
   uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sgen + L::kMisc);
   if (warp == kBwdMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_base_ptr), kBwdTmemCols);
@@ -193,14 +227,16 @@ __device__ __forceinline__ uint32_t bwd_setup(uint32_t sbase, uint8_t* sgen, int
   if (threadIdx.x == kBwdLoadWarp * 32) {
     *reinterpret_cast<volatile int*>(sgen + L::kMisc + 4) = 0;
     auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
-    for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::bFull + s), 1);
-      ptx::mbar_init(bar(L::bEmpty + s), 1);
+    for (int s = 0; s < L::kStagesA; ++s) {
+      ptx::mbar_init(bar(L::bFullA + s), 1);
+      ptx::mbar_init(bar(L::bEmptyA + s), 1);
+    }
+    for (int s = 0; s < L::kStagesB; ++s) {
+      ptx::mbar_init(bar(L::bFullB + s), 1);
+      ptx::mbar_init(bar(L::bEmptyB + s), 1);
     }
     ptx::mbar_init(bar(L::bRes), 1);
-    ptx::mbar_init(bar(L::bSFull), 1);
-    ptx::mbar_init(bar(L::bPFull), pfull_count);
-    ptx::mbar_init(bar(L::bDone), 1);
+    init_x(bar);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -211,14 +247,14 @@ __device__ __forceinline__ uint32_t bwd_setup(uint32_t sbase, uint8_t* sgen, int
 }
 
 // The load thread: the resident pair (res_a, res_b at tile `res_tile`), then
-// the streamed pairs (str_a, str_b) of tiles first .. first + count - 1.
-template <int D>
+// tiles first .. first + count - 1 of str_a into ring A and of str_b into
+// ring B, in the order A_0, B_0, A_1, B_1, ...
+template <class L>
 __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* res_a,
                                              const CUtensorMap* res_b, int res_tile,
                                              const CUtensorMap* str_a, const CUtensorMap* str_b,
                                              int first, int count, int bh,
                                              const ptx::Watchdog& wd) {
-  using L = BwdSmem<D>;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   bool alive = true;
   ptx::mbar_arrive_expect_tx(bar(L::bRes), 2 * L::kTile);
@@ -228,40 +264,59 @@ __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* 
     ptx::tma_load_3d(sbase + L::kRes + L::kTile + c * L::kChunkBytes, res_b, bar(L::bRes), c * 64,
                      res_tile * kBwdTile, bh);
   }
-  int loads = 0;
-  for (int it = 0; it < count; ++it) {
-    const int slot = it % L::kStages, use = it / L::kStages;
+  // one tile of `tm` into slot `slot` of a ring, once its previous use is over
+  auto load = [&](const CUtensorMap* tm, int ring, int full0, int empty0, int stages, int it) {
+    const int slot = it % stages, use = it / stages;
     if (use > 0)
-      alive = ptx::wait_bounded(bar(L::bEmpty + slot), (use - 1) & 1, wd, kSiteBwdEmpty) && alive;
+      alive = ptx::wait_bounded(bar(empty0 + slot), (use - 1) & 1, wd, kSiteBwdEmpty) && alive;
+    if (!alive) return;
+    const uint32_t dst = sbase + ring + slot * L::kTile;
+    ptx::mbar_arrive_expect_tx(bar(full0 + slot), L::kTile);
+    for (int c = 0; c < L::kChunks; ++c)
+      ptx::tma_load_3d(dst + c * L::kChunkBytes, tm, bar(full0 + slot), c * 64,
+                       (first + it) * kBwdTile, bh);
+  };
+  int loads = 0;
+  for (int it = 0; it < count && alive; ++it) {
+    load(str_a, L::kRingA, L::bFullA, L::bEmptyA, L::kStagesA, it);
     if (!alive) break;
-    const uint32_t dst = sbase + L::kRing + slot * 2 * L::kTile;
-    ptx::mbar_arrive_expect_tx(bar(L::bFull + slot), 2 * L::kTile);
-    for (int c = 0; c < L::kChunks; ++c) {
-      ptx::tma_load_3d(dst + c * L::kChunkBytes, str_a, bar(L::bFull + slot), c * 64,
-                       (first + it) * kBwdTile, bh);
-      ptx::tma_load_3d(dst + L::kTile + c * L::kChunkBytes, str_b, bar(L::bFull + slot), c * 64,
-                       (first + it) * kBwdTile, bh);
+    load(str_b, L::kRingB, L::bFullB, L::bEmptyB, L::kStagesB, it);
+    if (!alive) {   // tile `it` of ring A was issued: drain it too
+      ptx::wait_drain(bar(L::bFullA + it % L::kStagesA), (it / L::kStagesA) & 1, 200000000ull);
+      break;
     }
     ++loads;
   }
   // Drain: every issued copy has landed before the CTA can exit.
   const unsigned long long drain = 200000000ull;
   ptx::wait_drain(bar(L::bRes), 0, drain);
-  for (int l = loads > L::kStages ? loads - L::kStages : 0; l < loads; ++l)
-    ptx::wait_drain(bar(L::bFull + l % L::kStages), (l / L::kStages) & 1, drain);
+  for (int l = loads > L::kStagesA ? loads - L::kStagesA : 0; l < loads; ++l)
+    ptx::wait_drain(bar(L::bFullA + l % L::kStagesA), (l / L::kStagesA) & 1, drain);
+  for (int l = loads > L::kStagesB ? loads - L::kStagesB : 0; l < loads; ++l)
+    ptx::wait_drain(bar(L::bFullB + l % L::kStagesB), (l / L::kStagesB) & 1, drain);
 }
 
 // ---------------------------------------------------------------- dK, dV
+// Per-query vectors of the dkdv kernel: one buffer at d = 128 (shared memory
+// is full), two at d = 64.
+template <int D>
+struct DkdvVec {
+  static constexpr int kBufs = (D == 128) ? 1 : 2;
+  static constexpr int kBytes = kBufs * 2 * kBwdTile * 4;
+};
+
 template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, DkdvVec<D>::kBytes>;
+  using X = DkdvBars;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  auto xbar = [&](int i) -> uint32_t { return bar(L::bX + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
 
   // Key tile kt of head bh; for causal runs the first key tiles (the most
@@ -271,46 +326,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int i0 = kCausal ? kt : 0;           // query tiles i >= kt see this key tile
   const int nq = p.n_tiles - i0;
 
-  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, kBwdEwThreads);
+  const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
+    ptx::mbar_init(b(L::bX + X::kSFull), 1);
+    ptx::mbar_init(b(L::bX + X::kDpFull), 1);
+    ptx::mbar_init(b(L::bX + X::kPReady), kBwdEwThreads);
+    ptx::mbar_init(b(L::bX + X::kDsReady), kBwdEwThreads);
+    ptx::mbar_init(b(L::bX + X::kDone), 1);
+  });
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0) bwd_producer<D>(sbase, &p.tm_k, &p.tm_v, kt, &p.tm_q, &p.tm_do, i0, nq, bh, wd);
+    if (lane == 0) bwd_producer<L>(sbase, &p.tm_k, &p.tm_v, kt, &p.tm_q, &p.tm_do, i0, nq, bh, wd);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBwdTile, kBwdTile, fmt, 0);
       constexpr uint32_t idesc_o = ptx::idesc_f16(kBwdTile, D, fmt, 1);
+      constexpr uint32_t kSlotLo = L::kTile >> 4;
       const uint32_t k_lo = ptx::desc_lo(sbase + L::kRes, 16);
       const uint32_t v_lo = ptx::desc_lo(sbase + L::kRes + L::kTile, 16);
-      const uint32_t q_lo0 = ptx::desc_lo(sbase + L::kRing, 16);                  // K-major use
-      const uint32_t do_lo0 = ptx::desc_lo(sbase + L::kRing + L::kTile, 16);
-      const uint32_t q_mn0 = ptx::desc_lo(sbase + L::kRing, L::kChunkBytes);      // MN-major use
-      const uint32_t do_mn0 = ptx::desc_lo(sbase + L::kRing + L::kTile, L::kChunkBytes);
-      constexpr uint32_t kSlotLo = (2 * L::kTile) >> 4;
+      const uint32_t q_lo0 = ptx::desc_lo(sbase + L::kRingA, 16);                  // K-major use
+      const uint32_t do_lo0 = ptx::desc_lo(sbase + L::kRingB, 16);
+      const uint32_t q_mn0 = ptx::desc_lo(sbase + L::kRingA, L::kChunkBytes);      // MN-major use
+      const uint32_t do_mn0 = ptx::desc_lo(sbase + L::kRingB, L::kChunkBytes);
       const uint32_t tS = tmem_base + kColS, tDp = tmem_base + kColDp;
       const uint32_t tDv = tmem_base + kColAcc, tDk = tmem_base + kColAcc + D;
+      auto full_a = [&](int it) {
+        return ptx::wait_bounded(bar(L::bFullA + it % L::kStagesA), (it / L::kStagesA) & 1, wd,
+                                 kSiteBwdFull);
+      };
+      auto full_b = [&](int it) {
+        return ptx::wait_bounded(bar(L::bFullB + it % L::kStagesB), (it / L::kStagesB) & 1, wd,
+                                 kSiteBwdFull);
+      };
+      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (keys on the TMEM lanes)
+      auto issue_s = [&](int it) {
+        issue_kmajor<D, L::kChunkBytes>(tS, k_lo, q_lo0 + (it % L::kStagesA) * kSlotLo, idesc_s);
+        ptx::mma_commit(xbar(X::kSFull));
+      };
+      auto issue_dp = [&](int it) {
+        issue_kmajor<D, L::kChunkBytes>(tDp, v_lo, do_lo0 + (it % L::kStagesB) * kSlotLo, idesc_s);
+        ptx::mma_commit(xbar(X::kDpFull));
+      };
       bool alive = ptx::wait_bounded(bar(L::bRes), 0, wd, kSiteBwdRes);
-      for (int it = 0; it < nq; ++it) {
-        const uint32_t slot = it % L::kStages;
-        alive = ptx::wait_bounded(bar(L::bFull + slot), (it / L::kStages) & 1, wd, kSiteBwdFull) && alive;
-        ptx::tc_fence_after();
-        if (!alive) break;
-        // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (keys on the TMEM lanes)
-        issue_kmajor<D, L::kChunkBytes>(tS, k_lo, q_lo0 + slot * kSlotLo, idesc_s);
-        issue_kmajor<D, L::kChunkBytes>(tDp, v_lo, do_lo0 + slot * kSlotLo, idesc_s);
-        ptx::mma_commit(bar(L::bSFull));
-        alive = ptx::wait_bounded(bar(L::bPFull), it & 1, wd, kSiteBwdPFull) && alive;
-        ptx::tc_fence_after();
-        if (!alive) break;
-        // dV_j += P^T dO_i and dK_j += dS^T Q_i (scale applied at the end)
-        issue_tmem_a(tDv, tS, do_mn0 + slot * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
-        issue_tmem_a(tDk, tDp, q_mn0 + slot * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(L::bEmpty + slot));
+      alive = alive && full_a(0) && full_b(0);
+      ptx::tc_fence_after();
+      if (alive) {
+        issue_s(0);
+        issue_dp(0);
       }
-      ptx::mma_commit(bar(L::bDone));
-      ptx::wait_drain(bar(L::bDone), 0, 200000000ull);
+      for (int it = 0; alive && it < nq; ++it) {
+        const bool more = it + 1 < nq;
+        alive = ptx::wait_bounded(xbar(X::kPReady), it & 1, wd, kSiteBwdPFull);
+        ptx::tc_fence_after();
+        if (!alive) break;
+        // dV_j += P^T dO_i; P^T sits in TMEM columns 0-31 and 64-95
+        issue_tmem_a<true>(tDv, tS, do_mn0 + (it % L::kStagesB) * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(L::bEmptyB + it % L::kStagesB));
+        if (more) {
+          alive = full_a(it + 1);
+          ptx::tc_fence_after();
+          if (!alive) break;
+          issue_s(it + 1);   // after dV in this thread's order: P^T has been read
+        }
+        alive = ptx::wait_bounded(xbar(X::kDsReady), it & 1, wd, kSiteBwdDsReady);
+        ptx::tc_fence_after();
+        if (!alive) break;
+        // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
+        issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
+        if (more) {
+          alive = full_b(it + 1);
+          ptx::tc_fence_after();
+          if (!alive) break;
+          issue_dp(it + 1);  // after dK: dS^T has been read
+        }
+      }
+      ptx::mma_commit(xbar(X::kDone));
+      ptx::wait_drain(xbar(X::kDone), 0, 200000000ull);
     }
     __syncwarp();
   } else {
@@ -318,63 +412,111 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quarter = warp & 3, half = warp >> 2;
     const int t = quarter * 32 + lane;                    // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem_base + lane_off + kColS, tDp = tmem_base + lane_off + kColDp;
+    // this thread's 64 query columns of S^T and dP^T
+    const uint32_t tS = tmem_base + lane_off + kColS + half * 64;
+    const uint32_t tDp = tmem_base + lane_off + kColDp + half * 64;
     const long long key = static_cast<long long>(kt) * kBwdTile + t;
-    const float c = p.scale_log2;
-    float* vec = reinterpret_cast<float*>(sgen + L::kVec);   // [2][2][128]
+    const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     const float* lse_h = p.lse + static_cast<long long>(bh) * p.N;
     const float* del_h = p.delta + static_cast<long long>(bh) * p.N;
+    // -LSE (log2 units) and D of query row t of tile i, fetched one tile
+    // ahead by the first half of the warps; a query past N gets -LSE = -inf,
+    // so its P is 0.
+    auto fetch = [&](int i, float& nl, float& dd) {
+      const int qrow = i * kBwdTile + t;
+      nl = qrow < p.N ? -lse_h[qrow] * 1.4426950408889634f : -INFINITY;
+      dd = qrow < p.N ? del_h[qrow] : 0.f;
+    };
+    float nl_next = 0.f, d_next = 0.f;
+    if (half == 0) fetch(i0, nl_next, d_next);
     for (int it = 0; it < nq; ++it) {
       const int i = i0 + it;
-      // LSE (in log2 units) and D of the 128 queries of tile i; a query past
-      // N gets LSE = +inf, so its P is 0.
-      float* lv = vec + (it & 1) * 256;
+      // vectors of tile i: [0,128) -LSE, [128,256) D
+      float* vec = reinterpret_cast<float*>(sgen + L::kVec) + (it % DkdvVec<D>::kBufs) * 256;
+      // with one buffer, every thread must be done with the previous tile's
+      if (DkdvVec<D>::kBufs == 1 && it > 0) ptx::named_bar_sync(1, kBwdEwThreads);
       if (half == 0) {
-        const int qrow = i * kBwdTile + t;
-        lv[t] = qrow < p.N ? lse_h[qrow] * 1.4426950408889634f : INFINITY;
-        lv[128 + t] = qrow < p.N ? del_h[qrow] : 0.f;
+        vec[t] = nl_next;
+        vec[128 + t] = d_next;
+        if (it + 1 < nq) fetch(i + 1, nl_next, d_next);
       }
-      ptx::named_bar_sync(1, kBwdEwThreads);
-      ptx::wait_bounded(bar(L::bSFull), it & 1, wd, kSiteBwdSFull);
+      ptx::named_bar_sync(2, kBwdEwThreads);
+      const float4* nl4 = reinterpret_cast<const float4*>(vec) + half * 16;
+      const float4* dl4 = reinterpret_cast<const float4*>(vec + 128) + half * 16;
+
+      // ---- phase 1: P^T = 2^(S^T c - LSE) over this thread's 64 queries
+      ptx::wait_bounded(xbar(X::kSFull), it & 1, wd, kSiteBwdSFull);
       __syncwarp();
       ptx::tc_fence_after();
-      // this thread's 64 query columns of S^T and dP^T, 32 at a time
-      const bool diag = kCausal && i == kt;
-      uint32_t pk[32], dk[32];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32], dpr[32];
-        ptx::tmem_ld32(tS + half * 64 + ch * 32, sr);
-        ptx::tmem_ld32(tDp + half * 64 + ch * 32, dpr);
+      float pf[64];
+      {
+        uint32_t sr[64];
+        ptx::tmem_ld32(tS, sr);
+        ptx::tmem_ld32(tS + 32, sr + 32);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int qc = half * 64 + ch * 32 + e;         // query column within the tile
-          float p0 = ptx::ex2(fmaf(__uint_as_float(sr[e]), c, -lv[qc]));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(sr[e + 1]), c, -lv[qc + 1]));
-          if (diag) {                                     // key after the query: masked
-            if (i * kBwdTile + qc < key) p0 = 0.f;
-            if (i * kBwdTile + qc + 1 < key) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(dpr[e]) - lv[128 + qc]);
-          const float d1 = p1 * (__uint_as_float(dpr[e + 1]) - lv[128 + qc + 1]);
-          pk[ch * 16 + e / 2] = ptx::pack2<kBf16>(p0, p1);
-          dk[ch * 16 + e / 2] = ptx::pack2<kBf16>(d0, d1);
+        for (int e = 0; e < 64; e += 4) {
+          const float4 nl = nl4[e / 4];
+          float x0, x1, x2, x3;
+          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                    c2, ptx::f2_pack(nl.x, nl.y)), x0, x1);
+          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
+                                    c2, ptx::f2_pack(nl.z, nl.w)), x2, x3);
+          pf[e] = ptx::ex2(x0);
+          pf[e + 1] = ptx::ex2(x1);
+          pf[e + 2] = ptx::ex2(x2);
+          pf[e + 3] = ptx::ex2(x3);
         }
       }
-      // P^T and dS^T go to the first 64 columns of S^T and dP^T, which the
-      // other half's warps read: every load is done before any store.
-      ptx::named_bar_sync(2, kBwdEwThreads);
-      ptx::tmem_st16(tS + half * 32, pk);
-      ptx::tmem_st16(tS + half * 32 + 16, pk + 16);
-      ptx::tmem_st16(tDp + half * 32, dk);
-      ptx::tmem_st16(tDp + half * 32 + 16, dk + 16);
+      if (kCausal && i == kt) {   // diagonal tile: a key after the query is masked
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (i * kBwdTile + half * 64 + e < key) pf[e] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
+        ptx::tmem_st16(tS, pk);          // over S^T columns this warp has read
+        ptx::tmem_st16(tS + 16, pk + 16);
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bPFull));
+      ptx::mbar_arrive(xbar(X::kPReady));
+
+      // ---- phase 2: dS^T = P^T * (dP^T - D)
+      ptx::wait_bounded(xbar(X::kDpFull), it & 1, wd, kSiteBwdDpFull);
+      __syncwarp();
+      ptx::tc_fence_after();
+      uint32_t dk[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dpr[32];
+        ptx::tmem_ld32(tDp + ch * 32, dpr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 dd = dl4[(ch * 32 + e) / 4];
+          const int f = ch * 32 + e;
+          float d0, d1, d2, d3;
+          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f], pf[f + 1]),
+                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])),
+                                               ptx::f2_pack(-dd.x, -dd.y))), d0, d1);
+          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f + 2], pf[f + 3]),
+                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e + 2]), __uint_as_float(dpr[e + 3])),
+                                               ptx::f2_pack(-dd.z, -dd.w))), d2, d3);
+          dk[f / 2] = ptx::pack2<kBf16>(d0, d1);
+          dk[f / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
+        }
+      }
+      ptx::tmem_st16(tDp, dk);           // over dP^T columns this warp has read
+      ptx::tmem_st16(tDp + 16, dk + 16);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(xbar(X::kDsReady));
     }
     // dV_j rows (warps 0-3) and dK_j = scale * (dS^T Q) rows (warps 4-7)
-    ptx::wait_bounded(bar(L::bDone), 0, wd, kSiteBwdDone);
+    ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
     const long long row = static_cast<long long>(bh) * p.N + key;
@@ -394,16 +536,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dQ
+// TMEM columns of the two dS buffers (16-bit, 64 packed columns each), after dQ.
+template <int D>
+__device__ __forceinline__ uint32_t dq_ds_col(int b) {
+  return kColAcc + D + 64u * b;
+}
+
 template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, 0>;
+  using X = DqBars;
+  static_assert(kColAcc + D + 128 <= kBwdTmemCols, "dS buffers fit in TMEM");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+  auto xbar = [&](int i) -> uint32_t { return bar(L::bX + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
 
   // Query tile qt of head bh; for causal runs the last query tiles (the most
@@ -413,44 +564,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
   const int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
 
-  const uint32_t tmem_base = bwd_setup<D>(sbase, sgen, warp, kBwdEwThreads);
+  const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
+    ptx::mbar_init(b(L::bX + X::kSFull), 1);
+    ptx::mbar_init(b(L::bX + X::kSFree), kBwdEwThreads);
+    for (int k = 0; k < 2; ++k) {
+      ptx::mbar_init(b(L::bX + X::kPFull + k), kBwdEwThreads);
+      ptx::mbar_init(b(L::bX + X::kDsFree + k), 1);
+    }
+    ptx::mbar_init(b(L::bX + X::kDone), 1);
+  });
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0) bwd_producer<D>(sbase, &p.tm_q, &p.tm_do, qt, &p.tm_k, &p.tm_v, 0, nk, bh, wd);
+    if (lane == 0) bwd_producer<L>(sbase, &p.tm_q, &p.tm_do, qt, &p.tm_k, &p.tm_v, 0, nk, bh, wd);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBwdTile, kBwdTile, fmt, 0);
       constexpr uint32_t idesc_o = ptx::idesc_f16(kBwdTile, D, fmt, 1);
+      constexpr uint32_t kSlotLo = L::kTile >> 4;
       const uint32_t q_lo = ptx::desc_lo(sbase + L::kRes, 16);
       const uint32_t do_lo = ptx::desc_lo(sbase + L::kRes + L::kTile, 16);
-      const uint32_t k_lo0 = ptx::desc_lo(sbase + L::kRing, 16);                 // K-major use
-      const uint32_t v_lo0 = ptx::desc_lo(sbase + L::kRing + L::kTile, 16);
-      const uint32_t k_mn0 = ptx::desc_lo(sbase + L::kRing, L::kChunkBytes);     // MN-major use
-      constexpr uint32_t kSlotLo = (2 * L::kTile) >> 4;
+      const uint32_t k_lo0 = ptx::desc_lo(sbase + L::kRingA, 16);                 // K-major use
+      const uint32_t v_lo0 = ptx::desc_lo(sbase + L::kRingB, 16);
+      const uint32_t k_mn0 = ptx::desc_lo(sbase + L::kRingA, L::kChunkBytes);     // MN-major use
       const uint32_t tS = tmem_base + kColS, tDp = tmem_base + kColDp;
       const uint32_t tDq = tmem_base + kColAcc;
+      // dQ_i += dS_j K_j for key tile j (scale applied at the end)
+      auto issue_dq = [&](int j) -> bool {
+        const bool ok = ptx::wait_bounded(xbar(X::kPFull + (j & 1)), (j >> 1) & 1, wd, kSiteBwdPFull);
+        ptx::tc_fence_after();
+        if (!ok) return false;
+        const int slot = j % L::kStagesA;
+        issue_tmem_a<false>(tDq, tmem_base + dq_ds_col<D>(j & 1), k_mn0 + slot * kSlotLo, idesc_o,
+                            j > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(L::bEmptyA + slot));
+        ptx::mma_commit(xbar(X::kDsFree + (j & 1)));
+        return true;
+      };
       bool alive = ptx::wait_bounded(bar(L::bRes), 0, wd, kSiteBwdRes);
-      for (int it = 0; it < nk; ++it) {
-        const uint32_t slot = it % L::kStages;
-        alive = ptx::wait_bounded(bar(L::bFull + slot), (it / L::kStages) & 1, wd, kSiteBwdFull) && alive;
+      for (int it = 0; alive && it < nk; ++it) {
+        const int sa = it % L::kStagesA, sb = it % L::kStagesB;
+        alive = ptx::wait_bounded(bar(L::bFullA + sa), (it / L::kStagesA) & 1, wd, kSiteBwdFull);
+        alive = alive && ptx::wait_bounded(bar(L::bFullB + sb), (it / L::kStagesB) & 1, wd, kSiteBwdFull);
+        // the element-wise warps have read S and dP of the previous key tile
+        if (it > 0) alive = alive && ptx::wait_bounded(xbar(X::kSFree), (it - 1) & 1, wd, kSiteBwdSFree);
         ptx::tc_fence_after();
         if (!alive) break;
         // S = Q_i K_j^T and dP = dO_i V_j^T (queries on the TMEM lanes)
-        issue_kmajor<D, L::kChunkBytes>(tS, q_lo, k_lo0 + slot * kSlotLo, idesc_s);
-        issue_kmajor<D, L::kChunkBytes>(tDp, do_lo, v_lo0 + slot * kSlotLo, idesc_s);
-        ptx::mma_commit(bar(L::bSFull));
-        alive = ptx::wait_bounded(bar(L::bPFull), it & 1, wd, kSiteBwdPFull) && alive;
-        ptx::tc_fence_after();
-        if (!alive) break;
-        // dQ_i += dS K_j (scale applied at the end)
-        issue_tmem_a(tDq, tS, k_mn0 + slot * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(L::bEmpty + slot));
+        issue_kmajor<D, L::kChunkBytes>(tS, q_lo, k_lo0 + sa * kSlotLo, idesc_s);
+        issue_kmajor<D, L::kChunkBytes>(tDp, do_lo, v_lo0 + sb * kSlotLo, idesc_s);
+        ptx::mma_commit(xbar(X::kSFull));
+        ptx::mma_commit(bar(L::bEmptyB + sb));   // V_j is not read again
+        if (it > 0) alive = issue_dq(it - 1);
       }
-      ptx::mma_commit(bar(L::bDone));
-      ptx::wait_drain(bar(L::bDone), 0, 200000000ull);
+      if (alive) issue_dq(nk - 1);
+      ptx::mma_commit(xbar(X::kDone));
+      ptx::wait_drain(xbar(X::kDone), 0, 200000000ull);
     }
     __syncwarp();
   } else {
@@ -458,49 +629,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quarter = warp & 3, half = warp >> 2;
     const int t = quarter * 32 + lane;                    // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem_base + lane_off + kColS, tDp = tmem_base + lane_off + kColDp;
+    // this thread's 64 key columns of S and dP
+    const uint32_t tS = tmem_base + lane_off + kColS + half * 64;
+    const uint32_t tDp = tmem_base + lane_off + kColDp + half * 64;
     const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
     const bool q_in = qrow < p.N;
     const long long grow = static_cast<long long>(bh) * p.N + qrow;
-    const float lse2 = q_in ? p.lse[grow] * 1.4426950408889634f : INFINITY;
+    const float nl = q_in ? -p.lse[grow] * 1.4426950408889634f : -INFINITY;
     const float dl = q_in ? p.delta[grow] : 0.f;
-    const float c = p.scale_log2;
+    const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl2 = ptx::f2_pack(nl, nl);
+    const uint64_t ndl2 = ptx::f2_pack(-dl, -dl);
     for (int j = 0; j < nk; ++j) {
-      ptx::wait_bounded(bar(L::bSFull), j & 1, wd, kSiteBwdSFull);
+      ptx::wait_bounded(xbar(X::kSFull), j & 1, wd, kSiteBwdSFull);
       __syncwarp();
       ptx::tc_fence_after();
-      // keys past N, and on the diagonal tile keys after this query, are masked
-      int lim = p.N - j * kBwdTile;
-      if (kCausal && j == qt) lim = min(lim, t + 1);
+      // keys past N, and on the diagonal tile keys after this query, are
+      // masked (limits relative to this thread's first key column)
+      int lim = p.N - j * kBwdTile - half * 64;
+      if (kCausal && j == qt) lim = min(lim, t + 1 - half * 64);
       uint32_t dk[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sr[32], dpr[32];
-        ptx::tmem_ld32(tS + half * 64 + ch * 32, sr);
-        ptx::tmem_ld32(tDp + half * 64 + ch * 32, dpr);
+        ptx::tmem_ld32(tS + ch * 32, sr);
+        ptx::tmem_ld32(tDp + ch * 32, dpr);
         ptx::tmem_wait_ld();
+        if (ch == 1) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int kc = half * 64 + ch * 32 + e;         // key column within the tile
-          float p0 = ptx::ex2(fmaf(__uint_as_float(sr[e]), c, -lse2));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(sr[e + 1]), c, -lse2));
+          const int kc = ch * 32 + e;
+          float x0, x1;
+          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                    c2, nl2), x0, x1);
+          float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
           if (kc >= lim) p0 = 0.f;
           if (kc + 1 >= lim) p1 = 0.f;
-          dk[ch * 16 + e / 2] = ptx::pack2<kBf16>(p0 * (__uint_as_float(dpr[e]) - dl),
-                                                  p1 * (__uint_as_float(dpr[e + 1]) - dl));
+          float d0, d1;
+          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1),
+                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])),
+                                               ndl2)), d0, d1);
+          dk[kc / 2] = ptx::pack2<kBf16>(d0, d1);
         }
       }
-      // dS goes to the first 64 columns of S, which the other half's warps
-      // read: every load is done before any store.
-      ptx::named_bar_sync(1, kBwdEwThreads);
-      ptx::tmem_st16(tS + half * 32, dk);
-      ptx::tmem_st16(tS + half * 32 + 16, dk + 16);
+      // dS to its TMEM buffer once the tensor core has read what it held
+      // (dQ of key tile j - 2)
+      const int b = j & 1;
+      if (j >= 2) ptx::wait_bounded(xbar(X::kDsFree + b), ((j >> 1) - 1) & 1, wd, kSiteBwdDsFree);
+      __syncwarp();
+      ptx::tc_fence_after();
+      const uint32_t tDs = tmem_base + lane_off + dq_ds_col<D>(b) + half * 32;
+      ptx::tmem_st16(tDs, dk);
+      ptx::tmem_st16(tDs + 16, dk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bPFull));
+      ptx::mbar_arrive(xbar(X::kPFull + b));
     }
     // dQ = scale * (dS K): each half of the warps writes half of the columns
-    ptx::wait_bounded(bar(L::bDone), 0, wd, kSiteBwdDone);
+    ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
     store_acc_cols<D, D / 2, kBf16>(tmem_base + lane_off + kColAcc, half * (D / 2), p.scale, p.dq,

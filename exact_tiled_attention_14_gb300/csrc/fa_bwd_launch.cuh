@@ -41,16 +41,17 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   if (e != cudaSuccess) return e;
 
   static std::atomic<uint64_t> done_kv{0}, done_q{0};
-  constexpr int kAlloc = BwdSmem<D>::kAlloc;
-  e = bwd_smem_attr(fa_bwd_dkdv_kernel<D, kBf16, kCausal>, done_kv, kAlloc);
+  constexpr int kAllocKv = BwdSmem<D, DkdvVec<D>::kBytes>::kAlloc;
+  constexpr int kAllocQ = BwdSmem<D, 0>::kAlloc;
+  e = bwd_smem_attr(fa_bwd_dkdv_kernel<D, kBf16, kCausal>, done_kv, kAllocKv);
   if (e != cudaSuccess) return e;
-  e = bwd_smem_attr(fa_bwd_dq_kernel<D, kBf16, kCausal>, done_q, kAlloc);
+  e = bwd_smem_attr(fa_bwd_dq_kernel<D, kBf16, kCausal>, done_q, kAllocQ);
   if (e != cudaSuccess) return e;
   const int grid = p.BH * p.n_tiles;
-  fa_bwd_dkdv_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAlloc, stream>>>(p);
+  fa_bwd_dkdv_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAllocKv, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAlloc, stream>>>(p);
+  fa_bwd_dq_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAllocQ, stream>>>(p);
   return cudaGetLastError();
 }
 
