@@ -382,7 +382,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tc_fence_after();
         if (!alive) break;
         // dV_j += P^T dO_i; P^T sits in TMEM columns 0-31 and 64-95
-        issue_tmem_a<true>(tDv, tS, do_mn0 + (it % L::kStagesB) * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
+        issue_tmem_a<true>(tDv, tS, do_mn0 + (it % L::kStagesB) * kSlotLo, idesc_o,
+                           it > 0 ? 1u : 0u);
         ptx::mma_commit(bar(L::bEmptyB + it % L::kStagesB));
         if (more) {
           alive = full_a(it + 1);
@@ -648,32 +649,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // masked (limits relative to this thread's first key column)
       int lim = p.N - j * kBwdTile - half * 64;
       if (kCausal && j == qt) lim = min(lim, t + 1 - half * 64);
+      // all of S and dP into registers first: the next products wait for this
+      uint32_t sr[64], dpr[64];
+      ptx::tmem_ld32(tS, sr);
+      ptx::tmem_ld32(tS + 32, sr + 32);
+      ptx::tmem_ld32(tDp, dpr);
+      ptx::tmem_ld32(tDp + 32, dpr + 32);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
       uint32_t dk[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32], dpr[32];
-        ptx::tmem_ld32(tS + ch * 32, sr);
-        ptx::tmem_ld32(tDp + ch * 32, dpr);
-        ptx::tmem_wait_ld();
-        if (ch == 1) {
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int kc = ch * 32 + e;
-          float x0, x1;
-          ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                    c2, nl2), x0, x1);
-          float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-          if (kc >= lim) p0 = 0.f;
-          if (kc + 1 >= lim) p1 = 0.f;
-          float d0, d1;
-          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1),
-                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])),
-                                               ndl2)), d0, d1);
-          dk[kc / 2] = ptx::pack2<kBf16>(d0, d1);
-        }
+      for (int kc = 0; kc < 64; kc += 2) {
+        float x0, x1;
+        ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(__uint_as_float(sr[kc]), __uint_as_float(sr[kc + 1])),
+                                  c2, nl2), x0, x1);
+        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+        if (kc >= lim) p0 = 0.f;
+        if (kc + 1 >= lim) p1 = 0.f;
+        float d0, d1;
+        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1),
+                                  ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[kc]), __uint_as_float(dpr[kc + 1])),
+                                             ndl2)), d0, d1);
+        dk[kc / 2] = ptx::pack2<kBf16>(d0, d1);
       }
       // dS to its TMEM buffer once the tensor core has read what it held
       // (dQ of key tile j - 2)
