@@ -75,6 +75,7 @@ SHAPES = [
     (1, 1, 640, 128, "bf16", True),
     (1, 2, 1000, 64, "bf16", False),
     (1, 1, 1111, 128, "fp16", True),
+    (1, 1, 1500, 64, "fp16", True),     # causal d = 64 past the 6-slot and 4-slot rings
 ]
 
 
