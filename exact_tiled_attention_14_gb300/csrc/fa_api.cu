@@ -307,7 +307,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_tiles = (static_cast<long long>(N) + fa::kBwdTile - 1) / fa::kBwdTile;
-  if (bh > INT_MAX || bh * n_tiles > INT_MAX) return FA_ERR_SHAPE;
+  if (bh > INT_MAX || 2 * bh * n_tiles > INT_MAX) return FA_ERR_SHAPE;   // one grid, two passes
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;

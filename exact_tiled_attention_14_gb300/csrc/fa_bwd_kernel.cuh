@@ -12,14 +12,15 @@
 //   dV_j += P^T dO_i,   dP = dO_i V_j^T,   dS = P * (dP - D),
 //   dK_j += scale dS^T Q_i,   dQ_i += scale dS K_j.
 //
-// Three kernels, launched in this order on one stream:
+// Two kernels, launched in this order on one stream:
 //   fa_bwd_delta_kernel  D = rowsum(dO * O), memory-bound, one pass over O, dO.
-//   fa_bwd_dkdv_kernel   one CTA per (batch*head, key tile j): K_j, V_j stay in
+//   fa_bwd_kernel        both tensor-core passes in one grid:
+//   - dK/dV CTAs         one per (batch*head, key tile j): K_j, V_j stay in
 //                        shared memory while Q_i and dO_i stream past; rebuilds
 //                        S^T = K_j Q_i^T and dP^T = V_j dO_i^T on the tensor
 //                        core, forms P^T and dS^T in registers, accumulates
 //                        dV_j and dK_j in TMEM.
-//   fa_bwd_dq_kernel     one CTA per (batch*head, query tile i): Q_i, dO_i stay
+//   - dQ CTAs            one per (batch*head, query tile i): Q_i, dO_i stay
 //                        while K_j and V_j stream past; rebuilds S and dP, forms
 //                        dS, accumulates dQ_i in TMEM.
 // Each gradient row is written by exactly one CTA, so there are no atomics
@@ -305,9 +306,9 @@ struct DkdvVec {
   static constexpr int kBytes = kBufs * 2 * kBwdTile * 4;
 };
 
+// One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
 template <int D, bool kBf16, bool kCausal>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, DkdvVec<D>::kBytes>;
   using X = DkdvBars;
   extern __shared__ uint8_t smem_raw[];
@@ -321,8 +322,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // Key tile kt of head bh; for causal runs the first key tiles (the most
   // query tiles to visit) are dealt first.
-  const int kt = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - kt * p.BH;
+  const int kt = blk / p.BH;
+  const int bh = blk - kt * p.BH;
   const int i0 = kCausal ? kt : 0;           // query tiles i >= kt see this key tile
   const int nq = p.n_tiles - i0;
 
@@ -543,9 +544,9 @@ __device__ __forceinline__ uint32_t dq_ds_col(int b) {
   return kColAcc + D + 64u * b;
 }
 
+// One CTA of the dQ pass: block `blk` of BH * n_tiles.
 template <int D, bool kBf16, bool kCausal>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, 0>;
   using X = DqBars;
   static_assert(kColAcc + D + 128 <= kBwdTmemCols, "dS buffers fit in TMEM");
@@ -560,8 +561,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // Query tile qt of head bh; for causal runs the last query tiles (the most
   // key tiles to visit) are dealt first.
-  const int r = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - r * p.BH;
+  const int r = blk / p.BH;
+  const int bh = blk - r * p.BH;
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
   const int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
 
@@ -700,6 +701,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kBwdTmemCols);
   }
+}
+
+// ---------------------------------------------------------------- entry point
+// Both tensor-core passes in one grid: blocks [0, BH * n_tiles) are dK/dV
+// CTAs (the ones with the most query tiles first), the rest dQ CTAs (most
+// key tiles first).  One launch lets SMs that finish their dK/dV CTAs take
+// dQ CTAs at once, so the two passes share one partial last wave instead of
+// each ending on its own.  Shared memory is sized for the larger layout.
+template <int D, bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  const int per_pass = p.BH * p.n_tiles;
+  if (static_cast<int>(blockIdx.x) < per_pass)
+    bwd_dkdv_cta<D, kBf16, kCausal>(p, blockIdx.x);
+  else
+    bwd_dq_cta<D, kBf16, kCausal>(p, blockIdx.x - per_pass);
 }
 
 }  // namespace fa

@@ -25,8 +25,8 @@ cudaError_t bwd_smem_attr(Fn fn, std::atomic<uint64_t>& done, int bytes) {
   return cudaSuccess;
 }
 
-// D = rowsum(dO * O), then dK/dV (one CTA per key tile), then dQ (one CTA per
-// query tile), all on `stream`.  `o`, `dout` are [BH, N, D] in the storage dtype.
+// D = rowsum(dO * O), then one grid of dK/dV CTAs (one per key tile) and dQ
+// CTAs (one per query tile), all on `stream`.  `o`, `dout` are [BH, N, D] in the storage dtype.
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* dout, float* delta,
                                int sms, cudaStream_t stream) {
@@ -40,18 +40,15 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  static std::atomic<uint64_t> done_kv{0}, done_q{0};
+  static std::atomic<uint64_t> done{0};
   constexpr int kAllocKv = BwdSmem<D, DkdvVec<D>::kBytes>::kAlloc;
   constexpr int kAllocQ = BwdSmem<D, 0>::kAlloc;
-  e = bwd_smem_attr(fa_bwd_dkdv_kernel<D, kBf16, kCausal>, done_kv, kAllocKv);
+  constexpr int kAlloc = kAllocKv > kAllocQ ? kAllocKv : kAllocQ;
+  e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal>, done, kAlloc);
   if (e != cudaSuccess) return e;
-  e = bwd_smem_attr(fa_bwd_dq_kernel<D, kBf16, kCausal>, done_q, kAllocQ);
-  if (e != cudaSuccess) return e;
-  const int grid = p.BH * p.n_tiles;
-  fa_bwd_dkdv_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAllocKv, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D, kBf16, kCausal><<<grid, kBwdThreads, kAllocQ, stream>>>(p);
+  // dK/dV CTAs then dQ CTAs (see fa_bwd_kernel)
+  const long long grid = 2ll * p.BH * p.n_tiles;
+  fa_bwd_kernel<D, kBf16, kCausal><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc, stream>>>(p);
   return cudaGetLastError();
 }
 
