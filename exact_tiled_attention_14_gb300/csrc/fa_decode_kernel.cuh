@@ -286,27 +286,58 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // c owning output column c.  Parts with no visible key (l = 0) are skipped;
 // a query with none at all gets O = 0 and LSE = -inf.
 template <int D, bool kBf16>
-__global__ void __launch_bounds__(D) fa_decode_combine_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(D, 1) fa_decode_combine_kernel(const float* __restrict__ part_o,
                                                               const float2* __restrict__ part_ml,
                                                               void* o, float* lse, int splits,
                                                               int Nq) {
+  // Merge of the parts of one (head, query) row by the rescale identity:
+  // with m* the largest part maximum (log2 units), O = sum_s 2^(m_s - m*) O_s
+  // / sum_s 2^(m_s - m*) l_s.  Thread c owns output column c.  First m*
+  // (block reduction), then the scaled sums, eight parts per step so their
+  // loads are in flight together.  Parts with l = 0 (no visible key) carry
+  // no weight and their partial row is never read into the sum.
+  __shared__ float red[D / 32];
   const int c = threadIdx.x;
   const int q = blockIdx.x % Nq, bh = blockIdx.x / Nq;
-  float m = -INFINITY, lt = 0.f, acc = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t part = (static_cast<size_t>(bh) * splits + s) * Nq + q;
+  const size_t base = static_cast<size_t>(bh) * splits * Nq + q;   // part of split s: base + s*Nq
+  float m = -INFINITY;
+  for (int s = c; s < splits; s += D) {
+    const float2 ml = part_ml[base + static_cast<size_t>(s) * Nq];
+    if (ml.y > 0.f) m = fmaxf(m, ml.x);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((c & 31) == 0) red[c >> 5] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
+  float acc = 0.f, lt = 0.f;
+  int s = 0;
+  for (; s + 8 <= splits; s += 8) {
+    float2 ml[8];
+    float ov[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const size_t part = base + static_cast<size_t>(s + i) * Nq;
+      ml[i] = part_ml[part];
+      ov[i] = part_o[part * D + c];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool live = ml[i].y > 0.f;
+      const float f = live ? ptx::ex2(ml[i].x - m) : 0.f;
+      acc = live ? fmaf(f, ov[i], acc) : acc;
+      lt = live ? fmaf(f, ml[i].y, lt) : lt;
+    }
+  }
+  for (; s < splits; ++s) {
+    const size_t part = base + static_cast<size_t>(s) * Nq;
     const float2 ml = part_ml[part];
-    if (!(ml.y > 0.f)) continue;
-    const float ov = part_o[part * D + c];
-    if (ml.x > m) {           // larger maximum: move the reference
-      const float a = (m == -INFINITY) ? 0.f : ptx::ex2(m - ml.x);
-      acc = acc * a + ov;
-      lt = lt * a + ml.y;
-      m = ml.x;
-    } else {
+    if (ml.y > 0.f) {
       const float f = ptx::ex2(ml.x - m);
-      acc += f * ov;
-      lt += f * ml.y;
+      acc = fmaf(f, part_o[part * D + c], acc);
+      lt = fmaf(f, ml.y, lt);
     }
   }
   const size_t row = static_cast<size_t>(bh) * Nq + q;
