@@ -285,6 +285,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // One block of D threads per (batch*head, query): combine the parts, thread
 // c owning output column c.  Parts with no visible key (l = 0) are skipped;
 // a query with none at all gets O = 0 and LSE = -inf.
+constexpr int kCombineFast = 32;   // parts merged from registers in one pass
+
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(D, 1) fa_decode_combine_kernel(const float* __restrict__ part_o,
                                                               const float2* __restrict__ part_ml,
@@ -294,50 +296,73 @@ __global__ void __launch_bounds__(D, 1) fa_decode_combine_kernel(const float* __
   // with m* the largest part maximum (log2 units), O = sum_s 2^(m_s - m*) O_s
   // / sum_s 2^(m_s - m*) l_s.  Thread c owns output column c.  First m*
   // (block reduction), then the scaled sums, eight parts per step so their
-  // loads are in flight together.  Parts with l = 0 (no visible key) carry
+  // loads are in flight together (up to 32 parts: all loads at once).  Parts with l = 0 (no visible key) carry
   // no weight and their partial row is never read into the sum.
   __shared__ float red[D / 32];
   const int c = threadIdx.x;
   const int q = blockIdx.x % Nq, bh = blockIdx.x / Nq;
   const size_t base = static_cast<size_t>(bh) * splits * Nq + q;   // part of split s: base + s*Nq
-  float m = -INFINITY;
-  for (int s = c; s < splits; s += D) {
-    const float2 ml = part_ml[base + static_cast<size_t>(s) * Nq];
-    if (ml.y > 0.f) m = fmaxf(m, ml.x);
-  }
+  float m = -INFINITY, acc = 0.f, lt = 0.f;
+  if (splits <= kCombineFast) {
+    // Up to 32 parts: every thread loads all (m, l) pairs and its column of
+    // every part at once (one round trip), then takes m* and the sums from
+    // registers.
+    float2 ml[kCombineFast];
+    float ov[kCombineFast];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if ((c & 31) == 0) red[c >> 5] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
-  float acc = 0.f, lt = 0.f;
-  int s = 0;
-  for (; s + 8 <= splits; s += 8) {
-    float2 ml[8];
-    float ov[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const size_t part = base + static_cast<size_t>(s + i) * Nq;
-      ml[i] = part_ml[part];
-      ov[i] = part_o[part * D + c];
+    for (int i = 0; i < kCombineFast; ++i) {
+      const size_t part = base + static_cast<size_t>(i) * Nq;
+      ml[i] = i < splits ? part_ml[part] : make_float2(0.f, 0.f);
+      ov[i] = i < splits ? part_o[part * D + c] : 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kCombineFast; ++i)
+      if (ml[i].y > 0.f) m = fmaxf(m, ml[i].x);
+#pragma unroll
+    for (int i = 0; i < kCombineFast; ++i) {
       const bool live = ml[i].y > 0.f;
       const float f = live ? ptx::ex2(ml[i].x - m) : 0.f;
       acc = live ? fmaf(f, ov[i], acc) : acc;
       lt = live ? fmaf(f, ml[i].y, lt) : lt;
     }
-  }
-  for (; s < splits; ++s) {
-    const size_t part = base + static_cast<size_t>(s) * Nq;
-    const float2 ml = part_ml[part];
-    if (ml.y > 0.f) {
-      const float f = ptx::ex2(ml.x - m);
-      acc = fmaf(f, part_o[part * D + c], acc);
-      lt = fmaf(f, ml.y, lt);
+  } else {
+    for (int s = c; s < splits; s += D) {
+      const float2 ml = part_ml[base + static_cast<size_t>(s) * Nq];
+      if (ml.y > 0.f) m = fmaxf(m, ml.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((c & 31) == 0) red[c >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
+    int s = 0;
+    for (; s + 8 <= splits; s += 8) {
+      float2 ml[8];
+      float ov[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const size_t part = base + static_cast<size_t>(s + i) * Nq;
+        ml[i] = part_ml[part];
+        ov[i] = part_o[part * D + c];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool live = ml[i].y > 0.f;
+        const float f = live ? ptx::ex2(ml[i].x - m) : 0.f;
+        acc = live ? fmaf(f, ov[i], acc) : acc;
+        lt = live ? fmaf(f, ml[i].y, lt) : lt;
+      }
+    }
+    for (; s < splits; ++s) {
+      const size_t part = base + static_cast<size_t>(s) * Nq;
+      const float2 ml = part_ml[part];
+      if (ml.y > 0.f) {
+        const float f = ptx::ex2(ml.x - m);
+        acc = fmaf(f, part_o[part * D + c], acc);
+        lt = fmaf(f, ml.y, lt);
+      }
     }
   }
   const size_t row = static_cast<size_t>(bh) * Nq + q;
