@@ -1,7 +1,7 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
 ``fa_status``, ``fa_set_watchdog_ns``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
@@ -14,7 +14,8 @@ every call raises.
 and LSE (and, when asked, the balancing workspace) with PyTorch — device
 memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
 current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
-(dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``.
+(dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``,
+``attention_forward_kv`` for ``fa_fwd_kv``.
 """
 import ctypes
 import math
@@ -40,7 +41,7 @@ FA_ERR_CUDA = 11
 FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_work_tiles", "fa_version")
 
@@ -69,6 +70,8 @@ def load_library(path=None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, i, vp]
+    lib.fa_fwd_kv.restype = i
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_ws.restype = i
     lib.fa_fwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
@@ -121,6 +124,15 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None):
     return lib.fa_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
                       int(N), int(d), int(bool(causal)), float(scale), int(dtype),
                       _stream(stream))
+
+
+def fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, seqlens_k, scale, dtype, stream=None):
+    """Raw C call: Nq queries against Nk keys (seqlens_k: per-batch key counts
+    or None; causal 0 none, 1 upper-left, 2 bottom-right); returns the code."""
+    lib = load_library()
+    return lib.fa_fwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                         int(Nq), int(Nk), int(d), int(causal), _addr(seqlens_k), float(scale),
+                         int(dtype), _stream(stream))
 
 
 def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, workspace_bytes,
@@ -267,6 +279,54 @@ def attention_forward(q, k, v, causal=False, scale=None, out=None, lse=None, str
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         rc = fa_fwd_ws(q, k, v, out, lse, B, H, N, d, causal, scale, code, workspace, ws_bytes,
                        stream)
+    if rc != FA_OK:
+        raise FaError(rc)
+    return out, lse
+
+
+CAUSAL_MODES = {None: 0, False: 0, "upper_left": 1, "bottom_right": 2}
+
+
+def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=None, lse=None,
+                         stream=None):
+    """O, LSE of queries q [B, H, Nq, d] against keys/values k, v [B, H, Nk, d]
+    (CUDA, contiguous, one 16-bit dtype).
+
+    ``causal``: None (no mask), "upper_left" (query i at position i) or
+    "bottom_right" (query i at position len_b - Nq + i).  ``seqlens_k``: None
+    or an int32 CUDA tensor [B] of key counts per batch (the rest of the Nk
+    keys is padding).  A query that sees no key gets O = 0 and LSE = -inf.
+    Calls ``fa_fwd_kv`` on ``stream`` (default: current stream).
+    """
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d] of one shape")
+    if q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q and k differ in batch, heads or head width")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if causal not in CAUSAL_MODES:
+        raise ValueError("causal must be None, 'upper_left' or 'bottom_right'")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if seqlens_k is not None:
+        if seqlens_k.dtype != torch.int32 or seqlens_k.shape != (B,) or not seqlens_k.is_cuda:
+            raise ValueError("seqlens_k must be an int32 CUDA tensor of shape [B]")
+        seqlens_k = seqlens_k.contiguous()
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, CAUSAL_MODES[causal], seqlens_k, scale,
+                   dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse

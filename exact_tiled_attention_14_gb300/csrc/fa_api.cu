@@ -260,6 +260,10 @@ int launch_forward(const void* q, const void* k, const void* v, void* o, float* 
   p.split = sp.split ? 1 : 0;
   p.full_rounds = sp.full_rounds;
   p.tail_units = sp.split ? sp.tail_units : 0;
+  p.Nk = N;
+  p.H = H;
+  p.seqlens_k = nullptr;
+  p.align_br = 0;
   p.ws_count = sp.split ? static_cast<int*>(workspace) : nullptr;
   p.ws_part = sp.split ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.counter_bytes)
                        : nullptr;
@@ -299,6 +303,70 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, 
               cudaStream_t stream) {
   return launch_forward(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace,
                         workspace_bytes, stream);
+}
+
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, int causal, const int* seqlens_k, float scale, int dtype,
+              cudaStream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_SHAPE;
+  if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_qblk = (static_cast<long long>(Nq) + 2 * fa::kBM - 1) / (2 * fa::kBM);
+  if (bh > INT_MAX || bh * n_qblk > INT_MAX) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0 || Nq == 0) return FA_OK;  // nothing to write
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(seqlens_k);
+  if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::FwdParams p;
+  // With no keys no key tile is ever loaded; the maps still need a row and
+  // an address (k, v may then be NULL: q stands in).
+  const int nk_rows = Nk > 0 ? Nk : 1;
+  const void* kp = Nk > 0 ? k : q;
+  const void* vp = Nk > 0 ? v : q;
+  if (!make_tmap(&p.tm_q, q, static_cast<int>(bh), Nq, d, bf16) ||
+      !make_tmap(&p.tm_k, kp, static_cast<int>(bh), nk_rows, d, bf16) ||
+      !make_tmap(&p.tm_v, vp, static_cast<int>(bh), nk_rows, d, bf16) ||
+      !make_tmap(&p.tm_o, o, static_cast<int>(bh), Nq, d, bf16))
+    return FA_ERR_TENSORMAP;
+  p.o = o;
+  p.lse = lse;
+  p.trace = g_trace.load();
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
+  p.BH = static_cast<int>(bh);
+  p.N = Nq;
+  p.n_qblk = static_cast<int>(n_qblk);
+  p.n_kv = (Nk + fa::kBN - 1) / fa::kBN;
+  p.num_units = static_cast<int>(bh * n_qblk);
+  const long long kv_bytes = bh * 2ll * Nk * d * 2ll;
+  p.head_major = kv_bytes > (64ll << 20) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.split = 0;
+  p.full_rounds = 0;
+  p.tail_units = 0;
+  p.ws_count = nullptr;
+  p.ws_part = nullptr;
+  p.Nk = Nk;
+  p.H = H;
+  p.seqlens_k = seqlens_k;
+  p.align_br = causal == 2 ? 1 : 0;
+  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
+  const cudaError_t e = (d == 64) ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
+                                  : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -99,6 +99,16 @@ struct FwdParams {
   int* ws_count;           // 2 * tail_units counters, zero at launch
   float scale_log2;        // scale * log2(e)
   unsigned long long* trace;  // event trace buffer (only read in FA_TRACE builds)
+  // Queries against a key set of another length (kKv variants only; N is
+  // then the number of queries): keys per head Nk (tm_k / tm_v have Nk
+  // rows), per-batch key counts seqlens_k[b] (NULL: all Nk; batch b = bh / H),
+  // and the causal alignment: align_br = 0 puts query i at position i,
+  // align_br = 1 at position len_b - N + i (the queries are the last N
+  // positions of the batch's keys).
+  int Nk;
+  int H;
+  const int* seqlens_k;
+  int align_br;
 };
 
 // ---------------------------------------------------------------- tracing
@@ -213,6 +223,7 @@ __device__ __forceinline__ uint32_t p_col(int w) { return 256u + 2u * D + (w ? 6
 
 struct Unit {
   int bh, mblk, n0, n1;
+  int len, off;   // keys of this head; position of query row r is r + off (kKv)
 };
 
 // A piece of work: key tiles [kb, kb + n_w) of query tile w of one unit.
@@ -220,6 +231,7 @@ struct Unit {
 // workspace slot `slot` and are merged by whichever piece finishes last.
 struct Piece {
   int bh, mblk, kb, n0, n1, tail, slot;
+  int len, off;   // as in Unit
 };
 
 // Floats of one workspace slot: unnormalised O of both query tiles stored
@@ -241,7 +253,7 @@ __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
-template <bool kCausal>
+template <bool kCausal, bool kKv = false>
 __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   Unit u;
   if (p.head_major) {
@@ -253,12 +265,32 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
     u.mblk = p.n_qblk - 1 - level;
   }
   const int t0 = 2 * u.mblk;
-  if (kCausal) {
-    u.n0 = min(t0 + 1, p.n_kv);
-    u.n1 = min(t0 + 2, p.n_kv);
+  if constexpr (kKv) {
+    // keys of this batch, and the key tiles each query tile can see: with
+    // causal masking, keys up to the position of the tile's last row
+    int len = p.seqlens_k ? p.seqlens_k[u.bh / p.H] : p.Nk;
+    len = min(max(len, 0), p.Nk);
+    u.len = len;
+    u.off = (kCausal && p.align_br) ? len - p.N : 0;
+    const int nkv = (len + kBN - 1) / kBN;
+    int n[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int last = (t0 + w) * kBM + kBM - 1 + u.off;   // position of the tile's last row
+      n[w] = !kCausal ? nkv : (last < 0 ? 0 : min(last / kBN + 1, nkv));
+    }
+    u.n0 = n[0];
+    u.n1 = n[1];
   } else {
-    u.n0 = p.n_kv;
-    u.n1 = p.n_kv;
+    u.len = p.N;
+    u.off = 0;
+    if (kCausal) {
+      u.n0 = min(t0 + 1, p.n_kv);
+      u.n1 = min(t0 + 2, p.n_kv);
+    } else {
+      u.n0 = p.n_kv;
+      u.n1 = p.n_kv;
+    }
   }
   if ((t0 + 1) * kBM >= p.N) u.n1 = 0;  // second query tile lies wholly past N
   return u;
@@ -284,16 +316,16 @@ __device__ __forceinline__ void cursor_init(const FwdParams& p, int cta, int gri
   cu.end = kSplit ? tail_start(p, cta + 1, grid) : 0;
   cu.first_t = kSplit ? static_cast<int>(cu.pos / p.n_kv) : 0;
 }
-template <bool kCausal, bool kSplit>
+template <bool kCausal, bool kSplit, bool kKv = false>
 __device__ __forceinline__ bool next_piece(const FwdParams& p, int cta, int grid, Cursor& cu,
                                            Piece& pc) {
   if (!kSplit || cu.r < p.full_rounds) {
     const int s = unit_at(cu.r, cta, grid);
     if (!kSplit && s >= p.num_units) return false;
     ++cu.r;
-    const Unit u = decode_unit<kCausal>(s, p);
+    const Unit u = decode_unit<kCausal, kKv>(s, p);
     pc.bh = u.bh; pc.mblk = u.mblk; pc.kb = 0; pc.n0 = u.n0; pc.n1 = u.n1;
-    pc.tail = -1; pc.slot = 0;
+    pc.tail = -1; pc.slot = 0; pc.len = u.len; pc.off = u.off;
     return true;
   }
   if (cu.pos >= cu.end) return false;
@@ -308,6 +340,7 @@ __device__ __forceinline__ bool next_piece(const FwdParams& p, int cta, int grid
   pc.n1 = u.n1 > 0 ? ke - kb : 0;
   pc.tail = (kb == 0 && ke == p.n_kv) ? -1 : t;
   pc.slot = 2 * cta + (t == cu.first_t ? 0 : 1);
+  pc.len = u.len; pc.off = u.off;
   return true;
 }
 
@@ -346,7 +379,9 @@ struct TailWalk {
 
 // kSplit: compile the split-tail path (unmasked calls with a workspace only);
 // the other variants carry none of its code.
-template <int D, bool kBf16, bool kCausal, bool kSplit>
+// kKv: queries against a key set of their own length, per-batch key counts
+// and a causal alignment (see FwdParams); square calls compile none of it.
+template <int D, bool kBf16, bool kCausal, bool kSplit, bool kKv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
@@ -412,8 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Cursor cu;
       cursor_init<kSplit>(p, cta, grid, cu);
       Piece u;
-      while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+      while (next_piece<kCausal, kSplit, kKv>(p, cta, grid, cu, u)) {
         const int nkv = max(u.n0, u.n1);
+        if (kKv && nkv == 0) continue;   // no visible key: the softmax warps write the rows
         // Q of this piece may only overwrite the buffer once the previous
         // piece's last S MMA has read it; the first K tile does not wait for
         // that, so it is requested first.
@@ -580,8 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t base = 0;
       if (warp == kMmaWarp) {
         // S = Q K^T for both query tiles, one key tile ahead of the softmax
-        while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+        while (next_piece<kCausal, kSplit, kKv>(p, cta, grid, cu, u)) {
           const int nkv = max(u.n0, u.n1);
+          if (kKv && nkv == 0) continue;
           pf.lap(6);
           alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
           pf.lap(2);
@@ -601,8 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // O += P V for both query tiles, as soon as the softmax has written P
-        while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+        while (next_piece<kCausal, kSplit, kKv>(p, cta, grid, cu, u)) {
           const int nkv = max(u.n0, u.n1);
+          if (kKv && nkv == 0) continue;
           for (int j = 0; j < nkv; ++j) {
             const uint32_t vslot =
                 ring_wait(base + (j + 1 < nkv ? 2u * j + 2u : 2u * nkv - 1u));
@@ -650,11 +688,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor cu;
     cursor_init<kSplit>(p, cta, grid, cu);
     Piece u;
-    while (next_piece<kCausal, kSplit>(p, cta, grid, cu, u)) {
+    while (next_piece<kCausal, kSplit, kKv>(p, cta, grid, cu, u)) {
       const int n = w ? u.n1 : u.n0;
-      if (n == 0) continue;
       const int tile = 2 * u.mblk + w;
       const int row = tile * kBM + t;
+      if (n == 0) {
+        if constexpr (kKv) {
+          // a query tile that sees no key: O = 0 and LSE = -inf (the policy
+          // for an empty key set)
+          if (row < p.N) {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
+                                                   (static_cast<size_t>(u.bh) * p.N + row) * (D * 2));
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[static_cast<size_t>(u.bh) * p.N + row] = -INFINITY;
+          }
+        }
+        continue;
+      }
 
       float m_ref = -INFINITY;  // reference maximum of the raw scores q.k
       float neg_m = 0.f;        // -m_ref * c (0 while m_ref is -inf)
@@ -681,14 +732,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // mask: keys past N, and on the diagonal tile keys after this row
         const int kj = u.kb + j;                 // key tile index
-        const int rem = p.N - kj * kBN;
-        const bool diag = kCausal && kj == tile;
-        if (diag || rem < kBN) {
-          int lim = rem < kBN ? rem : kBN;
-          if (diag) lim = min(lim, t + 1);
+        if constexpr (kKv) {
+          // keys past this batch's count, and keys after this row's position
+          int lim = min(kBN, u.len - kj * kBN);
+          if (kCausal) lim = min(lim, row + u.off - kj * kBN + 1);
+          if (lim < kBN) {
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (i >= lim) sv[i] = -INFINITY;
+            for (int i = 0; i < kBN; ++i)
+              if (i >= lim) sv[i] = -INFINITY;
+          }
+        } else {
+          const int rem = p.N - kj * kBN;
+          const bool diag = kCausal && kj == tile;
+          if (diag || rem < kBN) {
+            int lim = rem < kBN ? rem : kBN;
+            if (diag) lim = min(lim, t + 1);
+#pragma unroll
+            for (int i = 0; i < kBN; ++i)
+              if (i >= lim) sv[i] = -INFINITY;
+          }
         }
 
         float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
@@ -792,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tracer) trace_event(p, w, tr, kEvEpiStart, ucnt - 1);
       __syncwarp();
       ptx::tc_fence_after();
-      const float inv_l = 1.0f / l;
+      // a row that saw no key (kKv masks) keeps l = 0: O = 0, LSE = -inf
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       if (kSplit && u.tail >= 0) {
         // Partial piece of a split unit: unnormalised O rows and (-m*c, l)
         // go to this piece's workspace slot; the piece that finishes last
@@ -947,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
       }
       if ((!kSplit || u.tail < 0) && row < p.N)
-        p.lse[static_cast<size_t>(u.bh) * p.N + row] = (ptx::lg2(l) - neg_m) * kLn2;
+        p.lse[static_cast<size_t>(u.bh) * p.N + row] = l > 0.f ? (ptx::lg2(l) - neg_m) * kLn2 : -INFINITY;
       if (tracer) trace_event(p, w, tr, kEvEpiEnd, ucnt - 1);
       pf.lap(6);
     }

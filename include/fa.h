@@ -83,6 +83,45 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            cudaStream_t stream);
 
 /*
+ * fa_fwd_kv — exact attention of Nq queries against a key set of its own
+ * length, with per-batch key counts (padding) and an explicit causal
+ * alignment.
+ *
+ * The pages' square formulation puts query i at absolute position i
+ * (upper-left alignment) and name two extensions it leaves out: non-square
+ * causal alignment with query positions offset by the cache length (for
+ * incremental decoding and chunked prefill), and masks such as padding
+ * under which a query row can see no key at all, which then needs a stated
+ * policy ("FlashAttention: The Matrix You Never Have to Write Down",
+ * section "Two things this deliberately doesn't do"; the empty key set's
+ * policy, O = 0 and LSE = -inf, in the same page's reference
+ * implementation).  This entry point does both with the same tiled online
+ * softmax as fa_fwd.
+ *
+ *   q, o      : device pointers, [B, H, Nq, d], dtype `dtype`, 16-byte aligned.
+ *   k, v      : device pointers, [B, H, Nk, d], dtype `dtype`, 16-byte aligned
+ *               (may be NULL when Nk = 0).
+ *   lse       : device pointer, [B, H, Nq] float32, 4-byte aligned.
+ *   Nq, Nk    : queries and key capacity per head (>= 0).
+ *   seqlens_k : NULL (every batch has Nk keys) or a device pointer to B
+ *               int32 key counts, 4-byte aligned; batch b uses keys
+ *               0 .. len_b - 1 (values are clamped to [0, Nk]); the rest
+ *               is padding and never contributes.
+ *   causal    : 0 no mask; 1 upper-left (query i at position i); 2
+ *               bottom-right (query i at position len_b - Nq + i: the
+ *               queries are the last Nq positions of the batch's keys).
+ *               Key j is visible to a query at position q_pos iff j <= q_pos.
+ *   A query row that sees no key gets O = 0 and LSE = -inf.
+ *   d, scale, dtype, stream : as fa_fwd.
+ *
+ * Errors as fa_fwd; FA_ERR_SHAPE also when causal is not 0, 1 or 2;
+ * FA_ERR_ALIGN also for a misaligned seqlens_k.  B*H*Nq == 0 writes nothing.
+ */
+int fa_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int H, int Nq, int Nk, int d, int causal, const int *seqlens_k,
+              float scale, int dtype, cudaStream_t stream);
+
+/*
  * fa_fwd_ws — fa_fwd with a caller-provided workspace used to balance the
  * last round of work across all SMs.
  *

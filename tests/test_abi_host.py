@@ -187,6 +187,25 @@ def test_decode_host_errors(lib):
     assert lib.fa_decode_workspace_size(1, 1, 4, 0, 64, C.byref(out)) == fa.FA_OK and out.value == 0
 
 
+def test_fwd_kv_host_errors(lib):
+    """fa_fwd_kv checks shapes, the causal mode (0, 1, 2), width, dtype, scale,
+    pointers (k, v may be NULL only without keys) and alignment before the device."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=2, H=4, Nq=300, Nk=5000, d=128,
+                causal=2, seqlens_k=None, scale=0.1, dtype=fa.FA_BF16)
+    cases = [(dict(Nq=-1), fa.FA_ERR_SHAPE), (dict(Nk=-1), fa.FA_ERR_SHAPE),
+             (dict(causal=3), fa.FA_ERR_SHAPE), (dict(causal=-1), fa.FA_ERR_SHAPE),
+             (dict(d=96), fa.FA_ERR_UNSUPPORTED_D), (dict(dtype=7), fa.FA_ERR_DTYPE),
+             (dict(scale=0.0), fa.FA_ERR_SCALE), (dict(Nq=0, q=None), fa.FA_OK),
+             (dict(H=0), fa.FA_OK), (dict(o=None), fa.FA_ERR_NULLPTR),
+             (dict(k=None), fa.FA_ERR_NULLPTR), (dict(q=FAKE + 4), fa.FA_ERR_ALIGN),
+             (dict(seqlens_k=FAKE + 2), fa.FA_ERR_ALIGN)]
+    for args, code in cases:
+        assert fa.fa_fwd_kv(**{**call, **args}) == code, args
+    # without keys, k and v may be NULL: the next check is the device's
+    rc = fa.fa_fwd_kv(**{**call, "Nk": 0, "k": None, "v": None})
+    assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
