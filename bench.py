@@ -24,6 +24,10 @@ timed region), ``clocks`` (nvidia-smi samples during the timed region) and
 ``--pass decode`` times split-KV decoding (``fa_decode``) on a decoding
 workload (GB/s of K/V read against the measured HBM copy bandwidth).
 
+``--pass kv`` times ``fa_fwd_kv`` (queries against a key set of another
+length, with padding and causal alignment) on a kv workload; FLOPs are 4 d
+per visible (query, key) pair.
+
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
 call (three kernels) with the forward's O and LSE and a seeded dO resident
 on the device; FLOPs are 2.5x the forward's (five matmuls against two).
@@ -56,6 +60,8 @@ METRIC = "attention fwd TFLOP/s (causal halved) and % of GB300 dense BF16 tensor
 METRIC_DEC = "attention decode (split-KV) K/V read GB/s and % of GB300 HBM copy bandwidth"
 METRIC_BWD = ("attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved) and % of GB300 "
               "dense BF16 tensor peak")
+METRIC_KV = ("attention fwd, queries against a key set of another length: TFLOP/s (4 d per "
+             "visible query-key pair) and % of GB300 dense BF16 tensor peak")
 FALLBACK_PEAK_TFLOPS = 1900.0
 
 
@@ -81,6 +87,40 @@ def io_bytes_bwd(w):
 def io_bytes(w):
     elems = w["B"] * w["H"] * w["N"] * w["d"]
     return dict(h2d=3 * elems * 2, d2h=elems * 2 + w["B"] * w["H"] * w["N"] * 4)
+
+
+def kv_positions(w, seqlens):
+    """Per batch: (key count, position of query row 0) of an fa_fwd_kv workload."""
+    out = []
+    for b in range(w["B"]):
+        n = w["Nk"] if seqlens is None else max(0, min(int(seqlens[b]), w["Nk"]))
+        out.append((n, n - w["Nq"] if w["causal"] == "bottom_right" else 0))
+    return out
+
+
+def kv_visible_pairs(w, n, off):
+    """(query, key) pairs of one head that the mask leaves visible: the
+    forward's FLOP count is 4 d per visible pair (the square causal
+    convention N^2/2 is this count up to the N/2 diagonal term)."""
+    Nq = w["Nq"]
+    if not w["causal"]:
+        return Nq * n
+    # row i sees min(n, max(0, i + off + 1)) keys: rows [lo, hi) see a partial
+    # prefix, rows from `full` on see all n keys
+    lo = max(0, -off)
+    hi = min(Nq, n - off - 1)
+    total = 0
+    if hi > lo:
+        total += (hi - lo) * (off + 1) + (hi * (hi - 1) - lo * (lo - 1)) // 2
+    full = max(lo, n - off - 1)
+    if Nq > full:
+        total += (Nq - full) * n
+    return total
+
+
+def step_flops_kv(w, seqlens):
+    return sum(4.0 * w["d"] * w["H"] * kv_visible_pairs(w, n, off)
+               for n, off in kv_positions(w, seqlens))
 
 
 def kernel_source_hash():
@@ -370,6 +410,40 @@ def run_reference(args, w):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
                    "causal": w["causal"], "storage_dtype": w["dtype"], "seed": w["seed"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_kv(args, w):
+    """Reference arm of ``--pass kv``: the float64 oracle on the host cores,
+    bounded samples of whole (batch, head) pairs per step (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = seeded_inputs.make_decode(w["B"], w["H"], w["Nq"], w["Nk"], w["d"], w["dtype"],
+                                        seed=w["seed"])
+    seqlens = seeded_inputs.make_seqlens(w["B"], w["Nk"], w["seed"]) if w["padded"] else None
+    total = args.steps + args.warmup
+    per_step = max(0.2, min(10.0, args.reference_seconds / max(total, 1)))
+    vals = []
+    for i in range(total):
+        tf, dt, heads, cores, desc = kv_oracle_sample(w, q, k, v, seqlens, per_step, start_head=i)
+        if i >= args.warmup:
+            vals.append((tf, dt))
+    value = statistics.median(tf for tf, _ in vals)
+    line = {
+        "metric": METRIC_KV, "value": value, "unit": "TFLOP/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.median(dt for _, dt in vals) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "pass": "kv", "B": w["B"], "H": w["H"], "Nq": w["Nq"],
+                   "Nk": w["Nk"], "d": w["d"], "causal": w["causal"], "storage_dtype": w["dtype"],
+                   "seed": w["seed"]},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "each step: " + desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -785,6 +859,171 @@ def run_ours_decode(args, w):
     return 0
 
 
+def kv_oracle_sample(w, q, k, v, seqlens, budget_s, start_head=0):
+    """Time the float64 oracle on whole (batch, head) pairs of an fa_fwd_kv
+    workload for about budget_s: each row at its absolute position against
+    the batch's keys.  Returns (TFLOP/s, seconds, heads, cores, description)."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    B, H = w["B"], w["H"]
+    pos = kv_positions(w, seqlens)
+    cores = oracle.num_threads(lib)
+    done, spent, flops = 0, 0.0, 0.0
+    while done < B * H and (done == 0 or spent < budget_s):
+        b, h = divmod((start_head + done) % (B * H), H)
+        n, off = pos[b]
+        rows = np.arange(w["Nq"], dtype=np.int64) + off
+        qh = q[b, h].double().numpy()
+        kh, vh = (t[b, h, :n].double().numpy() for t in (k, v))
+        t0 = time.perf_counter()
+        oracle.attention_rows(qh, rows, kh, vh, causal=bool(w["causal"]), scale=w["scale"], lib=lib)
+        spent += time.perf_counter() - t0
+        flops += 4.0 * w["d"] * kv_visible_pairs(w, n, off)
+        done += 1
+    desc = (f"{done} of {B * H} whole (batch, head) pairs of {w['name']} (float64, {cores} "
+            "threads); FLOPs counted per pair from its visible keys")
+    return flops / spent / 1e12, spent, done, cores, desc
+
+
+def run_ours_kv(args, w):
+    """Queries against a key set of another length: one step = one fa_fwd_kv
+    launch over the workload resident in device memory (key counts included)."""
+    import exact_tiled_attention_14_gb300 as fa
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+    sampler = ClockSampler(local).start()
+    B, H, Nq, Nk, d = w["B"], w["H"], w["Nq"], w["Nk"], w["d"]
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, w["dtype"], seed=w["seed"])
+    seqlens = seeded_inputs.make_seqlens(B, Nk, w["seed"]) if w["padded"] else None
+    mode = fa.CAUSAL_MODES[w["causal"]]
+    flops = step_flops_kv(w, seqlens)
+    io = dict(h2d=B * H * (Nq + 2 * Nk) * d * 2 + (0 if seqlens is None else 4 * B),
+              d2h=B * H * Nq * (d * 2 + 4))
+    per_replica = io["h2d"] + io["d2h"]
+    replicas = 1 if per_replica > 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_replica)) + 1
+    replicas = min(replicas, 64)
+    stream = torch.cuda.current_stream(device)
+    code = fa.dtype_code(q.dtype)
+    dsl = None if seqlens is None else seqlens.to(device)
+    bufs = []
+    for _ in range(replicas):
+        dq_, dk_, dv_ = (t.to(device) for t in (q, k, v))
+        bufs.append((dq_, dk_, dv_, torch.empty_like(dq_),
+                     torch.empty((B, H, Nq), dtype=torch.float32, device=device)))
+
+    def step(i):
+        dq_, dk_, dv_, o, lse = bufs[i % replicas]
+        rc = fa.fa_fwd_kv(dq_, dk_, dv_, o, lse, B, H, Nq, Nk, d, mode, dsl, w["scale"], code,
+                          stream)
+        if rc:
+            raise fa.FaError(rc, "fa_fwd_kv")
+
+    t_warm = time.time()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"warmup status {word:#x}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    t1 = time.time()
+    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
+    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
+                             world, device)
+    st, word = fa.fa_status(stream)
+    if st:
+        raise fa.FaError(st, f"timed status {word:#x}")
+
+    # end to end: pinned host q, k, v (and key counts) in, o and lse out
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    hsl = None if seqlens is None else seqlens.pin_memory()
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    dq_, dk_, dv_, o, lse = bufs[0]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        if hsl is not None:
+            dsl.copy_(hsl, non_blocking=True)
+        fa.attention_forward_kv(dq_, dk_, dv_, causal=w["causal"], seqlens_k=dsl,
+                                scale=w["scale"], out=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1, fallback_window=(t_warm, t1))
+    if rank != 0:
+        return 0
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak, peak_sustained, peak_src = measured_peaks()
+    traffic, traffic_note = stored_traffic(w["name"])
+    line = {
+        "metric": METRIC_KV, "value": world * flops * args.steps / (total_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "pass": "kv", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
+                   "d": d, "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
+                   "seqlens_k": None if seqlens is None else seqlens.tolist(),
+                   "entry": "fa_fwd_kv",
+                   "parallelism": "single GPU" if world == 1 else f"replicas x{world}",
+                   "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
+                          if replicas > 1 else "inputs larger than L2")},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
+                     "kernel_ms": kern_ms, "flops_per_launch": flops,
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "compulsory_bytes": io["h2d"] + io["d2h"]},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "gpu": torch.cuda.get_device_name(device),
+    }
+    if not args.no_cpu_baseline:
+        tf, dt, heads, cores, desc = kv_oracle_sample(w, q, k, v, seqlens, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(json.dumps(line) + "\n")
+    return 0
+
+
 def measured_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -811,9 +1050,10 @@ def main(argv=None):
     ap.add_argument("--split", action="store_true",
                     help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode"], default="fwd",
-                    help="time the forward pass (default), the backward pass (fa_bwd) or "
-                         "split-KV decoding (fa_decode; --workload names a decoding workload)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv"], default="fwd",
+                    help="time the forward pass (default), the backward pass (fa_bwd), "
+                         "split-KV decoding (fa_decode; --workload names a decoding workload) "
+                         "or fa_fwd_kv (--workload names a kv workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -830,6 +1070,17 @@ def main(argv=None):
             wd["H"] = args.heads if args.heads is not None else wd["H"]
             wd["name"] = f"{wd['name']}@B{wd['B']}H{wd['H']}"
         return run_ours_decode(args, wd)
+    if args.pass_ == "kv":
+        name = args.workload if args.workload != DEFAULT_WORKLOAD else \
+            seeded_inputs.KV_WORKLOADS[0]["name"]
+        wk = seeded_inputs.kv_workload(name)
+        if args.batch is not None or args.heads is not None:
+            wk["B"] = args.batch if args.batch is not None else wk["B"]
+            wk["H"] = args.heads if args.heads is not None else wk["H"]
+            wk["name"] = f"{wk['name']}@B{wk['B']}H{wk['H']}"
+        if args.impl == "reference":
+            return run_reference_kv(args, wk)
+        return run_ours_kv(args, wk)
     w = seeded_inputs.workload(args.workload)
     if args.batch is not None or args.heads is not None:
         w["B"] = args.batch if args.batch is not None else w["B"]

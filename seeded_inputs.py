@@ -51,6 +51,39 @@ for _i, _w in enumerate(DECODE_WORKLOADS):
     _w["scale"] = 1.0 / math.sqrt(_w["d"])
 
 
+# Queries against a key set of another length (fa_fwd_kv).  The pages name
+# chunked prefill after a cache and padded batches but print no sizes; these
+# are: a 2048-query chunk appended to a 14336-key cache (bottom-right causal,
+# B4 H32 d128 bf16), and a padded batch of 16 with per-batch key counts drawn
+# uniformly from [Nk/8, Nk] (unmasked, B16 H16 Nq1024 Nk2048 d64 bf16).
+# Seeds 3000 + i; key counts from ``make_seqlens``.
+KV_WORKLOADS = [
+    dict(name="prefill_b4_h32_q2048_k16384_d128_bf16_bottom_right", B=4, H=32, Nq=2048,
+         Nk=16384, d=128, dtype="bf16", causal="bottom_right", padded=False),
+    dict(name="padded_b16_h16_q1024_k2048_d64_bf16", B=16, H=16, Nq=1024, Nk=2048, d=64,
+         dtype="bf16", causal=None, padded=True),
+]
+for _i, _w in enumerate(KV_WORKLOADS):
+    _w["seed"] = 3000 + _i
+    _w["scale"] = 1.0 / math.sqrt(_w["d"])
+
+
+def kv_workload(name):
+    """The fa_fwd_kv workload dict with this name."""
+    for w in KV_WORKLOADS:
+        if w["name"] == name:
+            return dict(w)
+    raise KeyError(name)
+
+
+def make_seqlens(B, Nk, seed):
+    """Per-batch key counts, uniform integers in [max(1, Nk // 8), Nk], from
+    their own generator (seeded 700000 + seed)."""
+    g = torch.Generator("cpu").manual_seed(700000 + int(seed))
+    lo = max(1, Nk // 8)
+    return torch.randint(lo, Nk + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
 def decode_workload(name):
     """The decoding workload dict with this name."""
     for w in DECODE_WORKLOADS:
