@@ -920,8 +920,8 @@ def run_ours_kv(args, w):
 
     def step(i):
         dq_, dk_, dv_, o, lse = bufs[i % replicas]
-        rc = fa.fa_fwd_kv(dq_, dk_, dv_, o, lse, B, H, Nq, Nk, d, mode, dsl, w["scale"], code,
-                          stream)
+        rc = fa.fa_fwd_kv(dq_, dk_, dv_, o, lse, B, H, Nq, Nk, d, d, mode, dsl, w["scale"],
+                          code, stream)
         if rc:
             raise fa.FaError(rc, "fa_fwd_kv")
 

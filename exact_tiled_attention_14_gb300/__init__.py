@@ -70,7 +70,7 @@ def load_library(path=None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
-    lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, i, vp]
+    lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, f, i, vp]
     lib.fa_fwd_kv.restype = i
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_ws.restype = i
@@ -126,13 +126,15 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None):
                       _stream(stream))
 
 
-def fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, seqlens_k, scale, dtype, stream=None):
-    """Raw C call: Nq queries against Nk keys (seqlens_k: per-batch key counts
-    or None; causal 0 none, 1 upper-left, 2 bottom-right); returns the code."""
+def fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, dv, causal, seqlens_k, scale, dtype,
+              stream=None):
+    """Raw C call: Nq queries of width d against Nk keys, values of width dv
+    (seqlens_k: per-batch key counts or None; causal 0 none, 1 upper-left,
+    2 bottom-right); returns the code."""
     lib = load_library()
     return lib.fa_fwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
-                         int(Nq), int(Nk), int(d), int(causal), _addr(seqlens_k), float(scale),
-                         int(dtype), _stream(stream))
+                         int(Nq), int(Nk), int(d), int(dv), int(causal), _addr(seqlens_k),
+                         float(scale), int(dtype), _stream(stream))
 
 
 def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, workspace_bytes,
@@ -289,8 +291,9 @@ CAUSAL_MODES = {None: 0, False: 0, "upper_left": 1, "bottom_right": 2}
 
 def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=None, lse=None,
                          stream=None):
-    """O, LSE of queries q [B, H, Nq, d] against keys/values k, v [B, H, Nk, d]
-    (CUDA, contiguous, one 16-bit dtype).
+    """O [B, H, Nq, dv], LSE of queries q [B, H, Nq, d] against keys
+    k [B, H, Nk, d] and values v [B, H, Nk, dv] (CUDA, contiguous, one 16-bit
+    dtype; d and dv each 64 or 128).
 
     ``causal``: None (no mask), "upper_left" (query i at position i) or
     "bottom_right" (query i at position len_b - Nq + i).  ``seqlens_k``: None
@@ -301,8 +304,8 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
     import torch
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
-    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
-        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d] of one shape")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape[:3] != v.shape[:3]:
+        raise ValueError("q must be [B, H, Nq, d], k [B, H, Nk, d] and v [B, H, Nk, dv]")
     if q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
         raise ValueError("q and k differ in batch, heads or head width")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -313,6 +316,7 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
         raise ValueError("causal must be None, 'upper_left' or 'bottom_right'")
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
+    dv = v.shape[3]
     if seqlens_k is not None:
         if seqlens_k.dtype != torch.int32 or seqlens_k.shape != (B,) or not seqlens_k.is_cuda:
             raise ValueError("seqlens_k must be an int32 CUDA tensor of shape [B]")
@@ -320,13 +324,13 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, H, Nq, dv), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, CAUSAL_MODES[causal], seqlens_k, scale,
-                   dtype_code(q.dtype), stream)
+    rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, dv, CAUSAL_MODES[causal], seqlens_k,
+                   scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse

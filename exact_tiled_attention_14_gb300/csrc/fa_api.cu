@@ -264,6 +264,8 @@ int launch_forward(const void* q, const void* k, const void* v, void* o, float* 
   p.H = H;
   p.seqlens_k = nullptr;
   p.align_br = 0;
+  p.dqk = d;
+  p.dv = d;
   p.ws_count = sp.split ? static_cast<int*>(workspace) : nullptr;
   p.ws_part = sp.split ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.counter_bytes)
                        : nullptr;
@@ -306,14 +308,14 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, 
 }
 
 int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int Nq, int Nk, int d, int causal, const int* seqlens_k, float scale, int dtype,
-              cudaStream_t stream) {
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_SHAPE;
+              int Nq, int Nk, int d, int dv, int causal, const int* seqlens_k, float scale,
+              int dtype, cudaStream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || dv <= 0) return FA_ERR_SHAPE;
   if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_qblk = (static_cast<long long>(Nq) + 2 * fa::kBM - 1) / (2 * fa::kBM);
   if (bh > INT_MAX || bh * n_qblk > INT_MAX) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
   if (bh == 0 || Nq == 0) return FA_OK;  // nothing to write
@@ -335,10 +337,12 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   const int nk_rows = Nk > 0 ? Nk : 1;
   const void* kp = Nk > 0 ? k : q;
   const void* vp = Nk > 0 ? v : q;
+  // Each map has its tensor's own width: with d != dv the kernel of width
+  // max(d, dv) loads only the narrower tensors' own columns.
   if (!make_tmap(&p.tm_q, q, static_cast<int>(bh), Nq, d, bf16) ||
       !make_tmap(&p.tm_k, kp, static_cast<int>(bh), nk_rows, d, bf16) ||
-      !make_tmap(&p.tm_v, vp, static_cast<int>(bh), nk_rows, d, bf16) ||
-      !make_tmap(&p.tm_o, o, static_cast<int>(bh), Nq, d, bf16))
+      !make_tmap(&p.tm_v, vp, static_cast<int>(bh), nk_rows, dv, bf16) ||
+      !make_tmap(&p.tm_o, o, static_cast<int>(bh), Nq, dv, bf16))
     return FA_ERR_TENSORMAP;
   p.o = o;
   p.lse = lse;
@@ -351,7 +355,7 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.n_qblk = static_cast<int>(n_qblk);
   p.n_kv = (Nk + fa::kBN - 1) / fa::kBN;
   p.num_units = static_cast<int>(bh * n_qblk);
-  const long long kv_bytes = bh * 2ll * Nk * d * 2ll;
+  const long long kv_bytes = bh * static_cast<long long>(Nk) * (d + dv) * 2ll;
   p.head_major = kv_bytes > (64ll << 20) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.split = 0;
@@ -363,9 +367,12 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.H = H;
   p.seqlens_k = seqlens_k;
   p.align_br = causal == 2 ? 1 : 0;
+  p.dqk = d;
+  p.dv = dv;
   const int grid = p.num_units < info->sms ? p.num_units : info->sms;
-  const cudaError_t e = (d == 64) ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
-                                  : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
+  const bool w64 = d == 64 && dv == 64;   // else the kernel of width 128
+  const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
+                            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -109,6 +109,13 @@ struct FwdParams {
   int H;
   const int* seqlens_k;
   int align_br;
+  // Widths (kKv variants only): dqk of Q and K, dv of V and O, each 64 or
+  // 128 with D = max(dqk, dv).  Each tensor map has its tensor's own width
+  // and only those 64-column chunks are loaded; S takes only dqk / 16 K
+  // steps and O += P V computes only dv columns, so the chunks not loaded
+  // are never read.
+  int dqk;
+  int dv;
 };
 
 // ---------------------------------------------------------------- tracing
@@ -458,9 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             alive = ptx::wait_bounded(bar(L::bQEmpty), (k_units - 1) & 1, wd, kSiteQEmpty) && alive;
           if (alive) {
             const int ntile = u.n1 > 0 ? 2 : 1;
-            ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * L::kTile);
+            // kKv with d < D: only the chunks of Q's own columns are loaded
+            // (the S products never read the others)
+            const int qc = kKv ? p.dqk / 64 : L::kChunks;
+            ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * qc * L::kChunkBytes);
             for (int w = 0; w < ntile; ++w)
-              for (int c = 0; c < L::kChunks; ++c)
+              for (int c = 0; c < qc; ++c)
                 ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
                                  bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
             q_issued = k_units + 1;
@@ -473,9 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             alive = ptx::wait_bounded(bar(L::bKvEmpty + slot), (use - 1) & 1, wd, kSiteKvEmpty) &&
                     alive;
           if (alive) {
-            ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), L::kTile);
+            // kKv: only the chunks of the tensor's own width (d for K, dv for V)
+            const int nc = kKv ? (kv ? p.dv : p.dqk) / 64 : L::kChunks;
+            ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), nc * L::kChunkBytes);
             const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
-            for (int c = 0; c < L::kChunks; ++c)
+            for (int c = 0; c < nc; ++c)
               ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
                                bar(L::bKvFull + slot), c * 64, (u.kb + j) * kBN, u.bh);
             trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
@@ -509,7 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBM, kBN, fmt, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t idesc_o = ptx::idesc_f16(kBM, D, fmt, 1);    // P x V (MN-major)
+      constexpr uint32_t idesc_o_full = ptx::idesc_f16(kBM, D, fmt, 1);  // P x V (MN-major)
+      // a value width below D (kKv) computes only dv columns of O
+      const uint32_t idesc_o =
+          (kKv && p.dv < D) ? ptx::idesc_f16(kBM, 64, fmt, 1) : idesc_o_full;
       // Address words of the shared-memory descriptors (start >> 4 | LBO >> 4 << 16).
       const uint32_t q_lo0 = ptx::desc_lo(sbase + L::kQ, 16);
       const uint32_t q_lo1 = ptx::desc_lo(sbase + L::kQ + L::kTile, 16);
@@ -522,9 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S = Q_w K^T over the head width: K-major operands, 128-byte swizzle;
       // a K step of 16 columns moves 32 bytes inside a swizzle row, and every
       // 64 columns start a new chunk.
+      const int s_steps = kKv ? p.dqk / 16 : D / 16;   // K steps of S (columns of Q, K / 16)
       auto issue_s = [&](uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kKv && kk >= s_steps) break;
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
           ptx::mma_ss(d_tmem, ptx::desc_sw128(q_lo + off), ptx::desc_sw128(k_lo + off), idesc_s,
                       kk > 0);
@@ -698,9 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // for an empty key set)
           if (row < p.N) {
             uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
-                                                   (static_cast<size_t>(u.bh) * p.N + row) * (D * 2));
-#pragma unroll
-            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0u, 0u, 0u, 0u);
+                                                   (static_cast<size_t>(u.bh) * p.N + row) * (p.dv * 2));
+            for (int v = 0; v < p.dv / 8; ++v) orow[v] = make_uint4(0u, 0u, 0u, 0u);
             p.lse[static_cast<size_t>(u.bh) * p.N + row] = -INFINITY;
           }
         }
@@ -982,11 +998,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::bulk_commit_group();
         }
       } else {
-        // straight from registers: each thread writes its own row
+        // straight from registers: each thread writes its own row (of dv
+        // columns in the kKv variants)
+        const int ocols = kKv ? p.dv : D;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
-                                               (static_cast<size_t>(u.bh) * p.N + row) * (D * 2));
+                                               (static_cast<size_t>(u.bh) * p.N + row) * (ocols * 2));
 #pragma unroll 1
-        for (int q4 = 0; q4 < D / 32; ++q4) {
+        for (int q4 = 0; q4 < ocols / 32; ++q4) {
           uint32_t orr[32];
           ptx::tmem_ld32(tO + q4 * 32, orr);
           ptx::tmem_wait_ld();

@@ -96,13 +96,22 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * section "Two things this deliberately doesn't do"; the empty key set's
  * policy, O = 0 and LSE = -inf, in the same page's reference
  * implementation).  This entry point does both with the same tiled online
- * softmax as fa_fwd.
+ * softmax as fa_fwd.  It also takes a value width dv different from the
+ * query/key width d: the same page's reference lets V be wider or narrower
+ * than Q and K and tests shapes with dv != d (section "Check it", the sweep
+ * over shapes and block sizes).
  *
- *   q, o      : device pointers, [B, H, Nq, d], dtype `dtype`, 16-byte aligned.
- *   k, v      : device pointers, [B, H, Nk, d], dtype `dtype`, 16-byte aligned
- *               (may be NULL when Nk = 0).
- *   lse       : device pointer, [B, H, Nq] float32, 4-byte aligned.
+ *   q         : device pointer, [B, H, Nq, d], dtype `dtype`, 16-byte aligned.
+ *   k         : device pointer, [B, H, Nk, d], 16-byte aligned.
+ *   v         : device pointer, [B, H, Nk, dv], 16-byte aligned (k and v may
+ *               be NULL when Nk = 0).
+ *   o         : device pointer, [B, H, Nq, dv], 16-byte aligned (written).
+ *   lse       : device pointer, [B, H, Nq] float32, 4-byte aligned (written).
  *   Nq, Nk    : queries and key capacity per head (>= 0).
+ *   d, dv     : widths of Q/K and of V/O, each 64 or 128.  With d != dv the
+ *               kernel of width 128 runs; it loads only each tensor's own
+ *               columns, S takes only d's products and O += P V computes
+ *               only dv's columns.
  *   seqlens_k : NULL (every batch has Nk keys) or a device pointer to B
  *               int32 key counts, 4-byte aligned; batch b uses keys
  *               0 .. len_b - 1 (values are clamped to [0, Nk]); the rest
@@ -112,14 +121,15 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *               queries are the last Nq positions of the batch's keys).
  *               Key j is visible to a query at position q_pos iff j <= q_pos.
  *   A query row that sees no key gets O = 0 and LSE = -inf.
- *   d, scale, dtype, stream : as fa_fwd.
+ *   scale, dtype, stream : as fa_fwd.
  *
- * Errors as fa_fwd; FA_ERR_SHAPE also when causal is not 0, 1 or 2;
- * FA_ERR_ALIGN also for a misaligned seqlens_k.  B*H*Nq == 0 writes nothing.
+ * Errors as fa_fwd (FA_ERR_UNSUPPORTED_D for d or dv outside {64, 128});
+ * FA_ERR_SHAPE also when causal is not 0, 1 or 2; FA_ERR_ALIGN also for a
+ * misaligned seqlens_k.  B*H*Nq == 0 writes nothing.
  */
 int fa_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
-              int B, int H, int Nq, int Nk, int d, int causal, const int *seqlens_k,
-              float scale, int dtype, cudaStream_t stream);
+              int B, int H, int Nq, int Nk, int d, int dv, int causal,
+              const int *seqlens_k, float scale, int dtype, cudaStream_t stream);
 
 /*
  * fa_fwd_ws — fa_fwd with a caller-provided workspace used to balance the

@@ -119,14 +119,15 @@ def make_qkv(B, H, N, d, dtype="bf16", q_std=1.0, seed=0):
     return q.to(t), k.to(t), v.to(t)
 
 
-def make_decode(B, H, Nq, Nk, d, dtype="bf16", seed=0):
-    """Decoding inputs: Q [B, H, Nq, d] and a cache K, V [B, H, Nk, d], drawn
-    Q, K, V from one generator (seeded 900000 + seed), N(0,1), rounded."""
+def make_decode(B, H, Nq, Nk, d, dtype="bf16", seed=0, dv=None):
+    """Decoding inputs: Q [B, H, Nq, d] and a cache K [B, H, Nk, d], V
+    [B, H, Nk, dv] (dv defaults to d), drawn Q, K, V from one generator
+    (seeded 900000 + seed), N(0,1), rounded."""
     g = torch.Generator("cpu").manual_seed(900000 + int(seed))
     t = DTYPES[dtype]
     q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)
     k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
-    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d if dv is None else dv), generator=g, dtype=torch.float32)
     return q.to(t), k.to(t), v.to(t)
 
 

@@ -188,13 +188,14 @@ def test_decode_host_errors(lib):
 
 
 def test_fwd_kv_host_errors(lib):
-    """fa_fwd_kv checks shapes, the causal mode (0, 1, 2), width, dtype, scale,
+    """fa_fwd_kv checks shapes, the causal mode (0, 1, 2), widths, dtype, scale,
     pointers (k, v may be NULL only without keys) and alignment before the device."""
     call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=2, H=4, Nq=300, Nk=5000, d=128,
-                causal=2, seqlens_k=None, scale=0.1, dtype=fa.FA_BF16)
+                dv=64, causal=2, seqlens_k=None, scale=0.1, dtype=fa.FA_BF16)
     cases = [(dict(Nq=-1), fa.FA_ERR_SHAPE), (dict(Nk=-1), fa.FA_ERR_SHAPE),
              (dict(causal=3), fa.FA_ERR_SHAPE), (dict(causal=-1), fa.FA_ERR_SHAPE),
-             (dict(d=96), fa.FA_ERR_UNSUPPORTED_D), (dict(dtype=7), fa.FA_ERR_DTYPE),
+             (dict(d=96), fa.FA_ERR_UNSUPPORTED_D), (dict(dv=32), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dv=0), fa.FA_ERR_SHAPE), (dict(dtype=7), fa.FA_ERR_DTYPE),
              (dict(scale=0.0), fa.FA_ERR_SCALE), (dict(Nq=0, q=None), fa.FA_OK),
              (dict(H=0), fa.FA_OK), (dict(o=None), fa.FA_ERR_NULLPTR),
              (dict(k=None), fa.FA_ERR_NULLPTR), (dict(q=FAKE + 4), fa.FA_ERR_ALIGN),

@@ -37,7 +37,7 @@ def run_kv(q, k, v, causal, seqlens, scale):
 def oracle_kv(q, k, v, causal, seqlens, scale):
     B, H, Nq, _ = q.shape
     Nk = k.shape[2]
-    o = np.zeros(q.shape)
+    o = np.zeros((B, H, Nq, v.shape[3]))
     lse = np.zeros((B, H, Nq))
     for b in range(B):
         n = Nk if seqlens is None else max(0, min(seqlens[b], Nk))
@@ -109,6 +109,47 @@ def test_square_equals_fa_fwd(d, dtype, causal):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+DV_CASES = [
+    # B, H, Nq, Nk, d, dv, dtype, causal, seqlens
+    (1, 2, 300, 700, 64, 128, "bf16", "bottom_right", None),
+    (2, 1, 257, 257, 128, 64, "fp16", "upper_left", None),
+    (2, 2, 200, 1000, 128, 64, "bf16", None, [1000, 333]),
+    (1, 1, 129, 64, 64, 128, "fp16", "bottom_right", None),     # first rows see nothing
+    (1, 3, 640, 640, 64, 128, "fp16", None, None),
+    (2, 1, 1, 3000, 128, 64, "bf16", "bottom_right", [3000, 17]),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,dtype,causal,seqlens", DV_CASES,
+                         ids=[f"B{c[0]}H{c[1]}q{c[2]}k{c[3]}d{c[4]}dv{c[5]}{c[6]}{c[7] or 'nc'}"
+                              for c in DV_CASES])
+def test_value_width_vs_oracle(B, H, Nq, Nk, d, dv, dtype, causal, seqlens):
+    """A value width dv different from the query/key width d (the pages'
+    reference allows it and tests it): O is [B, H, Nq, dv]."""
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, dtype, seed=7 * Nq + Nk + dv, dv=dv)
+    scale = default_scale(d)
+    o, lse = run_kv(q, k, v, causal, seqlens, scale)
+    assert o.shape == (B, H, Nq, dv)
+    o_ref, lse_ref = oracle_kv(q, k, v, causal, seqlens, scale)
+    check(o, lse, o_ref, lse_ref, dtype, f"B{B}H{H}q{Nq}k{Nk}d{d}dv{dv}{dtype}{causal}{seqlens}")
+
+
+def test_value_width_guard_columns():
+    """With dv = 64 < d = 128 the kernel must write exactly dv columns per
+    row: a guard band around O stays untouched."""
+    B, H, Nq, Nk, d, dv = 1, 2, 300, 400, 128, 64
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, "bf16", seed=77, dv=dv)
+    dq, dk, dvv = (t.cuda() for t in (q, k, v))
+    n = B * H * Nq * dv
+    buf = torch.full((n + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = buf[4096:4096 + n].view(B, H, Nq, dv)
+    fa.attention_forward_kv(dq, dk, dvv, causal="bottom_right", out=o)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:4096] == 7.0) and torch.all(buf[4096 + n:] == 7.0)
+    o_ref, _ = oracle_kv(q, k, v, "bottom_right", None, default_scale(d))
+    assert np.abs(o.cpu().double().numpy() - o_ref).max() <= TOL["bf16"][0]
+
+
 def test_no_keys():
     """Nk = 0, and every batch padded to zero keys: O = 0, LSE = -inf."""
     q, k, v = seeded_inputs.make_decode(2, 2, 150, 1, 64, "bf16", seed=5)
@@ -130,9 +171,11 @@ def test_errors():
     o = torch.empty_like(q)
     lse = torch.empty(1, 1, 128, dtype=torch.float32, device="cuda")
     s = 0.125
-    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, 128, 64, 3, None, s, fa.FA_BF16) == fa.FA_ERR_SHAPE
-    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, -1, 64, 0, None, s, fa.FA_BF16) == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, 128, 64, 64, 3, None, s, fa.FA_BF16) == fa.FA_ERR_SHAPE
+    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, -1, 64, 64, 0, None, s, fa.FA_BF16) == fa.FA_ERR_SHAPE
     sl = torch.zeros(2, dtype=torch.int32, device="cuda")
-    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, 128, 64, 1, sl.data_ptr() + 2, s,
+    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, 128, 64, 64, 1, sl.data_ptr() + 2, s,
                         fa.FA_BF16) == fa.FA_ERR_ALIGN
-    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 0, 128, 64, 1, None, s, fa.FA_BF16) == fa.FA_OK
+    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 0, 128, 64, 64, 1, None, s, fa.FA_BF16) == fa.FA_OK
+    assert fa.fa_fwd_kv(q, q, q, o, lse, 1, 1, 128, 128, 64, 96, 0, None, s,
+                        fa.FA_BF16) == fa.FA_ERR_UNSUPPORTED_D
