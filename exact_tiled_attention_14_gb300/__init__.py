@@ -1,7 +1,7 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
 ``fa_status``, ``fa_set_watchdog_ns``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
@@ -15,7 +15,8 @@ and LSE (and, when asked, the balancing workspace) with PyTorch — device
 memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
 current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
 (dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``,
-``attention_forward_kv`` for ``fa_fwd_kv``.
+``attention_forward_kv`` for ``fa_fwd_kv``, ``attention_forward_varlen`` for
+``fa_fwd_varlen``.
 """
 import ctypes
 import math
@@ -41,7 +42,7 @@ FA_ERR_CUDA = 11
 FA_ERR_WORKSPACE = 12
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_work_tiles", "fa_version")
 
@@ -72,6 +73,8 @@ def load_library(path=None):
     lib.fa_fwd.restype = i
     lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, f, i, vp]
     lib.fa_fwd_kv.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_varlen.restype = i
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
     lib.fa_fwd_ws.restype = i
     lib.fa_fwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
@@ -135,6 +138,17 @@ def fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, dv, causal, seqlens_k, scale, dt
     return lib.fa_fwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
                          int(Nq), int(Nk), int(d), int(dv), int(causal), _addr(seqlens_k),
                          float(scale), int(dtype), _stream(stream))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, total_q,
+                  total_k, d, dv, causal, scale, dtype, stream=None):
+    """Raw C call: packed sequences (token-major q, k, v, o; lse [H, total_q];
+    cu_seqlens_* int32 offsets, B + 1 each); returns the code."""
+    lib = load_library()
+    return lib.fa_fwd_varlen(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse),
+                             _addr(cu_seqlens_q), _addr(cu_seqlens_k), int(B), int(H),
+                             int(max_seqlen_q), int(total_q), int(total_k), int(d), int(dv),
+                             int(causal), float(scale), int(dtype), _stream(stream))
 
 
 def fa_fwd_ws(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, workspace, workspace_bytes,
@@ -331,6 +345,54 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
         stream = torch.cuda.current_stream(q.device)
     rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, dv, CAUSAL_MODES[causal], seqlens_k,
                    scale, dtype_code(q.dtype), stream)
+    if rc != FA_OK:
+        raise FaError(rc)
+    return out, lse
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, causal=None,
+                             scale=None, out=None, lse=None, stream=None):
+    """O [total_q, H, dv], LSE [H, total_q] of a packed batch: q [total_q, H, d],
+    k [total_k, H, d], v [total_k, H, dv] (CUDA, contiguous, one 16-bit dtype);
+    cu_seqlens_q / cu_seqlens_k int32 CUDA tensors [B + 1] of token offsets;
+    ``max_seqlen_q`` (a host int) bounds every sequence's query count.
+
+    ``causal``: None, "upper_left" or "bottom_right" (per sequence).  A
+    query that sees no key gets O = 0 and LSE = -inf.  Calls ``fa_fwd_varlen``
+    on ``stream`` (default: current stream).
+    """
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape[:2] != v.shape[:2]:
+        raise ValueError("q must be [total_q, H, d], k [total_k, H, d] and v [total_k, H, dv]")
+    if q.shape[1] != k.shape[1] or q.shape[2] != k.shape[2]:
+        raise ValueError("q and k differ in heads or head width")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if causal not in CAUSAL_MODES:
+        raise ValueError("causal must be None, 'upper_left' or 'bottom_right'")
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_cuda or not cu.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor [B + 1]")
+    if cu_seqlens_q.shape != cu_seqlens_k.shape or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 entries")
+    total_q, H, d = q.shape
+    total_k, dv = k.shape[0], v.shape[2]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((total_q, H, dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, B, H, int(max_seqlen_q),
+                       total_q, total_k, d, dv, CAUSAL_MODES[causal], scale, dtype_code(q.dtype),
+                       stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse

@@ -113,6 +113,25 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int BH, int N, int d, bool bf16)
   return r == CUDA_SUCCESS;
 }
 
+// A packed token-major tensor [tokens, H, width] as a (column, head, token)
+// map: a box of 64 columns x 1 head x 128 tokens fills shared memory exactly
+// like a 128 x 64 tile of the [B, H, N, d] layout.
+bool make_tmap_tokens(CUtensorMap* m, const void* ptr, int H, int tokens, int width, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(width) * 2,
+                                 static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(width) * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kBM)};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(ptr), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,6 +285,10 @@ int launch_forward(const void* q, const void* k, const void* v, void* o, float* 
   p.align_br = 0;
   p.dqk = d;
   p.dv = d;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.varlen = 0;
+  p.total_q = 0;
   p.ws_count = sp.split ? static_cast<int*>(workspace) : nullptr;
   p.ws_part = sp.split ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.counter_bytes)
                        : nullptr;
@@ -369,8 +392,88 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.align_br = causal == 2 ? 1 : 0;
   p.dqk = d;
   p.dv = dv;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.varlen = 0;
+  p.total_q = 0;
   const int grid = p.num_units < info->sms ? p.num_units : info->sms;
   const bool w64 = d == 64 && dv == 64;   // else the kernel of width 128
+  const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
+                            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
+                  float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || H < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0 || d <= 0 || dv <= 0)
+    return FA_ERR_SHAPE;
+  if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_qblk = (static_cast<long long>(max_seqlen_q) + 2 * fa::kBM - 1) / (2 * fa::kBM);
+  if (bh > INT_MAX || bh * n_qblk > INT_MAX ||
+      static_cast<long long>(total_q) * H > INT_MAX || static_cast<long long>(total_k) * H > INT_MAX)
+    return FA_ERR_SHAPE;
+  if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return FA_ERR_UNSUPPORTED_D;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0 || max_seqlen_q == 0 || total_q == 0) return FA_OK;  // nothing to write
+  if (!q || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v)))
+    return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) |
+                       reinterpret_cast<uintptr_t>(cu_seqlens_q) |
+                       reinterpret_cast<uintptr_t>(cu_seqlens_k);
+  if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::FwdParams p;
+  const int nk_tok = total_k > 0 ? total_k : 1;   // no key tile is loaded without keys
+  const void* kp = total_k > 0 ? k : q;
+  const void* vp = total_k > 0 ? v : q;
+  if (!make_tmap_tokens(&p.tm_q, q, H, total_q, d, bf16) ||
+      !make_tmap_tokens(&p.tm_k, kp, H, nk_tok, d, bf16) ||
+      !make_tmap_tokens(&p.tm_v, vp, H, nk_tok, dv, bf16) ||
+      !make_tmap_tokens(&p.tm_o, o, H, total_q, dv, bf16))   // unused: rows are stored directly
+    return FA_ERR_TENSORMAP;
+  p.o = o;
+  p.lse = lse;
+  p.trace = g_trace.load();
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
+  p.BH = static_cast<int>(bh);
+  p.N = max_seqlen_q;
+  p.n_qblk = static_cast<int>(n_qblk);
+  p.n_kv = 0;   // per sequence, from cu_seqlens_k
+  p.num_units = static_cast<int>(bh * n_qblk);
+  const long long kv_bytes = static_cast<long long>(total_k) * H * (d + dv) * 2ll;
+  p.head_major = kv_bytes > (64ll << 20) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.split = 0;
+  p.full_rounds = 0;
+  p.tail_units = 0;
+  p.ws_count = nullptr;
+  p.ws_part = nullptr;
+  p.Nk = total_k;
+  p.H = H;
+  p.seqlens_k = nullptr;
+  p.align_br = causal == 2 ? 1 : 0;
+  p.dqk = d;
+  p.dv = dv;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.varlen = 1;
+  p.total_q = total_q;
+  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
+  const bool w64 = d == 64 && dv == 64;
   const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
                             : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

@@ -116,6 +116,17 @@ struct FwdParams {
   // are never read.
   int dqk;
   int dv;
+  // Packed variable-length batches (kKv variants with varlen = 1): Q, O
+  // token-major [total_q, H, d|dv], K, V [Nk = total_k, H, d|dv], LSE
+  // [H, total_q]; sequence b owns query tokens cu_q[b] .. cu_q[b+1] - 1 and
+  // key tokens cu_k[b] .. cu_k[b+1] - 1 (clamped to the totals); N is then
+  // the longest query count the call was sized for.  The tensor maps are
+  // (column, head, token), so a TMA box of 128 tokens of one head lands in
+  // the same shared-memory layout as a tile of the [B, H, N, d] layout.
+  const int* cu_q;
+  const int* cu_k;
+  int varlen;
+  int total_q;
 };
 
 // ---------------------------------------------------------------- tracing
@@ -231,6 +242,7 @@ __device__ __forceinline__ uint32_t p_col(int w) { return 256u + 2u * D + (w ? 6
 struct Unit {
   int bh, mblk, n0, n1;
   int len, off;   // keys of this head; position of query row r is r + off (kKv)
+  int lenq, q0, k0;   // queries of this head; first query and key token (varlen)
 };
 
 // A piece of work: key tiles [kb, kb + n_w) of query tile w of one unit.
@@ -238,7 +250,7 @@ struct Unit {
 // workspace slot `slot` and are merged by whichever piece finishes last.
 struct Piece {
   int bh, mblk, kb, n0, n1, tail, slot;
-  int len, off;   // as in Unit
+  int len, off, lenq, q0, k0;   // as in Unit
 };
 
 // Floats of one workspace slot: unnormalised O of both query tiles stored
@@ -273,24 +285,40 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   }
   const int t0 = 2 * u.mblk;
   if constexpr (kKv) {
-    // keys of this batch, and the key tiles each query tile can see: with
-    // causal masking, keys up to the position of the tile's last row
-    int len = p.seqlens_k ? p.seqlens_k[u.bh / p.H] : p.Nk;
-    len = min(max(len, 0), p.Nk);
+    // keys and queries of this batch, and the key tiles each query tile can
+    // see: with causal masking, keys up to the position of its last row
+    const int b = u.bh / p.H;
+    int len, lenq = p.N, q0 = 0, k0 = 0;
+    if (p.varlen) {
+      q0 = min(max(p.cu_q[b], 0), p.total_q);
+      lenq = min(max(p.cu_q[b + 1], q0), p.total_q) - q0;
+      k0 = min(max(p.cu_k[b], 0), p.Nk);
+      len = min(max(p.cu_k[b + 1], k0), p.Nk) - k0;
+    } else {
+      len = p.seqlens_k ? p.seqlens_k[b] : p.Nk;
+      len = min(max(len, 0), p.Nk);
+    }
     u.len = len;
-    u.off = (kCausal && p.align_br) ? len - p.N : 0;
+    u.lenq = lenq;
+    u.q0 = q0;
+    u.k0 = k0;
+    u.off = (kCausal && p.align_br) ? len - lenq : 0;
     const int nkv = (len + kBN - 1) / kBN;
     int n[2];
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
-      const int last = (t0 + w) * kBM + kBM - 1 + u.off;   // position of the tile's last row
-      n[w] = !kCausal ? nkv : (last < 0 ? 0 : min(last / kBN + 1, nkv));
+      const int first = (t0 + w) * kBM;                       // the tile's first row
+      const int last = min(first + kBM, lenq) - 1 + u.off;    // position of its last row
+      n[w] = first >= lenq ? 0 : !kCausal ? nkv : (last < 0 ? 0 : min(last / kBN + 1, nkv));
     }
     u.n0 = n[0];
     u.n1 = n[1];
   } else {
     u.len = p.N;
     u.off = 0;
+    u.lenq = p.N;
+    u.q0 = 0;
+    u.k0 = 0;
     if (kCausal) {
       u.n0 = min(t0 + 1, p.n_kv);
       u.n1 = min(t0 + 2, p.n_kv);
@@ -333,6 +361,7 @@ __device__ __forceinline__ bool next_piece(const FwdParams& p, int cta, int grid
     const Unit u = decode_unit<kCausal, kKv>(s, p);
     pc.bh = u.bh; pc.mblk = u.mblk; pc.kb = 0; pc.n0 = u.n0; pc.n1 = u.n1;
     pc.tail = -1; pc.slot = 0; pc.len = u.len; pc.off = u.off;
+    pc.lenq = u.lenq; pc.q0 = u.q0; pc.k0 = u.k0;
     return true;
   }
   if (cu.pos >= cu.end) return false;
@@ -348,6 +377,7 @@ __device__ __forceinline__ bool next_piece(const FwdParams& p, int cta, int grid
   pc.tail = (kb == 0 && ke == p.n_kv) ? -1 : t;
   pc.slot = 2 * cta + (t == cu.first_t ? 0 : 1);
   pc.len = u.len; pc.off = u.off;
+  pc.lenq = u.lenq; pc.q0 = u.q0; pc.k0 = u.k0;
   return true;
 }
 
@@ -383,6 +413,24 @@ struct TailWalk {
     ++c;
   }
 };
+
+// Output row of query row `row` of piece u (O is addressed in rows of the
+// value width) and its LSE element: [B, H, N, .] and [B, H, N], or with
+// packed batches [total_q, H, .] and [H, total_q].
+template <bool kKv>
+__device__ __forceinline__ size_t out_row(const FwdParams& p, const Piece& u, int row) {
+  if constexpr (kKv) {
+    if (p.varlen) return static_cast<size_t>(u.q0 + row) * p.H + (u.bh % p.H);
+  }
+  return static_cast<size_t>(u.bh) * p.N + row;
+}
+template <bool kKv>
+__device__ __forceinline__ size_t lse_at(const FwdParams& p, const Piece& u, int row) {
+  if constexpr (kKv) {
+    if (p.varlen) return static_cast<size_t>(u.bh % p.H) * p.total_q + u.q0 + row;
+  }
+  return static_cast<size_t>(u.bh) * p.N + row;
+}
 
 // kSplit: compile the split-tail path (unmasked calls with a workspace only);
 // the other variants carry none of its code.
@@ -469,10 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the S products never read the others)
             const int qc = kKv ? p.dqk / 64 : L::kChunks;
             ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * qc * L::kChunkBytes);
-            for (int w = 0; w < ntile; ++w)
+            for (int w = 0; w < ntile; ++w) {
+              int y = (2 * u.mblk + w) * kBM, z = u.bh;      // row, batch*head
+              if (kKv && p.varlen) { z = u.q0 + y; y = u.bh % p.H; }   // head, token
               for (int c = 0; c < qc; ++c)
                 ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
-                                 bar(L::bQFull), c * 64, (2 * u.mblk + w) * kBM, u.bh);
+                                 bar(L::bQFull), c * 64, y, z);
+            }
             q_issued = k_units + 1;
             trace_event(p, 3, tr, kEvLoadQ, k_units);
           }
@@ -487,9 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nc = kKv ? (kv ? p.dv : p.dqk) / 64 : L::kChunks;
             ptx::mbar_arrive_expect_tx(bar(L::bKvFull + slot), nc * L::kChunkBytes);
             const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
+            int y = (u.kb + j) * kBN, z = u.bh;              // row, batch*head
+            if (kKv && p.varlen) { z = u.k0 + y; y = u.bh % p.H; }   // head, token
             for (int c = 0; c < nc; ++c)
               ptx::tma_load_3d(sbase + L::kKV + slot * L::kTile + c * L::kChunkBytes, tm,
-                               bar(L::bKvFull + slot), c * 64, (u.kb + j) * kBN, u.bh);
+                               bar(L::bKvFull + slot), c * 64, y, z);
             trace_event(p, 3, tr, kv ? kEvLoadV : kEvLoadK, j);
             ++loads;
           }
@@ -713,11 +766,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kKv) {
           // a query tile that sees no key: O = 0 and LSE = -inf (the policy
           // for an empty key set)
-          if (row < p.N) {
+          if (row < u.lenq) {
             uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
-                                                   (static_cast<size_t>(u.bh) * p.N + row) * (p.dv * 2));
+                                                   out_row<kKv>(p, u, row) * (p.dv * 2));
             for (int v = 0; v < p.dv / 8; ++v) orow[v] = make_uint4(0u, 0u, 0u, 0u);
-            p.lse[static_cast<size_t>(u.bh) * p.N + row] = -INFINITY;
+            p.lse[lse_at<kKv>(p, u, row)] = -INFINITY;
           }
         }
         continue;
@@ -963,8 +1016,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf.lap(13);
         }
         pf.count(15);
-      } else if constexpr (L::kTmaStore) {
-        // through a swizzled staging tile and a TMA store (rows past N clipped)
+      } else if (L::kTmaStore && !(kKv && p.varlen)) {
+        // through a swizzled staging tile and a TMA store (rows past N
+        // clipped; packed batches, whose tiles end mid-tensor, store directly)
         if (t == 0) ptx::bulk_wait_group_read0();   // staging tile free again
         ptx::named_bar_sync(1 + w, 128);
 #pragma unroll 1
@@ -1002,7 +1056,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns in the kKv variants)
         const int ocols = kKv ? p.dv : D;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) +
-                                               (static_cast<size_t>(u.bh) * p.N + row) * (ocols * 2));
+                                               out_row<kKv>(p, u, row) * (ocols * 2));
+        const int nrows = kKv ? u.lenq : p.N;
 #pragma unroll 1
         for (int q4 = 0; q4 < ocols / 32; ++q4) {
           uint32_t orr[32];
@@ -1017,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    __uint_as_float(orr[2 * e + 1])), il2), a, b);
             pk16[e] = ptx::pack2<kBf16>(a, b);
           }
-          if (row < p.N) {
+          if (row < nrows) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               orow[q4 * 4 + v] = make_uint4(pk16[4 * v], pk16[4 * v + 1], pk16[4 * v + 2],
@@ -1027,8 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bOFree + w));        // O_w may be overwritten now
       }
-      if ((!kSplit || u.tail < 0) && row < p.N)
-        p.lse[static_cast<size_t>(u.bh) * p.N + row] = l > 0.f ? (ptx::lg2(l) - neg_m) * kLn2 : -INFINITY;
+      if ((!kSplit || u.tail < 0) && row < (kKv ? u.lenq : p.N))
+        p.lse[lse_at<kKv>(p, u, row)] = l > 0.f ? (ptx::lg2(l) - neg_m) * kLn2 : -INFINITY;
       if (tracer) trace_event(p, w, tr, kEvEpiEnd, ucnt - 1);
       pf.lap(6);
     }

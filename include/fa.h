@@ -132,6 +132,51 @@ int fa_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
               const int *seqlens_k, float scale, int dtype, cudaStream_t stream);
 
 /*
+ * fa_fwd_varlen — exact attention over a packed batch of sequences of
+ * different lengths, with no padding.
+ *
+ * The pages point out that padding every sequence of a batch to the longest
+ * one makes a fused kernel do work for the padded positions, and that at
+ * mixed lengths packing or a variable-length kernel matters more than the
+ * choice of attention implementation ("FlashAttention: The Matrix You Never
+ * Have to Write Down", section on PyTorch's scaled_dot_product_attention,
+ * the padding note).  This entry point runs the same tiled online softmax
+ * as fa_fwd_kv on packed tensors: each sequence attends only to its own
+ * keys, and no tile is spent past a sequence's end.
+ *
+ *   q            : device pointer, [total_q, H, d], dtype `dtype`, 16-byte aligned.
+ *   k            : device pointer, [total_k, H, d], 16-byte aligned.
+ *   v            : device pointer, [total_k, H, dv], 16-byte aligned (k and v
+ *                  may be NULL when total_k = 0).
+ *   o            : device pointer, [total_q, H, dv], 16-byte aligned (written).
+ *   lse          : device pointer, [H, total_q] float32, 4-byte aligned (written).
+ *   cu_seqlens_q : device pointer, B + 1 int32, 4-byte aligned: sequence b
+ *                  owns query tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1] - 1.
+ *   cu_seqlens_k : the same for key/value tokens.
+ *                  Offsets are clamped to [0, total] and an end below its
+ *                  start counts as an empty sequence, so no value of these
+ *                  arrays makes the kernel read or write out of bounds;
+ *                  overlapping sequences are the caller's error.
+ *   max_seqlen_q : an upper bound on every sequence's query count (sizes the
+ *                  grid); query rows past it are not computed.
+ *   total_q, total_k : packed token counts (>= 0).
+ *   d, dv        : widths of Q/K and of V/O, each 64 or 128.
+ *   causal       : 0 none; 1 upper-left (query i of a sequence at position
+ *                  i); 2 bottom-right (at position len_k - len_q + i), per
+ *                  sequence.  A query row that sees no key gets O = 0 and
+ *                  LSE = -inf.
+ *   scale, dtype, stream : as fa_fwd.
+ *
+ * Errors as fa_fwd_kv; FA_ERR_NULLPTR also for missing cu_seqlens arrays,
+ * FA_ERR_ALIGN also for misaligned ones.  B*H == 0, max_seqlen_q == 0 or
+ * total_q == 0 writes nothing.
+ */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
+                  float scale, int dtype, cudaStream_t stream);
+
+/*
  * fa_fwd_ws — fa_fwd with a caller-provided workspace used to balance the
  * last round of work across all SMs.
  *

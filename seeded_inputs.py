@@ -11,6 +11,7 @@ workload dtype (round-to-nearest-even, torch's ``.to``).  Both sides of a
 parity test see exactly these rounded values (the oracle upcasts them to
 float64).
 """
+import itertools
 import math
 
 import torch
@@ -129,6 +130,21 @@ def make_decode(B, H, Nq, Nk, d, dtype="bf16", seed=0, dv=None):
     k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
     v = torch.randn((B, H, Nk, d if dv is None else dv), generator=g, dtype=torch.float32)
     return q.to(t), k.to(t), v.to(t)
+
+
+def make_varlen(lens_q, lens_k, H, d, dtype="bf16", seed=0, dv=None):
+    """Packed batch: Q [sum(lens_q), H, d], K [sum(lens_k), H, d], V
+    [sum(lens_k), H, dv] token-major, N(0,1) from one generator (seeded
+    800000 + seed), rounded; and the int32 offsets cu_q, cu_k [B + 1]."""
+    g = torch.Generator("cpu").manual_seed(800000 + int(seed))
+    t = DTYPES[dtype]
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = torch.randn((tq, H, d), generator=g, dtype=torch.float32)
+    k = torch.randn((tk, H, d), generator=g, dtype=torch.float32)
+    v = torch.randn((tk, H, d if dv is None else dv), generator=g, dtype=torch.float32)
+    cu_q = torch.tensor([0] + list(itertools.accumulate(int(x) for x in lens_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(int(x) for x in lens_k)), dtype=torch.int32)
+    return q.to(t), k.to(t), v.to(t), cu_q, cu_k
 
 
 def make_dout(B, H, N, d, dtype="bf16", seed=0):

@@ -207,6 +207,28 @@ def test_fwd_kv_host_errors(lib):
     assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
 
 
+def test_fwd_varlen_host_errors(lib):
+    """fa_fwd_varlen checks sizes, the causal mode, widths, dtype, scale,
+    pointers (the offset arrays always; k, v only with keys) and alignment
+    before the device."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE,
+                B=3, H=4, max_seqlen_q=500, total_q=900, total_k=2000, d=64, dv=128, causal=1,
+                scale=0.1, dtype=fa.FA_FP16)
+    cases = [(dict(B=-1), fa.FA_ERR_SHAPE), (dict(total_k=-1), fa.FA_ERR_SHAPE),
+             (dict(max_seqlen_q=-5), fa.FA_ERR_SHAPE), (dict(causal=7), fa.FA_ERR_SHAPE),
+             (dict(d=32), fa.FA_ERR_UNSUPPORTED_D), (dict(dv=256), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dtype=2), fa.FA_ERR_DTYPE), (dict(scale=float("inf")), fa.FA_ERR_SCALE),
+             (dict(total_q=0, q=None), fa.FA_OK), (dict(max_seqlen_q=0), fa.FA_OK),
+             (dict(B=0), fa.FA_OK), (dict(cu_seqlens_k=None), fa.FA_ERR_NULLPTR),
+             (dict(v=None), fa.FA_ERR_NULLPTR), (dict(o=FAKE + 8), fa.FA_ERR_ALIGN),
+             (dict(cu_seqlens_q=FAKE + 1), fa.FA_ERR_ALIGN),
+             (dict(total_q=2 ** 30, H=4), fa.FA_ERR_SHAPE)]
+    for args, code in cases:
+        assert fa.fa_fwd_varlen(**{**call, **args}) == code, args
+    rc = fa.fa_fwd_varlen(**{**call, "total_k": 0, "k": None, "v": None})
+    assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
