@@ -28,6 +28,10 @@ workload (GB/s of K/V read against the measured HBM copy bandwidth).
 length, with padding and causal alignment) on a kv workload; FLOPs are 4 d
 per visible (query, key) pair.
 
+``--pass varlen`` times ``fa_fwd_varlen`` on a packed batch of sequences of
+mixed lengths (and, for context, the same batch padded through
+``fa_fwd_kv``).
+
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
 call (three kernels) with the forward's O and LSE and a seeded dO resident
 on the device; FLOPs are 2.5x the forward's (five matmuls against two).
@@ -62,6 +66,8 @@ METRIC_BWD = ("attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved) a
               "dense BF16 tensor peak")
 METRIC_KV = ("attention fwd, queries against a key set of another length: TFLOP/s (4 d per "
              "visible query-key pair) and % of GB300 dense BF16 tensor peak")
+METRIC_VARLEN = ("attention fwd over a packed variable-length batch: TFLOP/s (4 d per visible "
+                 "query-key pair) and % of GB300 dense BF16 tensor peak")
 FALLBACK_PEAK_TFLOPS = 1900.0
 
 
@@ -1024,6 +1030,195 @@ def run_ours_kv(args, w):
     return 0
 
 
+def run_ours_varlen(args, w):
+    """Packed variable-length batch: one step = one fa_fwd_varlen launch over
+    the packed workload resident in device memory.  For context the same
+    batch padded to its longest sequence is also timed through fa_fwd_kv
+    (key counts given, padded query rows still computed)."""
+    import exact_tiled_attention_14_gb300 as fa
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+    sampler = ClockSampler(local).start()
+    B, H, d = w["B"], w["H"], w["d"]
+    lens = seeded_inputs.varlen_lengths(B, w["lo"], w["hi"], w["seed"])
+    q, k, v, cu_q, cu_k = seeded_inputs.make_varlen(lens, lens, H, d, w["dtype"], seed=w["seed"])
+    total, max_len = sum(lens), max(lens)
+    mode = fa.CAUSAL_MODES[w["causal"]]
+    flops = sum(4.0 * d * H * kv_visible_pairs(dict(Nq=n, causal=w["causal"]), n, 0)
+                for n in lens)
+    io = dict(h2d=3 * total * H * d * 2 + 2 * 4 * (B + 1), d2h=total * H * (d * 2 + 4))
+    stream = torch.cuda.current_stream(device)
+    code = fa.dtype_code(q.dtype)
+    per_replica = io["h2d"] + io["d2h"]
+    replicas = 1 if per_replica > 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / per_replica)) + 1
+    replicas = min(replicas, 64)
+    dcq, dck = cu_q.to(device), cu_k.to(device)
+    bufs = []
+    for _ in range(replicas):
+        dq_, dk_, dv_ = (t.to(device) for t in (q, k, v))
+        bufs.append((dq_, dk_, dv_, torch.empty_like(dq_),
+                     torch.empty((H, total), dtype=torch.float32, device=device)))
+
+    def step(i):
+        dq_, dk_, dv_, o, lse = bufs[i % replicas]
+        rc = fa.fa_fwd_varlen(dq_, dk_, dv_, o, lse, dcq, dck, B, H, max_len, total, total, d, d,
+                              mode, w["scale"], code, stream)
+        if rc:
+            raise fa.FaError(rc, "fa_fwd_varlen")
+
+    def timed(fn, steps):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        st, word = fa.fa_status(stream)
+        if st:
+            raise fa.FaError(st, f"warmup status {word:#x}")
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(world, device)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(steps):
+            starts[i].record(stream)
+            fn(i)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world, device)
+        t1 = time.time()
+        st, word = fa.fa_status(stream)
+        if st:
+            raise fa.FaError(st, f"timed status {word:#x}")
+        total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
+        kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
+                                 world, device)
+        return total_ms, kern_ms, t0, t1
+
+    t_warm = time.time()
+    total_ms, kern_ms, t0, t1 = timed(step, args.steps)
+    clocks_window = (t0, t1)
+
+    # end to end: pinned host packed q, k, v and offsets in, o and lse out
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    hcq, hck = cu_q.pin_memory(), cu_k.pin_memory()
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hl = torch.empty((H, total), dtype=torch.float32).pin_memory()
+    dq_, dk_, dv_, o, lse = bufs[0]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        dcq.copy_(hcq, non_blocking=True)
+        dck.copy_(hck, non_blocking=True)
+        fa.attention_forward_varlen(dq_, dk_, dv_, dcq, dck, max_len, causal=w["causal"],
+                                    scale=w["scale"], out=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+
+    # the same batch padded to the longest sequence, through fa_fwd_kv
+    del bufs
+    pq = torch.zeros((B, H, max_len, d), dtype=q.dtype, device=device)
+    pk, pv = torch.zeros_like(pq), torch.zeros_like(pq)
+    for b, n in enumerate(lens):
+        a = int(cu_q[b])
+        pq[b, :, :n] = q[a:a + n].to(device).transpose(0, 1)
+        pk[b, :, :n] = k[a:a + n].to(device).transpose(0, 1)
+        pv[b, :, :n] = v[a:a + n].to(device).transpose(0, 1)
+    po = torch.empty_like(pq)
+    pl = torch.empty((B, H, max_len), dtype=torch.float32, device=device)
+    psl = torch.tensor(lens, dtype=torch.int32, device=device)
+
+    def padded_step(i):
+        rc = fa.fa_fwd_kv(pq, pk, pv, po, pl, B, H, max_len, max_len, d, d, mode, psl,
+                          w["scale"], code, stream)
+        if rc:
+            raise fa.FaError(rc, "fa_fwd_kv (padded)")
+
+    _, padded_ms, _, _ = timed(padded_step, max(10, args.steps // 4))
+    sampler.stop()
+    clocks = sampler.summary(*clocks_window, fallback_window=(t_warm, clocks_window[1]))
+    if rank != 0:
+        return 0
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak, peak_sustained, peak_src = measured_peaks()
+    traffic, traffic_note = stored_traffic(w["name"])
+    line = {
+        "metric": METRIC_VARLEN, "value": world * flops * args.steps / (total_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "pass": "varlen", "B": B, "H": H, "d": d,
+                   "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
+                   "lengths": lens, "total_tokens": total, "entry": "fa_fwd_varlen",
+                   "padded_equivalent": {"entry": "fa_fwd_kv", "ms": padded_ms,
+                                         "note": "same batch padded to the longest sequence"},
+                   "parallelism": "single GPU" if world == 1 else f"replicas x{world}",
+                   "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
+                          if replicas > 1 else "inputs larger than L2")},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
+                     "kernel_ms": kern_ms, "flops_per_launch": flops,
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "compulsory_bytes": io["h2d"] + io["d2h"]},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "gpu": torch.cuda.get_device_name(device),
+    }
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        lib = oracle.load()
+        cores = oracle.num_threads(lib)
+        spent, done_flops, heads = 0.0, 0.0, 0
+        order = sorted(range(B), key=lambda b: lens[b])       # shortest sequences first
+        for b in order:
+            n, a = lens[b], int(cu_q[b])
+            for h in range(H):
+                t_a = time.perf_counter()
+                oracle.attention_rows(q[a:a + n, h].double().numpy(), np.arange(n, dtype=np.int64),
+                                      k[a:a + n, h].double().numpy(), v[a:a + n, h].double().numpy(),
+                                      causal=True, scale=w["scale"], lib=lib)
+                spent += time.perf_counter() - t_a
+                done_flops += 4.0 * d * kv_visible_pairs(dict(Nq=n, causal=w["causal"]), n, 0)
+                heads += 1
+                if spent >= args.cpu_seconds:
+                    break
+            if spent >= args.cpu_seconds:
+                break
+        line["cpu_baseline"] = {"value": done_flops / spent / 1e12, "unit": "TFLOP/s",
+                                "cores": cores, "kind": "oracle", "seconds": spent,
+                                "sample": f"{heads} whole (sequence, head) pairs of {w['name']}, "
+                                          "shortest sequences first (float64)"}
+    print(json.dumps(line), flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(json.dumps(line) + "\n")
+    return 0
+
+
 def measured_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -1050,10 +1245,10 @@ def main(argv=None):
     ap.add_argument("--split", action="store_true",
                     help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv"], default="fwd",
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv", "varlen"], default="fwd",
                     help="time the forward pass (default), the backward pass (fa_bwd), "
                          "split-KV decoding (fa_decode; --workload names a decoding workload) "
-                         "or fa_fwd_kv (--workload names a kv workload)")
+                         ", fa_fwd_kv (--workload names a kv workload) or fa_fwd_varlen")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1070,6 +1265,15 @@ def main(argv=None):
             wd["H"] = args.heads if args.heads is not None else wd["H"]
             wd["name"] = f"{wd['name']}@B{wd['B']}H{wd['H']}"
         return run_ours_decode(args, wd)
+    if args.pass_ == "varlen":
+        name = args.workload if args.workload != DEFAULT_WORKLOAD else \
+            seeded_inputs.VARLEN_WORKLOADS[0]["name"]
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the varlen pass has no reference arm; the oracle checks it in tests "
+                              "and its cpu_baseline times it"}))
+            return 0
+        return run_ours_varlen(args, seeded_inputs.varlen_workload(name))
     if args.pass_ == "kv":
         name = args.workload if args.workload != DEFAULT_WORKLOAD else \
             seeded_inputs.KV_WORKLOADS[0]["name"]

@@ -3,7 +3,7 @@
 This module only marshals arguments to the C ABI in ``include/fa.h``
 (``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
-``fa_status``, ``fa_set_watchdog_ns``, ``fa_watchdog_selftest``,
+``fa_status``, ``fa_set_watchdog_ns``, ``fa_set_unit_group``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
 under the same names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
@@ -44,7 +44,8 @@ FA_ERR_WORKSPACE = 12
 # Functions the C ABI exports (checked against include/fa.h by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
-           "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_work_tiles", "fa_version")
+           "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
+           "fa_version")
 
 _lib = None
 
@@ -93,6 +94,8 @@ def load_library(path=None):
     lib.fa_status.restype = i
     lib.fa_set_watchdog_ns.argtypes = [ctypes.c_ulonglong]
     lib.fa_set_watchdog_ns.restype = None
+    lib.fa_set_unit_group.argtypes = [ctypes.c_int]
+    lib.fa_set_unit_group.restype = ctypes.c_int
     lib.fa_watchdog_selftest.argtypes = [ctypes.c_ulonglong, vp]
     lib.fa_watchdog_selftest.restype = i
     lib.fa_work_tiles.argtypes = [i, i, ctypes.POINTER(ctypes.c_longlong)]
@@ -228,6 +231,12 @@ def fa_status(stream=None):
 
 def fa_set_watchdog_ns(ns):
     load_library().fa_set_watchdog_ns(int(ns))
+
+
+def fa_set_unit_group(heads):
+    """Unit-order override for the forward kernels (0 = choose per call);
+    returns the C return code."""
+    return load_library().fa_set_unit_group(int(heads))
 
 
 def fa_watchdog_selftest(budget_ns, stream=None):

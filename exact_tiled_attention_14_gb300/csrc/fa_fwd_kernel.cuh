@@ -87,7 +87,7 @@ struct FwdParams {
   int n_qblk;              // ceil(N / 256): units per head
   int n_kv;                // ceil(N / 128): key tiles per head
   int num_units;           // BH * n_qblk
-  int head_major;          // unit order: 1 = head by head, 0 = level by level (see unit_at)
+  int hgroup;              // unit order: heads per group, 1 .. BH (see unit_at)
   // Split tail (unmasked only, see next_piece): after full_rounds rounds of
   // whole units, the last tail_units units are cut along the key axis so
   // every CTA gets the same number of key tiles.  Partial results go to
@@ -261,13 +261,13 @@ __host__ __device__ constexpr int kSlotFloats() { return 2 * kBM * (D + 2); }
 
 // Static persistent schedule, deterministic so every role of a CTA walks the
 // same list without communicating.  Units are dealt to CTAs in a snake
-// (boustrophedon) order, round by round, from one of two orderings:
-//  - level by level (head_major = 0): the heaviest query block of every
-//    head first (for causal, the last blocks), which balances best;
-//  - head by head (head_major = 1): all query blocks of a head, heaviest
-//    first, then the next head.  Units in flight then share a few heads'
-//    K/V, which stay in L2; the host picks this when the K/V of all heads
-//    would not fit in L2 (at the price of a few percent of balance).
+// (boustrophedon) order, round by round, from one ordering: heads in groups
+// of `hgroup`, one group after the other, and inside a group level by level
+// (the heaviest query block of each of its heads first; for causal masking
+// the last blocks).  hgroup = BH is plain level order, which balances best
+// when the K/V of all heads fit in L2; hgroup = 1 walks one head at a time,
+// so the units in flight share a few heads' K/V in L2.  The host picks the
+// group from the L2 budget and the balance of the deal (fa_api.cu).
 __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
@@ -275,12 +275,13 @@ __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
 template <bool kCausal, bool kKv = false>
 __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   Unit u;
-  if (p.head_major) {
-    u.bh = s / p.n_qblk;
-    u.mblk = p.n_qblk - 1 - (s - u.bh * p.n_qblk);
-  } else {
-    const int level = s / p.BH;
-    u.bh = s - level * p.BH;
+  {
+    const int per_group = p.hgroup * p.n_qblk;
+    const int g = s / per_group;
+    const int r = s - g * per_group;
+    const int gl = min(p.hgroup, p.BH - g * p.hgroup);   // heads in this group (the last may be short)
+    const int level = r / gl;
+    u.bh = g * p.hgroup + (r - level * gl);
     u.mblk = p.n_qblk - 1 - level;
   }
   const int t0 = 2 * u.mblk;

@@ -340,6 +340,21 @@ int fa_status(cudaStream_t stream, unsigned int *detail);
 void fa_set_watchdog_ns(unsigned long long ns);
 
 /*
+ * fa_set_unit_group — override of the forward kernels' unit order (the pages
+ * have no counterpart; it changes only which CTA computes which block, never
+ * a result).  The persistent forward kernels deal (batch*head, 256-row query
+ * block) units to the SMs from groups of `heads` heads, level by level inside
+ * a group (the heaviest query block of each head of the group first).  0
+ * (the default) lets each call choose: the largest group whose K/V fit an L2
+ * budget, and for causal calls of known lengths the group whose simulated
+ * deal is most even.  A positive value is used as is (clamped to B*H) by
+ * every fa_fwd, fa_fwd_ws, fa_fwd_static, fa_fwd_kv and fa_fwd_varlen
+ * launched afterwards.  Host-side setting shared by all threads of the
+ * process.  Returns FA_ERR_SHAPE for a negative value.
+ */
+int fa_set_unit_group(int heads);
+
+/*
  * fa_watchdog_selftest — failure-detection self-test (the pages have no
  * counterpart).  Launches on `stream` a one-thread kernel whose bounded
  * wait, the same routine every kernel of this library waits with, is on a

@@ -69,6 +69,34 @@ for _i, _w in enumerate(KV_WORKLOADS):
     _w["scale"] = 1.0 / math.sqrt(_w["d"])
 
 
+# Packed variable-length batches (fa_fwd_varlen): self-attention over B
+# sequences whose lengths are uniform integers in [lo, hi] (seeded), query
+# and key lengths equal, upper-left causal (a prefill of mixed prompts).
+# The pages give no sizes; seed 4000 + i.
+VARLEN_WORKLOADS = [
+    dict(name="varlen_b16_h16_len256to4096_d128_bf16_causal", B=16, H=16, d=128, dtype="bf16",
+         causal="upper_left", lo=256, hi=4096),
+]
+for _i, _w in enumerate(VARLEN_WORKLOADS):
+    _w["seed"] = 4000 + _i
+    _w["scale"] = 1.0 / math.sqrt(_w["d"])
+
+
+def varlen_workload(name):
+    """The fa_fwd_varlen workload dict with this name."""
+    for w in VARLEN_WORKLOADS:
+        if w["name"] == name:
+            return dict(w)
+    raise KeyError(name)
+
+
+def varlen_lengths(B, lo, hi, seed):
+    """Sequence lengths, uniform integers in [lo, hi], from their own
+    generator (seeded 610000 + seed)."""
+    g = torch.Generator("cpu").manual_seed(610000 + int(seed))
+    return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+
+
 def kv_workload(name):
     """The fa_fwd_kv workload dict with this name."""
     for w in KV_WORKLOADS:

@@ -229,6 +229,13 @@ def test_fwd_varlen_host_errors(lib):
     assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
 
 
+def test_unit_group_setter(lib):
+    """fa_set_unit_group takes 0 (automatic) or a positive group size."""
+    assert fa.fa_set_unit_group(-1) == fa.FA_ERR_SHAPE
+    assert fa.fa_set_unit_group(4) == fa.FA_OK
+    assert fa.fa_set_unit_group(0) == fa.FA_OK
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
