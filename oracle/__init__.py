@@ -9,10 +9,14 @@ never import, link or call it, and it imports nothing from them.
 * ``attention_grad`` / ``grad_query_rows`` / ``grad_key_rows`` — the
   gradients of that definition with respect to Q, K and V (chain rule through
   the softmax) in C, ``attn_grad_oracle.c``.
+* ``attention_dropout`` / ``attention_dropout_grad`` / ``dropout_mask`` /
+  ``philox4x32_10`` — attention with dropout on the weights, its gradients,
+  the keep mask and the counter-based generator it is drawn from, in C,
+  ``attn_dropout_oracle.c``.
 * ``online_model`` — the block-wise online recurrence in numpy, the second
   derivation the C code is pinned against.
 
-``build()`` compiles both C files with gcc (OpenMP over rows) into
+``build()`` compiles the C files with gcc (OpenMP over rows) into
 ``oracle/_build/liboracle.so``; the first call to ``attention`` builds it if
 it is missing.
 """
@@ -28,7 +32,8 @@ from . import online_model  # noqa: F401  (re-exported)
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
 _GRAD_SRC = os.path.join(_HERE, "attn_grad_oracle.c")
-SOURCES = (_SRC, _GRAD_SRC)
+_DROP_SRC = os.path.join(_HERE, "attn_dropout_oracle.c")
+SOURCES = (_SRC, _GRAD_SRC, _DROP_SRC)
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lib = None
@@ -76,6 +81,18 @@ def _bind(path):
         lib.oracle_grad_key_rows.argtypes = [i64, i64, i64, p, p, p, p, i64, p, p, p, i32,
                                              f64, p, p]
         lib.oracle_grad_key_rows.restype = i32
+    if hasattr(lib, "oracle_attention_dropout"):
+        i32, f64, u32, u64 = ctypes.c_int, ctypes.c_double, ctypes.c_uint32, ctypes.c_uint64
+        lib.oracle_philox4x32_10.argtypes = [p, p, p]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_dropout_mask.argtypes = [i64, i64, i64, u64, u32, i32, p]
+        lib.oracle_dropout_mask.restype = i32
+        lib.oracle_attention_dropout.argtypes = [i64, i64, i64, i64, i64, p, p, p, i32, f64,
+                                                 u64, u32, i32, p, p]
+        lib.oracle_attention_dropout.restype = i32
+        lib.oracle_attention_dropout_grad.argtypes = [i64, i64, i64, i64, i64, p, p, p, p, i32,
+                                                      f64, u64, u32, i32, p, p, p]
+        lib.oracle_attention_dropout_grad.restype = i32
     return lib
 
 
@@ -237,3 +254,76 @@ def grad_key_rows(k_rows, v_rows, k_pos, q, dout, lse, delta, causal=False, scal
     if rc != 0:
         raise RuntimeError(f"oracle_grad_key_rows failed ({rc})")
     return dk, dvv
+
+
+def dropout_threshold(p):
+    """Byte threshold t = round((1 - p) * 256) of the keep rule (keep iff the
+    element's random byte < t); dropout probability p must leave t >= 1."""
+    t = int(round((1.0 - float(p)) * 256.0))
+    if not (0.0 <= float(p) < 1.0) or t < 1:
+        raise ValueError("dropout probability must be in [0, 1) with round((1 - p) * 256) >= 1")
+    return t
+
+
+def philox4x32_10(ctr, key, lib=None):
+    """The four 32-bit words of Philox4x32-10 for counter ctr[4], key key[2]."""
+    lib = lib or load()
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(c.ctypes.data_as(ctypes.c_void_p), k.ctypes.data_as(ctypes.c_void_p),
+                             out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def dropout_mask(bh, nq, nk, seed, offset, p, lib=None):
+    """Keep mask [nq, nk] (uint8 0/1) of head ``bh`` (small shapes)."""
+    lib = lib or load()
+    mask = np.zeros((nq, nk), dtype=np.uint8)
+    rc = lib.oracle_dropout_mask(int(bh), int(nq), int(nk), int(seed), int(offset),
+                                 dropout_threshold(p), _ptr(mask))
+    if rc != 0:
+        raise RuntimeError(f"oracle_dropout_mask failed ({rc})")
+    return mask
+
+
+def attention_dropout(q, k, v, bh, seed, offset, p, causal=False, scale=None, lib=None):
+    """O, LSE of ONE head (q [Tq, d], k [Tk, d], v [Tk, dv]; head index ``bh``
+    in the batch*head numbering the mask is drawn with) with dropout
+    probability p on the attention weights."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    tq, d = q.shape
+    tk, dv = v.shape
+    if k.shape != (tk, d):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o, lse = np.zeros((tq, dv)), np.zeros(tq)
+    rc = lib.oracle_attention_dropout(int(bh), tq, tk, d, dv, _ptr(q), _ptr(k), _ptr(v),
+                                      int(bool(causal)), float(scale), int(seed), int(offset),
+                                      dropout_threshold(p), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_dropout failed ({rc})")
+    return o, lse
+
+
+def attention_dropout_grad(q, k, v, dout, bh, seed, offset, p, causal=False, scale=None,
+                           lib=None):
+    """dQ, dK, dV of sum(dout * O) for O = attention_dropout(...) of ONE head."""
+    lib = lib or load()
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    tq, d = q.shape
+    tk, dv = v.shape
+    if k.shape != (tk, d) or g.shape != (tq, dv):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dvv = np.zeros((tq, d)), np.zeros((tk, d)), np.zeros((tk, dv))
+    rc = lib.oracle_attention_dropout_grad(int(bh), tq, tk, d, dv, _ptr(q), _ptr(k), _ptr(v),
+                                           _ptr(g), int(bool(causal)), float(scale), int(seed),
+                                           int(offset), dropout_threshold(p), _ptr(dq), _ptr(dk),
+                                           _ptr(dvv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_dropout_grad failed ({rc})")
+    return dq, dk, dvv
