@@ -1,7 +1,7 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
 ``fa_status``, ``fa_set_watchdog_ns``, ``fa_set_unit_group``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
@@ -40,9 +40,10 @@ FA_ERR_LAUNCH = 9
 FA_ERR_TIMEOUT = 10
 FA_ERR_CUDA = 11
 FA_ERR_WORKSPACE = 12
+FA_ERR_DROPOUT = 13
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
            "fa_version")
@@ -84,6 +85,11 @@ def load_library(path=None):
     lib.fa_fwd_static.restype = i
     lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_fwd_dropout.argtypes = [vp] * 5 + [i, i, i, i, i, f, f, u64, u32, i, vp]
+    lib.fa_fwd_dropout.restype = i
+    lib.fa_bwd_dropout.argtypes = [vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp]
+    lib.fa_bwd_dropout.restype = i
     lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, vp, ctypes.c_size_t, vp]
     lib.fa_decode.restype = i
     lib.fa_decode_workspace_size.argtypes = [i] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
@@ -169,6 +175,25 @@ def fa_fwd_static(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream=None
     return lib.fa_fwd_static(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
                              int(N), int(d), int(bool(causal)), float(scale), int(dtype),
                              _stream(stream))
+
+
+def fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, causal, scale, dropout_p, seed, offset, dtype,
+                   stream=None):
+    """Raw C call of the forward pass with dropout; returns the code."""
+    lib = load_library()
+    return lib.fa_fwd_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                              int(N), int(d), int(bool(causal)), float(scale), float(dropout_p),
+                              int(seed), int(offset), int(dtype), _stream(stream))
+
+
+def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale,
+                   dropout_p, seed, offset, dtype, stream=None):
+    """Raw C call of the backward pass with dropout; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
+                              _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
+                              int(N), int(d), int(bool(causal)), float(scale), float(dropout_p),
+                              int(seed), int(offset), int(dtype), _stream(stream))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
@@ -435,6 +460,60 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=N
     rc = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, code, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def attention_forward_dropout(q, k, v, dropout_p, seed, offset, causal=False, scale=None,
+                              stream=None):
+    """O, LSE of ``attention_forward`` with dropout on the attention weights
+    (``fa_fwd_dropout``): the same (dropout_p, seed, offset) given to
+    ``attention_backward_dropout`` regenerate the mask."""
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"dtypes differ: {q.dtype}, {k.dtype}, {v.dtype}")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [B, H, N, d] of one shape")
+    if not all(t.is_cuda and t.is_contiguous() for t in (q, k, v)):
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_fwd_dropout(q, k, v, out, lse, B, H, N, d, causal, scale, dropout_p, seed, offset,
+                        dtype_code(q.dtype), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_dropout")
+    return out, lse
+
+
+def attention_backward_dropout(q, k, v, o, lse, dout, dropout_p, seed, offset, causal=False,
+                               scale=None, stream=None):
+    """dQ, dK, dV for O, LSE = attention_forward_dropout(q, k, v, dropout_p,
+    seed, offset) (``fa_bwd_dropout``; the mask is regenerated)."""
+    import torch
+    ts = (q, k, v, o, dout)
+    if any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, o, dout must all be [B, H, N, d] of one shape")
+    if lse.dtype != torch.float32 or lse.shape != q.shape[:3]:
+        raise ValueError("lse must be float32 [B, H, N]")
+    if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale,
+                        dropout_p, seed, offset, dtype_code(q.dtype), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_dropout")
     return dq, dk, dv
 
 

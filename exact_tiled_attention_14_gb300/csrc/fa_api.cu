@@ -134,6 +134,26 @@ bool make_tmap_tokens(CUtensorMap* m, const void* ptr, int H, int tokens, int wi
   return r == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------- dropout
+// Keep threshold of the dropout rule: an element is kept when its random
+// byte is below t = floor((1 - p) * 256 + 1/2), computed in double from the
+// float p; kept weights are scaled by 256 / t.  -1 when p is not in [0, 1)
+// or leaves t = 0.  t = 256 keeps everything (no dropout).
+int drop_threshold(float p) {
+  if (!(p >= 0.0f) || !(p < 1.0f)) return -1;
+  const int t = static_cast<int>(std::floor((1.0 - static_cast<double>(p)) * 256.0 + 0.5));
+  return t >= 1 ? t : -1;
+}
+
+template <class Params>
+void set_dropout(Params* p, int t, unsigned long long seed, unsigned int off) {
+  p->drop_t = static_cast<uint32_t>(t);
+  p->drop_k0 = static_cast<uint32_t>(seed);
+  p->drop_k1 = static_cast<uint32_t>(seed >> 32);
+  p->drop_off = off;
+  p->drop_scale = 256.0f / static_cast<float>(t);
+}
+
 // ---------------------------------------------------------------- unit order
 // The kernels deal (batch*head, 256-row query block) units to the CTAs in a
 // snake order over groups of `hgroup` heads (level by level inside a group).
@@ -279,6 +299,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_TIMEOUT: return "a bounded wait in a kernel ran out (watchdog)";
     case FA_ERR_CUDA: return "CUDA runtime error";
     case FA_ERR_WORKSPACE: return "workspace smaller than fa_fwd_workspace_size reports";
+    case FA_ERR_DROPOUT: return "dropout probability must be in [0, 1) and keep at least 1/256";
     default: return "unknown error code";
   }
 }
@@ -417,6 +438,7 @@ int launch_forward(const void* q, const void* k, const void* v, void* o, float* 
   p.align_br = 0;
   p.dqk = d;
   p.dv = d;
+  set_dropout(&p, 256, 0, 0);
   p.cu_q = nullptr;
   p.cu_k = nullptr;
   p.varlen = 0;
@@ -462,9 +484,12 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, 
                         workspace_bytes, stream);
 }
 
-int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int Nq, int Nk, int d, int dv, int causal, const int* seqlens_k, float scale,
-              int dtype, cudaStream_t stream) {
+// fa_fwd_kv, and fa_fwd_dropout when drop_t < 256 (square shapes, no key
+// counts; the caller checks that).
+static int forward_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, int dv, int causal, const int* seqlens_k,
+                      float scale, int dtype, int drop_t, unsigned long long seed,
+                      unsigned int drop_off, cudaStream_t stream) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || dv <= 0) return FA_ERR_SHAPE;
   if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
@@ -531,10 +556,35 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.cu_k = nullptr;
   p.varlen = 0;
   p.total_q = 0;
+  set_dropout(&p, drop_t, seed, drop_off);
   const bool w64 = d == 64 && dv == 64;   // else the kernel of width 128
-  const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
-                            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
+  cudaError_t e;
+  if (drop_t < 256)
+    e = w64 ? fa::launch_fwd_drop_d64(p, grid, bf16, causal != 0, stream)
+            : fa::launch_fwd_drop_d128(p, grid, bf16, causal != 0, stream);
+  else
+    e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
+            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, int dv, int causal, const int* seqlens_k, float scale,
+              int dtype, cudaStream_t stream) {
+  return forward_kv(q, k, v, o, lse, B, H, Nq, Nk, d, dv, causal, seqlens_k, scale, dtype, 256, 0,
+                    0, stream);
+}
+
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int N, int d, int causal, float scale, float dropout_p,
+                   unsigned long long seed, unsigned int offset, int dtype,
+                   cudaStream_t stream) {
+  if (causal < 0 || causal > 1) return FA_ERR_SHAPE;
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  if (t == 256) return fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, stream);
+  return forward_kv(q, k, v, o, lse, B, H, N, N, d, d, causal, nullptr, scale, dtype, t, seed,
+                    offset, stream);
 }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -607,6 +657,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   p.cu_k = cu_seqlens_k;
   p.varlen = 1;
   p.total_q = total_q;
+  set_dropout(&p, 256, 0, 0);
   const int grid = p.num_units < info->sms ? p.num_units : info->sms;
   const bool w64 = d == 64 && dv == 64;
   const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
@@ -614,9 +665,11 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-           const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int N,
-           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+// fa_bwd, and fa_bwd_dropout when drop_t < 256.
+static int backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
+                    int N, int d, int causal, float scale, int dtype, int drop_t,
+                    unsigned long long seed, unsigned int drop_off, cudaStream_t stream) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_tiles = (static_cast<long long>(N) + fa::kBwdTile - 1) / fa::kBwdTile;
@@ -658,10 +711,33 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.n_tiles = static_cast<int>(n_tiles);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const cudaError_t e =
-      (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
-                : fa::launch_bwd_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+  set_dropout(&p, drop_t, seed, drop_off);
+  cudaError_t e;
+  if (drop_t < 256)
+    e = (d == 64) ? fa::launch_bwd_drop_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
+                  : fa::launch_bwd_drop_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+  else
+    e = (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
+                  : fa::launch_bwd_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int N,
+           int d, int causal, float scale, int dtype, cudaStream_t stream) {
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype, 256,
+                  0, 0, stream);
+}
+
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
+                   int N, int d, int causal, float scale, float dropout_p,
+                   unsigned long long seed, unsigned int offset, int dtype,
+                   cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype, t,
+                  seed, offset, stream);
 }
 
 }  // extern "C"

@@ -55,6 +55,7 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "fa_philox.cuh"
 #include "ptx_sm103.cuh"
 
 namespace fa {
@@ -90,6 +91,13 @@ struct BwdParams {
   int n_tiles;         // ceil(N / 128)
   float scale;
   float scale_log2;    // scale * log2(e)
+  // Dropout of the forward pass (kDrop variants only): keep threshold t,
+  // seed words, offset and 256 / t.  The mask is regenerated from them:
+  // dV += (P Z)^T dO and dS = P (Z dP 256/t - D), dV scaled by 256 / t.
+  uint32_t drop_t;
+  uint32_t drop_k0, drop_k1;
+  uint32_t drop_off;
+  float drop_scale;
 };
 
 // Shared memory of the two tensor-core kernels: the resident pair of tiles
@@ -307,7 +315,7 @@ struct DkdvVec {
 };
 
 // One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop>
 __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, DkdvVec<D>::kBytes>;
   using X = DkdvBars;
@@ -475,10 +483,19 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
         for (int e = 0; e < 64; ++e)
           if (i * kBwdTile + half * 64 + e < key) pf[e] = 0.f;
       }
+      // dropout: keep bits of this key against the thread's 64 queries; the
+      // dV product reads P with the dropped weights zeroed
+      uint64_t zb = ~0ull;
+      if constexpr (kDrop)
+        zb = keep_col64(static_cast<uint32_t>(key), static_cast<uint32_t>(i * kBwdTile + half * 64),
+                        static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) {
+          pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
+          if constexpr (kDrop) pk[e] &= pair_mask(zb, 2 * e);
+        }
         ptx::tmem_st16(tS, pk);          // over S^T columns this warp has read
         ptx::tmem_st16(tS + 16, pk + 16);
       }
@@ -500,12 +517,18 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
         for (int e = 0; e < 32; e += 4) {
           const float4 dd = dl4[(ch * 32 + e) / 4];
           const int f = ch * 32 + e;
+          // dP^T, with dropout Z dP^T 256 / t
+          auto dpv = [&](int x) -> float {
+            const float v = __uint_as_float(dpr[e + x]);
+            if constexpr (kDrop) return ((zb >> (f + x)) & 1ull) ? v * p.drop_scale : 0.f;
+            return v;
+          };
           float d0, d1, d2, d3;
           ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f], pf[f + 1]),
-                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])),
+                                    ptx::fadd2(ptx::f2_pack(dpv(0), dpv(1)),
                                                ptx::f2_pack(-dd.x, -dd.y))), d0, d1);
           ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f + 2], pf[f + 3]),
-                                    ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e + 2]), __uint_as_float(dpr[e + 3])),
+                                    ptx::fadd2(ptx::f2_pack(dpv(2), dpv(3)),
                                                ptx::f2_pack(-dd.z, -dd.w))), d2, d3);
           dk[f / 2] = ptx::pack2<kBf16>(d0, d1);
           dk[f / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
@@ -523,7 +546,8 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     ptx::tc_fence_after();
     const long long row = static_cast<long long>(bh) * p.N + key;
     if (half == 0)
-      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, 1.f, p.dv, row, key < p.N);
+      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, kDrop ? p.drop_scale : 1.f,
+                                  p.dv, row, key < p.N);
     else
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
                                   key < p.N);
@@ -545,7 +569,7 @@ __device__ __forceinline__ uint32_t dq_ds_col(int b) {
 }
 
 // One CTA of the dQ pass: block `blk` of BH * n_tiles.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop>
 __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, 0>;
   using X = DqBars;
@@ -659,6 +683,11 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
+      // dropout: keep bits of this query against the thread's 64 keys
+      uint64_t zb = ~0ull;
+      if constexpr (kDrop)
+        zb = keep_row64(static_cast<uint32_t>(qrow), static_cast<uint32_t>(j * kBwdTile + half * 64),
+                        static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
       uint32_t dk[32];
 #pragma unroll
       for (int kc = 0; kc < 64; kc += 2) {
@@ -668,10 +697,14 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
         float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
         if (kc >= lim) p0 = 0.f;
         if (kc + 1 >= lim) p1 = 0.f;
+        float g0 = __uint_as_float(dpr[kc]), g1 = __uint_as_float(dpr[kc + 1]);
+        if constexpr (kDrop) {   // Z dP 256 / t
+          g0 = ((zb >> kc) & 1ull) ? g0 * p.drop_scale : 0.f;
+          g1 = ((zb >> (kc + 1)) & 1ull) ? g1 * p.drop_scale : 0.f;
+        }
         float d0, d1;
-        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1),
-                                  ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[kc]), __uint_as_float(dpr[kc + 1])),
-                                             ndl2)), d0, d1);
+        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1), ptx::fadd2(ptx::f2_pack(g0, g1), ndl2)),
+                       d0, d1);
         dk[kc / 2] = ptx::pack2<kBf16>(d0, d1);
       }
       // dS to its TMEM buffer once the tensor core has read what it held
@@ -709,14 +742,14 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
 // key tiles first).  One launch lets SMs that finish their dK/dV CTAs take
 // dQ CTAs at once, so the two passes share one partial last wave instead of
 // each ending on its own.  Shared memory is sized for the larger layout.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   const int per_pass = p.BH * p.n_tiles;
   if (static_cast<int>(blockIdx.x) < per_pass)
-    bwd_dkdv_cta<D, kBf16, kCausal>(p, blockIdx.x);
+    bwd_dkdv_cta<D, kBf16, kCausal, kDrop>(p, blockIdx.x);
   else
-    bwd_dq_cta<D, kBf16, kCausal>(p, blockIdx.x - per_pass);
+    bwd_dq_cta<D, kBf16, kCausal, kDrop>(p, blockIdx.x - per_pass);
 }
 
 }  // namespace fa

@@ -27,7 +27,7 @@ cudaError_t bwd_smem_attr(Fn fn, std::atomic<uint64_t>& done, int bytes) {
 
 // D = rowsum(dO * O), then one grid of dK/dV CTAs (one per key tile) and dQ
 // CTAs (one per query tile), all on `stream`.  `o`, `dout` are [BH, N, D] in the storage dtype.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false>
 cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* dout, float* delta,
                                int sms, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.BH) * p.N;
@@ -44,11 +44,12 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   constexpr int kAllocKv = BwdSmem<D, DkdvVec<D>::kBytes>::kAlloc;
   constexpr int kAllocQ = BwdSmem<D, 0>::kAlloc;
   constexpr int kAlloc = kAllocKv > kAllocQ ? kAllocKv : kAllocQ;
-  e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal>, done, kAlloc);
+  e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal, kDrop>, done, kAlloc);
   if (e != cudaSuccess) return e;
   // dK/dV CTAs then dQ CTAs (see fa_bwd_kernel)
   const long long grid = 2ll * p.BH * p.n_tiles;
-  fa_bwd_kernel<D, kBf16, kCausal><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc, stream>>>(p);
+  fa_bwd_kernel<D, kBf16, kCausal, kDrop><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc,
+                                            stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -56,5 +57,10 @@ cudaError_t launch_bwd_d64(const BwdParams& p, const void* o, const void* dout, 
                            bool bf16, bool causal, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
                             bool bf16, bool causal, int sms, cudaStream_t stream);
+// With dropout in the forward pass (the kDrop variants).
+cudaError_t launch_bwd_drop_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
+                                bool bf16, bool causal, int sms, cudaStream_t stream);
+cudaError_t launch_bwd_drop_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
+                                 bool bf16, bool causal, int sms, cudaStream_t stream);
 
 }  // namespace fa

@@ -46,6 +46,7 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "fa_philox.cuh"
 #include "ptx_sm103.cuh"
 
 namespace fa {
@@ -127,6 +128,12 @@ struct FwdParams {
   const int* cu_k;
   int varlen;
   int total_q;
+  // Dropout on the attention weights (kDrop variants only): keep threshold
+  // t (1 .. 255), the seed as two words, the caller's offset, and 256 / t.
+  uint32_t drop_t;
+  uint32_t drop_k0, drop_k1;
+  uint32_t drop_off;
+  float drop_scale;
 };
 
 // ---------------------------------------------------------------- tracing
@@ -437,7 +444,8 @@ __device__ __forceinline__ size_t lse_at(const FwdParams& p, const Piece& u, int
 // the other variants carry none of its code.
 // kKv: queries against a key set of their own length, per-batch key counts
 // and a causal alignment (see FwdParams); square calls compile none of it.
-template <int D, bool kBf16, bool kCausal, bool kSplit, bool kKv = false>
+// kDrop: dropout on the attention weights (with kKv on square shapes).
+template <int D, bool kBf16, bool kCausal, bool kSplit, bool kKv = false, bool kDrop = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
@@ -885,6 +893,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::f2_unpack(acc1, cc, dd);
           l += (a + b) + (cc + dd);
         }
+        if constexpr (kDrop) {
+          // dropout: the weights of dropped keys leave P (l keeps them: the
+          // normalisation is the softmax's); 256 / t is applied with 1 / l
+          const uint32_t key0 = static_cast<uint32_t>(kj * kBN);
+          const uint64_t b0 = keep_row64(static_cast<uint32_t>(row), key0, u.bh, p.drop_off,
+                                         p.drop_k0, p.drop_k1, p.drop_t);
+          const uint64_t b1 = keep_row64(static_cast<uint32_t>(row), key0 + 64, u.bh, p.drop_off,
+                                         p.drop_k0, p.drop_k1, p.drop_t);
+#pragma unroll
+          for (int m = 0; m < 32; ++m) {
+            pk[m] &= pair_mask(b0, 2 * m);
+            pk[32 + m] &= pair_mask(b1, 2 * m);
+          }
+        }
         pf.lap(3);
         // P_w and O_w are still in use by PV_w_{j-1} until it completes.
         if (j > 0) {
@@ -925,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ptx::tc_fence_after();
       // a row that saw no key (kKv masks) keeps l = 0: O = 0, LSE = -inf
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const float inv_l = (l > 0.f ? 1.0f / l : 0.f) * (kDrop ? p.drop_scale : 1.f);
       if (kSplit && u.tail >= 0) {
         // Partial piece of a split unit: unnormalised O rows and (-m*c, l)
         // go to this piece's workspace slot; the piece that finishes last

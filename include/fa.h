@@ -52,7 +52,8 @@ enum {
   FA_ERR_LAUNCH = 9,         /* the launch itself failed (CUDA error)          */
   FA_ERR_TIMEOUT = 10,       /* a kernel's bounded wait ran out (fa_status)    */
   FA_ERR_CUDA = 11,          /* a CUDA runtime call failed (fa_status)         */
-  FA_ERR_WORKSPACE = 12      /* workspace smaller than fa_fwd_workspace_size   */
+  FA_ERR_WORKSPACE = 12,     /* workspace smaller than fa_fwd_workspace_size   */
+  FA_ERR_DROPOUT = 13        /* dropout probability outside [0, 1 - 1/512)     */
 };
 
 /*
@@ -177,6 +178,39 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   float scale, int dtype, cudaStream_t stream);
 
 /*
+ * fa_fwd_dropout — fa_fwd with dropout on the attention weights, the mask
+ * drawn from a counter-based generator whose state (seed, offset) is all
+ * the backward pass needs to draw it again.
+ *
+ * The pages: with dropout enabled, the full algorithm keeps the
+ * pseudorandom generator's state so that backward regenerates the same
+ * dropout mask instead of storing a square mask ("Why FlashAttention Can
+ * Avoid a Square Attention Array Without Making Attention Linear", section
+ * "Backward can recreate tiles instead of retaining the square").  The
+ * generator and the keep rule are this library's reading:
+ *   - Philox4x32-10 (Salmon et al., SC 2011); one call per 4 x 4 block of a
+ *     head's attention matrix, counter (key / 4, query / 4, b * H + h,
+ *     offset), key = seed (low word first); element (i, j) takes byte j % 4
+ *     of output word i % 4;
+ *   - kept when that byte < t = floor((1 - dropout_p) * 256 + 1/2) (keep
+ *     probability t / 256), kept weights scaled by 256 / t;
+ *   - the softmax normalisation and LSE are those without dropout:
+ *     O_i = (256 / t) sum_j exp(s_ij - m_i) Z_ij V_j / l_i.
+ *
+ *   dropout_p : in [0, 1) with t >= 1; 0 runs fa_fwd (bit-identical).
+ *   seed, offset : generator state; the same values in fa_bwd_dropout
+ *               give the same mask.  Use a new offset (or seed) per call
+ *               that should draw a new mask.
+ *   causal    : 0 or 1 (upper-left; the shapes are square).
+ *   Other arguments, layouts and errors as fa_fwd; FA_ERR_DROPOUT for a
+ *   dropout_p outside the range.
+ */
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int N, int d, int causal, float scale, float dropout_p,
+                   unsigned long long seed, unsigned int offset, int dtype,
+                   cudaStream_t stream);
+
+/*
  * fa_fwd_ws — fa_fwd with a caller-provided workspace used to balance the
  * last round of work across all SMs.
  *
@@ -269,6 +303,21 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, float *delta,
            int B, int H, int N, int d, int causal, float scale, int dtype,
            cudaStream_t stream);
+
+/*
+ * fa_bwd_dropout — fa_bwd for an output of fa_fwd_dropout: the same
+ * dropout_p, seed and offset regenerate the forward's mask on the device
+ * (nothing square is stored or read), and with Z the keep mask and
+ * s = 256 / t:  dV_j = s sum_i P_ij Z_ij dO_i,  dP_ij = s Z_ij dO_i . V_j,
+ * dS = P (dP - D) with D = rowsum(dO * O) as in fa_bwd.
+ * Arguments, layouts and errors as fa_bwd; FA_ERR_DROPOUT for a dropout_p
+ * outside [0, 1) or leaving t = 0.
+ */
+int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                   float *delta, int B, int H, int N, int d, int causal, float scale,
+                   float dropout_p, unsigned long long seed, unsigned int offset, int dtype,
+                   cudaStream_t stream);
 
 /*
  * fa_decode — attention of a few new queries against a long key/value cache

@@ -257,11 +257,14 @@ def grad_key_rows(k_rows, v_rows, k_pos, q, dout, lse, delta, causal=False, scal
 
 
 def dropout_threshold(p):
-    """Byte threshold t = round((1 - p) * 256) of the keep rule (keep iff the
-    element's random byte < t); dropout probability p must leave t >= 1."""
-    t = int(round((1.0 - float(p)) * 256.0))
-    if not (0.0 <= float(p) < 1.0) or t < 1:
-        raise ValueError("dropout probability must be in [0, 1) with round((1 - p) * 256) >= 1")
+    """Byte threshold t = floor((1 - p) * 256 + 1/2) of the keep rule (keep
+    iff the element's random byte < t); dropout probability p must be in
+    [0, 1) and leave t >= 1."""
+    if not (0.0 <= float(p) < 1.0):
+        raise ValueError("dropout probability must be in [0, 1)")
+    t = int(math.floor((1.0 - float(p)) * 256.0 + 0.5))
+    if t < 1:
+        raise ValueError("dropout probability leaves no weight kept (t = 0)")
     return t
 
 

@@ -27,7 +27,7 @@
  *              batch*head index, offset), key = the 64-bit seed (low word
  *              first).  Element (i, j) takes byte j % 4 of word i % 4.
  *   keep       the element is kept when that byte is below
- *              t = round((1 - p) * 256), 1 <= t <= 256, so its keep
+ *              t = floor((1 - p) * 256 + 1/2), 1 <= t <= 256, so its keep
  *              probability is t / 256; kept weights are scaled by 256 / t,
  *              so the mask has mean exactly one.
  *

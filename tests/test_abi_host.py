@@ -236,6 +236,31 @@ def test_unit_group_setter(lib):
     assert fa.fa_set_unit_group(0) == fa.FA_OK
 
 
+def test_dropout_host_errors(lib):
+    """fa_fwd_dropout / fa_bwd_dropout check the dropout probability (and
+    the forward the causal mode) before anything else reaches the device."""
+    fwd = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, N=300, d=64, causal=1,
+               scale=0.125, dropout_p=0.1, seed=7, offset=0, dtype=fa.FA_BF16)
+    for args, code in [(dict(dropout_p=1.0), fa.FA_ERR_DROPOUT),
+                       (dict(dropout_p=-0.01), fa.FA_ERR_DROPOUT),
+                       (dict(dropout_p=float("nan")), fa.FA_ERR_DROPOUT),
+                       (dict(dropout_p=0.999), fa.FA_ERR_DROPOUT),
+                       (dict(d=32), fa.FA_ERR_UNSUPPORTED_D),
+                       (dict(o=None), fa.FA_ERR_NULLPTR), (dict(N=0), fa.FA_OK)]:
+        assert fa.fa_fwd_dropout(**{**fwd, **args}) == code, args
+    bwd = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+               delta=FAKE, B=1, H=2, N=300, d=128, causal=0, scale=0.1, dropout_p=0.3, seed=1,
+               offset=5, dtype=fa.FA_FP16)
+    for args, code in [(dict(dropout_p=1.5), fa.FA_ERR_DROPOUT), (dict(d=96), fa.FA_ERR_UNSUPPORTED_D),
+                       (dict(delta=None), fa.FA_ERR_NULLPTR), (dict(B=0), fa.FA_OK)]:
+        assert fa.fa_bwd_dropout(**{**bwd, **args}) == code, args
+    assert "dropout" in fa.fa_strerror(fa.FA_ERR_DROPOUT)
+    # the C entry point itself rejects a causal mode other than 0 or 1
+    C = ctypes
+    assert lib.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 300, 64, 2, C.c_float(0.125),
+                              C.c_float(0.1), 7, 0, fa.FA_BF16, None) == fa.FA_ERR_SHAPE
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE

@@ -77,6 +77,8 @@ def test_keep_rate_is_binomial():
 
 
 def test_threshold_reading():
+    """t = floor((1 - p) * 256 + 1/2): halves round up (not to even)."""
+    assert oracle.dropout_threshold(1 - 128.5 / 256) == 129
     assert oracle.dropout_threshold(0.0) == 256
     assert oracle.dropout_threshold(0.1) == 230
     assert oracle.dropout_threshold(0.5) == 128
