@@ -32,6 +32,10 @@ per visible (query, key) pair.
 mixed lengths (and, for context, the same batch padded through
 ``fa_fwd_kv``).
 
+``--dropout P`` times ``fa_fwd_dropout`` (or ``fa_bwd_dropout`` with
+``--pass bwd``): the mask drawn on the device from (seed, offset), a new
+offset per forward step.
+
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
 call (three kernels) with the forward's O and LSE and a seeded dO resident
 on the device; FLOPs are 2.5x the forward's (five matmuls against two).
@@ -385,6 +389,32 @@ def oracle_grad_sample(w, q, k, v, dout, budget_s, start_head=0):
     return flops / spent / 1e12, spent, done, cores, desc
 
 
+def dropout_oracle_sample(w, q, k, v, dout, p, budget_s):
+    """Time the float64 dropout oracle (forward, or gradients when ``dout``
+    is given) on whole heads for about budget_s; one thread per head."""
+    import oracle
+    lib = oracle.load()
+    B, H = w["B"], w["H"]
+    done, spent = 0, 0.0
+    while done < B * H and (done == 0 or spent < budget_s):
+        b, h = divmod(done, H)
+        qh, kh, vh = (t[b, h].double().numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        if dout is None:
+            oracle.attention_dropout(qh, kh, vh, done, w["seed"], 0, p, causal=w["causal"],
+                                     scale=w["scale"], lib=lib)
+        else:
+            oracle.attention_dropout_grad(qh, kh, vh, dout[b, h].double().numpy(), done,
+                                          w["seed"], 0, p, causal=w["causal"], scale=w["scale"],
+                                          lib=lib)
+        spent += time.perf_counter() - t0
+        done += 1
+    per_head = (step_flops(w) if dout is None else step_flops_bwd(w)) / (B * H)
+    desc = (f"{done} of {B * H} whole heads of {w['name']} with dropout {p} (float64, one "
+            "thread); every head does the same work")
+    return per_head * done / spent / 1e12, spent, done, 1, desc
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(args, w):
@@ -490,9 +520,14 @@ def run_ours(args, w):
     ws = fa.make_workspace(B, H, N, d, w["causal"], device=device) if args.split else None
     ws_bytes = 0 if ws is None else ws.numel()
 
+    drop = args.dropout
+
     def step(i):
         dq, dk, dv, o, lse = bufs[i % replicas]
-        if ws is None:
+        if drop > 0:
+            rc = fa.fa_fwd_dropout(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"], drop,
+                                   w["seed"], i, fa.dtype_code(dq.dtype), stream)
+        elif ws is None:
             rc = fa.fa_fwd(dq, dk, dv, o, lse, B, H, N, d, w["causal"], w["scale"],
                            fa.dtype_code(dq.dtype), stream)
         else:
@@ -540,8 +575,12 @@ def run_ours(args, w):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        fa.attention_forward(dq, dk, dv, causal=w["causal"], scale=w["scale"], out=o, lse=lse,
-                             stream=stream, workspace=ws)
+        if drop > 0:
+            fa.attention_forward_dropout(dq, dk, dv, drop, w["seed"], 0, causal=w["causal"],
+                                         scale=w["scale"], out=o, lse=lse, stream=stream)
+        else:
+            fa.attention_forward(dq, dk, dv, causal=w["causal"], scale=w["scale"], out=o,
+                                 lse=lse, stream=stream, workspace=ws)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -575,7 +614,9 @@ def run_ours(args, w):
         "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "entry": "fa_fwd_ws" if ws is not None else "fa_fwd",
+                   "entry": ("fa_fwd_dropout" if drop > 0 else
+                             "fa_fwd_ws" if ws is not None else "fa_fwd"),
+                   "dropout": drop,
                    "tail": (f"last-round units split along keys (workspace {ws_bytes / 2**20:.1f} MiB)"
                             if ws is not None else "whole units only"),
                    "l2": (f"{replicas} rotating input replicas "
@@ -597,7 +638,11 @@ def run_ours(args, w):
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
-        tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, args.cpu_seconds)
+        if drop > 0:
+            tf, dt, heads, cores, desc = dropout_oracle_sample(w, q, k, v, None, drop,
+                                                               args.cpu_seconds)
+        else:
+            tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     print(json.dumps(line), flush=True)
@@ -631,16 +676,26 @@ def run_ours_bwd(args, w):
     stream = torch.cuda.current_stream(device)
     code = fa.dtype_code(q.dtype)
     bufs = []
+    drop = args.dropout
     for _ in range(replicas):
         dq_, dk_, dv_, do_ = (t.to(device) for t in (q, k, v, dout))
-        o, lse = fa.attention_forward(dq_, dk_, dv_, causal=w["causal"], scale=w["scale"],
-                                      stream=stream)
+        if drop > 0:
+            o, lse = fa.attention_forward_dropout(dq_, dk_, dv_, drop, w["seed"], 0,
+                                                  causal=w["causal"], scale=w["scale"],
+                                                  stream=stream)
+        else:
+            o, lse = fa.attention_forward(dq_, dk_, dv_, causal=w["causal"], scale=w["scale"],
+                                          stream=stream)
         gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
         delta = torch.empty((B, H, N), dtype=torch.float32, device=device)
         bufs.append((dq_, dk_, dv_, o, lse, do_, gq, gk, gv, delta))
 
     def step(i):
-        rc = fa.fa_bwd(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], code, stream)
+        if drop > 0:
+            rc = fa.fa_bwd_dropout(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], drop,
+                                   w["seed"], 0, code, stream)
+        else:
+            rc = fa.fa_bwd(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], code, stream)
         if rc:
             raise fa.FaError(rc, "fa_bwd")
 
@@ -681,8 +736,13 @@ def run_ours_bwd(args, w):
     def e2e_step():
         for dst, src in zip((dq_, dk_, dv_, o, lse, do_), hosts + [ho, hl, hdo]):
             dst.copy_(src, non_blocking=True)
-        grads = fa.attention_backward(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
-                                      scale=w["scale"], stream=stream)
+        if drop > 0:
+            grads = fa.attention_backward_dropout(dq_, dk_, dv_, o, lse, do_, drop, w["seed"], 0,
+                                                  causal=w["causal"], scale=w["scale"],
+                                                  stream=stream)
+        else:
+            grads = fa.attention_backward(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
+                                          scale=w["scale"], stream=stream)
         for dst, src in zip(outs, grads):
             dst.copy_(src, non_blocking=True)
 
@@ -714,7 +774,7 @@ def run_ours_bwd(args, w):
         "config": {"workload": w["name"], "pass": "backward", "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "entry": "fa_bwd",
+                   "entry": "fa_bwd_dropout" if drop > 0 else "fa_bwd", "dropout": drop,
                    "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
                           if replicas > 1 else "inputs larger than L2")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -731,7 +791,11 @@ def run_ours_bwd(args, w):
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
-        tf, dt, heads, cores, desc = oracle_grad_sample(w, q, k, v, dout, args.cpu_seconds)
+        if drop > 0:
+            tf, dt, heads, cores, desc = dropout_oracle_sample(w, q, k, v, dout, drop,
+                                                               args.cpu_seconds)
+        else:
+            tf, dt, heads, cores, desc = oracle_grad_sample(w, q, k, v, dout, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     print(json.dumps(line), flush=True)
@@ -1245,6 +1309,9 @@ def main(argv=None):
     ap.add_argument("--split", action="store_true",
                     help="time fa_fwd_ws (last round split along keys) instead of fa_fwd")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability on the attention weights (fa_fwd_dropout, or "
+                         "fa_bwd_dropout with --pass bwd); 0 = none")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv", "varlen"], default="fwd",
                     help="time the forward pass (default), the backward pass (fa_bwd), "
                          "split-KV decoding (fa_decode; --workload names a decoding workload) "

@@ -464,7 +464,7 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=N
 
 
 def attention_forward_dropout(q, k, v, dropout_p, seed, offset, causal=False, scale=None,
-                              stream=None):
+                              out=None, lse=None, stream=None):
     """O, LSE of ``attention_forward`` with dropout on the attention weights
     (``fa_fwd_dropout``): the same (dropout_p, seed, offset) given to
     ``attention_backward_dropout`` regenerate the mask."""
@@ -478,8 +478,10 @@ def attention_forward_dropout(q, k, v, dropout_p, seed, offset, causal=False, sc
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    out = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     rc = fa_fwd_dropout(q, k, v, out, lse, B, H, N, d, causal, scale, dropout_p, seed, offset,
