@@ -487,8 +487,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
       // dV product reads P with the dropped weights zeroed
       uint64_t zb = ~0ull;
       if constexpr (kDrop)
-        zb = keep_col64(static_cast<uint32_t>(key), static_cast<uint32_t>(i * kBwdTile + half * 64),
-                        static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+        zb = keep_col_quad64(static_cast<uint32_t>(key),
+                             static_cast<uint32_t>(i * kBwdTile + half * 64),
+                             static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
       {
         uint32_t pk[32];
 #pragma unroll
@@ -685,9 +686,12 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
       ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
       // dropout: keep bits of this query against the thread's 64 keys
       uint64_t zb = ~0ull;
-      if constexpr (kDrop)
-        zb = keep_row64(static_cast<uint32_t>(qrow), static_cast<uint32_t>(j * kBwdTile + half * 64),
-                        static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+      if constexpr (kDrop) {
+        uint64_t kb[1];
+        keep_row_quad<16>(static_cast<uint32_t>(qrow), static_cast<uint32_t>(j * kBwdTile + half * 64),
+                          static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t, kb);
+        zb = kb[0];
+      }
       uint32_t dk[32];
 #pragma unroll
       for (int kc = 0; kc < 64; kc += 2) {

@@ -896,15 +896,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kDrop) {
           // dropout: the weights of dropped keys leave P (l keeps them: the
           // normalisation is the softmax's); 256 / t is applied with 1 / l
-          const uint32_t key0 = static_cast<uint32_t>(kj * kBN);
-          const uint64_t b0 = keep_row64(static_cast<uint32_t>(row), key0, u.bh, p.drop_off,
-                                         p.drop_k0, p.drop_k1, p.drop_t);
-          const uint64_t b1 = keep_row64(static_cast<uint32_t>(row), key0 + 64, u.bh, p.drop_off,
-                                         p.drop_k0, p.drop_k1, p.drop_t);
+          uint64_t kb[2];
+          keep_row_quad<32>(static_cast<uint32_t>(row), static_cast<uint32_t>(kj * kBN), u.bh,
+                            p.drop_off, p.drop_k0, p.drop_k1, p.drop_t, kb);
 #pragma unroll
           for (int m = 0; m < 32; ++m) {
-            pk[m] &= pair_mask(b0, 2 * m);
-            pk[32 + m] &= pair_mask(b1, 2 * m);
+            pk[m] &= pair_mask(kb[0], 2 * m);
+            pk[32 + m] &= pair_mask(kb[1], 2 * m);
           }
         }
         pf.lap(3);

@@ -77,6 +77,79 @@ __device__ __forceinline__ uint64_t keep_col64(uint32_t key, uint32_t q0, uint32
   return bits;
 }
 
+// Keep bits of a whole 4 x 4 block: bit 4 w + c for row w, column c.
+__device__ __forceinline__ uint32_t keep16(const uint4& r, uint32_t t) {
+  return keep_bits4(r.x, t) | (keep_bits4(r.y, t) << 4) | (keep_bits4(r.z, t) << 8) |
+         (keep_bits4(r.w, t) << 12);
+}
+
+// The same masks with the generator work shared by a quad of lanes (lanes
+// 4m .. 4m+3 hold four consecutive rows, or columns, of one block row, or
+// block column): lane k of the quad draws the blocks b = k, k + 4, ...,
+// two blocks' 16 bits per register, and the quad exchanges the registers
+// with broadcast shuffles; every lane then keeps its own row's (column's)
+// bits.  NB blocks (NB / 4 calls per lane).  All 32 lanes must call it.
+//
+// Row walk: bit 4 b + c of `out` (NB = 16 fills one word, 32 two) is key
+// key0 + 4 b + c of query row qrow.
+template <int NB>
+__device__ __forceinline__ void keep_row_quad(uint32_t qrow, uint32_t key0, uint32_t bh,
+                                              uint32_t off, uint32_t k0, uint32_t k1, uint32_t t,
+                                              uint64_t (&out)[NB / 16]) {
+  const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, r = qrow & 3u;
+  uint32_t v[NB / 8];
+#pragma unroll
+  for (int a = 0; a < NB / 4; ++a) {
+    const uint4 w = philox4x32_10(make_uint4((key0 >> 2) + 4u * a + k, qrow >> 2, bh, off), k0, k1);
+    const uint32_t bits = keep16(w, t);
+    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
+  }
+#pragma unroll
+  for (int i = 0; i < NB / 16; ++i) out[i] = 0;
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2) {
+#pragma unroll
+    for (int m = 0; m < NB / 8; ++m) {
+      const uint32_t y = __shfl_sync(0xffffffffu, v[m], (lane & ~3u) | k2);
+      const int b0 = 4 * (2 * m) + k2, b1 = b0 + 4;   // blocks of the two halves
+      out[b0 / 16] |= static_cast<uint64_t>((y >> (4 * r)) & 0xFu) << (4 * (b0 % 16));
+      out[b1 / 16] |= static_cast<uint64_t>((y >> (16 + 4 * r)) & 0xFu) << (4 * (b1 % 16));
+    }
+  }
+}
+
+// Column walk over 64 queries: bit 4 b + w of the result is query
+// q0 + 4 b + w against key column `key`.
+__device__ __forceinline__ uint64_t keep_col_quad64(uint32_t key, uint32_t q0, uint32_t bh,
+                                                    uint32_t off, uint32_t k0, uint32_t k1,
+                                                    uint32_t t) {
+  const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, c = key & 3u;
+  uint32_t v[2];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const uint4 w = philox4x32_10(make_uint4(key >> 2, (q0 >> 2) + 4u * a + k, bh, off), k0, k1);
+    const uint32_t bits = keep16(w, t);
+    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
+  }
+  uint64_t out = 0;
+  // column c of a block's 16 bits (bits c, 4 + c, 8 + c, 12 + c) as a nibble
+  auto col = [&](uint32_t h) -> uint32_t {
+    const uint32_t x = (h >> c) & 0x1111u;
+    return (x | (x >> 3) | (x >> 6) | (x >> 9)) & 0xFu;
+  };
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2) {
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint32_t y = __shfl_sync(0xffffffffu, v[m], (lane & ~3u) | k2);
+      const int b0 = 4 * (2 * m) + k2, b1 = b0 + 4;
+      out |= static_cast<uint64_t>(col(y & 0xFFFFu)) << (4 * b0);
+      out |= static_cast<uint64_t>(col(y >> 16)) << (4 * b1);
+    }
+  }
+  return out;
+}
+
 // The 16-bit pair mask of keep bits b0 (low half) and b1 (high half).
 __device__ __forceinline__ uint32_t pair_mask(uint64_t bits, int e) {
   return (((bits >> e) & 1ull) ? 0x0000FFFFu : 0u) | (((bits >> (e + 1)) & 1ull) ? 0xFFFF0000u : 0u);
