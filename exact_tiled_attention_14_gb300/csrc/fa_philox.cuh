@@ -12,8 +12,8 @@
 // matrix: counter (key / 4, query / 4, batch*head, offset), key = the 64-bit
 // seed.  Element (i, j) takes byte j % 4 of output word i % 4 and is kept
 // when that byte is below t = round((1 - p) * 256); kept weights are scaled
-// by 256 / t.  A thread that walks a query row uses one word of each call,
-// a thread that walks a key column one byte of each word.
+// by 256 / t.  A quad of lanes shares the calls of a block row (or block
+// column); see keep_row_quad.
 #pragma once
 
 #include <cstdint>
@@ -39,48 +39,25 @@ __device__ __forceinline__ uint32_t philox_word(const uint4& r, uint32_t sel) {
   return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
 }
 
-// Keep bits of the four bytes of w (bit b for byte b).
-__device__ __forceinline__ uint32_t keep_bits4(uint32_t w, uint32_t t) {
-  return ((w & 0xFFu) < t ? 1u : 0u) | (((w >> 8) & 0xFFu) < t ? 2u : 0u) |
-         (((w >> 16) & 0xFFu) < t ? 4u : 0u) | ((w >> 24) < t ? 8u : 0u);
-}
-
-// 64 keep bits of query row `qrow` over keys key0 .. key0 + 63 (key0 a
-// multiple of 4): bit e for key key0 + e.
-__device__ __forceinline__ uint64_t keep_row64(uint32_t qrow, uint32_t key0, uint32_t bh,
-                                               uint32_t off, uint32_t k0, uint32_t k1,
-                                               uint32_t t) {
-  uint64_t bits = 0;
-  const uint32_t sel = qrow & 3u;
-#pragma unroll
-  for (int g = 0; g < 16; ++g) {
-    const uint4 r = philox4x32_10(make_uint4((key0 >> 2) + g, qrow >> 2, bh, off), k0, k1);
-    bits |= static_cast<uint64_t>(keep_bits4(philox_word(r, sel), t)) << (4 * g);
-  }
-  return bits;
-}
-
-// 64 keep bits of key column `key` over queries q0 .. q0 + 63 (q0 a multiple
-// of 4): bit e for query q0 + e.
-__device__ __forceinline__ uint64_t keep_col64(uint32_t key, uint32_t q0, uint32_t bh,
-                                               uint32_t off, uint32_t k0, uint32_t k1,
-                                               uint32_t t) {
-  uint64_t bits = 0;
-  const uint32_t sh = (key & 3u) * 8u;
-#pragma unroll
-  for (int g = 0; g < 16; ++g) {
-    const uint4 r = philox4x32_10(make_uint4(key >> 2, (q0 >> 2) + g, bh, off), k0, k1);
-    const uint32_t b = (((r.x >> sh) & 0xFFu) < t ? 1u : 0u) | (((r.y >> sh) & 0xFFu) < t ? 2u : 0u) |
-                       (((r.z >> sh) & 0xFFu) < t ? 4u : 0u) | (((r.w >> sh) & 0xFFu) < t ? 8u : 0u);
-    bits |= static_cast<uint64_t>(b) << (4 * g);
-  }
-  return bits;
+// Keep bits of the four bytes of w (bit b for byte b), 1 <= t <= 255, given
+// c4 = (256 - t) in every byte (t = 256 keeps everything and never reaches
+// the kernels that draw a mask): byte < t exactly when byte + (256 - t) does not carry out of
+// the byte.  The low seven bits are added without reaching the next byte;
+// a byte's carry out is then the majority of its top bit, the complement's
+// top bit and the carry into bit 7, and one multiply gathers the four top
+// bits (7, 15, 23, 31 -> 28 .. 31; the other partial products stay below
+// bit 28 and never overlap, so nothing carries into them).
+__host__ __device__ __forceinline__ uint32_t keep_bits4_swar(uint32_t w, uint32_t c4) {
+  const uint32_t lo = (w & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
+  const uint32_t carry = (w & c4) | ((w ^ c4) & lo);
+  const uint32_t keep = ~carry & 0x80808080u;
+  return (keep * 0x00204081u) >> 28;
 }
 
 // Keep bits of a whole 4 x 4 block: bit 4 w + c for row w, column c.
-__device__ __forceinline__ uint32_t keep16(const uint4& r, uint32_t t) {
-  return keep_bits4(r.x, t) | (keep_bits4(r.y, t) << 4) | (keep_bits4(r.z, t) << 8) |
-         (keep_bits4(r.w, t) << 12);
+__device__ __forceinline__ uint32_t keep16(const uint4& r, uint32_t c4) {
+  return keep_bits4_swar(r.x, c4) | (keep_bits4_swar(r.y, c4) << 4) |
+         (keep_bits4_swar(r.z, c4) << 8) | (keep_bits4_swar(r.w, c4) << 12);
 }
 
 // The same masks with the generator work shared by a quad of lanes (lanes
@@ -97,11 +74,12 @@ __device__ __forceinline__ void keep_row_quad(uint32_t qrow, uint32_t key0, uint
                                               uint32_t off, uint32_t k0, uint32_t k1, uint32_t t,
                                               uint64_t (&out)[NB / 16]) {
   const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, r = qrow & 3u;
+  const uint32_t c4 = (256u - t) * 0x01010101u;
   uint32_t v[NB / 8];
 #pragma unroll
   for (int a = 0; a < NB / 4; ++a) {
     const uint4 w = philox4x32_10(make_uint4((key0 >> 2) + 4u * a + k, qrow >> 2, bh, off), k0, k1);
-    const uint32_t bits = keep16(w, t);
+    const uint32_t bits = keep16(w, c4);
     if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
   }
 #pragma unroll
@@ -124,11 +102,12 @@ __device__ __forceinline__ uint64_t keep_col_quad64(uint32_t key, uint32_t q0, u
                                                     uint32_t off, uint32_t k0, uint32_t k1,
                                                     uint32_t t) {
   const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, c = key & 3u;
+  const uint32_t c4 = (256u - t) * 0x01010101u;
   uint32_t v[2];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const uint4 w = philox4x32_10(make_uint4(key >> 2, (q0 >> 2) + 4u * a + k, bh, off), k0, k1);
-    const uint32_t bits = keep16(w, t);
+    const uint32_t bits = keep16(w, c4);
     if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
   }
   uint64_t out = 0;
