@@ -431,7 +431,10 @@ def run_reference(args, w):
     dout = seeded_inputs.make_dout(w["B"], w["H"], w["N"], w["d"], w["dtype"], seed=w["seed"]) \
         if bwd else None
     for i in range(total):
-        if bwd:
+        if args.dropout > 0:
+            tf, dt, heads, cores, desc = dropout_oracle_sample(w, q, k, v, dout, args.dropout,
+                                                               per_step)
+        elif bwd:
             tf, dt, heads, cores, desc = oracle_grad_sample(w, q, k, v, dout, per_step, start_head=i)
         else:
             tf, dt, heads, cores, desc = oracle_sample(w, q, k, v, per_step, start_head=i)
@@ -445,7 +448,8 @@ def run_reference(args, w):
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
-                   "causal": w["causal"], "storage_dtype": w["dtype"], "seed": w["seed"]},
+                   "causal": w["causal"], "storage_dtype": w["dtype"], "seed": w["seed"],
+                   "pass": "backward" if bwd else "forward", "dropout": args.dropout},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "each step: " + desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
