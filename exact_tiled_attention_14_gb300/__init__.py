@@ -1,7 +1,7 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd_kv``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
 ``fa_status``, ``fa_set_watchdog_ns``, ``fa_set_unit_group``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
@@ -43,7 +43,8 @@ FA_ERR_WORKSPACE = 12
 FA_ERR_DROPOUT = 13
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_kv",
+           "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
            "fa_version")
@@ -90,6 +91,8 @@ def load_library(path=None):
     lib.fa_fwd_dropout.restype = i
     lib.fa_bwd_dropout.argtypes = [vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp]
     lib.fa_bwd_dropout.restype = i
+    lib.fa_bwd_kv.argtypes = [vp] * 10 + [i, i, i, i, i, i, vp, f, i, vp]
+    lib.fa_bwd_kv.restype = i
     lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, vp, ctypes.c_size_t, vp]
     lib.fa_decode.restype = i
     lib.fa_decode_workspace_size.argtypes = [i] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
@@ -194,6 +197,16 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal,
                               _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
                               int(N), int(d), int(bool(causal)), float(scale), float(dropout_p),
                               int(seed), int(offset), int(dtype), _stream(stream))
+
+
+def fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal, seqlens_k,
+              scale, dtype, stream=None):
+    """Raw C call of the backward pass of fa_fwd_kv; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
+                         _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(Nq),
+                         int(Nk), int(d), int(causal), _addr(seqlens_k), float(scale), int(dtype),
+                         _stream(stream))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
@@ -516,6 +529,42 @@ def attention_backward_dropout(q, k, v, o, lse, dout, dropout_p, seed, offset, c
                         dropout_p, seed, offset, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_dropout")
+    return dq, dk, dv
+
+
+def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, scale=None,
+                          stream=None):
+    """dQ, dK, dV for O, LSE = attention_forward_kv(q, k, v, causal, seqlens_k)
+    (``fa_bwd_kv``; q, o, dout [B, H, Nq, d], k, v [B, H, Nk, d])."""
+    import torch
+    ts = (q, k, v, o, dout)
+    if any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 4 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape or \
+            k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q, o, dout must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if lse.dtype != torch.float32 or lse.shape != q.shape[:3]:
+        raise ValueError("lse must be float32 [B, H, Nq]")
+    if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    if causal not in CAUSAL_MODES:
+        raise ValueError("causal must be None, 'upper_left' or 'bottom_right'")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if seqlens_k is not None:
+        if seqlens_k.dtype != torch.int32 or seqlens_k.shape != (B,) or not seqlens_k.is_cuda:
+            raise ValueError("seqlens_k must be an int32 CUDA tensor of shape [B]")
+        seqlens_k = seqlens_k.contiguous()
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, CAUSAL_MODES[causal],
+                   seqlens_k, scale, dtype_code(q.dtype), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_kv")
     return dq, dk, dv
 
 

@@ -665,25 +665,31 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-// fa_bwd, and fa_bwd_dropout when drop_t < 256.
+// fa_bwd, fa_bwd_dropout when drop_t < 256, and fa_bwd_kv when kv (Nq
+// queries against Nk keys with per-batch key counts; causal 2 bottom-right).
 static int backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
-                    int N, int d, int causal, float scale, int dtype, int drop_t,
-                    unsigned long long seed, unsigned int drop_off, cudaStream_t stream) {
-  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
+                    int Nq, int Nk, int d, int causal, bool kv, const int* seqlens_k, float scale,
+                    int dtype, int drop_t, unsigned long long seed, unsigned int drop_off,
+                    cudaStream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_SHAPE;
+  if (causal < 0 || causal > (kv ? 2 : 1)) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
-  const long long n_tiles = (static_cast<long long>(N) + fa::kBwdTile - 1) / fa::kBwdTile;
-  if (bh > INT_MAX || 2 * bh * n_tiles > INT_MAX) return FA_ERR_SHAPE;   // one grid, two passes
+  const long long n_qtiles = (static_cast<long long>(Nq) + fa::kBwdTile - 1) / fa::kBwdTile;
+  const long long n_ktiles = (static_cast<long long>(Nk) + fa::kBwdTile - 1) / fa::kBwdTile;
+  if (bh > INT_MAX || bh * (n_qtiles + n_ktiles) > INT_MAX) return FA_ERR_SHAPE;   // one grid
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
-  if (bh == 0 || N == 0) return FA_OK;  // nothing to write
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta) return FA_ERR_NULLPTR;
+  if (bh == 0 || (Nq == 0 && Nk == 0)) return FA_OK;  // nothing to write
+  if (Nq > 0 && (!q || !o || !lse || !dout || !dq || !delta)) return FA_ERR_NULLPTR;
+  if (Nk > 0 && (!k || !v || !dk || !dv)) return FA_ERR_NULLPTR;
   const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
                         reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
                         reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
-  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta);
+  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta) |
+                       reinterpret_cast<uintptr_t>(seqlens_k);
   if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
 
   int dev = 0;
@@ -693,10 +699,17 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
 
   const bool bf16 = dtype == FA_BF16;
   fa::BwdParams p;
-  if (!make_tmap(&p.tm_q, q, static_cast<int>(bh), N, d, bf16) ||
-      !make_tmap(&p.tm_k, k, static_cast<int>(bh), N, d, bf16) ||
-      !make_tmap(&p.tm_v, v, static_cast<int>(bh), N, d, bf16) ||
-      !make_tmap(&p.tm_do, dout, static_cast<int>(bh), N, d, bf16))
+  // Without queries or keys no tile of them is ever loaded; the maps still
+  // need a row and an address.
+  const int nq_rows = Nq > 0 ? Nq : 1, nk_rows = Nk > 0 ? Nk : 1;
+  const void* qa = Nq > 0 ? q : k;
+  const void* ka = Nk > 0 ? k : q;
+  const void* va = Nk > 0 ? v : q;
+  const void* da = Nq > 0 ? dout : k;
+  if (!make_tmap(&p.tm_q, qa, static_cast<int>(bh), nq_rows, d, bf16) ||
+      !make_tmap(&p.tm_k, ka, static_cast<int>(bh), nk_rows, d, bf16) ||
+      !make_tmap(&p.tm_v, va, static_cast<int>(bh), nk_rows, d, bf16) ||
+      !make_tmap(&p.tm_do, da, static_cast<int>(bh), nq_rows, d, bf16))
     return FA_ERR_TENSORMAP;
   p.lse = lse;
   p.delta = delta;
@@ -707,26 +720,43 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   const unsigned long long wd = g_watchdog_ns.load();
   p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
   p.BH = static_cast<int>(bh);
-  p.N = N;
-  p.n_tiles = static_cast<int>(n_tiles);
+  p.N = Nq;
+  p.n_tiles = static_cast<int>(n_qtiles);
+  p.Nk = Nk;
+  p.n_ktiles = static_cast<int>(n_ktiles);
+  p.H = H;
+  p.seqlens_k = seqlens_k;
+  p.align_br = causal == 2 ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   set_dropout(&p, drop_t, seed, drop_off);
+  const bool c = causal != 0;
   cudaError_t e;
-  if (drop_t < 256)
-    e = (d == 64) ? fa::launch_bwd_drop_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
-                  : fa::launch_bwd_drop_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+  if (kv)
+    e = (d == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                  : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  else if (drop_t < 256)
+    e = (d == 64) ? fa::launch_bwd_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                  : fa::launch_bwd_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   else
-    e = (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, causal != 0, info->sms, stream)
-                  : fa::launch_bwd_d128(p, o, dout, delta, bf16, causal != 0, info->sms, stream);
+    e = (d == 64) ? fa::launch_bwd_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                  : fa::launch_bwd_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int N,
            int d, int causal, float scale, int dtype, cudaStream_t stream) {
-  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype, 256,
-                  0, 0, stream);
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, causal, false, nullptr,
+                  scale, dtype, 256, 0, 0, stream);
+}
+
+int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int Nq,
+              int Nk, int d, int causal, const int* seqlens_k, float scale, int dtype,
+              cudaStream_t stream) {
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal, true,
+                  seqlens_k, scale, dtype, 256, 0, 0, stream);
 }
 
 int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -736,8 +766,8 @@ int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, c
                    cudaStream_t stream) {
   const int t = drop_threshold(dropout_p);
   if (t < 0) return FA_ERR_DROPOUT;
-  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype, t,
-                  seed, offset, stream);
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, causal, false, nullptr,
+                  scale, dtype, t, seed, offset, stream);
 }
 
 }  // extern "C"

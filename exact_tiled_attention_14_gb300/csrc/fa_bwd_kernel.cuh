@@ -98,7 +98,26 @@ struct BwdParams {
   uint32_t drop_k0, drop_k1;
   uint32_t drop_off;
   float drop_scale;
+  // Queries against a key set of another length (kKv variants; N and
+  // n_tiles then count queries): Nk keys per head in n_ktiles tiles (K, V,
+  // dK, dV are [BH, Nk, d]), per-batch key counts seqlens_k[b] (NULL: all
+  // Nk; batch b = bh / H), and the causal alignment: align_br = 0 puts
+  // query i at position i, 1 at len_b - N + i.  Square calls set
+  // Nk = N, n_ktiles = n_tiles.
+  int Nk;
+  int n_ktiles;
+  int H;
+  const int* seqlens_k;
+  int align_br;
 };
+
+// Key count and query offset of head bh in a kKv call (see BwdParams).
+__device__ __forceinline__ void bwd_kv_head(const BwdParams& p, int bh, bool causal, int& len,
+                                            int& off) {
+  len = p.seqlens_k ? p.seqlens_k[bh / p.H] : p.Nk;
+  len = min(max(len, 0), p.Nk);
+  off = (causal && p.align_br) ? len - p.N : 0;
+}
 
 // Shared memory of the two tensor-core kernels: the resident pair of tiles
 // (K_j, V_j or Q_i, dO_i), ring A and ring B of streamed tiles, kVecBytes of
@@ -315,7 +334,7 @@ struct DkdvVec {
 };
 
 // One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
-template <int D, bool kBf16, bool kCausal, bool kDrop>
+template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
 __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, DkdvVec<D>::kBytes>;
   using X = DkdvBars;
@@ -332,8 +351,29 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   // query tiles to visit) are dealt first.
   const int kt = blk / p.BH;
   const int bh = blk - kt * p.BH;
-  const int i0 = kCausal ? kt : 0;           // query tiles i >= kt see this key tile
+  int i0 = kCausal ? kt : 0;                 // query tiles i >= kt see this key tile
+  int len = p.N, off = 0;                    // keys of this head, query offset (kKv)
+  if constexpr (kKv) {
+    // the first query that sees key kt * 128 sits at row kt * 128 - off
+    bwd_kv_head(p, bh, kCausal, len, off);
+    const int first = kt * kBwdTile - off;
+    i0 = !kCausal || first <= 0 ? 0 : first / kBwdTile;
+    if (kt * kBwdTile >= len) i0 = p.n_tiles;   // padding: no query sees these keys
+  }
   const int nq = p.n_tiles - i0;
+  if (kKv && nq <= 0) {
+    // no query sees this key tile: its dK and dV rows are zero
+    if (threadIdx.x < kBwdEwThreads) {
+      const int t = threadIdx.x & 127;
+      const long long key = static_cast<long long>(kt) * kBwdTile + t;
+      if (key < p.Nk) {
+        uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(threadIdx.x < 128 ? p.dv : p.dk) +
+                                              (static_cast<long long>(bh) * p.Nk + key) * (D * 2));
+        for (int c = 0; c < D / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
 
   const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
     ptx::mbar_init(b(L::bX + X::kSFull), 1);
@@ -478,7 +518,15 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
           pf[e + 3] = ptx::ex2(x3);
         }
       }
-      if (kCausal && i == kt) {   // diagonal tile: a key after the query is masked
+      if constexpr (kKv) {
+        // padding keys see nothing; with causal masking query q sees this
+        // key once q + off >= key
+        const int qb = i * kBwdTile + half * 64;
+        const int lo = key >= len ? 64 : (kCausal ? static_cast<int>(key) - off - qb : 0);
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e < lo) pf[e] = 0.f;
+      } else if (kCausal && i == kt) {   // diagonal tile: a key after the query is masked
 #pragma unroll
         for (int e = 0; e < 64; ++e)
           if (i * kBwdTile + half * 64 + e < key) pf[e] = 0.f;
@@ -545,13 +593,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
-    const long long row = static_cast<long long>(bh) * p.N + key;
+    const long long row = static_cast<long long>(bh) * p.Nk + key;
     if (half == 0)
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, kDrop ? p.drop_scale : 1.f,
-                                  p.dv, row, key < p.N);
+                                  p.dv, row, key < p.Nk);
     else
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
-                                  key < p.N);
+                                  key < p.Nk);
   }
 
   ptx::tc_fence_before();
@@ -570,7 +618,7 @@ __device__ __forceinline__ uint32_t dq_ds_col(int b) {
 }
 
 // One CTA of the dQ pass: block `blk` of BH * n_tiles.
-template <int D, bool kBf16, bool kCausal, bool kDrop>
+template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
 __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   using L = BwdSmem<D, 0>;
   using X = DqBars;
@@ -589,7 +637,29 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   const int r = blk / p.BH;
   const int bh = blk - r * p.BH;
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
-  const int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
+  int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
+  int len = p.N, off = 0;                  // keys of this head, query offset (kKv)
+  if constexpr (kKv) {
+    // key tiles up to the position of the tile's last query row
+    bwd_kv_head(p, bh, kCausal, len, off);
+    const int nkv = (len + kBwdTile - 1) / kBwdTile;
+    const int last = min(qt * kBwdTile + kBwdTile, p.N) - 1 + off;
+    nk = !kCausal ? nkv : (last < 0 ? 0 : min(last / kBwdTile + 1, nkv));
+  }
+  if (kKv && nk <= 0) {
+    // no query of this tile sees a key: its dQ rows are zero
+    if (threadIdx.x < kBwdEwThreads) {
+      const int t = threadIdx.x & 127, hf = threadIdx.x >> 7;
+      const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
+      if (qrow < p.N) {
+        uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dq) +
+                                              (static_cast<long long>(bh) * p.N + qrow) * (D * 2) +
+                                              hf * D);
+        for (int c = 0; c < D / 16; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
 
   const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
     ptx::mbar_init(b(L::bX + X::kSFull), 1);
@@ -674,7 +744,14 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
       // keys past N, and on the diagonal tile keys after this query, are
       // masked (limits relative to this thread's first key column)
       int lim = p.N - j * kBwdTile - half * 64;
-      if (kCausal && j == qt) lim = min(lim, t + 1 - half * 64);
+      if constexpr (kKv) {
+        // keys past this head's count, and with causal masking keys after
+        // this query's position
+        lim = len - j * kBwdTile - half * 64;
+        if (kCausal) lim = min(lim, static_cast<int>(qrow) + off + 1 - j * kBwdTile - half * 64);
+      } else if (kCausal && j == qt) {
+        lim = min(lim, t + 1 - half * 64);
+      }
       // all of S and dP into registers first: the next products wait for this
       uint32_t sr[64], dpr[64];
       ptx::tmem_ld32(tS, sr);
@@ -746,14 +823,14 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
 // key tiles first).  One launch lets SMs that finish their dK/dV CTAs take
 // dQ CTAs at once, so the two passes share one partial last wave instead of
 // each ending on its own.  Shared memory is sized for the larger layout.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-  const int per_pass = p.BH * p.n_tiles;
+  const int per_pass = p.BH * p.n_ktiles;   // dK/dV CTAs, one per key tile
   if (static_cast<int>(blockIdx.x) < per_pass)
-    bwd_dkdv_cta<D, kBf16, kCausal, kDrop>(p, blockIdx.x);
+    bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, blockIdx.x);
   else
-    bwd_dq_cta<D, kBf16, kCausal, kDrop>(p, blockIdx.x - per_pass);
+    bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, blockIdx.x - per_pass);
 }
 
 }  // namespace fa

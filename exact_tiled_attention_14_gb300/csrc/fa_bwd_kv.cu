@@ -1,0 +1,26 @@
+// fa_bwd_kv.cu — the backward variants for queries against a key set of
+// another length (key counts, causal alignment): widths 64 and 128 x
+// bf16/fp16 x causal/unmasked.
+#include "fa_bwd_launch.cuh"
+
+namespace fa {
+
+cudaError_t launch_bwd_kv_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
+                              bool bf16, bool causal, int sms, cudaStream_t stream) {
+  if (causal)
+    return bf16 ? launch_bwd_variant<64, true, true, false, true>(p, o, dout, delta, sms, stream)
+                : launch_bwd_variant<64, false, true, false, true>(p, o, dout, delta, sms, stream);
+  return bf16 ? launch_bwd_variant<64, true, false, false, true>(p, o, dout, delta, sms, stream)
+              : launch_bwd_variant<64, false, false, false, true>(p, o, dout, delta, sms, stream);
+}
+
+cudaError_t launch_bwd_kv_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
+                               bool bf16, bool causal, int sms, cudaStream_t stream) {
+  if (causal)
+    return bf16 ? launch_bwd_variant<128, true, true, false, true>(p, o, dout, delta, sms, stream)
+                : launch_bwd_variant<128, false, true, false, true>(p, o, dout, delta, sms, stream);
+  return bf16 ? launch_bwd_variant<128, true, false, false, true>(p, o, dout, delta, sms, stream)
+              : launch_bwd_variant<128, false, false, false, true>(p, o, dout, delta, sms, stream);
+}
+
+}  // namespace fa

@@ -27,7 +27,7 @@ cudaError_t bwd_smem_attr(Fn fn, std::atomic<uint64_t>& done, int bytes) {
 
 // D = rowsum(dO * O), then one grid of dK/dV CTAs (one per key tile) and dQ
 // CTAs (one per query tile), all on `stream`.  `o`, `dout` are [BH, N, D] in the storage dtype.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
 cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* dout, float* delta,
                                int sms, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.BH) * p.N;
@@ -35,21 +35,24 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   long long blocks = (threads + 255) / 256;
   const long long cap = 8ll * sms;
   if (blocks > cap) blocks = cap;
-  fa_bwd_delta_kernel<D, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (blocks > 0) {   // no queries (a kv call with Nq = 0): no D to form
+    fa_bwd_delta_kernel<D, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
 
   static std::atomic<uint64_t> done{0};
   constexpr int kAllocKv = BwdSmem<D, DkdvVec<D>::kBytes>::kAlloc;
   constexpr int kAllocQ = BwdSmem<D, 0>::kAlloc;
   constexpr int kAlloc = kAllocKv > kAllocQ ? kAllocKv : kAllocQ;
-  e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal, kDrop>, done, kAlloc);
+  e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv>, done, kAlloc);
   if (e != cudaSuccess) return e;
-  // dK/dV CTAs then dQ CTAs (see fa_bwd_kernel)
-  const long long grid = 2ll * p.BH * p.n_tiles;
-  fa_bwd_kernel<D, kBf16, kCausal, kDrop><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc,
-                                            stream>>>(p);
+  // dK/dV CTAs (one per key tile) then dQ CTAs (one per query tile)
+  const long long grid = static_cast<long long>(p.BH) * (p.n_ktiles + p.n_tiles);
+  fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc,
+                                                 stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -62,5 +65,10 @@ cudaError_t launch_bwd_drop_d64(const BwdParams& p, const void* o, const void* d
                                 bool bf16, bool causal, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_drop_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
                                  bool bf16, bool causal, int sms, cudaStream_t stream);
+// Queries against a key set of another length (the kKv variants).
+cudaError_t launch_bwd_kv_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
+                              bool bf16, bool causal, int sms, cudaStream_t stream);
+cudaError_t launch_bwd_kv_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
+                               bool bf16, bool causal, int sms, cudaStream_t stream);
 
 }  // namespace fa

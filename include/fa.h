@@ -305,6 +305,29 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            cudaStream_t stream);
 
 /*
+ * fa_bwd_kv — the backward pass of fa_fwd_kv (value width equal to d): dQ,
+ * dK, dV of sum(dO * O) for O, LSE = fa_fwd_kv(q, k, v, ...) with the same
+ * Nq, Nk, key counts and causal alignment.  The pages give the backward's
+ * principle (keep Q, K, V, O and the row statistics, rebuild the tiles;
+ * "Why FlashAttention Can Avoid a Square Attention Array Without Making
+ * Attention Linear", section "Backward can recreate tiles instead of
+ * retaining the square"); the masks are fa_fwd_kv's.
+ *
+ *   q, o, dout, dq : [B, H, Nq, d];  k, v, dk, dv : [B, H, Nk, d];
+ *   lse, delta     : [B, H, Nq] float32 (delta is scratch, as in fa_bwd).
+ *   seqlens_k, causal (0, 1 upper-left, 2 bottom-right) : as fa_fwd_kv.
+ *   Keys that no query sees (padding past a batch's key count, or keys
+ *   after every query's position) get dK = dV = 0; query rows that see no
+ *   key get dQ = 0.  k, v, dk, dv may be NULL when Nk = 0, and q, o, dout,
+ *   dq, lse, delta when Nq = 0.
+ *   Errors as fa_bwd; FA_ERR_SHAPE also for causal outside 0 .. 2.
+ */
+int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const float *lse,
+              const void *dout, void *dq, void *dk, void *dv, float *delta,
+              int B, int H, int Nq, int Nk, int d, int causal, const int *seqlens_k,
+              float scale, int dtype, cudaStream_t stream);
+
+/*
  * fa_bwd_dropout — fa_bwd for an output of fa_fwd_dropout: the same
  * dropout_p, seed and offset regenerate the forward's mask on the device
  * (nothing square is stored or read), and with Z the keep mask and

@@ -261,6 +261,31 @@ def test_dropout_host_errors(lib):
                               C.c_float(0.1), 7, 0, fa.FA_BF16, None) == fa.FA_ERR_SHAPE
 
 
+def test_bwd_kv_host_errors(lib):
+    """fa_bwd_kv checks sizes, the causal mode (0 .. 2), width, dtype, scale,
+    pointers (keys' only with keys, queries' only with queries) and
+    alignment before the device."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                delta=FAKE, B=2, H=3, Nq=300, Nk=900, d=128, causal=2, seqlens_k=None, scale=0.1,
+                dtype=fa.FA_BF16)
+    cases = [(dict(Nq=-1), fa.FA_ERR_SHAPE), (dict(causal=3), fa.FA_ERR_SHAPE),
+             (dict(d=80), fa.FA_ERR_UNSUPPORTED_D), (dict(dtype=5), fa.FA_ERR_DTYPE),
+             (dict(scale=-1.0), fa.FA_ERR_SCALE), (dict(Nq=0, Nk=0), fa.FA_OK), (dict(B=0), fa.FA_OK),
+             (dict(dk=None), fa.FA_ERR_NULLPTR), (dict(delta=None), fa.FA_ERR_NULLPTR),
+             (dict(seqlens_k=FAKE + 2), fa.FA_ERR_ALIGN), (dict(dq=FAKE + 8), fa.FA_ERR_ALIGN)]
+    for args, code in cases:
+        assert fa.fa_bwd_kv(**{**call, **args}) == code, args
+    # without keys the key-side pointers, without queries the query-side
+    # ones may be NULL: the next check is the device's
+    for args in (dict(Nk=0, k=None, v=None, dk=None, dv=None),
+                 dict(Nq=0, q=None, o=None, dout=None, dq=None, lse=None, delta=None)):
+        assert fa.fa_bwd_kv(**{**call, **args}) in (fa.FA_ERR_DEVICE, fa.FA_OK), args
+    # the square entry point keeps its causal contract (0 or 1)
+    C = ctypes
+    assert lib.fa_bwd(*([FAKE] * 10), 1, 2, 256, 64, 2, C.c_float(0.125), fa.FA_BF16,
+                      None) == fa.FA_ERR_SHAPE
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
