@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const uint4* __restri
                                                            const uint4* __restrict__ dout,
                                                            float* __restrict__ delta,
                                                            long long rows) {
+  // the tensor-core grid may be scheduled once every CTA here has started:
+  // its prologue and first loads overlap this pass, and its element-wise
+  // warps wait for D before reading it
+  ptx::griddep_launch_dependents();
   constexpr int kPer = D / 8;   // threads per row
   const long long total = rows * kPer;
   const int lane = threadIdx.x & 31;
@@ -459,6 +463,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     __syncwarp();
   } else {
     // ============================================================ element-wise
+    ptx::griddep_wait();   // D of the pass launched just before this grid
     const int quarter = warp & 3, half = warp >> 2;
     const int t = quarter * 32 + lane;                    // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -723,6 +728,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
     __syncwarp();
   } else {
     // ============================================================ element-wise
+    ptx::griddep_wait();   // D of the pass launched just before this grid
     const int quarter = warp & 3, half = warp >> 2;
     const int t = quarter * 32 + lane;                    // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;

@@ -49,11 +49,21 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   constexpr int kAlloc = kAllocKv > kAllocQ ? kAllocKv : kAllocQ;
   e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv>, done, kAlloc);
   if (e != cudaSuccess) return e;
-  // dK/dV CTAs (one per key tile) then dQ CTAs (one per query tile)
+  // dK/dV CTAs (one per key tile) then dQ CTAs (one per query tile), with
+  // programmatic dependent launch: CTAs start their setup and loads while
+  // the D pass ends, and wait on the device before reading D.
   const long long grid = static_cast<long long>(p.BH) * (p.n_ktiles + p.n_tiles);
-  fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv><<<static_cast<unsigned>(grid), kBwdThreads, kAlloc,
-                                                 stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv>, p);
 }
 
 cudaError_t launch_bwd_d64(const BwdParams& p, const void* o, const void* dout, float* delta,

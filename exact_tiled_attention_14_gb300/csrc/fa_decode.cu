@@ -40,9 +40,20 @@ cudaError_t launch_decode_variant(const DecodeParams& p, void* o, float* lse, cu
     else e = launch_partial<D, 16, kBf16>(p, stream);
     if (e != cudaSuccess) return e;
   }
-  fa_decode_combine_kernel<D, kBf16><<<p.BH * p.Nq, D, 0, stream>>>(p.part_o, p.part_ml, o, lse,
-                                                                    p.splits, p.Nq);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the combine grid is set up while the
+  // partial kernel runs its last CTAs and waits on the device for its parts.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.BH * p.Nq));
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D, kBf16>, p.part_o, p.part_ml, o, lse,
+                            p.splits, p.Nq);
 }
 
 }  // namespace

@@ -111,6 +111,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc);
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
+  // the combine kernel may be scheduled once every CTA has started (it waits
+  // for this grid to complete before reading the parts)
+  ptx::griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31;
   const int split = blockIdx.x % p.splits, bh = blockIdx.x / p.splits;
   const int Nq = p.Nq;
@@ -292,6 +295,8 @@ __global__ void __launch_bounds__(D, 1) fa_decode_combine_kernel(const float* __
                                                               const float2* __restrict__ part_ml,
                                                               void* o, float* lse, int splits,
                                                               int Nq) {
+  // launched while the partial kernel finishes: its parts must be complete
+  ptx::griddep_wait();
   // Merge of the parts of one (head, query) row by the rescale identity:
   // with m* the largest part maximum (log2 units), O = sum_s 2^(m_s - m*) O_s
   // / sum_s 2^(m_s - m*) l_s.  Thread c owns output column c.  First m*

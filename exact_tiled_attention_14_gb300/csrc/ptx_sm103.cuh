@@ -153,6 +153,18 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
 }
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) be scheduled
+// once every CTA of this grid has issued it or exited; grid_wait blocks the
+// calling thread until the grids this one depends on have completed and
+// their memory writes are visible.  Without such a dependency both return
+// at once.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
