@@ -1,7 +1,7 @@
 """Exact tiled attention forward for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd_kv``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
+(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd_kv``, ``fa_bwd_varlen``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
 ``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
 ``fa_status``, ``fa_set_watchdog_ns``, ``fa_set_unit_group``, ``fa_watchdog_selftest``,
 ``fa_work_tiles``, ``fa_version``),
@@ -43,7 +43,7 @@ FA_ERR_WORKSPACE = 12
 FA_ERR_DROPOUT = 13
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_kv",
+EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_kv", "fa_bwd_varlen",
            "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
@@ -93,6 +93,8 @@ def load_library(path=None):
     lib.fa_bwd_dropout.restype = i
     lib.fa_bwd_kv.argtypes = [vp] * 10 + [i, i, i, i, i, i, vp, f, i, vp]
     lib.fa_bwd_kv.restype = i
+    lib.fa_bwd_varlen.argtypes = [vp] * 12 + [i] * 8 + [f, i, vp]
+    lib.fa_bwd_varlen.restype = i
     lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, vp, ctypes.c_size_t, vp]
     lib.fa_decode.restype = i
     lib.fa_decode_workspace_size.argtypes = [i] * 5 + [ctypes.POINTER(ctypes.c_size_t)]
@@ -207,6 +209,18 @@ def fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal,
                          _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(Nq),
                          int(Nk), int(d), int(causal), _addr(seqlens_k), float(scale), int(dtype),
                          _stream(stream))
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B, H,
+                  max_seqlen_q, max_seqlen_k, total_q, total_k, d, causal, scale, dtype,
+                  stream=None):
+    """Raw C call of the backward pass of fa_fwd_varlen; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_varlen(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
+                             _addr(dq), _addr(dk), _addr(dv), _addr(delta), _addr(cu_seqlens_q),
+                             _addr(cu_seqlens_k), int(B), int(H), int(max_seqlen_q),
+                             int(max_seqlen_k), int(total_q), int(total_k), int(d), int(causal),
+                             float(scale), int(dtype), _stream(stream))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
@@ -565,6 +579,46 @@ def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, sc
                    seqlens_k, scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_kv")
+    return dq, dk, dv
+
+
+def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                              max_seqlen_k, causal=None, scale=None, stream=None):
+    """dQ, dK, dV for O, LSE = attention_forward_varlen(q, k, v, cu_seqlens_q,
+    cu_seqlens_k, max_seqlen_q, causal) (``fa_bwd_varlen``; token-major
+    [total, H, d] tensors, LSE [H, total_q]; max_seqlen_k a host int)."""
+    import torch
+    ts = (q, k, v, o, dout)
+    if any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 3 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape or \
+            k.shape[1:] != q.shape[1:]:
+        raise ValueError("q, o, dout must be [total_q, H, d] and k, v [total_k, H, d]")
+    if lse.dtype != torch.float32 or lse.shape != (q.shape[1], q.shape[0]):
+        raise ValueError("lse must be float32 [H, total_q]")
+    if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    if causal not in CAUSAL_MODES:
+        raise ValueError("causal must be None, 'upper_left' or 'bottom_right'")
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_cuda or not cu.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor [B + 1]")
+    if cu_seqlens_q.shape != cu_seqlens_k.shape or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 entries")
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((total_q, H), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B, H,
+                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, d,
+                       CAUSAL_MODES[causal], scale, dtype_code(q.dtype), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
 
 

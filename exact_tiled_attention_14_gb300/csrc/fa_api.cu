@@ -727,6 +727,10 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   p.H = H;
   p.seqlens_k = seqlens_k;
   p.align_br = causal == 2 ? 1 : 0;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.varlen = 0;
+  p.total_q = 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   set_dropout(&p, drop_t, seed, drop_off);
@@ -757,6 +761,83 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const 
               cudaStream_t stream) {
   return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal, true,
                   seqlens_k, scale, dtype, 256, 0, 0, stream);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* delta,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
+                  int causal, float scale, int dtype, cudaStream_t stream) {
+  if (B < 0 || H < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 ||
+      d <= 0)
+    return FA_ERR_SHAPE;
+  if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_qtiles = (static_cast<long long>(max_seqlen_q) + fa::kBwdTile - 1) / fa::kBwdTile;
+  const long long n_ktiles = (static_cast<long long>(max_seqlen_k) + fa::kBwdTile - 1) / fa::kBwdTile;
+  if (bh > INT_MAX || bh * (n_qtiles + n_ktiles) > INT_MAX ||
+      static_cast<long long>(total_q) * H > INT_MAX || static_cast<long long>(total_k) * H > INT_MAX)
+    return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
+  if (bh == 0 || (total_q == 0 && total_k == 0) || (n_qtiles == 0 && n_ktiles == 0)) return FA_OK;
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULLPTR;
+  if (total_q > 0 && (!q || !o || !lse || !dout || !dq || !delta)) return FA_ERR_NULLPTR;
+  if (total_k > 0 && (!k || !v || !dk || !dv)) return FA_ERR_NULLPTR;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta) |
+                       reinterpret_cast<uintptr_t>(cu_seqlens_q) |
+                       reinterpret_cast<uintptr_t>(cu_seqlens_k);
+  if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
+
+  int dev = 0;
+  const DeviceInfo* info = device_info(&dev);
+  if (!info || !info->supported) return FA_ERR_DEVICE;
+  if (info->err != FA_OK) return info->err;
+
+  const bool bf16 = dtype == FA_BF16;
+  fa::BwdParams p;
+  const int q_tok = total_q > 0 ? total_q : 1, k_tok = total_k > 0 ? total_k : 1;
+  const void* qa = total_q > 0 ? q : k;
+  const void* da = total_q > 0 ? dout : k;
+  const void* ka = total_k > 0 ? k : q;
+  const void* va = total_k > 0 ? v : q;
+  if (!make_tmap_tokens(&p.tm_q, qa, H, q_tok, d, bf16) ||
+      !make_tmap_tokens(&p.tm_k, ka, H, k_tok, d, bf16) ||
+      !make_tmap_tokens(&p.tm_v, va, H, k_tok, d, bf16) ||
+      !make_tmap_tokens(&p.tm_do, da, H, q_tok, d, bf16))
+    return FA_ERR_TENSORMAP;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = info->status;
+  const unsigned long long wd = g_watchdog_ns.load();
+  p.watchdog_cycles = (wd ? wd : kDefaultWatchdogNs) * 21ull / 10ull;
+  p.BH = static_cast<int>(bh);
+  p.N = max_seqlen_q;
+  p.n_tiles = static_cast<int>(n_qtiles);
+  p.Nk = total_k;
+  p.n_ktiles = static_cast<int>(n_ktiles);
+  p.H = H;
+  p.seqlens_k = nullptr;
+  p.align_br = causal == 2 ? 1 : 0;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.varlen = 1;
+  p.total_q = total_q;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  set_dropout(&p, 256, 0, 0);
+  const bool c = causal != 0;
+  const cudaError_t e = (d == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                                  : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -109,14 +109,58 @@ struct BwdParams {
   int H;
   const int* seqlens_k;
   int align_br;
+  // Packed variable-length batches (kKv variants with varlen = 1): Q, dO, O,
+  // dQ token-major [total_q, H, d], K, V, dK, dV [Nk = total_k, H, d], LSE
+  // [H, total_q] (as the forward writes it), D [total_q, H]; sequence b owns
+  // query tokens cu_q[b] .. cu_q[b+1] - 1 and key tokens cu_k[b] ..
+  // cu_k[b+1] - 1 (clamped to the totals).  N and n_tiles are then the
+  // longest query count and its tiles, n_ktiles the longest key count's.
+  // The tensor maps are (column, head, token).
+  const int* cu_q;
+  const int* cu_k;
+  int varlen;
+  int total_q;
 };
 
-// Key count and query offset of head bh in a kKv call (see BwdParams).
-__device__ __forceinline__ void bwd_kv_head(const BwdParams& p, int bh, bool causal, int& len,
-                                            int& off) {
-  len = p.seqlens_k ? p.seqlens_k[bh / p.H] : p.Nk;
-  len = min(max(len, 0), p.Nk);
-  off = (causal && p.align_br) ? len - p.N : 0;
+// Where head bh's rows sit in a kKv call: its key count len and query
+// offset off (query i at position i + off), its query count lenq, and with
+// packed batches the first query and key token q0, k0.
+struct BwdHead {
+  int len, off, lenq, q0, k0;
+};
+__device__ __forceinline__ BwdHead bwd_kv_head(const BwdParams& p, int bh, bool causal) {
+  BwdHead h;
+  const int b = bh / p.H;
+  h.lenq = p.N;
+  h.q0 = 0;
+  h.k0 = 0;
+  if (p.varlen) {
+    h.q0 = min(max(p.cu_q[b], 0), p.total_q);
+    h.lenq = min(max(p.cu_q[b + 1], h.q0), p.total_q) - h.q0;
+    h.k0 = min(max(p.cu_k[b], 0), p.Nk);
+    h.len = min(max(p.cu_k[b + 1], h.k0), p.Nk) - h.k0;
+  } else {
+    h.len = p.seqlens_k ? p.seqlens_k[b] : p.Nk;
+    h.len = min(max(h.len, 0), p.Nk);
+  }
+  h.off = (causal && p.align_br) ? h.len - h.lenq : 0;
+  return h;
+}
+
+// Row indices of head bh (h = bh % H): of query row qrow in Q, dO, dQ (rows
+// of d values), of key row key in K, V, dK, dV, and of the query's LSE and D.
+__device__ __forceinline__ long long bwd_qrow(const BwdParams& p, bool tok, const BwdHead& hd,
+                                              int bh, long long qrow) {
+  return tok ? (hd.q0 + qrow) * p.H + bh % p.H : static_cast<long long>(bh) * p.N + qrow;
+}
+__device__ __forceinline__ long long bwd_krow(const BwdParams& p, bool tok, const BwdHead& hd,
+                                              int bh, long long key) {
+  return tok ? (hd.k0 + key) * p.H + bh % p.H : static_cast<long long>(bh) * p.Nk + key;
+}
+__device__ __forceinline__ long long bwd_lse_at(const BwdParams& p, bool tok, const BwdHead& hd,
+                                                int bh, long long qrow) {
+  return tok ? static_cast<long long>(bh % p.H) * p.total_q + hd.q0 + qrow
+             : static_cast<long long>(bh) * p.N + qrow;
 }
 
 // Shared memory of the two tensor-core kernels: the resident pair of tiles
@@ -286,15 +330,21 @@ __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* 
                                              const CUtensorMap* res_b, int res_tile,
                                              const CUtensorMap* str_a, const CUtensorMap* str_b,
                                              int first, int count, int bh,
-                                             const ptx::Watchdog& wd) {
+                                             const ptx::Watchdog& wd, int tok_h = -1,
+                                             int res_tok0 = 0, int str_tok0 = 0) {
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   bool alive = true;
+  // tile `tile` of a [BH, rows, d] map: (column, row, batch*head); with
+  // packed batches (tok_h = head) of a (column, head, token) map from token
+  // tok0 on
+  auto y_of = [&](int tile, int tok0) { return tok_h < 0 ? tile * kBwdTile : tok_h; };
+  auto z_of = [&](int tile, int tok0) { return tok_h < 0 ? bh : tok0 + tile * kBwdTile; };
   ptx::mbar_arrive_expect_tx(bar(L::bRes), 2 * L::kTile);
   for (int c = 0; c < L::kChunks; ++c) {
     ptx::tma_load_3d(sbase + L::kRes + c * L::kChunkBytes, res_a, bar(L::bRes), c * 64,
-                     res_tile * kBwdTile, bh);
+                     y_of(res_tile, res_tok0), z_of(res_tile, res_tok0));
     ptx::tma_load_3d(sbase + L::kRes + L::kTile + c * L::kChunkBytes, res_b, bar(L::bRes), c * 64,
-                     res_tile * kBwdTile, bh);
+                     y_of(res_tile, res_tok0), z_of(res_tile, res_tok0));
   }
   // one tile of `tm` into slot `slot` of a ring, once its previous use is over
   auto load = [&](const CUtensorMap* tm, int ring, int full0, int empty0, int stages, int it) {
@@ -306,7 +356,7 @@ __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* 
     ptx::mbar_arrive_expect_tx(bar(full0 + slot), L::kTile);
     for (int c = 0; c < L::kChunks; ++c)
       ptx::tma_load_3d(dst + c * L::kChunkBytes, tm, bar(full0 + slot), c * 64,
-                       (first + it) * kBwdTile, bh);
+                       y_of(first + it, str_tok0), z_of(first + it, str_tok0));
   };
   int loads = 0;
   for (int it = 0; it < count && alive; ++it) {
@@ -357,22 +407,32 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   const int bh = blk - kt * p.BH;
   int i0 = kCausal ? kt : 0;                 // query tiles i >= kt see this key tile
   int len = p.N, off = 0;                    // keys of this head, query offset (kKv)
+  int n_q = p.n_tiles;                       // query tiles of this head
+  const bool tok = kKv && p.varlen;          // packed batch: token-major rows
+  BwdHead hd{p.N, 0, p.N, 0, 0};
   if constexpr (kKv) {
     // the first query that sees key kt * 128 sits at row kt * 128 - off
-    bwd_kv_head(p, bh, kCausal, len, off);
+    hd = bwd_kv_head(p, bh, kCausal);
+    len = hd.len;
+    off = hd.off;
+    if (tok) n_q = (hd.lenq + kBwdTile - 1) / kBwdTile;
     const int first = kt * kBwdTile - off;
     i0 = !kCausal || first <= 0 ? 0 : first / kBwdTile;
-    if (kt * kBwdTile >= len) i0 = p.n_tiles;   // padding: no query sees these keys
+    if (kt * kBwdTile >= len) i0 = n_q;      // padding: no query sees these keys
   }
-  const int nq = p.n_tiles - i0;
+  // key rows this CTA owns: padded keys are written (as zeros); a packed
+  // sequence's rows end at its key count
+  const int key_rows = tok ? len : p.Nk;
+  const int q_rows = tok ? hd.lenq : p.N;
+  const int nq = n_q - i0;
   if (kKv && nq <= 0) {
     // no query sees this key tile: its dK and dV rows are zero
     if (threadIdx.x < kBwdEwThreads) {
       const int t = threadIdx.x & 127;
       const long long key = static_cast<long long>(kt) * kBwdTile + t;
-      if (key < p.Nk) {
+      if (key < key_rows) {
         uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(threadIdx.x < 128 ? p.dv : p.dk) +
-                                              (static_cast<long long>(bh) * p.Nk + key) * (D * 2));
+                                              bwd_krow(p, tok, hd, bh, key) * (D * 2));
         for (int c = 0; c < D / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -389,7 +449,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0) bwd_producer<L>(sbase, &p.tm_k, &p.tm_v, kt, &p.tm_q, &p.tm_do, i0, nq, bh, wd);
+    if (lane == 0)
+      bwd_producer<L>(sbase, &p.tm_k, &p.tm_v, kt, &p.tm_q, &p.tm_do, i0, nq, bh, wd,
+                      tok ? bh % p.H : -1, hd.k0, hd.q0);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
@@ -472,15 +534,16 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     const uint32_t tDp = tmem_base + lane_off + kColDp + half * 64;
     const long long key = static_cast<long long>(kt) * kBwdTile + t;
     const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
-    const float* lse_h = p.lse + static_cast<long long>(bh) * p.N;
-    const float* del_h = p.delta + static_cast<long long>(bh) * p.N;
+
     // -LSE (log2 units) and D of query row t of tile i, fetched one tile
     // ahead by the first half of the warps; a query past N gets -LSE = -inf,
     // so its P is 0.
     auto fetch = [&](int i, float& nl, float& dd) {
       const int qrow = i * kBwdTile + t;
-      nl = qrow < p.N ? -lse_h[qrow] * 1.4426950408889634f : -INFINITY;
-      dd = qrow < p.N ? del_h[qrow] : 0.f;
+      const bool in = qrow < q_rows;
+      const long long qi = bwd_lse_at(p, tok, hd, bh, qrow);
+      nl = in ? -p.lse[qi] * 1.4426950408889634f : -INFINITY;
+      dd = in ? p.delta[tok ? bwd_qrow(p, tok, hd, bh, qrow) : qi] : 0.f;
     };
     float nl_next = 0.f, d_next = 0.f;
     if (half == 0) fetch(i0, nl_next, d_next);
@@ -598,13 +661,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
-    const long long row = static_cast<long long>(bh) * p.Nk + key;
+    const long long row = bwd_krow(p, tok, hd, bh, key);
     if (half == 0)
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, kDrop ? p.drop_scale : 1.f,
-                                  p.dv, row, key < p.Nk);
+                                  p.dv, row, key < key_rows);
     else
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
-                                  key < p.Nk);
+                                  key < key_rows);
   }
 
   ptx::tc_fence_before();
@@ -644,22 +707,27 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
   int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
   int len = p.N, off = 0;                  // keys of this head, query offset (kKv)
+  const bool tok = kKv && p.varlen;        // packed batch: token-major rows
+  BwdHead hd{p.N, 0, p.N, 0, 0};
   if constexpr (kKv) {
     // key tiles up to the position of the tile's last query row
-    bwd_kv_head(p, bh, kCausal, len, off);
+    hd = bwd_kv_head(p, bh, kCausal);
+    len = hd.len;
+    off = hd.off;
+    if (qt * kBwdTile >= hd.lenq) return;   // past this sequence's queries: no rows
     const int nkv = (len + kBwdTile - 1) / kBwdTile;
-    const int last = min(qt * kBwdTile + kBwdTile, p.N) - 1 + off;
+    const int last = min(qt * kBwdTile + kBwdTile, hd.lenq) - 1 + off;
     nk = !kCausal ? nkv : (last < 0 ? 0 : min(last / kBwdTile + 1, nkv));
   }
+  const int q_rows = tok ? hd.lenq : p.N;
   if (kKv && nk <= 0) {
     // no query of this tile sees a key: its dQ rows are zero
     if (threadIdx.x < kBwdEwThreads) {
       const int t = threadIdx.x & 127, hf = threadIdx.x >> 7;
       const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
-      if (qrow < p.N) {
+      if (qrow < q_rows) {
         uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dq) +
-                                              (static_cast<long long>(bh) * p.N + qrow) * (D * 2) +
-                                              hf * D);
+                                              bwd_qrow(p, tok, hd, bh, qrow) * (D * 2) + hf * D);
         for (int c = 0; c < D / 16; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
@@ -678,7 +746,9 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0) bwd_producer<L>(sbase, &p.tm_q, &p.tm_do, qt, &p.tm_k, &p.tm_v, 0, nk, bh, wd);
+    if (lane == 0)
+      bwd_producer<L>(sbase, &p.tm_q, &p.tm_do, qt, &p.tm_k, &p.tm_v, 0, nk, bh, wd,
+                      tok ? bh % p.H : -1, hd.q0, hd.k0);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
@@ -736,10 +806,11 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
     const uint32_t tS = tmem_base + lane_off + kColS + half * 64;
     const uint32_t tDp = tmem_base + lane_off + kColDp + half * 64;
     const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
-    const bool q_in = qrow < p.N;
-    const long long grow = static_cast<long long>(bh) * p.N + qrow;
-    const float nl = q_in ? -p.lse[grow] * 1.4426950408889634f : -INFINITY;
-    const float dl = q_in ? p.delta[grow] : 0.f;
+    const bool q_in = qrow < q_rows;
+    const long long grow = bwd_qrow(p, tok, hd, bh, qrow);
+    const long long li = bwd_lse_at(p, tok, hd, bh, qrow);
+    const float nl = q_in ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
+    const float dl = q_in ? p.delta[tok ? grow : li] : 0.f;
     const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t nl2 = ptx::f2_pack(nl, nl);
     const uint64_t ndl2 = ptx::f2_pack(-dl, -dl);

@@ -30,7 +30,9 @@ cudaError_t bwd_smem_attr(Fn fn, std::atomic<uint64_t>& done, int bytes) {
 template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
 cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* dout, float* delta,
                                int sms, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.BH) * p.N;
+  // rows of O and dO: every (batch*head, query), or the packed tokens x H
+  const long long rows = p.varlen ? static_cast<long long>(p.total_q) * p.H
+                                  : static_cast<long long>(p.BH) * p.N;
   const long long threads = rows * (D / 8);
   long long blocks = (threads + 255) / 256;
   const long long cap = 8ll * sms;

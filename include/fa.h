@@ -328,6 +328,30 @@ int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const 
               float scale, int dtype, cudaStream_t stream);
 
 /*
+ * fa_bwd_varlen — the backward pass of fa_fwd_varlen (packed batches of
+ * sequences of different lengths, value width equal to d): dQ, dK, dV of
+ * sum(dO * O) for O, LSE = fa_fwd_varlen(...) with the same offsets and
+ * causal mode; each sequence's gradients come from its own queries and
+ * keys only.
+ *
+ *   q, o, dout, dq : [total_q, H, d];  k, v, dk, dv : [total_k, H, d].
+ *   lse            : [H, total_q] float32, as fa_fwd_varlen wrote it.
+ *   delta          : [total_q, H] float32 scratch (written, as in fa_bwd).
+ *   cu_seqlens_q, cu_seqlens_k : the forward's offset arrays (clamped the
+ *                  same way, so no value of them reads or writes out of
+ *                  bounds).
+ *   max_seqlen_q, max_seqlen_k : upper bounds on every sequence's query and
+ *                  key counts (they size the grid).
+ *   Keys no query sees get dK = dV = 0, query rows that see no key dQ = 0.
+ *   Errors as fa_fwd_varlen.
+ */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, float *delta,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
+                  int causal, float scale, int dtype, cudaStream_t stream);
+
+/*
  * fa_bwd_dropout — fa_bwd for an output of fa_fwd_dropout: the same
  * dropout_p, seed and offset regenerate the forward's mask on the device
  * (nothing square is stored or read), and with Z the keep mask and

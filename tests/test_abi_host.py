@@ -286,6 +286,24 @@ def test_bwd_kv_host_errors(lib):
                       None) == fa.FA_ERR_SHAPE
 
 
+def test_bwd_varlen_host_errors(lib):
+    """fa_bwd_varlen checks sizes, causal mode, width, dtype, scale, the
+    offset arrays and the other pointers, and alignment before the device."""
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                delta=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, B=3, H=2, max_seqlen_q=500,
+                max_seqlen_k=700, total_q=900, total_k=1500, d=64, causal=1, scale=0.125,
+                dtype=fa.FA_FP16)
+    cases = [(dict(total_k=-1), fa.FA_ERR_SHAPE), (dict(max_seqlen_k=-1), fa.FA_ERR_SHAPE),
+             (dict(causal=3), fa.FA_ERR_SHAPE), (dict(d=32), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dtype=9), fa.FA_ERR_DTYPE), (dict(scale=0.0), fa.FA_ERR_SCALE),
+             (dict(B=0), fa.FA_OK), (dict(total_q=0, total_k=0), fa.FA_OK),
+             (dict(cu_seqlens_k=None), fa.FA_ERR_NULLPTR), (dict(dv=None), fa.FA_ERR_NULLPTR),
+             (dict(delta=FAKE + 2), fa.FA_ERR_ALIGN), (dict(k=FAKE + 8), fa.FA_ERR_ALIGN)]
+    for args, code in cases:
+        assert fa.fa_bwd_varlen(**{**call, **args}) == code, args
+    assert fa.fa_bwd_varlen(**call) in (fa.FA_ERR_DEVICE, fa.FA_OK)
+
+
 def test_watchdog_selftest_host_errors(lib):
     assert fa.fa_watchdog_selftest(0) == fa.FA_ERR_SHAPE
     assert fa.fa_watchdog_selftest(10 ** 10) == fa.FA_ERR_SHAPE
