@@ -415,6 +415,30 @@ def dropout_oracle_sample(w, q, k, v, dout, p, budget_s):
     return per_head * done / spent / 1e12, spent, done, 1, desc
 
 
+def time_launches(fn, reps, warmup=3):
+    """Mean milliseconds of fn() over reps launches (CUDA events on the
+    current stream, after warmup calls)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def backward_line(ms, flops, entry, peak):
+    """The "backward" object of a kv or varlen bench line: one call of the
+    backward entry point on the same workload, 2.5x the forward's FLOPs."""
+    return {"entry": entry, "ms": ms, "tflops": 2.5 * flops / (ms * 1e-3) / 1e12,
+            "frac": 2.5 * flops / (ms * 1e-3) / 1e12 / peak,
+            "flops_per_launch": 2.5 * flops, "scope": "D pass and the dK/dV + dQ grid"}
+
+
 def graph_replay(launch, n_launch, reps):
     """Milliseconds per launch when ``launch(i, stream)`` is captured
     n_launch times into one CUDA graph and the graph is replayed ``reps``
@@ -1092,6 +1116,13 @@ def run_ours_kv(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+    # the backward pass of the same workload (fa_bwd_kv; value width = d)
+    dout = seeded_inputs.make_dout(B, H, Nq, d, w["dtype"], seed=w["seed"]).to(device)
+    o_f, l_f = fa.attention_forward_kv(dq_, dk_, dv_, causal=w["causal"], seqlens_k=dsl,
+                                       scale=w["scale"])
+    bwd_ms = time_launches(lambda: fa.attention_backward_kv(
+        dq_, dk_, dv_, o_f, l_f, dout, causal=w["causal"], seqlens_k=dsl, scale=w["scale"]),
+        max(5, args.steps // 4))
     sampler.stop()
     clocks = sampler.summary(t0, t1, fallback_window=(t_warm, t1))
     if rank != 0:
@@ -1123,6 +1154,7 @@ def run_ours_kv(args, w):
         "clocks": clocks,
         "gpu_launches": args.steps,
         "gpu": torch.cuda.get_device_name(device),
+        "backward": backward_line(bwd_ms, flops, "fa_bwd_kv", peak),
     }
     if not args.no_cpu_baseline:
         tf, dt, heads, cores, desc = kv_oracle_sample(w, q, k, v, seqlens, args.cpu_seconds)
@@ -1239,6 +1271,16 @@ def run_ours_varlen(args, w):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
 
+    # the backward pass of the same batch (fa_bwd_varlen)
+    dout = torch.randn(q.shape, generator=torch.Generator("cpu").manual_seed(w["seed"]))
+    dout = dout.to(q.dtype).to(device)
+    o_f, l_f = fa.attention_forward_varlen(dq_, dk_, dv_, dcq, dck, max_len, causal=w["causal"],
+                                           scale=w["scale"])
+    bwd_ms = time_launches(lambda: fa.attention_backward_varlen(
+        dq_, dk_, dv_, o_f, l_f, dout, dcq, dck, max_len, max_len, causal=w["causal"],
+        scale=w["scale"]), max(5, args.steps // 4))
+    del dout, o_f, l_f
+
     # the same batch padded to the longest sequence, through fa_fwd_kv
     del bufs
     pq = torch.zeros((B, H, max_len, d), dtype=q.dtype, device=device)
@@ -1291,6 +1333,7 @@ def run_ours_varlen(args, w):
         "clocks": clocks,
         "gpu_launches": args.steps,
         "gpu": torch.cuda.get_device_name(device),
+        "backward": backward_line(bwd_ms, flops, "fa_bwd_varlen", peak),
     }
     if not args.no_cpu_baseline:
         import numpy as np
