@@ -16,7 +16,9 @@ memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
 current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
 (dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``,
 ``attention_forward_kv`` for ``fa_fwd_kv``, ``attention_forward_varlen`` for
-``fa_fwd_varlen``.
+``fa_fwd_varlen``.  ``flash_attention``, ``flash_attention_kv`` and
+``flash_attention_varlen`` wrap the forward and backward entry points in
+torch.autograd functions.
 """
 import ctypes
 import math
@@ -659,3 +661,121 @@ def attention_decode(q, k, v, causal=False, scale=None, out=None, lse=None, work
     if rc != FA_OK:
         raise FaError(rc, "fa_decode")
     return out, lse
+
+
+# ---------------------------------------------------------------- autograd
+# torch.autograd wrappers: the forward entry point in forward(), the matching
+# backward entry point in backward(), so a PyTorch training step can call
+# the library directly.  They only route tensors to the C ABI; what is saved
+# for backward is what the pages say a backward pass keeps (Q, K, V, O and
+# the row statistics LSE, plus the dropout generator's seed and offset).
+
+def _autograd():
+    import torch
+
+    class _FlashAttention(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, dropout_p, seed, offset):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            if dropout_p > 0:
+                o, lse = attention_forward_dropout(q, k, v, dropout_p, seed, offset, causal=causal,
+                                                   scale=scale)
+            else:
+                o, lse = attention_forward(q, k, v, causal=causal, scale=scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.args = (causal, scale, dropout_p, seed, offset)
+            ctx.mark_non_differentiable(lse)
+            return o, lse
+
+        @staticmethod
+        def backward(ctx, do, _dlse):
+            q, k, v, o, lse = ctx.saved_tensors
+            causal, scale, dropout_p, seed, offset = ctx.args
+            do = do.contiguous()
+            if dropout_p > 0:
+                g = attention_backward_dropout(q, k, v, o, lse, do, dropout_p, seed, offset,
+                                               causal=causal, scale=scale)
+            else:
+                g = attention_backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+            return g[0], g[1], g[2], None, None, None, None, None
+
+    class _FlashAttentionKv(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, causal, seqlens_k, scale):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            o, lse = attention_forward_kv(q, k, v, causal=causal, seqlens_k=seqlens_k, scale=scale)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.args = (causal, seqlens_k, scale)
+            ctx.mark_non_differentiable(lse)
+            return o, lse
+
+        @staticmethod
+        def backward(ctx, do, _dlse):
+            q, k, v, o, lse = ctx.saved_tensors
+            causal, seqlens_k, scale = ctx.args
+            if v.shape[3] != q.shape[3]:
+                raise NotImplementedError("the backward pass needs the value width equal to d")
+            g = attention_backward_kv(q, k, v, o, lse, do.contiguous(), causal=causal,
+                                      seqlens_k=seqlens_k, scale=scale)
+            return g[0], g[1], g[2], None, None, None
+
+    class _FlashAttentionVarlen(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, cu_q, cu_k, max_q, max_k, causal, scale):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            o, lse = attention_forward_varlen(q, k, v, cu_q, cu_k, max_q, causal=causal,
+                                              scale=scale)
+            ctx.save_for_backward(q, k, v, o, lse, cu_q, cu_k)
+            ctx.args = (max_q, max_k, causal, scale)
+            ctx.mark_non_differentiable(lse)
+            return o, lse
+
+        @staticmethod
+        def backward(ctx, do, _dlse):
+            q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
+            max_q, max_k, causal, scale = ctx.args
+            if v.shape[2] != q.shape[2]:
+                raise NotImplementedError("the backward pass needs the value width equal to d")
+            g = attention_backward_varlen(q, k, v, o, lse, do.contiguous(), cu_q, cu_k, max_q,
+                                          max_k, causal=causal, scale=scale)
+            return g[0], g[1], g[2], None, None, None, None, None, None
+
+    return _FlashAttention, _FlashAttentionKv, _FlashAttentionVarlen
+
+
+_AUTOGRAD = None
+
+
+def _fns():
+    global _AUTOGRAD
+    if _AUTOGRAD is None:
+        _AUTOGRAD = _autograd()
+    return _AUTOGRAD
+
+
+def flash_attention(q, k, v, causal=False, scale=None, dropout_p=0.0, seed=0, offset=0):
+    """Differentiable O, LSE of exact attention over [B, H, N, d] (fa_fwd, or
+    fa_fwd_dropout when dropout_p > 0; the backward through fa_bwd /
+    fa_bwd_dropout with the same seed and offset)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _fns()[0].apply(q, k, v, bool(causal), float(scale), float(dropout_p), int(seed),
+                           int(offset))
+
+
+def flash_attention_kv(q, k, v, causal=None, seqlens_k=None, scale=None):
+    """Differentiable O, LSE of queries [B, H, Nq, d] against keys [B, H, Nk, d]
+    (fa_fwd_kv / fa_bwd_kv; the backward needs the value width equal to d)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _fns()[1].apply(q, k, v, causal, seqlens_k, float(scale))
+
+
+def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           causal=None, scale=None):
+    """Differentiable O [total_q, H, dv], LSE [H, total_q] of a packed batch
+    (fa_fwd_varlen / fa_bwd_varlen)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _fns()[2].apply(q, k, v, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q),
+                           int(max_seqlen_k), causal, float(scale))
