@@ -1,5 +1,5 @@
 /*
- * fa.h — C ABI of the exact, tiled attention forward pass for GB300 (sm_103a).
+ * fa.h — C ABI of exact, tiled attention for GB300 (sm_103a).
  *
  * The operation is exact attention, O = softmax(Q K^T * scale) V, with the
  * per-row log-sum-exp LSE kept for a backward pass ("FlashAttention: The
@@ -11,18 +11,35 @@
  * Array Without Making Attention Linear", section "Tiles need a shared
  * softmax normalization").
  *
- * Conventions shared by every entry point:
+ * Entry points:
+ *  - forward: fa_fwd (square), fa_fwd_ws / fa_fwd_static (the same, with the
+ *    last round balanced through a caller's or the library's scratch),
+ *    fa_fwd_kv (queries against a key set of another length, key counts,
+ *    causal alignment, value width), fa_fwd_varlen (packed batches),
+ *    fa_fwd_dropout (dropout on the attention weights);
+ *  - backward: fa_bwd, fa_bwd_kv, fa_bwd_varlen, fa_bwd_dropout, each the
+ *    gradient of the forward of the same name;
+ *  - decoding: fa_decode (a few queries against a long cache, key axis
+ *    split across the GPU);
+ *  - status and settings: fa_strerror, fa_status, fa_set_watchdog_ns,
+ *    fa_set_unit_group, fa_watchdog_selftest, fa_work_tiles, fa_version.
+ *
+ * Conventions shared by every entry point (the kv, varlen and decode entry
+ * points state their own layouts and alignments below):
  *  - Tensors are dense, contiguous, row-major, on the CURRENT CUDA device:
  *      q, k, v, o : [B, H, N, d] in the storage dtype (bf16 or fp16);
  *      lse        : [B, H, N] float32, natural log of the scaled scores.
  *  - The caller owns every buffer.  The library allocates no device memory
- *    and never builds an N x N buffer; fa_fwd_ws takes a caller-provided
- *    workspace of O(SMs * 128 * d) floats for balancing, not an N x N one.
+ *    and never builds an N x N buffer: workspaces (fa_fwd_ws, fa_decode)
+ *    and the backward's per-row scratch are the caller's, O(SMs * 128 * d)
+ *    or O(rows), never O(N^2); fa_fwd_static uses a fixed array of the
+ *    library instead.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  A
  *    non-zero return means nothing was launched.
- *  - Causal masking is upper-left aligned: query i sees keys j <= i (section
- *    "Build it", note on non-square causal alignment); with equal query and
- *    key lengths this is also the bottom-right convention.
+ *  - Causal masking of the square entry points is upper-left aligned: query
+ *    i sees keys j <= i (section "Build it", note on non-square causal
+ *    alignment); with equal query and key lengths this is also the
+ *    bottom-right convention.
  */
 #ifndef FA_H_
 #define FA_H_
