@@ -274,7 +274,7 @@ __host__ __device__ constexpr int kSlotFloats() { return 2 * kBM * (D + 2); }
 // the last blocks).  hgroup = BH is plain level order, which balances best
 // when the K/V of all heads fit in L2; hgroup = 1 walks one head at a time,
 // so the units in flight share a few heads' K/V in L2.  The host picks the
-// group from the L2 budget and the balance of the deal (fa_api.cu).
+// group from the L2 budget and the balance of the deal (fa_fwd_api.cu).
 __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
