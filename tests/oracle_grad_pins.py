@@ -149,6 +149,32 @@ def pin_grad_rows_api(lib):
         assert np.abs(dv_r - dvv[sel]).max() <= 1e-13
 
 
+def pin_grad_rows_lower_right_vs_torch(lib):
+    """The row passes with bottom-right positions (queries at i + Nk - Nq,
+    keys at j, or equivalently keys at j - (Nk - Nq) against queries at i,
+    the form the kv and packed backward tests use) against torch float64
+    autograd through SDPA with its lower-right causal bias, Nq <= Nk."""
+    import torch
+    from torch.nn.attention.bias import causal_lower_right
+    F = torch.nn.functional
+    for (tq, tk, d, dv, seed) in [(5, 23, 8, 8, 31), (12, 12, 4, 6, 32), (1, 9, 8, 3, 33)]:
+        r = _rng(seed)
+        q, k = r.standard_normal((tq, d)), r.standard_normal((tk, d))
+        v, g = r.standard_normal((tk, dv)), r.standard_normal((tq, dv))
+        scale = 1.0 / math.sqrt(d)
+        tq_, tk_, tv_ = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        o = F.scaled_dot_product_attention(tq_[None, None], tk_[None, None], tv_[None, None],
+                                           attn_mask=causal_lower_right(tq, tk), scale=scale)[0, 0]
+        (o * torch.tensor(g)).sum().backward()
+        off = tk - tq
+        dq, lse, delta = oracle.grad_query_rows(q, g, np.arange(tq) + off, k, v, causal=True,
+                                                scale=scale, lib=lib)
+        dk, dvv = oracle.grad_key_rows(k, v, np.arange(tk) - off, q, g, lse, delta, causal=True,
+                                       scale=scale, lib=lib)
+        for mine, ref in ((dq, tq_.grad), (dk, tk_.grad), (dvv, tv_.grad)):
+            assert np.abs(mine - ref.numpy()).max() <= 1e-10 * (1 + np.abs(ref.numpy()).max())
+
+
 ALL_GRAD_PINS = [pin_grad_finite_differences, pin_grad_vs_torch, pin_grad_single_key,
                  pin_grad_key_sum_zero, pin_grad_equal_keys, pin_grad_uniform,
-                 pin_grad_rows_api]
+                 pin_grad_rows_api, pin_grad_rows_lower_right_vs_torch]

@@ -266,6 +266,36 @@ def pin_vs_torch(lib):
         assert np.max(np.abs(o - want.numpy())) < 1e-12
 
 
+def pin_rows_lower_right_vs_torch(lib):
+    """Queries at positions shifted by the key/query length difference (the
+    bottom-right causal alignment of a chunk after a cache) against torch's
+    float64 SDPA with its lower-right causal bias; with more queries than
+    keys the first rows see nothing and must come back O = 0, LSE = -inf."""
+    from torch.nn.attention.bias import causal_lower_right
+    import warnings
+    F = torch.nn.functional
+    gen = torch.Generator().manual_seed(23)
+    for tq, tk in [(3, 7), (5, 40), (1, 17), (16, 16), (9, 4)]:
+        q = torch.randn(tq, 8, generator=gen, dtype=torch.float64)
+        k = torch.randn(tk, 8, generator=gen, dtype=torch.float64)
+        v = torch.randn(tk, 5, generator=gen, dtype=torch.float64)
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            bias = causal_lower_right(tq, tk)
+            want = F.scaled_dot_product_attention(q[None, None], k[None, None], v[None, None],
+                                                  attn_mask=bias)[0, 0].numpy()
+        pos = np.arange(tq, dtype=np.int64) + (tk - tq)
+        o, lse = oracle.attention_rows(q.numpy(), pos, k.numpy(), v.numpy(), causal=True, lib=lib)
+        seen = pos >= 0
+        assert np.max(np.abs(o[seen] - want[seen])) < 1e-12, (tq, tk)
+        s = (q @ k.T).numpy() / math.sqrt(8)
+        mask = np.arange(tk)[None, :] <= pos[:, None]
+        want_l = np.array([np.log(np.sum(np.exp(s[i][mask[i]] - s[i][mask[i]].max())))
+                           + s[i][mask[i]].max() for i in range(tq) if seen[i]])
+        assert np.max(np.abs(lse[seen] - want_l)) < 1e-12
+        assert np.all(o[~seen] == 0.0) and np.all(np.isneginf(lse[~seen]))
+
+
 def pin_online_model(lib):
     """Block-wise online recurrence vs the one-shot oracle, ragged blocks."""
     r = _rng(22)
@@ -293,7 +323,7 @@ def pin_rows_api(lib):
         assert np.max(np.abs(o2 - o[rows])) == 0.0 and np.max(np.abs(l2 - lse[rows])) == 0.0
 
 
-ALL_PINS = [pin_four_numbers, pin_two_block, pin_late_max, pin_empty_keys,
+ALL_PINS = [pin_rows_lower_right_vs_torch, pin_four_numbers, pin_two_block, pin_late_max, pin_empty_keys,
             pin_rows_sum_to_one, pin_equal_scores, pin_single_key, pin_causal_row0,
             pin_permutation, pin_score_shift, pin_large_scores, pin_value_affine,
             pin_vs_torch, pin_online_model, pin_rows_api]
