@@ -37,7 +37,7 @@ mixed lengths (and, for context, the same batch padded through
 offset per forward step.
 
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
-call (three kernels) with the forward's O and LSE and a seeded dO resident
+call (two kernels: the D pass and the dK/dV + dQ grid) with the forward's O and LSE and a seeded dO resident
 on the device; FLOPs are 2.5x the forward's (five matmuls against two).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
@@ -721,7 +721,7 @@ def run_ours(args, w):
 
 
 def run_ours_bwd(args, w):
-    """The backward pass: one step = one fa_bwd call (three kernels) on
+    """The backward pass: one step = one fa_bwd call (two kernels) on
     inputs, the forward's O and LSE, and dO resident in device memory."""
     import exact_tiled_attention_14_gb300 as fa
 
@@ -855,7 +855,7 @@ def run_ours_bwd(args, w):
                 "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,   # the D pass and the dK/dV + dQ grid
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
