@@ -37,8 +37,9 @@ mixed lengths (and, for context, the same batch padded through
 offset per forward step.
 
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
-call (two kernels: the D pass and the dK/dV + dQ grid) with the forward's O and LSE and a seeded dO resident
-on the device; FLOPs are 2.5x the forward's (five matmuls against two).
+call (two kernels: the D pass and the dK/dV + dQ grid) with the forward's O
+and LSE and a seeded dO resident on the device; FLOPs are 2.5x the
+forward's (five matmuls against two).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 forward pass has no exchange step); value = all ranks' FLOPs / the slowest
