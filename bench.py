@@ -7,8 +7,15 @@ synthetic workload already resident in device memory.  FLOPs per step follow
 the usual convention 4*B*H*N^2*d (two matmuls of 2*N^2*d each), halved for
 causal masking.
 
-Default workload: B=1, H=16, N=4096, d=128, bf16, unmasked, seeded inputs.
-``--workload`` selects another of the five synthetic workloads.
+Default workload: the largest of the five synthetic workloads, B=4, H=32,
+N=8192, d=128, bf16, causal, seeded inputs.  ``--workload`` selects another.
+
+Timing: one pass times exactly ``--steps`` steps (CUDA events around each
+launch on the launching stream, a barrier and a device synchronise on both
+sides); passes repeat back to back until ``--min-timed-ms`` (default 1000)
+of device time is covered, so the clock sampler sees the GPU under load for
+at least that long.  The line reports ``timed_passes``; value and
+ms_per_step cover all passes.
 
 Printed (rank 0, one JSON line): value (whole job TFLOP/s), ms_per_step,
 ``roofline`` (achieved vs the measured bf16 peak; DRAM traffic from the last
@@ -64,7 +71,7 @@ sys.path.insert(0, ROOT)
 import seeded_inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
-DEFAULT_WORKLOAD = "b1_h16_n4096_d128_bf16"
+DEFAULT_WORKLOAD = "b4_h32_n8192_d128_bf16_causal"
 METRIC = "attention fwd TFLOP/s (causal halved) and % of GB300 dense BF16 tensor peak"
 METRIC_DEC = "attention decode (split-KV) K/V read GB/s and % of GB300 HBM copy bandwidth"
 METRIC_BWD = ("attention bwd TFLOP/s (2.5x the forward's FLOPs, causal halved) and % of GB300 "
@@ -419,6 +426,43 @@ def dropout_oracle_sample(w, q, k, v, dout, p, budget_s):
     return per_head * done / spent / 1e12, spent, done, 1, desc
 
 
+def timed_region(step, steps, min_ms, stream, world, device, max_passes=1000):
+    """The timed region of a bench arm.
+
+    One pass times exactly ``steps`` calls of ``step(i)`` with a CUDA event
+    pair around each call on ``stream``, bracketed by a barrier and a device
+    synchronise on both sides.  Passes follow each other until the device
+    time of all passes (the slowest rank's, so every rank stops after the
+    same pass) reaches ``min_ms``: with a short step the GPU then runs under
+    load long enough for the clock sampler to see it.  Step indices keep
+    counting across passes (input replicas and dropout offsets rotate on).
+
+    Returns (total device ms over all passes, list of per-step ms, passes,
+    host time at the start, host time at the end).
+    """
+    total_ms, per_step, passes = 0.0, [], 0
+    t0 = None
+    while True:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(world, device)
+        torch.cuda.synchronize()
+        if t0 is None:
+            t0 = time.time()
+        for i in range(steps):
+            starts[i].record(stream)
+            step(passes * steps + i)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world, device)
+        total_ms += max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
+        per_step += [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        passes += 1
+        if total_ms >= min_ms or passes >= max_passes:
+            break
+    return total_ms, per_step, passes, t0, time.time()
+
+
 def time_launches(fn, reps, warmup=3):
     """Mean milliseconds of fn() over reps launches (CUDA events on the
     current stream, after warmup calls)."""
@@ -606,24 +650,12 @@ def run_ours(args, w):
     if code:
         raise fa.FaError(code, f"warmup status {word:#x}")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world, device)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world, device)
-    t1 = time.time()
-    total_ms = starts[0].elapsed_time(ends[-1])
-    kern_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    total_ms, per_step, passes, t0, t1 = timed_region(step, args.steps, args.min_timed_ms, stream,
+                                                      world, device)
+    kern_ms = statistics.mean(per_step)
     code, word = fa.fa_status(stream)
     if code:
         raise fa.FaError(code, f"timed status {word:#x}")
-    total_ms = max_over_ranks(total_ms, world, device)
     kern_ms_max = max_over_ranks(kern_ms, world, device)
     # launch-bound workloads: also the per-launch time of CUDA-graph replay
     # (100 launches captured once, the graph replayed 10 times)
@@ -666,15 +698,15 @@ def run_ours(args, w):
     if rank != 0:
         return 0
     flops = step_flops(w)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = world * flops * args.steps * passes / (total_ms * 1e-3) / 1e12
     achieved = flops / (kern_ms_max * 1e-3) / 1e12
     peak, peak_sustained, peak_src = measured_peaks()
     traffic, traffic_note = stored_traffic(w["name"])
     io = io_bytes(w)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "timed_passes": passes,
+        "ms_per_step": total_ms / (args.steps * passes), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
@@ -694,12 +726,16 @@ def run_ours(args, w):
                      "kernel_ms": kern_ms_max, "flops_per_launch": flops,
                      "traffic": traffic,
                      "traffic_note": traffic_note,
+                     "traffic_scope": ("dram__bytes read + write during one launch; O lines still "
+                                       "dirty in L2 when the kernel ends are written back after "
+                                       "it, so with O smaller than L2 the figure can fall below "
+                                       "the compulsory bytes"),
                      "compulsory_bytes": io["h2d"] + io["d2h"]},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * passes,
         "gpu": torch.cuda.get_device_name(device),
     }
     if graph is not None:
@@ -775,21 +811,9 @@ def run_ours_bwd(args, w):
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"warmup status {word:#x}")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world, device)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world, device)
-    t1 = time.time()
-    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
-    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
-                             world, device)
+    total_ms, per_step, passes, t0, t1 = timed_region(step, args.steps, args.min_timed_ms, stream,
+                                                      world, device)
+    kern_ms = max_over_ranks(statistics.mean(per_step), world, device)
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"timed status {word:#x}")
@@ -832,13 +856,13 @@ def run_ours_bwd(args, w):
     if rank != 0:
         return 0
     flops = step_flops_bwd(w)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = world * flops * args.steps * passes / (total_ms * 1e-3) / 1e12
     achieved = flops / (kern_ms * 1e-3) / 1e12
     peak, peak_sustained, peak_src = measured_peaks()
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "timed_passes": passes,
+        "ms_per_step": total_ms / (args.steps * passes), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": w["name"], "pass": "backward", "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
@@ -856,7 +880,7 @@ def run_ours_bwd(args, w):
                 "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,   # the D pass and the dK/dV + dQ grid
+        "gpu_launches": 2 * args.steps * passes,   # the D pass and the dK/dV + dQ grid
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
@@ -919,21 +943,9 @@ def run_ours_decode(args, w):
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"warmup status {word:#x}")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world, device)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world, device)
-    t1 = time.time()
-    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
-    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
-                             world, device)
+    total_ms, per_step, passes, t0, t1 = timed_region(step, args.steps, args.min_timed_ms, stream,
+                                                      world, device)
+    kern_ms = max_over_ranks(statistics.mean(per_step), world, device)
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"timed status {word:#x}")
@@ -971,9 +983,9 @@ def run_ours_decode(args, w):
     gbs = lambda ms: world * kv_bytes / (ms * 1e-3) / 1e9   # noqa: E731
     peak, src = measured_hbm()
     line = {
-        "metric": METRIC_DEC, "value": world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9,
-        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC_DEC, "value": world * kv_bytes * args.steps * passes / (total_ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "timed_passes": passes,
+        "ms_per_step": total_ms / (args.steps * passes), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": w["name"], "pass": "decode", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
                    "d": d, "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
@@ -988,7 +1000,7 @@ def run_ours_decode(args, w):
         "e2e": {"value": gbs(e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": io["h2d"],
                 "d2h_bytes_per_step": io["d2h"], "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.steps * passes,
         "gpu": torch.cuda.get_device_name(device),
     }
     print(json.dumps(line), flush=True)
@@ -1071,21 +1083,9 @@ def run_ours_kv(args, w):
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"warmup status {word:#x}")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world, device)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world, device)
-    t1 = time.time()
-    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), world, device)
-    kern_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)),
-                             world, device)
+    total_ms, per_step, passes, t0, t1 = timed_region(step, args.steps, args.min_timed_ms, stream,
+                                                      world, device)
+    kern_ms = max_over_ranks(statistics.mean(per_step), world, device)
     st, word = fa.fa_status(stream)
     if st:
         raise fa.FaError(st, f"timed status {word:#x}")
@@ -1135,9 +1135,9 @@ def run_ours_kv(args, w):
     peak, peak_sustained, peak_src = measured_peaks()
     traffic, traffic_note = stored_traffic(w["name"])
     line = {
-        "metric": METRIC_KV, "value": world * flops * args.steps / (total_ms * 1e-3) / 1e12,
-        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC_KV, "value": world * flops * args.steps * passes / (total_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "timed_passes": passes,
+        "ms_per_step": total_ms / (args.steps * passes), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": w["name"], "pass": "kv", "B": B, "H": H, "Nq": Nq, "Nk": Nk,
                    "d": d, "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
@@ -1156,7 +1156,7 @@ def run_ours_kv(args, w):
                 "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * passes,
         "gpu": torch.cuda.get_device_name(device),
         "backward": backward_line(bwd_ms, flops, "fa_bwd_kv", peak),
     }
@@ -1383,6 +1383,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--min-timed-ms", type=float, default=1000.0,
+                    help="repeat the --steps pass until this much device time is timed")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,

@@ -55,9 +55,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// cuCtxGetCurrent and cuCtxGetId through the runtime's driver entry points
+// (the library links no driver library).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<CtxGetIdFn>(ptr);
+  });
+  return fns;
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 bool g_dev_ready[kMaxDevices] = {};
+unsigned long long g_dev_ctx[kMaxDevices] = {};   // context the entry was set up in
 DeviceInfo g_dev[kMaxDevices];
 
 }  // namespace
@@ -68,11 +96,24 @@ namespace host {
 std::atomic<unsigned long long> g_watchdog_ns{0};
 std::atomic<unsigned long long*> g_trace{nullptr};  // FA_TRACE builds only
 
+unsigned long long current_context_id() {
+  const CtxFns& f = ctx_fns();
+  if (!f.get_current || !f.get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return f.get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 const DeviceInfo* device_info(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   *dev_out = dev;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
+  // A device reset replaces the context, and with it the addresses of this
+  // library's device symbols: set the entry up again in the new context.
+  const unsigned long long ctx = current_context_id();
+  if (g_dev_ready[dev] && ctx != 0 && ctx != g_dev_ctx[dev]) g_dev_ready[dev] = false;
   if (!g_dev_ready[dev]) {
     DeviceInfo info;
     int major = 0, minor = 0;
@@ -88,6 +129,9 @@ const DeviceInfo* device_info(int* dev_out) {
     }
     g_dev[dev] = info;
     g_dev_ready[dev] = true;
+    // the symbol lookup above made the device's primary context current if
+    // no context was
+    g_dev_ctx[dev] = ctx != 0 ? ctx : current_context_id();
   }
   return &g_dev[dev];
 }
@@ -177,8 +221,23 @@ int fa_debug_prof_slots(void) { return fa::kProfSlots; }
 int fa_work_tiles(int N, int causal, long long* pairs) {
   if (!pairs) return FA_ERR_NULLPTR;
   if (N < 0) return FA_ERR_SHAPE;
-  const long long n = (static_cast<long long>(N) + fa::kBN - 1) / fa::kBN;
-  *pairs = causal ? n * (n + 1) / 2 : n * n;
+  // One head's schedule, walked unit by unit with the kernel's own decode:
+  // the sum of the key tiles its query tiles stream.
+  fa::FwdParams p{};
+  p.BH = 1;
+  p.H = 1;
+  p.N = N;
+  p.Nk = N;
+  p.n_qblk = (N + 2 * fa::kBM - 1) / (2 * fa::kBM);
+  p.n_kv = (N + fa::kBN - 1) / fa::kBN;
+  p.num_units = p.n_qblk;
+  p.hgroup = 1;
+  long long total = 0;
+  for (int s = 0; s < p.num_units; ++s) {
+    const fa::Unit u = causal ? fa::decode_unit<true>(s, p) : fa::decode_unit<false>(s, p);
+    total += u.n0 + u.n1;
+  }
+  *pairs = total;
   return FA_OK;
 }
 

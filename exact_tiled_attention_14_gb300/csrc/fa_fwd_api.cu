@@ -192,10 +192,15 @@ SplitPlan plan_split(long long bh, int N, int d, int causal, int sms) {
   return sp;
 }
 
-// Shared by fa_fwd (no workspace) and fa_fwd_ws.
-int launch_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int N, int d, int causal, float scale, int dtype, void* workspace,
-                   size_t workspace_bytes, cudaStream_t stream) {
+}  // namespace
+
+namespace fa {
+namespace host {
+
+int check_forward_args(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, int B, int H, int N, int d, float scale, int dtype,
+                       bool* empty) {
+  *empty = false;
   if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_qblk = (static_cast<long long>(N) + 2 * fa::kBM - 1) / (2 * fa::kBM);
@@ -203,11 +208,31 @@ int launch_forward(const void* q, const void* k, const void* v, void* o, float* 
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
-  if (bh == 0 || N == 0) return FA_OK;  // nothing to write
+  if (bh == 0 || N == 0) {  // nothing to write
+    *empty = true;
+    return FA_OK;
+  }
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULLPTR;
   const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
   if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+}  // namespace host
+}  // namespace fa
+
+namespace {
+
+// Shared by fa_fwd (no workspace) and fa_fwd_ws.
+int launch_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, int causal, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  const int arg_rc = check_forward_args(q, k, v, o, lse, B, H, N, d, scale, dtype, &empty);
+  if (arg_rc != FA_OK || empty) return arg_rc;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_qblk = (static_cast<long long>(N) + 2 * fa::kBM - 1) / (2 * fa::kBM);
 
   int dev = 0;
   const DeviceInfo* info = device_info(&dev);

@@ -279,14 +279,21 @@ __device__ __forceinline__ int unit_at(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
+
+// Unit s of the schedule: its (batch*head, query block) and the number of key
+// tiles each of its two query tiles streams.  Host code calls it too
+// (fa_work_tiles counts the tile pairs of a head with it), so the count the
+// host reports is the loop bound the kernel runs.
 template <bool kCausal, bool kKv = false>
-__device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
+__host__ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
   Unit u;
   {
     const int per_group = p.hgroup * p.n_qblk;
     const int g = s / per_group;
     const int r = s - g * per_group;
-    const int gl = min(p.hgroup, p.BH - g * p.hgroup);   // heads in this group (the last may be short)
+    const int gl = imin(p.hgroup, p.BH - g * p.hgroup);   // heads in this group (the last may be short)
     const int level = r / gl;
     u.bh = g * p.hgroup + (r - level * gl);
     u.mblk = p.n_qblk - 1 - level;
@@ -298,13 +305,13 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
     const int b = u.bh / p.H;
     int len, lenq = p.N, q0 = 0, k0 = 0;
     if (p.varlen) {
-      q0 = min(max(p.cu_q[b], 0), p.total_q);
-      lenq = min(max(p.cu_q[b + 1], q0), p.total_q) - q0;
-      k0 = min(max(p.cu_k[b], 0), p.Nk);
-      len = min(max(p.cu_k[b + 1], k0), p.Nk) - k0;
+      q0 = imin(imax(p.cu_q[b], 0), p.total_q);
+      lenq = imin(imax(p.cu_q[b + 1], q0), p.total_q) - q0;
+      k0 = imin(imax(p.cu_k[b], 0), p.Nk);
+      len = imin(imax(p.cu_k[b + 1], k0), p.Nk) - k0;
     } else {
       len = p.seqlens_k ? p.seqlens_k[b] : p.Nk;
-      len = min(max(len, 0), p.Nk);
+      len = imin(imax(len, 0), p.Nk);
     }
     u.len = len;
     u.lenq = lenq;
@@ -316,8 +323,8 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
       const int first = (t0 + w) * kBM;                       // the tile's first row
-      const int last = min(first + kBM, lenq) - 1 + u.off;    // position of its last row
-      n[w] = first >= lenq ? 0 : !kCausal ? nkv : (last < 0 ? 0 : min(last / kBN + 1, nkv));
+      const int last = imin(first + kBM, lenq) - 1 + u.off;   // position of its last row
+      n[w] = first >= lenq ? 0 : !kCausal ? nkv : (last < 0 ? 0 : imin(last / kBN + 1, nkv));
     }
     u.n0 = n[0];
     u.n1 = n[1];
@@ -327,9 +334,11 @@ __device__ __forceinline__ Unit decode_unit(int s, const FwdParams& p) {
     u.lenq = p.N;
     u.q0 = 0;
     u.k0 = 0;
+    // causal: key tiles 0 .. t of query tile t (the last one is the diagonal
+    // tile, the only one masked); tiles wholly in the future are never visited
     if (kCausal) {
-      u.n0 = min(t0 + 1, p.n_kv);
-      u.n1 = min(t0 + 2, p.n_kv);
+      u.n0 = imin(t0 + 1, p.n_kv);
+      u.n1 = imin(t0 + 2, p.n_kv);
     } else {
       u.n0 = p.n_kv;
       u.n1 = p.n_kv;

@@ -23,9 +23,22 @@ struct DeviceInfo {
   int err = FA_ERR_DEVICE;
 };
 
-// Per-device facts, queried once with that device current; NULL when no
-// device is current.
+// Per-device facts, queried with that device current once per CUDA context
+// on it (again after a device reset has replaced the context, since the
+// library's device symbols then have new addresses); NULL when no device is
+// current.
 const DeviceInfo* device_info(int* dev_out);
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), 0 when
+// none is current or the driver cannot tell.
+unsigned long long current_context_id();
+
+// Argument checks of the square forward entry points, in their documented
+// order: shape, head width, dtype, scale, then (unless the call is empty,
+// which sets *empty and returns FA_OK) null pointers and alignment.
+int check_forward_args(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, int B, int H, int N, int d, float scale, int dtype,
+                       bool* empty);
 
 // 3-D view [BH, N, d] of a contiguous [B, H, N, d] tensor; boxes of 128 rows x
 // 64 columns (128 bytes), 128-byte swizzle, zero fill past N.

@@ -76,6 +76,16 @@ enum {
 /*
  * fa_fwd — exact attention forward.
  *
+ * Computes the function of "FlashAttention: The Matrix You Never Have to
+ * Write Down", section "What attention computes, in one page" (scores
+ * scale * q_i . k_j, a softmax over each row, the weighted sum of the
+ * values), by the online recurrence of section "From softmax to attention:
+ * rescale the output too" over 128 x 128 tiles, and returns the two outputs
+ * of section "Build it": O, and the per-row log-sum-exp L kept for the
+ * backward pass.  Causal calls skip key tiles wholly in a query tile's
+ * future and mask only the diagonal tile (section "Causal masking: half the
+ * score tiles disappear").
+ *
  *   q, k, v : device pointers, [B, H, N, d], dtype `dtype`, 16-byte aligned.
  *   o       : device pointer, [B, H, N, d], dtype `dtype`, 16-byte aligned;
  *             O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) v_j, rounded to
@@ -274,11 +284,16 @@ int fa_fwd_workspace_size(int B, int H, int N, int d, int causal, size_t *bytes)
  * runs fa_fwd_ws with a 40 MiB scratch array that the library keeps on every
  * GPU it is loaded on, from load until the process exits.
  *
- *   Arguments, results and errors as fa_fwd_ws, without the workspace.
- *   FA_ERR_WORKSPACE when the shape needs more than the 40 MiB array holds
- *   (no supported shape does on a GPU with up to 152 SMs).
+ *   Arguments, results and errors as fa_fwd_ws, without the workspace, and
+ *   checked in the same order; FA_ERR_WORKSPACE (after those checks) when
+ *   the shape needs more than the 40 MiB array holds (no supported shape
+ *   does on a GPU with up to 152 SMs).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
+ *   A device reset (cudaDeviceReset) replaces the device's context and
+ *   reloads the library's code there; the next call notices the new context
+ *   and looks the address up again, so that call too belongs outside any
+ *   capture.
  *   Every call on a device shares the one array and leaves its last contents
  *   in it (the counters that must start at zero are cleared by each call):
  *   calls that overlap on the GPU — other streams, other host threads —
@@ -428,7 +443,15 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
  */
 int fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, size_t *bytes);
 
-/* Human-readable name of a return code (static string, never NULL). */
+/*
+ * fa_strerror — human-readable name of a return code (a static string, never
+ * NULL; "unknown error code" for a value outside the enum).  The codes are
+ * the C form of the input contract of "FlashAttention: The Matrix You Never
+ * Have to Write Down": section "Build it" (its validation function raises on
+ * a bad rank, width, length or dtype before any work) and section "Check
+ * it" (the failing cases it expects to raise).  Codes from FA_ERR_DEVICE on
+ * concern the GPU and have no counterpart there.
+ */
 const char *fa_strerror(int code);
 
 /*
@@ -482,10 +505,12 @@ int fa_watchdog_selftest(unsigned long long budget_ns, cudaStream_t stream);
 
 /*
  * fa_work_tiles — host-side count of the (query tile, key tile) pairs the
- * forward kernel computes for one head with 128-row tiles: n^2 unmasked, or
- * n(n+1)/2 causal with n = ceil(N/128) (section "Causal masking: half the
- * score tiles disappear": whole future tiles are skipped, diagonal tiles are
- * masked).  Writes the count to *pairs.  Returns FA_ERR_SHAPE for N < 0,
+ * forward kernel computes for one head with 128-row tiles, obtained by
+ * walking that head's units through the kernel's own unit decoder (the same
+ * function the kernel uses for its loop bounds): n^2 unmasked, or n(n+1)/2
+ * causal with n = ceil(N/128) (section "Causal masking: half the score tiles
+ * disappear": whole future tiles are skipped, diagonal tiles are masked).
+ * Writes the count to *pairs.  Returns FA_ERR_SHAPE for N < 0,
  * FA_ERR_NULLPTR for a NULL `pairs`.
  */
 int fa_work_tiles(int N, int causal, long long *pairs);

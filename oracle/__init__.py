@@ -13,8 +13,9 @@ never import, link or call it, and it imports nothing from them.
   ``philox4x32_10`` — attention with dropout on the weights, its gradients,
   the keep mask and the counter-based generator it is drawn from, in C,
   ``attn_dropout_oracle.c``.
-* ``online_model`` — the block-wise online recurrence in numpy, the second
-  derivation the C code is pinned against.
+* ``online_model`` — the online softmax in numpy, as a left-to-right fold
+  of block summaries (maximum, exp-sum, weighted values) combined by the
+  rescale identity: the second derivation the C code is pinned against.
 
 ``build()`` compiles the C files with gcc (OpenMP over rows) into
 ``oracle/_build/liboracle.so``; the first call to ``attention`` builds it if

@@ -75,11 +75,9 @@ def pin_four_numbers(lib):
     alpha = math.exp(m1 - float(g["block2_max"]))
     assert abs(alpha / float(g["alpha"]) - 1) < float(g["alpha_rel"])
     trace = []
-    online_model.online_attention(q, k, v, block_q=1, block_k=2, scale=1.0,
-                                  trace=trace)
-    assert _round_eq(trace[-1][4][0], g["after_block2_sum"],
-                     g["after_block2_sum_digits"])
-    assert abs(trace[-1][3][0] - alpha) < 1e-18
+    online_model.online_attention(q, k, v, block_k=2, scale=1.0, trace=trace)
+    assert _round_eq(trace[-1][4], g["after_block2_sum"], g["after_block2_sum_digits"])
+    assert abs(trace[-1][3] - alpha) < 1e-18
 
 
 def pin_two_block(lib):
@@ -96,15 +94,14 @@ def pin_two_block(lib):
     # LSE = ln(1 + 1 + 2 + 2) = ln 6.
     assert abs(lse[0] - math.log(6.0)) < 1e-14
     trace = []
-    o2, _ = online_model.online_attention(q, k, vals, block_q=1, block_k=2,
-                                          scale=1.0, trace=trace)
+    o2, _ = online_model.online_attention(q, k, vals, block_k=2, scale=1.0, trace=trace)
     assert abs(o2[0, 0] - want) < 1e-13
     _, _, m1, _, l1 = trace[0]
     _, _, m2, a2, l2 = trace[1]
-    assert m1[0] == _num(g["block1_max"]) and l1[0] == float(g["block1_sum"])
-    assert abs(m2[0] - _num(g["block2_max"])) < 1e-15
-    assert abs(a2[0] - float(g["block1_rescale"])) < 1e-15
-    assert abs(l2[0] - float(g["combined_denominator"])) < 1e-14
+    assert m1 == _num(g["block1_max"]) and l1 == float(g["block1_sum"])
+    assert abs(m2 - _num(g["block2_max"])) < 1e-15
+    assert abs(a2 - float(g["block1_rescale"])) < 1e-15
+    assert abs(l2 - float(g["combined_denominator"])) < 1e-14
 
 
 def pin_late_max(lib):
@@ -119,8 +116,7 @@ def pin_late_max(lib):
     exact = (1 * e + 2 * e + 3 * e + 4) / (3 * e + 1)
     assert abs(o[0, 0] - exact) < 1e-15
     assert abs(lse[0] - (20.0 + math.log(1 + 3 * e))) < 1e-13
-    o2, _ = online_model.online_attention(q, k, v, block_q=int(g["block_q"]),
-                                          block_k=int(g["block_k"]))
+    o2, _ = online_model.online_attention(q, k, v, block_k=int(g["block_k"]))
     assert abs(o2[0, 0] - exact) < 1e-15
 
 
@@ -297,17 +293,17 @@ def pin_rows_lower_right_vs_torch(lib):
 
 
 def pin_online_model(lib):
-    """Block-wise online recurrence vs the one-shot oracle, ragged blocks."""
+    """Online fold over key blocks vs the one-shot oracle, ragged blocks."""
     r = _rng(22)
     shapes = [(64, 64, 16, 16), (100, 100, 32, 32), (128, 96, 64, 24), (37, 53, 8, 11)]
     for tq, tk, d, dv in shapes:
         for causal in ([False, True] if tq == tk else [False]):
-            for bq, bk in [(32, 32), (16, 64), (7, 13)]:
+            for bk in (32, 64, 13, 7):
                 q = r.standard_normal((tq, d)) * 2
                 k, v = r.standard_normal((tk, d)), r.standard_normal((tk, dv))
-                o1, l1 = online_model.online_attention(q, k, v, causal, bq, bk)
+                o1, l1 = online_model.online_attention(q, k, v, causal, bk)
                 o2, l2 = oracle.attention(q, k, v, causal=causal, lib=lib)
-                assert np.max(np.abs(o1 - o2)) < 1e-12, (tq, tk, causal, bq, bk)
+                assert np.max(np.abs(o1 - o2)) < 1e-12, (tq, tk, causal, bk)
                 assert np.max(np.abs(l1 - l2)) < 1e-12
 
 

@@ -54,7 +54,7 @@ def test_library_has_no_oracle_or_torch_dependency():
 
 
 def test_strerror_covers_codes(lib):
-    for code in range(0, 13):
+    for code in range(0, fa.FA_ERR_DROPOUT + 1):
         s = fa.fa_strerror(code)
         assert s and s != "unknown error code"
     assert fa.fa_strerror(999) == "unknown error code"
@@ -62,7 +62,11 @@ def test_strerror_covers_codes(lib):
 
 
 def test_work_tiles_match_printed_table(lib):
-    """Causal tiles computed: 36 of 64 at 1024 and 528 of 1024 at 4096 (block 128)."""
+    """Causal tiles computed: 36 of 64 at 1024 and 528 of 1024 at 4096 (block 128).
+
+    fa_work_tiles walks one head's units through the kernel's own unit
+    decoder (the loop bounds the forward kernel runs), not a closed form,
+    so this pins the kernel's skip of future tiles."""
     rows = [line.split() for line in open(os.path.join(ROOT, "tests", "golden", "causal_tiles.txt"))
             if line.strip() and not line.startswith("#")]
     assert rows
@@ -73,6 +77,12 @@ def test_work_tiles_match_printed_table(lib):
         assert round(100 * (1 - int(computed) / int(total))) == int(skipped)
     assert fa.fa_work_tiles(0, True) == 0
     assert fa.fa_work_tiles(129, True) == 3 and fa.fa_work_tiles(129, False) == 4
+    # the closed forms n(n+1)/2 and n^2 (n = ceil(N/128)) for ragged and
+    # odd tile counts, including a last unit whose second tile lies past N
+    for n_tok in (1, 127, 128, 255, 256, 257, 383, 640, 1000, 8192, 32768):
+        n = (n_tok + 127) // 128
+        assert fa.fa_work_tiles(n_tok, True) == n * (n + 1) // 2
+        assert fa.fa_work_tiles(n_tok, False) == n * n
     with pytest.raises(fa.FaError):
         fa.fa_work_tiles(-1, False)
 

@@ -17,7 +17,7 @@ def test_pin(lib, pin):
 
 
 def test_streaming_lse_guards():
-    """All -inf gives -inf; a pure -inf block is skipped (pages' two guards)."""
+    """All -inf gives -inf; a block of only -inf carries no weight."""
     import math
     from oracle.online_model import streaming_lse
     assert streaming_lse([-math.inf] * 4) == -math.inf
