@@ -126,9 +126,11 @@ def test_backward_invariants():
 
 
 @pytest.mark.parametrize("name", ["b1_h16_n4096_d128_bf16", "b16_h16_n1024_d64_bf16",
-                                  "b4_h32_n8192_d128_bf16_causal"])
+                                  "b4_h32_n8192_d128_bf16_causal",
+                                  "b1_h8_n32768_d64_fp16_causal_qstd4"])
 def test_backward_on_workloads(name):
-    """Full-size workloads: two whole heads (dQ every row, dK and dV on sampled keys)."""
+    """Full-size workloads: two whole heads up to N = 4096, one beyond (dQ
+    every row, dK and dV on sampled keys)."""
     w = seeded_inputs.workload(name)
     q, k, v = seeded_inputs.make_workload_qkv(w)
     dout = seeded_inputs.make_dout(w["B"], w["H"], w["N"], w["d"], w["dtype"], seed=w["seed"])
