@@ -905,14 +905,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kDrop) {
           // dropout: the weights of dropped keys leave P (l keeps them: the
           // normalisation is the softmax's); 256 / t is applied with 1 / l
-          uint64_t kb[2];
-          keep_row_quad<32>(static_cast<uint32_t>(row), static_cast<uint32_t>(kj * kBN), u.bh,
-                            p.drop_off, p.drop_k0, p.drop_k1, p.drop_t, kb);
-#pragma unroll
-          for (int m = 0; m < 32; ++m) {
-            pk[m] &= pair_mask(kb[0], 2 * m);
-            pk[32 + m] &= pair_mask(kb[1], 2 * m);
-          }
+          drop_row128(pk, static_cast<uint32_t>(row), static_cast<uint32_t>(kj * kBN), u.bh,
+                      p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
         }
         pf.lap(3);
         // P_w and O_w are still in use by PV_w_{j-1} until it completes.

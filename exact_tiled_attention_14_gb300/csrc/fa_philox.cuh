@@ -96,6 +96,54 @@ __device__ __forceinline__ void keep_row_quad(uint32_t qrow, uint32_t key0, uint
   }
 }
 
+// prmt.b32 in its default mode: each selector nibble picks a byte of
+// {b, a} (low three bits) and, with its top bit set, replicates that byte's
+// sign bit over all eight bits instead of copying it.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Clears, in the 16-bit weights pk of query row `qrow` against keys key0 ..
+// key0 + 127 (pk[i] holds keys 2i and 2i + 1), every weight the mask drops.
+// The generator work is shared by the quad exactly as in keep_row_quad
+// (lane k draws blocks k, k + 4, ...; broadcast shuffles hand each lane the
+// other blocks), and the row's four keep bits of block b become the masks
+// of pk[2b] and pk[2b + 1] directly: one multiply moves bit i of the
+// nibble to the top bit of byte i (the partial products fall on distinct
+// bits, so nothing carries), and two byte permutes with sign replication
+// turn those top bits into 0x0000FFFF / 0xFFFF0000 halves.  All 32 lanes
+// must call it; the result is the same as applying keep_row_quad<32>'s bits
+// pair by pair.
+__device__ __forceinline__ void drop_row128(uint32_t (&pk)[64], uint32_t qrow, uint32_t key0,
+                                            uint32_t bh, uint32_t off, uint32_t k0, uint32_t k1,
+                                            uint32_t t) {
+  const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, sh = 4u * (qrow & 3u);
+  const uint32_t c4 = (256u - t) * 0x01010101u;
+  uint32_t v[4];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    const uint4 w = philox4x32_10(make_uint4((key0 >> 2) + 4u * a + k, qrow >> 2, bh, off), k0, k1);
+    const uint32_t bits = keep16(w, c4);
+    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t y = __shfl_sync(0xffffffffu, v[m], (lane & ~3u) | k2);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = 4 * (2 * m + h) + k2;          // block of keys 4b .. 4b + 3
+        const uint32_t spread = ((y >> (sh + 16u * h)) & 0xFu) * 0x10204080u;
+        pk[2 * b] &= prmt(spread, 0u, 0x9988u);
+        pk[2 * b + 1] &= prmt(spread, 0u, 0xBBAAu);
+      }
+    }
+  }
+}
+
 // Column walk over 64 queries: bit 4 b + w of the result is query
 // q0 + 4 b + w against key column `key`.
 __device__ __forceinline__ uint64_t keep_col_quad64(uint32_t key, uint32_t q0, uint32_t bh,
