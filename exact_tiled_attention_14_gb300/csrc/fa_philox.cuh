@@ -121,13 +121,18 @@ __device__ __forceinline__ void drop_row128(uint32_t (&pk)[64], uint32_t qrow, u
                                             uint32_t t) {
   const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, sh = 4u * (qrow & 3u);
   const uint32_t c4 = (256u - t) * 0x01010101u;
-  uint32_t v[4];
-#pragma unroll
+  // The eight generator calls run as a loop (one copy of the generator's
+  // code in the instruction stream instead of eight), their 16-bit keep
+  // words collected in a small per-thread array.
+  uint16_t v16[8];
+#pragma unroll 1
   for (int a = 0; a < 8; ++a) {
     const uint4 w = philox4x32_10(make_uint4((key0 >> 2) + 4u * a + k, qrow >> 2, bh, off), k0, k1);
-    const uint32_t bits = keep16(w, c4);
-    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
+    v16[a] = static_cast<uint16_t>(keep16(w, c4));
   }
+  uint32_t v[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) v[m] = v16[2 * m] | (static_cast<uint32_t>(v16[2 * m + 1]) << 16);
 #pragma unroll
   for (int k2 = 0; k2 < 4; ++k2) {
 #pragma unroll
