@@ -289,17 +289,11 @@ __device__ __forceinline__ void store_acc_cols(uint32_t t_acc, int c0, float mul
   }
 }
 
-// Shared setup of the two tensor-core kernels: TMEM allocation by the MMA
-// warp; the ring barriers and, through `init_x(bar)`, the kernel's own
-// barriers initialised by the load thread.
+// Shared setup of one work item of the tensor-core grid: the ring barriers
+// and, through `init_x(bar)`, the item's own barriers, initialised by the
+// load thread.  The CTA's TMEM is allocated once for all its items.
 template <class L, class InitX>
-__device__ __forceinline__ uint32_t bwd_setup(uint32_t sbase, uint8_t* sgen, int warp,
-                                              InitX init_x) {
-  uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sgen + L::kMisc);
-  if (warp == kBwdMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_base_ptr), kBwdTmemCols);
-    ptx::tmem_relinquish();
-  }
+__device__ __forceinline__ void bwd_setup(uint32_t sbase, uint8_t* sgen, InitX init_x) {
   if (threadIdx.x == kBwdLoadWarp * 32) {
     *reinterpret_cast<volatile int*>(sgen + L::kMisc + 4) = 0;
     auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
@@ -319,7 +313,19 @@ __device__ __forceinline__ uint32_t bwd_setup(uint32_t sbase, uint8_t* sgen, int
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  return *tmem_base_ptr;
+}
+
+// End of one work item: every role is done (the MMA thread has seen its
+// last commit, the load thread its last copy), so the load thread
+// invalidates the item's barriers; the next item, whose layout may put
+// other data there, initialises its own.
+template <class L>
+__device__ __forceinline__ void bwd_teardown(uint32_t sbase) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (threadIdx.x == kBwdLoadWarp * 32)
+    for (int i = 0; i < L::kNumBars; ++i) ptx::mbar_inval(sbase + L::kBar + 8u * i);
 }
 
 // The load thread: the resident pair (res_a, res_b at tile `res_tile`), then
@@ -389,7 +395,7 @@ struct DkdvVec {
 
 // One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
 template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
-__device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
+__device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32_t tmem_base) {
   using L = BwdSmem<D, DkdvVec<D>::kBytes>;
   using X = DkdvBars;
   extern __shared__ uint8_t smem_raw[];
@@ -439,7 +445,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
     return;
   }
 
-  const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
+  bwd_setup<L>(sbase, sgen, [&](auto b) {
     ptx::mbar_init(b(L::bX + X::kSFull), 1);
     ptx::mbar_init(b(L::bX + X::kDpFull), 1);
     ptx::mbar_init(b(L::bX + X::kPReady), kBwdEwThreads);
@@ -669,13 +675,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk) {
       store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
                                   key < key_rows);
   }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == kBwdMmaWarp) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kBwdTmemCols);
-  }
+  bwd_teardown<L>(sbase);
 }
 
 // ---------------------------------------------------------------- dQ
@@ -687,7 +687,7 @@ __device__ __forceinline__ uint32_t dq_ds_col(int b) {
 
 // One CTA of the dQ pass: block `blk` of BH * n_tiles.
 template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
-__device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
+__device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t tmem_base) {
   using L = BwdSmem<D, 0>;
   using X = DqBars;
   static_assert(kColAcc + D + 128 <= kBwdTmemCols, "dS buffers fit in TMEM");
@@ -734,7 +734,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
     return;
   }
 
-  const uint32_t tmem_base = bwd_setup<L>(sbase, sgen, warp, [&](auto b) {
+  bwd_setup<L>(sbase, sgen, [&](auto b) {
     ptx::mbar_init(b(L::bX + X::kSFull), 1);
     ptx::mbar_init(b(L::bX + X::kSFree), kBwdEwThreads);
     for (int k = 0; k < 2; ++k) {
@@ -885,29 +885,46 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk) {
     store_acc_cols<D, D / 2, kBf16>(tmem_base + lane_off + kColAcc, half * (D / 2), p.scale, p.dq,
                                     grow, q_in);
   }
+  bwd_teardown<L>(sbase);
+}
 
+// ---------------------------------------------------------------- entry point
+// Both tensor-core passes in one persistent grid of at most one CTA per SM.
+// The work items are [0, BH * n_ktiles) dK/dV items (the ones with the most
+// query tiles first), then the dQ items (most key tiles first); CTA c takes
+// items c, c + grid, c + 2 grid, ...  (A snake order, c then grid - 1 - c,
+// measured no better.)  One grid lets SMs that finish their dK/dV items
+// take dQ items at once, so the two passes share one partial last round,
+// and a CTA that stays resident across items skips the relaunch and the
+// TMEM allocation of every item after its first.  Shared memory is sized
+// for the larger layout.
+template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  __shared__ uint32_t s_tmem_base;
+  const int warp = threadIdx.x >> 5;
+  if (warp == kBwdMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&s_tmem_base), kBwdTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int per_pass = p.BH * p.n_ktiles;   // dK/dV items, one per key tile
+  const int total = per_pass + p.BH * p.n_tiles;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    if (item < per_pass)
+      bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, item, tmem_base);
+    else
+      bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, item - per_pass, tmem_base);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kBwdMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kBwdTmemCols);
   }
-}
-
-// ---------------------------------------------------------------- entry point
-// Both tensor-core passes in one grid: blocks [0, BH * n_tiles) are dK/dV
-// CTAs (the ones with the most query tiles first), the rest dQ CTAs (most
-// key tiles first).  One launch lets SMs that finish their dK/dV CTAs take
-// dQ CTAs at once, so the two passes share one partial last wave instead of
-// each ending on its own.  Shared memory is sized for the larger layout.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-  const int per_pass = p.BH * p.n_ktiles;   // dK/dV CTAs, one per key tile
-  if (static_cast<int>(blockIdx.x) < per_pass)
-    bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, blockIdx.x);
-  else
-    bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, blockIdx.x - per_pass);
 }
 
 }  // namespace fa

@@ -51,10 +51,12 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   constexpr int kAlloc = kAllocKv > kAllocQ ? kAllocKv : kAllocQ;
   e = bwd_smem_attr(fa_bwd_kernel<D, kBf16, kCausal, kDrop, kKv>, done, kAlloc);
   if (e != cudaSuccess) return e;
-  // dK/dV CTAs (one per key tile) then dQ CTAs (one per query tile), with
-  // programmatic dependent launch: CTAs start their setup and loads while
-  // the D pass ends, and wait on the device before reading D.
-  const long long grid = static_cast<long long>(p.BH) * (p.n_ktiles + p.n_tiles);
+  // dK/dV items (one per key tile) then dQ items (one per query tile), on
+  // at most one persistent CTA per SM, with programmatic dependent launch:
+  // CTAs start their setup and loads while the D pass ends, and wait on the
+  // device before reading D.
+  const long long items = static_cast<long long>(p.BH) * (p.n_ktiles + p.n_tiles);
+  const long long grid = items < sms ? items : sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kBwdThreads);
