@@ -93,9 +93,9 @@ def load_library(path=None):
     lib.fa_fwd_dropout.restype = i
     lib.fa_bwd_dropout.argtypes = [vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp]
     lib.fa_bwd_dropout.restype = i
-    lib.fa_bwd_kv.argtypes = [vp] * 10 + [i, i, i, i, i, i, vp, f, i, vp]
+    lib.fa_bwd_kv.argtypes = [vp] * 10 + [i, i, i, i, i, i, i, vp, f, i, vp]
     lib.fa_bwd_kv.restype = i
-    lib.fa_bwd_varlen.argtypes = [vp] * 12 + [i] * 8 + [f, i, vp]
+    lib.fa_bwd_varlen.argtypes = [vp] * 12 + [i] * 9 + [f, i, vp]
     lib.fa_bwd_varlen.restype = i
     lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, vp, ctypes.c_size_t, vp]
     lib.fa_decode.restype = i
@@ -203,26 +203,28 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal,
                               int(seed), int(offset), int(dtype), _stream(stream))
 
 
-def fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal, seqlens_k,
-              scale, dtype, stream=None):
-    """Raw C call of the backward pass of fa_fwd_kv; returns the code."""
+def fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, dv_width, causal,
+              seqlens_k, scale, dtype, stream=None):
+    """Raw C call of the backward pass of fa_fwd_kv (query/key width d, value
+    width dv_width); returns the code."""
     lib = load_library()
     return lib.fa_bwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
                          _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(Nq),
-                         int(Nk), int(d), int(causal), _addr(seqlens_k), float(scale), int(dtype),
-                         _stream(stream))
+                         int(Nk), int(d), int(dv_width), int(causal), _addr(seqlens_k),
+                         float(scale), int(dtype), _stream(stream))
 
 
 def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B, H,
-                  max_seqlen_q, max_seqlen_k, total_q, total_k, d, causal, scale, dtype,
+                  max_seqlen_q, max_seqlen_k, total_q, total_k, d, dv_width, causal, scale, dtype,
                   stream=None):
-    """Raw C call of the backward pass of fa_fwd_varlen; returns the code."""
+    """Raw C call of the backward pass of fa_fwd_varlen (query/key width d,
+    value width dv_width); returns the code."""
     lib = load_library()
     return lib.fa_bwd_varlen(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
                              _addr(dq), _addr(dk), _addr(dv), _addr(delta), _addr(cu_seqlens_q),
                              _addr(cu_seqlens_k), int(B), int(H), int(max_seqlen_q),
-                             int(max_seqlen_k), int(total_q), int(total_k), int(d), int(causal),
-                             float(scale), int(dtype), _stream(stream))
+                             int(max_seqlen_k), int(total_q), int(total_k), int(d), int(dv_width),
+                             int(causal), float(scale), int(dtype), _stream(stream))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
@@ -551,14 +553,17 @@ def attention_backward_dropout(q, k, v, o, lse, dout, dropout_p, seed, offset, c
 def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, scale=None,
                           stream=None):
     """dQ, dK, dV for O, LSE = attention_forward_kv(q, k, v, causal, seqlens_k)
-    (``fa_bwd_kv``; q, o, dout [B, H, Nq, d], k, v [B, H, Nk, d])."""
+    (``fa_bwd_kv``; q [B, H, Nq, d], k [B, H, Nk, d], v [B, H, Nk, dv],
+    o, dout [B, H, Nq, dv]; d and dv each 64 or 128)."""
     import torch
     ts = (q, k, v, o, dout)
     if any(t.dtype != q.dtype for t in ts):
         raise TypeError("q, k, v, o, dout must share one dtype")
-    if q.dim() != 4 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape or \
-            k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
-        raise ValueError("q, o, dout must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape[:3] != v.shape[:3] or \
+            k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3] or \
+            o.shape != q.shape[:3] + (v.shape[3],) or dout.shape != o.shape:
+        raise ValueError("q must be [B, H, Nq, d], k [B, H, Nk, d], v [B, H, Nk, dv] and "
+                         "o, dout [B, H, Nq, dv]")
     if lse.dtype != torch.float32 or lse.shape != q.shape[:3]:
         raise ValueError("lse must be float32 [B, H, Nq]")
     if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
@@ -577,8 +582,8 @@ def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, sc
     delta = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, CAUSAL_MODES[causal],
-                   seqlens_k, scale, dtype_code(q.dtype), stream)
+    rc = fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, v.shape[3],
+                   CAUSAL_MODES[causal], seqlens_k, scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_kv")
     return dq, dk, dv
@@ -593,9 +598,11 @@ def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k,
     ts = (q, k, v, o, dout)
     if any(t.dtype != q.dtype for t in ts):
         raise TypeError("q, k, v, o, dout must share one dtype")
-    if q.dim() != 3 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape or \
-            k.shape[1:] != q.shape[1:]:
-        raise ValueError("q, o, dout must be [total_q, H, d] and k, v [total_k, H, d]")
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape[:2] != v.shape[:2] or \
+            k.shape[1:] != q.shape[1:] or o.shape != q.shape[:2] + (v.shape[2],) or \
+            dout.shape != o.shape:
+        raise ValueError("q must be [total_q, H, d], k [total_k, H, d], v [total_k, H, dv] and "
+                         "o, dout [total_q, H, dv]")
     if lse.dtype != torch.float32 or lse.shape != (q.shape[1], q.shape[0]):
         raise ValueError("lse must be float32 [H, total_q]")
     if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
@@ -617,7 +624,7 @@ def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     rc = fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B, H,
-                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, d,
+                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, d, v.shape[2],
                        CAUSAL_MODES[causal], scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_varlen")

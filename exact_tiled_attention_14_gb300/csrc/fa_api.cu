@@ -18,19 +18,21 @@ using namespace fa::host;
 extern "C" {
 
 // fa_bwd, fa_bwd_dropout when drop_t < 256, and fa_bwd_kv when kv (Nq
-// queries against Nk keys with per-batch key counts; causal 2 bottom-right).
+// queries against Nk keys with per-batch key counts; causal 2 bottom-right;
+// values of width dv_width, which only kv calls may set apart from d).
 static int backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
-                    int Nq, int Nk, int d, int causal, bool kv, const int* seqlens_k, float scale,
-                    int dtype, int drop_t, unsigned long long seed, unsigned int drop_off,
-                    cudaStream_t stream) {
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_SHAPE;
+                    int Nq, int Nk, int d, int dv_width, int causal, bool kv,
+                    const int* seqlens_k, float scale, int dtype, int drop_t,
+                    unsigned long long seed, unsigned int drop_off, cudaStream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || dv_width <= 0) return FA_ERR_SHAPE;
   if (causal < 0 || causal > (kv ? 2 : 1)) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_qtiles = (static_cast<long long>(Nq) + fa::kBwdTile - 1) / fa::kBwdTile;
   const long long n_ktiles = (static_cast<long long>(Nk) + fa::kBwdTile - 1) / fa::kBwdTile;
   if (bh > INT_MAX || bh * (n_qtiles + n_ktiles) > INT_MAX) return FA_ERR_SHAPE;   // one grid
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dv_width != 64 && dv_width != 128) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
   if (bh == 0 || (Nq == 0 && Nk == 0)) return FA_OK;  // nothing to write
@@ -60,9 +62,13 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   const void* da = Nq > 0 ? dout : k;
   if (!make_tmap(&p.tm_q, qa, static_cast<int>(bh), nq_rows, d, bf16) ||
       !make_tmap(&p.tm_k, ka, static_cast<int>(bh), nk_rows, d, bf16) ||
-      !make_tmap(&p.tm_v, va, static_cast<int>(bh), nk_rows, d, bf16) ||
-      !make_tmap(&p.tm_do, da, static_cast<int>(bh), nq_rows, d, bf16))
+      !make_tmap(&p.tm_v, va, static_cast<int>(bh), nk_rows, dv_width, bf16) ||
+      !make_tmap(&p.tm_do, da, static_cast<int>(bh), nq_rows, dv_width, bf16))
     return FA_ERR_TENSORMAP;
+  p.width_qk = d;
+  p.width_v = dv_width;
+  // the kernels are compiled for the larger of the two widths
+  const int dk_max = d > dv_width ? d : dv_width;
   p.lse = lse;
   p.delta = delta;
   p.dq = dq;
@@ -89,8 +95,8 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   const bool c = causal != 0;
   cudaError_t e;
   if (kv)
-    e = (d == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
-                  : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+    e = (dk_max == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                       : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   else if (drop_t < 256)
     e = (d == 64) ? fa::launch_bwd_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
                   : fa::launch_bwd_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
@@ -103,25 +109,25 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int N,
            int d, int causal, float scale, int dtype, cudaStream_t stream) {
-  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, causal, false, nullptr,
-                  scale, dtype, 256, 0, 0, stream);
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
+                  nullptr, scale, dtype, 256, 0, 0, stream);
 }
 
 int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H, int Nq,
-              int Nk, int d, int causal, const int* seqlens_k, float scale, int dtype,
-              cudaStream_t stream) {
-  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, causal, true,
-                  seqlens_k, scale, dtype, 256, 0, 0, stream);
+              int Nk, int d, int dv_width, int causal, const int* seqlens_k, float scale,
+              int dtype, cudaStream_t stream) {
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, dv_width, causal,
+                  true, seqlens_k, scale, dtype, 256, 0, 0, stream);
 }
 
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, float* delta,
                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
                   int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
-                  int causal, float scale, int dtype, cudaStream_t stream) {
+                  int dv_width, int causal, float scale, int dtype, cudaStream_t stream) {
   if (B < 0 || H < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 ||
-      d <= 0)
+      d <= 0 || dv_width <= 0)
     return FA_ERR_SHAPE;
   if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
@@ -131,6 +137,7 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
       static_cast<long long>(total_q) * H > INT_MAX || static_cast<long long>(total_k) * H > INT_MAX)
     return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (dv_width != 64 && dv_width != 128) return FA_ERR_UNSUPPORTED_D;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_SCALE;
   if (bh == 0 || (total_q == 0 && total_k == 0) || (n_qtiles == 0 && n_ktiles == 0)) return FA_OK;
@@ -160,9 +167,12 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
   const void* va = total_k > 0 ? v : q;
   if (!make_tmap_tokens(&p.tm_q, qa, H, q_tok, d, bf16) ||
       !make_tmap_tokens(&p.tm_k, ka, H, k_tok, d, bf16) ||
-      !make_tmap_tokens(&p.tm_v, va, H, k_tok, d, bf16) ||
-      !make_tmap_tokens(&p.tm_do, da, H, q_tok, d, bf16))
+      !make_tmap_tokens(&p.tm_v, va, H, k_tok, dv_width, bf16) ||
+      !make_tmap_tokens(&p.tm_do, da, H, q_tok, dv_width, bf16))
     return FA_ERR_TENSORMAP;
+  p.width_qk = d;
+  p.width_v = dv_width;
+  const int dk_max = d > dv_width ? d : dv_width;
   p.lse = lse;
   p.delta = delta;
   p.dq = dq;
@@ -187,8 +197,9 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
   p.scale_log2 = scale * 1.4426950408889634f;
   set_dropout(&p, 256, 0, 0);
   const bool c = causal != 0;
-  const cudaError_t e = (d == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
-                                  : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  const cudaError_t e = (dk_max == 64)
+                            ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                            : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -199,8 +210,8 @@ int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, c
                    cudaStream_t stream) {
   const int t = drop_threshold(dropout_p);
   if (t < 0) return FA_ERR_DROPOUT;
-  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, causal, false, nullptr,
-                  scale, dtype, t, seed, offset, stream);
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
+                  nullptr, scale, dtype, t, seed, offset, stream);
 }
 
 }  // extern "C"

@@ -109,6 +109,14 @@ struct BwdParams {
   int H;
   const int* seqlens_k;
   int align_br;
+  // Widths (kKv variants; square calls set both to D): width_qk of Q, K,
+  // dQ, dK and width_v of V, dO, O, dV, each 64 or 128 with D the larger.
+  // Each tensor map has its tensor's own width and only those 64-column
+  // chunks are loaded; products over the head width take width_qk / 16 (S)
+  // or width_v / 16 (dP) K steps, and dV is accumulated over width_v
+  // columns, dK and dQ over width_qk.
+  int width_qk;
+  int width_v;
   // Packed variable-length batches (kKv variants with varlen = 1): Q, dO, O,
   // dQ token-major [total_q, H, d], K, V, dK, dV [Nk = total_k, H, d], LSE
   // [H, total_q] (as the forward writes it), D [total_q, H]; sequence b owns
@@ -243,9 +251,10 @@ constexpr uint32_t kColS = 0, kColDp = 128, kColAcc = 256;
 // d_tmem: M = N = 128, K = D in steps of 16 columns.
 template <int D, int Chunk>
 __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
-                                             uint32_t idesc) {
+                                             uint32_t idesc, int steps = D / 16) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
+    if (kk >= steps) break;
     const uint32_t off = static_cast<uint32_t>((kk >> 2) * Chunk + (kk & 3) * 32) >> 4;
     ptx::mma_ss(d_tmem, ptx::desc_sw128(a_lo + off), ptx::desc_sw128(b_lo + off), idesc, kk > 0);
   }
@@ -266,14 +275,15 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
   }
 }
 
-// Write columns [c0, c0 + NC) of one row of a TMEM accumulator (fp32), times
-// `mul`, to global memory in the storage dtype (rows past N are skipped).
-template <int D, int NC, bool kBf16>
-__device__ __forceinline__ void store_acc_cols(uint32_t t_acc, int c0, float mul, void* base,
-                                               long long row, bool in_range) {
-  uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * (D * 2) + c0 * 2);
+// Write columns [c0, c0 + nc) (nc a multiple of 32) of one row of a TMEM
+// accumulator (fp32), times `mul`, to global memory in the storage dtype, in
+// rows of `width` values (rows past N are skipped).
+template <bool kBf16>
+__device__ __forceinline__ void store_acc_cols(uint32_t t_acc, int c0, int nc, int width, float mul,
+                                               void* base, long long row, bool in_range) {
+  uint4* out = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + row * (width * 2) + c0 * 2);
 #pragma unroll 1
-  for (int q4 = 0; q4 < NC / 32; ++q4) {
+  for (int q4 = 0; q4 < nc / 32; ++q4) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + c0 + q4 * 32, r);
     ptx::tmem_wait_ld();
@@ -330,14 +340,17 @@ __device__ __forceinline__ void bwd_teardown(uint32_t sbase) {
 
 // The load thread: the resident pair (res_a, res_b at tile `res_tile`), then
 // tiles first .. first + count - 1 of str_a into ring A and of str_b into
-// ring B, in the order A_0, B_0, A_1, B_1, ...
+// ring B, in the order A_0, B_0, A_1, B_1, ...  The "a" tensors (K and Q)
+// have chunks_a 64-column chunks, the "b" tensors (V and dO) chunks_b; only
+// those are loaded.
 template <class L>
 __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* res_a,
                                              const CUtensorMap* res_b, int res_tile,
                                              const CUtensorMap* str_a, const CUtensorMap* str_b,
                                              int first, int count, int bh,
                                              const ptx::Watchdog& wd, int tok_h = -1,
-                                             int res_tok0 = 0, int str_tok0 = 0) {
+                                             int res_tok0 = 0, int str_tok0 = 0,
+                                             int chunks_a = L::kChunks, int chunks_b = L::kChunks) {
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
   bool alive = true;
   // tile `tile` of a [BH, rows, d] map: (column, row, batch*head); with
@@ -345,30 +358,31 @@ __device__ __forceinline__ void bwd_producer(uint32_t sbase, const CUtensorMap* 
   // tok0 on
   auto y_of = [&](int tile, int tok0) { return tok_h < 0 ? tile * kBwdTile : tok_h; };
   auto z_of = [&](int tile, int tok0) { return tok_h < 0 ? bh : tok0 + tile * kBwdTile; };
-  ptx::mbar_arrive_expect_tx(bar(L::bRes), 2 * L::kTile);
-  for (int c = 0; c < L::kChunks; ++c) {
+  ptx::mbar_arrive_expect_tx(bar(L::bRes), (chunks_a + chunks_b) * L::kChunkBytes);
+  for (int c = 0; c < chunks_a; ++c)
     ptx::tma_load_3d(sbase + L::kRes + c * L::kChunkBytes, res_a, bar(L::bRes), c * 64,
                      y_of(res_tile, res_tok0), z_of(res_tile, res_tok0));
+  for (int c = 0; c < chunks_b; ++c)
     ptx::tma_load_3d(sbase + L::kRes + L::kTile + c * L::kChunkBytes, res_b, bar(L::bRes), c * 64,
                      y_of(res_tile, res_tok0), z_of(res_tile, res_tok0));
-  }
   // one tile of `tm` into slot `slot` of a ring, once its previous use is over
-  auto load = [&](const CUtensorMap* tm, int ring, int full0, int empty0, int stages, int it) {
+  auto load = [&](const CUtensorMap* tm, int ring, int full0, int empty0, int stages, int it,
+                  int chunks) {
     const int slot = it % stages, use = it / stages;
     if (use > 0)
       alive = ptx::wait_bounded(bar(empty0 + slot), (use - 1) & 1, wd, kSiteBwdEmpty) && alive;
     if (!alive) return;
     const uint32_t dst = sbase + ring + slot * L::kTile;
-    ptx::mbar_arrive_expect_tx(bar(full0 + slot), L::kTile);
-    for (int c = 0; c < L::kChunks; ++c)
+    ptx::mbar_arrive_expect_tx(bar(full0 + slot), chunks * L::kChunkBytes);
+    for (int c = 0; c < chunks; ++c)
       ptx::tma_load_3d(dst + c * L::kChunkBytes, tm, bar(full0 + slot), c * 64,
                        y_of(first + it, str_tok0), z_of(first + it, str_tok0));
   };
   int loads = 0;
   for (int it = 0; it < count && alive; ++it) {
-    load(str_a, L::kRingA, L::bFullA, L::bEmptyA, L::kStagesA, it);
+    load(str_a, L::kRingA, L::bFullA, L::bEmptyA, L::kStagesA, it, chunks_a);
     if (!alive) break;
-    load(str_b, L::kRingB, L::bFullB, L::bEmptyB, L::kStagesB, it);
+    load(str_b, L::kRingB, L::bFullB, L::bEmptyB, L::kStagesB, it, chunks_b);
     if (!alive) {   // tile `it` of ring A was issued: drain it too
       ptx::wait_drain(bar(L::bFullA + it % L::kStagesA), (it / L::kStagesA) & 1, 200000000ull);
       break;
@@ -437,9 +451,10 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       const int t = threadIdx.x & 127;
       const long long key = static_cast<long long>(kt) * kBwdTile + t;
       if (key < key_rows) {
+        const int width = threadIdx.x < 128 ? p.width_v : p.width_qk;
         uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(threadIdx.x < 128 ? p.dv : p.dk) +
-                                              bwd_krow(p, tok, hd, bh, key) * (D * 2));
-        for (int c = 0; c < D / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                                              bwd_krow(p, tok, hd, bh, key) * (width * 2));
+        for (int c = 0; c < width / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     return;
@@ -457,13 +472,16 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
   if (warp == kBwdLoadWarp) {
     if (lane == 0)
       bwd_producer<L>(sbase, &p.tm_k, &p.tm_v, kt, &p.tm_q, &p.tm_do, i0, nq, bh, wd,
-                      tok ? bh % p.H : -1, hd.k0, hd.q0);
+                      tok ? bh % p.H : -1, hd.k0, hd.q0, p.width_qk / 64, p.width_v / 64);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBwdTile, kBwdTile, fmt, 0);
-      constexpr uint32_t idesc_o = ptx::idesc_f16(kBwdTile, D, fmt, 1);
+      // dV has width_v columns, dK width_qk
+      const uint32_t idesc_dv = ptx::idesc_f16(kBwdTile, p.width_v, fmt, 1);
+      const uint32_t idesc_dk = ptx::idesc_f16(kBwdTile, p.width_qk, fmt, 1);
+      const int steps_s = p.width_qk / 16, steps_dp = p.width_v / 16;
       constexpr uint32_t kSlotLo = L::kTile >> 4;
       const uint32_t k_lo = ptx::desc_lo(sbase + L::kRes, 16);
       const uint32_t v_lo = ptx::desc_lo(sbase + L::kRes + L::kTile, 16);
@@ -483,11 +501,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       };
       // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (keys on the TMEM lanes)
       auto issue_s = [&](int it) {
-        issue_kmajor<D, L::kChunkBytes>(tS, k_lo, q_lo0 + (it % L::kStagesA) * kSlotLo, idesc_s);
+        issue_kmajor<D, L::kChunkBytes>(tS, k_lo, q_lo0 + (it % L::kStagesA) * kSlotLo, idesc_s,
+                                        steps_s);
         ptx::mma_commit(xbar(X::kSFull));
       };
       auto issue_dp = [&](int it) {
-        issue_kmajor<D, L::kChunkBytes>(tDp, v_lo, do_lo0 + (it % L::kStagesB) * kSlotLo, idesc_s);
+        issue_kmajor<D, L::kChunkBytes>(tDp, v_lo, do_lo0 + (it % L::kStagesB) * kSlotLo, idesc_s,
+                                        steps_dp);
         ptx::mma_commit(xbar(X::kDpFull));
       };
       bool alive = ptx::wait_bounded(bar(L::bRes), 0, wd, kSiteBwdRes);
@@ -503,7 +523,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         ptx::tc_fence_after();
         if (!alive) break;
         // dV_j += P^T dO_i; P^T sits in TMEM columns 0-31 and 64-95
-        issue_tmem_a<true>(tDv, tS, do_mn0 + (it % L::kStagesB) * kSlotLo, idesc_o,
+        issue_tmem_a<true>(tDv, tS, do_mn0 + (it % L::kStagesB) * kSlotLo, idesc_dv,
                            it > 0 ? 1u : 0u);
         ptx::mma_commit(bar(L::bEmptyB + it % L::kStagesB));
         if (more) {
@@ -516,7 +536,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         ptx::tc_fence_after();
         if (!alive) break;
         // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
-        issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_o, it > 0 ? 1u : 0u);
+        issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk, it > 0 ? 1u : 0u);
         ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
         if (more) {
           alive = full_b(it + 1);
@@ -669,11 +689,11 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
     ptx::tc_fence_after();
     const long long row = bwd_krow(p, tok, hd, bh, key);
     if (half == 0)
-      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc, 0, kDrop ? p.drop_scale : 1.f,
-                                  p.dv, row, key < key_rows);
+      store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc, 0, p.width_v, p.width_v,
+                            kDrop ? p.drop_scale : 1.f, p.dv, row, key < key_rows);
     else
-      store_acc_cols<D, D, kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.scale, p.dk, row,
-                                  key < key_rows);
+      store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc + D, 0, p.width_qk, p.width_qk,
+                            p.scale, p.dk, row, key < key_rows);
   }
   bwd_teardown<L>(sbase);
 }
@@ -726,9 +746,11 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
       const int t = threadIdx.x & 127, hf = threadIdx.x >> 7;
       const long long qrow = static_cast<long long>(qt) * kBwdTile + t;
       if (qrow < q_rows) {
+        // each half of the threads clears half of the row's width_qk columns
         uint4* row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dq) +
-                                              bwd_qrow(p, tok, hd, bh, qrow) * (D * 2) + hf * D);
-        for (int c = 0; c < D / 16; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                                              bwd_qrow(p, tok, hd, bh, qrow) * (p.width_qk * 2) +
+                                              hf * p.width_qk);
+        for (int c = 0; c < p.width_qk / 16; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     return;
@@ -748,13 +770,14 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
   if (warp == kBwdLoadWarp) {
     if (lane == 0)
       bwd_producer<L>(sbase, &p.tm_q, &p.tm_do, qt, &p.tm_k, &p.tm_v, 0, nk, bh, wd,
-                      tok ? bh % p.H : -1, hd.q0, hd.k0);
+                      tok ? bh % p.H : -1, hd.q0, hd.k0, p.width_qk / 64, p.width_v / 64);
     __syncwarp();
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0) {
       constexpr int fmt = kBf16 ? 1 : 0;
       constexpr uint32_t idesc_s = ptx::idesc_f16(kBwdTile, kBwdTile, fmt, 0);
-      constexpr uint32_t idesc_o = ptx::idesc_f16(kBwdTile, D, fmt, 1);
+      const uint32_t idesc_dq = ptx::idesc_f16(kBwdTile, p.width_qk, fmt, 1);   // dQ: width_qk columns
+      const int steps_s = p.width_qk / 16, steps_dp = p.width_v / 16;
       constexpr uint32_t kSlotLo = L::kTile >> 4;
       const uint32_t q_lo = ptx::desc_lo(sbase + L::kRes, 16);
       const uint32_t do_lo = ptx::desc_lo(sbase + L::kRes + L::kTile, 16);
@@ -769,7 +792,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
         ptx::tc_fence_after();
         if (!ok) return false;
         const int slot = j % L::kStagesA;
-        issue_tmem_a<false>(tDq, tmem_base + dq_ds_col<D>(j & 1), k_mn0 + slot * kSlotLo, idesc_o,
+        issue_tmem_a<false>(tDq, tmem_base + dq_ds_col<D>(j & 1), k_mn0 + slot * kSlotLo, idesc_dq,
                             j > 0 ? 1u : 0u);
         ptx::mma_commit(bar(L::bEmptyA + slot));
         ptx::mma_commit(xbar(X::kDsFree + (j & 1)));
@@ -785,8 +808,8 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
         ptx::tc_fence_after();
         if (!alive) break;
         // S = Q_i K_j^T and dP = dO_i V_j^T (queries on the TMEM lanes)
-        issue_kmajor<D, L::kChunkBytes>(tS, q_lo, k_lo0 + sa * kSlotLo, idesc_s);
-        issue_kmajor<D, L::kChunkBytes>(tDp, do_lo, v_lo0 + sb * kSlotLo, idesc_s);
+        issue_kmajor<D, L::kChunkBytes>(tS, q_lo, k_lo0 + sa * kSlotLo, idesc_s, steps_s);
+        issue_kmajor<D, L::kChunkBytes>(tDp, do_lo, v_lo0 + sb * kSlotLo, idesc_s, steps_dp);
         ptx::mma_commit(xbar(X::kSFull));
         ptx::mma_commit(bar(L::bEmptyB + sb));   // V_j is not read again
         if (it > 0) alive = issue_dq(it - 1);
@@ -882,8 +905,8 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
     ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
     __syncwarp();
     ptx::tc_fence_after();
-    store_acc_cols<D, D / 2, kBf16>(tmem_base + lane_off + kColAcc, half * (D / 2), p.scale, p.dq,
-                                    grow, q_in);
+    store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc, half * (p.width_qk / 2), p.width_qk / 2,
+                          p.width_qk, p.scale, p.dq, grow, q_in);
   }
   bwd_teardown<L>(sbase);
 }

@@ -33,14 +33,19 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
   // rows of O and dO: every (batch*head, query), or the packed tokens x H
   const long long rows = p.varlen ? static_cast<long long>(p.total_q) * p.H
                                   : static_cast<long long>(p.BH) * p.N;
-  const long long threads = rows * (D / 8);
+  // D = rowsum(dO * O) over the value width
+  const long long threads = rows * (p.width_v / 8);
   long long blocks = (threads + 255) / 256;
   const long long cap = 8ll * sms;
   if (blocks > cap) blocks = cap;
   cudaError_t e = cudaSuccess;
   if (blocks > 0) {   // no queries (a kv call with Nq = 0): no D to form
-    fa_bwd_delta_kernel<D, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
+    if (p.width_v == 64)
+      fa_bwd_delta_kernel<64, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+          static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
+    else
+      fa_bwd_delta_kernel<128, kBf16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+          static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta, rows);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

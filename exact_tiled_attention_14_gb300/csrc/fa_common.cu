@@ -179,7 +179,7 @@ int drop_threshold(float p) {
 
 extern "C" {
 
-int fa_version(void) { return 103; }
+int fa_version(void) { return 104; }
 
 const char* fa_strerror(int code) {
   switch (code) {

@@ -337,15 +337,19 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            cudaStream_t stream);
 
 /*
- * fa_bwd_kv — the backward pass of fa_fwd_kv (value width equal to d): dQ,
- * dK, dV of sum(dO * O) for O, LSE = fa_fwd_kv(q, k, v, ...) with the same
- * Nq, Nk, key counts and causal alignment.  The pages give the backward's
+ * fa_bwd_kv — the backward pass of fa_fwd_kv: dQ, dK, dV of sum(dO * O) for
+ * O, LSE = fa_fwd_kv(q, k, v, ...) with the same Nq, Nk, widths, key counts
+ * and causal alignment.  The pages give the backward's
  * principle (keep Q, K, V, O and the row statistics, rebuild the tiles;
  * "Why FlashAttention Can Avoid a Square Attention Array Without Making
  * Attention Linear", section "Backward can recreate tiles instead of
  * retaining the square"); the masks are fa_fwd_kv's.
  *
- *   q, o, dout, dq : [B, H, Nq, d];  k, v, dk, dv : [B, H, Nk, d];
+ *   q, dq          : [B, H, Nq, d];  k, dk : [B, H, Nk, d];
+ *   o, dout        : [B, H, Nq, dv_width];  v, dv : [B, H, Nk, dv_width];
+ *   d, dv_width    : 64 or 128 each (the value width may differ from the
+ *                    query/key width, as in fa_fwd_kv; first page, section
+ *                    "Check it", shapes with dv != d);
  *   lse, delta     : [B, H, Nq] float32 (delta is scratch, as in fa_bwd).
  *   seqlens_k, causal (0, 1 upper-left, 2 bottom-right) : as fa_fwd_kv.
  *   Keys that no query sees (padding past a batch's key count, or keys
@@ -356,17 +360,18 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  */
 int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const float *lse,
               const void *dout, void *dq, void *dk, void *dv, float *delta,
-              int B, int H, int Nq, int Nk, int d, int causal, const int *seqlens_k,
-              float scale, int dtype, cudaStream_t stream);
+              int B, int H, int Nq, int Nk, int d, int dv_width, int causal,
+              const int *seqlens_k, float scale, int dtype, cudaStream_t stream);
 
 /*
  * fa_bwd_varlen — the backward pass of fa_fwd_varlen (packed batches of
- * sequences of different lengths, value width equal to d): dQ, dK, dV of
- * sum(dO * O) for O, LSE = fa_fwd_varlen(...) with the same offsets and
- * causal mode; each sequence's gradients come from its own queries and
- * keys only.
+ * sequences of different lengths): dQ, dK, dV of sum(dO * O) for O, LSE =
+ * fa_fwd_varlen(...) with the same offsets, widths and causal mode; each
+ * sequence's gradients come from its own queries and keys only.
  *
- *   q, o, dout, dq : [total_q, H, d];  k, v, dk, dv : [total_k, H, d].
+ *   q, dq : [total_q, H, d];  k, dk : [total_k, H, d];
+ *   o, dout : [total_q, H, dv_width];  v, dv : [total_k, H, dv_width]
+ *   (d and dv_width 64 or 128 each).
  *   lse            : [H, total_q] float32, as fa_fwd_varlen wrote it.
  *   delta          : [total_q, H] float32 scratch (written, as in fa_bwd).
  *   cu_seqlens_q, cu_seqlens_k : the forward's offset arrays (clamped the
@@ -381,7 +386,7 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
                   const void *dout, void *dq, void *dk, void *dv, float *delta,
                   const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
                   int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
-                  int causal, float scale, int dtype, cudaStream_t stream);
+                  int dv_width, int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
  * fa_bwd_dropout — fa_bwd for an output of fa_fwd_dropout: the same

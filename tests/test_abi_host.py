@@ -276,10 +276,11 @@ def test_bwd_kv_host_errors(lib):
     pointers (keys' only with keys, queries' only with queries) and
     alignment before the device."""
     call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
-                delta=FAKE, B=2, H=3, Nq=300, Nk=900, d=128, causal=2, seqlens_k=None, scale=0.1,
-                dtype=fa.FA_BF16)
+                delta=FAKE, B=2, H=3, Nq=300, Nk=900, d=128, dv_width=64, causal=2, seqlens_k=None,
+                scale=0.1, dtype=fa.FA_BF16)
     cases = [(dict(Nq=-1), fa.FA_ERR_SHAPE), (dict(causal=3), fa.FA_ERR_SHAPE),
-             (dict(d=80), fa.FA_ERR_UNSUPPORTED_D), (dict(dtype=5), fa.FA_ERR_DTYPE),
+             (dict(d=80), fa.FA_ERR_UNSUPPORTED_D), (dict(dv_width=96), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dv_width=0), fa.FA_ERR_SHAPE), (dict(dtype=5), fa.FA_ERR_DTYPE),
              (dict(scale=-1.0), fa.FA_ERR_SCALE), (dict(Nq=0, Nk=0), fa.FA_OK), (dict(B=0), fa.FA_OK),
              (dict(dk=None), fa.FA_ERR_NULLPTR), (dict(delta=None), fa.FA_ERR_NULLPTR),
              (dict(seqlens_k=FAKE + 2), fa.FA_ERR_ALIGN), (dict(dq=FAKE + 8), fa.FA_ERR_ALIGN)]
@@ -301,10 +302,11 @@ def test_bwd_varlen_host_errors(lib):
     offset arrays and the other pointers, and alignment before the device."""
     call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
                 delta=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, B=3, H=2, max_seqlen_q=500,
-                max_seqlen_k=700, total_q=900, total_k=1500, d=64, causal=1, scale=0.125,
-                dtype=fa.FA_FP16)
+                max_seqlen_k=700, total_q=900, total_k=1500, d=64, dv_width=128, causal=1,
+                scale=0.125, dtype=fa.FA_FP16)
     cases = [(dict(total_k=-1), fa.FA_ERR_SHAPE), (dict(max_seqlen_k=-1), fa.FA_ERR_SHAPE),
              (dict(causal=3), fa.FA_ERR_SHAPE), (dict(d=32), fa.FA_ERR_UNSUPPORTED_D),
+             (dict(dv_width=80), fa.FA_ERR_UNSUPPORTED_D),
              (dict(dtype=9), fa.FA_ERR_DTYPE), (dict(scale=0.0), fa.FA_ERR_SCALE),
              (dict(B=0), fa.FA_OK), (dict(total_q=0, total_k=0), fa.FA_OK),
              (dict(cu_seqlens_k=None), fa.FA_ERR_NULLPTR), (dict(dv=None), fa.FA_ERR_NULLPTR),

@@ -93,6 +93,37 @@ def test_kv_backward_vs_oracle(B, H, Nq, Nk, d, dtype, causal, seqlens):
             assert torch.all(gq[b] == 0)
 
 
+WIDTH_CASES = [
+    # B, H, Nq, Nk, d, dv, dtype, causal, seqlens
+    (1, 2, 200, 1000, 64, 128, "bf16", "bottom_right", None),    # a chunk after a cache
+    (2, 1, 333, 777, 128, 64, "fp16", "upper_left", None),
+    (3, 1, 256, 700, 128, 64, "bf16", None, [700, 100, 0]),       # padding, one empty batch
+    (1, 1, 300, 128, 64, 128, "fp16", "bottom_right", None),     # Nq > Nk: rows that see nothing
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,dtype,causal,seqlens", WIDTH_CASES,
+                         ids=[f"B{c[0]}H{c[1]}q{c[2]}k{c[3]}d{c[4]}dv{c[5]}{c[6]}{c[7] or 'nc'}"
+                              f"{'' if c[8] is None else 'pad'}" for c in WIDTH_CASES])
+def test_kv_backward_value_width(B, H, Nq, Nk, d, dv, dtype, causal, seqlens):
+    """Values (and O, dO, dV) of another width than queries and keys: the
+    kernels load each tensor at its own width, take d / 16 or dv / 16 K
+    steps and accumulate dV over dv columns, dK and dQ over d."""
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, dtype, seed=Nq + 5 * Nk + d + dv, dv=dv)
+    dout = seeded_inputs.make_dout(B, H, Nq, dv, dtype, seed=Nq + Nk + dv)
+    scale = default_scale(d)
+    gq, gk, gv = run_kv_bwd(q, k, v, dout, causal, seqlens, scale)
+    assert gq.shape == q.shape and gk.shape == k.shape and gv.shape == v.shape
+    rq, rk, rv = oracle_kv_grad(q, k, v, dout, causal, seqlens, scale)
+    name = f"B{B}H{H}q{Nq}k{Nk}d{d}dv{dv}{dtype}{causal}{seqlens}"
+    check_grad(name + " dQ", gq, rq, dtype)
+    check_grad(name + " dK", gk, rk, dtype)
+    check_grad(name + " dV", gv, rv, dtype)
+    for b in range(B):
+        n = Nk if seqlens is None else max(0, min(seqlens[b], Nk))
+        assert torch.all(gk[b, :, n:] == 0) and torch.all(gv[b, :, n:] == 0)
+
+
 @pytest.mark.parametrize("d,dtype,causal", [(64, "bf16", True), (128, "fp16", False)])
 def test_square_equals_fa_bwd(d, dtype, causal):
     """Nq = Nk, all keys, upper-left: the same tiles and masks as fa_bwd."""
@@ -128,7 +159,9 @@ def test_kv_backward_without_queries_or_keys():
 def test_kv_backward_errors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 1, 128, dtype=torch.float32, device="cuda")
-    assert fa.fa_bwd_kv(q, q, q, q, lse, q, q, q, q, lse, 1, 1, 128, 128, 64, 3, None, 0.125,
+    assert fa.fa_bwd_kv(q, q, q, q, lse, q, q, q, q, lse, 1, 1, 128, 128, 64, 64, 3, None, 0.125,
                         fa.FA_BF16) == fa.FA_ERR_SHAPE
-    assert fa.fa_bwd_kv(q, q, q, q, lse, q, q, q, q, lse, 1, 1, 128, 128, 96, 0, None, 0.125,
+    assert fa.fa_bwd_kv(q, q, q, q, lse, q, q, q, q, lse, 1, 1, 128, 128, 96, 64, 0, None, 0.125,
+                        fa.FA_BF16) == fa.FA_ERR_UNSUPPORTED_D
+    assert fa.fa_bwd_kv(q, q, q, q, lse, q, q, q, q, lse, 1, 1, 128, 128, 64, 32, 0, None, 0.125,
                         fa.FA_BF16) == fa.FA_ERR_UNSUPPORTED_D

@@ -81,6 +81,38 @@ def test_varlen_backward_vs_oracle(name, lens_q, lens_k, H, d, dtype, causal):
     check_grad(name + " dV", gv.cpu(), rv, dtype)
 
 
+WIDTH_CASES = [
+    # name, lens_q, lens_k, H, d, dv, dtype, causal
+    ("qk64_v128_ul", [1, 127, 129, 300, 0, 517], [1, 127, 129, 300, 0, 517], 2, 64, 128, "bf16",
+     "upper_left"),
+    ("qk128_v64_br", [64, 200, 1], [1000, 250, 3000], 2, 128, 64, "fp16", "bottom_right"),
+]
+
+
+@pytest.mark.parametrize("name,lens_q,lens_k,H,d,dv,dtype,causal", WIDTH_CASES,
+                         ids=[c[0] for c in WIDTH_CASES])
+def test_varlen_backward_value_width(name, lens_q, lens_k, H, d, dv, dtype, causal):
+    """Values (and O, dO, dV) of another width than queries and keys."""
+    q, k, v, cu_q, cu_k = seeded_inputs.make_varlen(lens_q, lens_k, H, d, dtype,
+                                                    seed=len(lens_q) + 7 * d + dv, dv=dv)
+    g = torch.Generator("cpu").manual_seed(len(lens_q) + dv)
+    dout = torch.randn((q.shape[0], H, dv), generator=g).to(q.dtype)
+    scale = default_scale(d)
+    dq_, dk_, dv_, do_, cq, ck = (t.cuda() for t in (q, k, v, dout, cu_q, cu_k))
+    mq, mk = max(lens_q + [0]), max(lens_k + [0])
+    o, lse = fa.attention_forward_varlen(dq_, dk_, dv_, cq, ck, mq, causal=causal, scale=scale)
+    gq, gk, gv = fa.attention_backward_varlen(dq_, dk_, dv_, o, lse, do_, cq, ck, mq, mk,
+                                              causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    code, word = fa.fa_status()
+    assert code == fa.FA_OK, f"device status {word:#x}"
+    assert gq.shape == q.shape and gk.shape == k.shape and gv.shape == v.shape
+    rq, rk, rv = oracle_varlen_grad(q, k, v, dout, cu_q, cu_k, causal, scale)
+    check_grad(name + " dQ", gq.cpu(), rq, dtype)
+    check_grad(name + " dK", gk.cpu(), rk, dtype)
+    check_grad(name + " dV", gv.cpu(), rv, dtype)
+
+
 @pytest.mark.parametrize("d,dtype,causal", [(64, "bf16", "upper_left"), (128, "fp16", None),
                                             (128, "bf16", "bottom_right")])
 def test_uniform_lengths_equal_fa_bwd_kv(d, dtype, causal):
@@ -118,7 +150,7 @@ def test_varlen_backward_guard_bands():
         outs.append((buf, buf[pad:pad + n].view(shape)))
     delta = torch.empty((q.shape[0], H), dtype=torch.float32, device="cuda")
     rc = fa.fa_bwd_varlen(dq_, dk_, dv_, o, lse, do_, outs[0][1], outs[1][1], outs[2][1], delta, cq,
-                          ck, 3, H, 600, 700, q.shape[0], k.shape[0], d, 2, default_scale(d),
+                          ck, 3, H, 600, 700, q.shape[0], k.shape[0], d, d, 2, default_scale(d),
                           fa.FA_BF16)
     torch.cuda.synchronize()
     assert rc == fa.FA_OK and fa.fa_status()[0] == fa.FA_OK
