@@ -88,11 +88,11 @@ def _bind(path):
         lib.oracle_philox4x32_10.restype = None
         lib.oracle_dropout_mask.argtypes = [i64, i64, i64, u64, u32, i32, p]
         lib.oracle_dropout_mask.restype = i32
-        lib.oracle_attention_dropout.argtypes = [i64, i64, i64, i64, i64, p, p, p, i32, f64,
-                                                 u64, u32, i32, p, p]
+        lib.oracle_attention_dropout.argtypes = [i64, i64, i64, i64, i64, p, p, p, i32, i64,
+                                                 f64, u64, u32, i32, p, p]
         lib.oracle_attention_dropout.restype = i32
         lib.oracle_attention_dropout_grad.argtypes = [i64, i64, i64, i64, i64, p, p, p, p, i32,
-                                                      f64, u64, u32, i32, p, p, p]
+                                                      i64, f64, u64, u32, i32, p, p, p]
         lib.oracle_attention_dropout_grad.restype = i32
     return lib
 
@@ -291,10 +291,13 @@ def dropout_mask(bh, nq, nk, seed, offset, p, lib=None):
     return mask
 
 
-def attention_dropout(q, k, v, bh, seed, offset, p, causal=False, scale=None, lib=None):
+def attention_dropout(q, k, v, bh, seed, offset, p, causal=False, scale=None, lib=None,
+                      q_offset=0):
     """O, LSE of ONE head (q [Tq, d], k [Tk, d], v [Tk, dv]; head index ``bh``
     in the batch*head numbering the mask is drawn with) with dropout
-    probability p on the attention weights."""
+    probability p on the attention weights.  Query row i sits at position
+    i + q_offset (causal: keys j <= i + q_offset); the mask is indexed by
+    the row i and the key j whatever the offset."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     tq, d = q.shape
@@ -305,16 +308,17 @@ def attention_dropout(q, k, v, bh, seed, offset, p, causal=False, scale=None, li
         scale = 1.0 / math.sqrt(d)
     o, lse = np.zeros((tq, dv)), np.zeros(tq)
     rc = lib.oracle_attention_dropout(int(bh), tq, tk, d, dv, _ptr(q), _ptr(k), _ptr(v),
-                                      int(bool(causal)), float(scale), int(seed), int(offset),
-                                      dropout_threshold(p), _ptr(o), _ptr(lse))
+                                      int(bool(causal)), int(q_offset), float(scale), int(seed),
+                                      int(offset), dropout_threshold(p), _ptr(o), _ptr(lse))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_dropout failed ({rc})")
     return o, lse
 
 
 def attention_dropout_grad(q, k, v, dout, bh, seed, offset, p, causal=False, scale=None,
-                           lib=None):
-    """dQ, dK, dV of sum(dout * O) for O = attention_dropout(...) of ONE head."""
+                           lib=None, q_offset=0):
+    """dQ, dK, dV of sum(dout * O) for O = attention_dropout(...) of ONE head
+    (query row i at position i + q_offset)."""
     lib = lib or load()
     q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
     tq, d = q.shape
@@ -325,9 +329,9 @@ def attention_dropout_grad(q, k, v, dout, bh, seed, offset, p, causal=False, sca
         scale = 1.0 / math.sqrt(d)
     dq, dk, dvv = np.zeros((tq, d)), np.zeros((tk, d)), np.zeros((tk, dv))
     rc = lib.oracle_attention_dropout_grad(int(bh), tq, tk, d, dv, _ptr(q), _ptr(k), _ptr(v),
-                                           _ptr(g), int(bool(causal)), float(scale), int(seed),
-                                           int(offset), dropout_threshold(p), _ptr(dq), _ptr(dk),
-                                           _ptr(dvv))
+                                           _ptr(g), int(bool(causal)), int(q_offset), float(scale),
+                                           int(seed), int(offset), dropout_threshold(p), _ptr(dq),
+                                           _ptr(dk), _ptr(dvv))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_dropout_grad failed ({rc})")
     return dq, dk, dvv

@@ -31,8 +31,16 @@
  *              probability is t / 256; kept weights are scaled by 256 / t,
  *              so the mask has mean exactly one.
  *
+ * Queries against a key set of another length (a chunk after a cache,
+ * padding, packed sequences): query row i sits at position i + q_off and,
+ * with causal masking, sees keys j <= i + q_off (none when that is
+ * negative: O = 0, LSE = -inf, the empty-key policy); the mask stays
+ * indexed by the row i and the key index j, so the offset moves only the
+ * causal boundary, never a keep decision (a reading; the pages fix no mask
+ * layout).
+ *
  * With Z[i][j] in {0, 1} the keep decision and s = 256 / t, the forward
- * output is, over the visible keys of row i (causal: j <= i),
+ * output is, over the visible keys of row i (causal: j <= i + q_off),
  *
  *     O[i] = s * sum_j exp(x_ij - m_i) Z[i][j] V[j] / l_i,
  *     l_i  = sum_j exp(x_ij - m_i),   LSE[i] = m_i + ln l_i,
@@ -105,17 +113,18 @@ int oracle_dropout_mask(int64_t bh, int64_t nq, int64_t nk, uint64_t seed, uint3
     return 0;
 }
 
-static int64_t visible(int64_t i, int64_t nk, int causal)
+static int64_t visible(int64_t i, int64_t nk, int causal, int64_t q_off)
 {
     if (!causal)
         return nk;
-    return i + 1 < nk ? i + 1 : nk;
+    const int64_t last = i + 1 + q_off;   /* keys 0 .. i + q_off */
+    return last <= 0 ? 0 : (last < nk ? last : nk);
 }
 
-/* Forward with dropout for one head (query i at position i). */
+/* Forward with dropout for one head (query i at position i + q_off). */
 int oracle_attention_dropout(int64_t bh, int64_t nq, int64_t nk, int64_t d, int64_t dv,
                              const double *q, const double *k, const double *v, int causal,
-                             double scale, uint64_t seed, uint32_t offset, int t,
+                             int64_t q_off, double scale, uint64_t seed, uint32_t offset, int t,
                              double *o, double *lse)
 {
     if (nq < 0 || nk < 0 || d <= 0 || dv <= 0 || t < 1 || t > 256)
@@ -128,7 +137,7 @@ int oracle_attention_dropout(int64_t bh, int64_t nq, int64_t nk, int64_t d, int6
         double *oi = o + i * dv;
         for (int64_t c = 0; c < dv; ++c)
             oi[c] = 0.0;
-        const int64_t nvis = visible(i, nk, causal);
+        const int64_t nvis = visible(i, nk, causal, q_off);
         if (nvis == 0) {
             lse[i] = -INFINITY;
             continue;
@@ -162,8 +171,9 @@ int oracle_attention_dropout(int64_t bh, int64_t nq, int64_t nk, int64_t d, int6
  * (written, not accumulated into). */
 int oracle_attention_dropout_grad(int64_t bh, int64_t nq, int64_t nk, int64_t d, int64_t dv,
                                   const double *q, const double *k, const double *v,
-                                  const double *dout, int causal, double scale, uint64_t seed,
-                                  uint32_t offset, int t, double *dq, double *dk, double *dvv)
+                                  const double *dout, int causal, int64_t q_off, double scale,
+                                  uint64_t seed, uint32_t offset, int t, double *dq, double *dk,
+                                  double *dvv)
 {
     if (nq < 0 || nk < 0 || d <= 0 || dv <= 0 || t < 1 || t > 256)
         return -1;
@@ -176,8 +186,8 @@ int oracle_attention_dropout_grad(int64_t bh, int64_t nq, int64_t nk, int64_t d,
         rc = -2;
         goto done;
     }
-    rc = oracle_attention_dropout(bh, nq, nk, d, dv, q, k, v, causal, scale, seed, offset, t,
-                                  o, lse);
+    rc = oracle_attention_dropout(bh, nq, nk, d, dv, q, k, v, causal, q_off, scale, seed, offset,
+                                  t, o, lse);
     if (rc != 0)
         goto done;
     const double s = 256.0 / (double)t;
@@ -188,7 +198,7 @@ int oracle_attention_dropout_grad(int64_t bh, int64_t nq, int64_t nk, int64_t d,
     for (int64_t x = 0; x < nk * dv; ++x)
         dvv[x] = 0.0;
     for (int64_t i = 0; i < nq; ++i) {
-        const int64_t nvis = visible(i, nk, causal);
+        const int64_t nvis = visible(i, nk, causal, q_off);
         if (nvis == 0)
             continue;
         const double *gi = dout + i * dv;

@@ -3,8 +3,10 @@ oracle library so the mutant tests can run them against planted mistakes.
 
 What they pin it to, from outside its own code: the generator's published
 known-answer vectors; the exact reduction to the dropout-free oracle at
-p = 0; the binomial law of the keep rate; the unbiasedness the 256 / t
-scale exists for; finite differences of the loss with the mask held fixed.
+p = 0 (also with queries at shifted positions, against the plain oracle's
+rows at those positions); the binomial law of the keep rate; the
+unbiasedness the 256 / t scale exists for; finite differences of the loss
+with the mask held fixed (also with shifted queries).
 """
 import os
 
@@ -115,6 +117,62 @@ def pin_gradient_matches_finite_differences(lib):
                 assert abs(fd - gx) <= 1e-6 * max(1.0, abs(fd)), ("qkv"[pos], idx, fd, gx)
 
 
+def pin_offset_moves_only_the_causal_boundary(lib):
+    """Queries at shifted positions (row i at i + q_offset): at p = 0 every
+    row is the plain oracle's row at that position (rows before the first
+    key empty: O = 0, LSE = -inf); without causal masking the offset changes
+    nothing (the mask is indexed by row and key, not by position); an offset
+    past the last key sees every key, as the unmasked call does with the
+    same mask."""
+    q, k, v, _ = rand_head(9, 20, 6, 5, 5)
+    for off in (-4, 0, 3, 11):
+        o, lse = oracle.attention_dropout(q, k, v, 3, 17, 2, 0.0, causal=True, lib=lib, q_offset=off)
+        pos = np.arange(9) + off
+        o2, l2 = oracle.attention_rows(q, pos, k, v, causal=True, lib=lib)
+        seen = np.isfinite(l2)
+        assert np.abs(o[seen] - o2[seen]).max() < 1e-12
+        assert np.abs(lse[seen] - l2[seen]).max() < 1e-12
+        assert np.all(o[~seen] == 0.0) and np.all(np.isneginf(lse[~seen]))
+    base = oracle.attention_dropout(q, k, v, 3, 17, 2, 0.3, causal=False, lib=lib)
+    for off in (-4, 5, 11):
+        o, lse = oracle.attention_dropout(q, k, v, 3, 17, 2, 0.3, causal=False, lib=lib, q_offset=off)
+        assert np.array_equal(o, base[0]) and np.array_equal(lse, base[1])
+    o, lse = oracle.attention_dropout(q, k, v, 3, 17, 2, 0.3, causal=True, lib=lib, q_offset=20)
+    assert np.abs(o - base[0]).max() < 1e-13 and np.abs(lse - base[1]).max() < 1e-13
+
+
+def pin_gradient_with_offset_matches_finite_differences(lib):
+    """Finite differences of sum(dO * O) with the queries shifted (some rows
+    see nothing, others see all keys) and the mask fixed."""
+    q, k, v, g = rand_head(7, 10, 4, 3, 6)
+    h = 1e-6
+    r = np.random.default_rng(7)
+    for off in (-3, 4):
+        args = (1, 999, 4, 0.35)
+        grads = oracle.attention_dropout_grad(q, k, v, g, *args, causal=True, lib=lib, q_offset=off)
+
+        def loss(x3):
+            return float(np.sum(g * oracle.attention_dropout(*x3, *args, causal=True, lib=lib,
+                                                             q_offset=off)[0]))
+
+        for pos in range(3):
+            x = (q, k, v)[pos]
+            for _ in range(10):
+                idx = tuple(int(r.integers(0, s)) for s in x.shape)
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                a = [q, k, v]
+                a[pos] = xp
+                lp = loss(a)
+                a[pos] = xm
+                lm = loss(a)
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd - grads[pos][idx]) <= 1e-6 * max(1.0, abs(fd)), ("qkv"[pos], off, idx)
+
+
 ALL_DROPOUT_PINS = [pin_philox_known_answers, pin_no_dropout_is_plain_attention,
                     pin_keep_rate_is_binomial, pin_dropout_is_unbiased,
-                    pin_gradient_matches_finite_differences]
+                    pin_gradient_matches_finite_differences,
+                    pin_offset_moves_only_the_causal_boundary,
+                    pin_gradient_with_offset_matches_finite_differences]

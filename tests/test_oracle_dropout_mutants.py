@@ -25,6 +25,9 @@ MUTANTS = {
     "normaliser_of_kept_weights": ("        l += e;\n", "        l += keep(bh, i, j, seed, offset, t) ? e : 0.0;\n"),
     "dp_without_mask": ("dp[j] = z ? s * gv : 0.0;", "dp[j] = s * gv;"),
     "dv_without_scale": ("dvv[j * dv + c] += s * pr[j] * gi[c];", "dvv[j * dv + c] += pr[j] * gi[c];"),
+    "offset_ignored": ("const int64_t last = i + 1 + q_off;", "const int64_t last = i + 1;"),
+    "mask_by_position": ("            if (keep(bh, i, j, seed, offset, t))",
+                         "            if (keep(bh, i + q_off, j, seed, offset, t))"),
 }
 
 
