@@ -46,6 +46,8 @@ FA_ERR_DROPOUT = 13
 
 # Functions the C ABI exports (checked against include/fa.h by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_kv", "fa_bwd_varlen",
+           "fa_fwd_kv_dropout", "fa_fwd_varlen_dropout", "fa_bwd_kv_dropout",
+           "fa_bwd_varlen_dropout",
            "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
@@ -93,6 +95,14 @@ def load_library(path=None):
     lib.fa_fwd_dropout.restype = i
     lib.fa_bwd_dropout.argtypes = [vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp]
     lib.fa_bwd_dropout.restype = i
+    lib.fa_fwd_kv_dropout.argtypes = [vp] * 5 + [i] * 7 + [vp, f, f, u64, u32, i, vp]
+    lib.fa_fwd_kv_dropout.restype = i
+    lib.fa_fwd_varlen_dropout.argtypes = [vp] * 7 + [i] * 8 + [f, f, u64, u32, i, vp]
+    lib.fa_fwd_varlen_dropout.restype = i
+    lib.fa_bwd_kv_dropout.argtypes = [vp] * 10 + [i] * 7 + [vp, f, f, u64, u32, i, vp]
+    lib.fa_bwd_kv_dropout.restype = i
+    lib.fa_bwd_varlen_dropout.argtypes = [vp] * 12 + [i] * 9 + [f, f, u64, u32, i, vp]
+    lib.fa_bwd_varlen_dropout.restype = i
     lib.fa_bwd_kv.argtypes = [vp] * 10 + [i, i, i, i, i, i, i, vp, f, i, vp]
     lib.fa_bwd_kv.restype = i
     lib.fa_bwd_varlen.argtypes = [vp] * 12 + [i] * 9 + [f, i, vp]
@@ -201,6 +211,53 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal,
                               _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
                               int(N), int(d), int(bool(causal)), float(scale), float(dropout_p),
                               int(seed), int(offset), int(dtype), _stream(stream))
+
+
+def fa_fwd_kv_dropout(q, k, v, o, lse, B, H, Nq, Nk, d, dv, causal, seqlens_k, scale, dropout_p,
+                      seed, offset, dtype, stream=None):
+    """Raw C call of fa_fwd_kv with dropout on the attention weights; returns the code."""
+    lib = load_library()
+    return lib.fa_fwd_kv_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B),
+                                 int(H), int(Nq), int(Nk), int(d), int(dv), int(causal),
+                                 _addr(seqlens_k), float(scale), float(dropout_p), int(seed),
+                                 int(offset), int(dtype), _stream(stream))
+
+
+def fa_fwd_varlen_dropout(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q,
+                          total_q, total_k, d, dv, causal, scale, dropout_p, seed, offset, dtype,
+                          stream=None):
+    """Raw C call of fa_fwd_varlen with dropout on the attention weights; returns the code."""
+    lib = load_library()
+    return lib.fa_fwd_varlen_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse),
+                                     _addr(cu_seqlens_q), _addr(cu_seqlens_k), int(B), int(H),
+                                     int(max_seqlen_q), int(total_q), int(total_k), int(d),
+                                     int(dv), int(causal), float(scale), float(dropout_p),
+                                     int(seed), int(offset), int(dtype), _stream(stream))
+
+
+def fa_bwd_kv_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, dv_width,
+                      causal, seqlens_k, scale, dropout_p, seed, offset, dtype, stream=None):
+    """Raw C call of the backward pass of fa_fwd_kv_dropout; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_kv_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
+                                 _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
+                                 int(Nq), int(Nk), int(d), int(dv_width), int(causal),
+                                 _addr(seqlens_k), float(scale), float(dropout_p), int(seed),
+                                 int(offset), int(dtype), _stream(stream))
+
+
+def fa_bwd_varlen_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B,
+                          H, max_seqlen_q, max_seqlen_k, total_q, total_k, d, dv_width, causal,
+                          scale, dropout_p, seed, offset, dtype, stream=None):
+    """Raw C call of the backward pass of fa_fwd_varlen_dropout; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_varlen_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse),
+                                     _addr(dout), _addr(dq), _addr(dk), _addr(dv), _addr(delta),
+                                     _addr(cu_seqlens_q), _addr(cu_seqlens_k), int(B), int(H),
+                                     int(max_seqlen_q), int(max_seqlen_k), int(total_q),
+                                     int(total_k), int(d), int(dv_width), int(causal),
+                                     float(scale), float(dropout_p), int(seed), int(offset),
+                                     int(dtype), _stream(stream))
 
 
 def fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, dv_width, causal,
@@ -369,7 +426,7 @@ CAUSAL_MODES = {None: 0, False: 0, "upper_left": 1, "bottom_right": 2}
 
 
 def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=None, lse=None,
-                         stream=None):
+                         stream=None, dropout_p=0.0, seed=0, offset=0):
     """O [B, H, Nq, dv], LSE of queries q [B, H, Nq, d] against keys
     k [B, H, Nk, d] and values v [B, H, Nk, dv] (CUDA, contiguous, one 16-bit
     dtype; d and dv each 64 or 128).
@@ -378,7 +435,8 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
     "bottom_right" (query i at position len_b - Nq + i).  ``seqlens_k``: None
     or an int32 CUDA tensor [B] of key counts per batch (the rest of the Nk
     keys is padding).  A query that sees no key gets O = 0 and LSE = -inf.
-    Calls ``fa_fwd_kv`` on ``stream`` (default: current stream).
+    Calls ``fa_fwd_kv`` on ``stream`` (default: current stream), or
+    ``fa_fwd_kv_dropout`` when ``dropout_p`` > 0 (mask from seed, offset).
     """
     import torch
     if not (q.dtype == k.dtype == v.dtype):
@@ -408,15 +466,21 @@ def attention_forward_kv(q, k, v, causal=None, seqlens_k=None, scale=None, out=N
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, dv, CAUSAL_MODES[causal], seqlens_k,
-                   scale, dtype_code(q.dtype), stream)
+    if dropout_p > 0:
+        rc = fa_fwd_kv_dropout(q, k, v, out, lse, B, H, Nq, Nk, d, dv, CAUSAL_MODES[causal],
+                               seqlens_k, scale, dropout_p, seed, offset, dtype_code(q.dtype),
+                               stream)
+    else:
+        rc = fa_fwd_kv(q, k, v, out, lse, B, H, Nq, Nk, d, dv, CAUSAL_MODES[causal], seqlens_k,
+                       scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse
 
 
 def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, causal=None,
-                             scale=None, out=None, lse=None, stream=None):
+                             scale=None, out=None, lse=None, stream=None, dropout_p=0.0, seed=0,
+                             offset=0):
     """O [total_q, H, dv], LSE [H, total_q] of a packed batch: q [total_q, H, d],
     k [total_k, H, d], v [total_k, H, dv] (CUDA, contiguous, one 16-bit dtype);
     cu_seqlens_q / cu_seqlens_k int32 CUDA tensors [B + 1] of token offsets;
@@ -455,9 +519,15 @@ def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, 
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, B, H, int(max_seqlen_q),
-                       total_q, total_k, d, dv, CAUSAL_MODES[causal], scale, dtype_code(q.dtype),
-                       stream)
+    if dropout_p > 0:
+        rc = fa_fwd_varlen_dropout(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, B, H,
+                                   int(max_seqlen_q), total_q, total_k, d, dv,
+                                   CAUSAL_MODES[causal], scale, dropout_p, seed, offset,
+                                   dtype_code(q.dtype), stream)
+    else:
+        rc = fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, B, H, int(max_seqlen_q),
+                           total_q, total_k, d, dv, CAUSAL_MODES[causal], scale,
+                           dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc)
     return out, lse
@@ -551,7 +621,7 @@ def attention_backward_dropout(q, k, v, o, lse, dout, dropout_p, seed, offset, c
 
 
 def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, scale=None,
-                          stream=None):
+                          stream=None, dropout_p=0.0, seed=0, offset=0):
     """dQ, dK, dV for O, LSE = attention_forward_kv(q, k, v, causal, seqlens_k)
     (``fa_bwd_kv``; q [B, H, Nq, d], k [B, H, Nk, d], v [B, H, Nk, dv],
     o, dout [B, H, Nq, dv]; d and dv each 64 or 128)."""
@@ -582,15 +652,21 @@ def attention_backward_kv(q, k, v, o, lse, dout, causal=None, seqlens_k=None, sc
     delta = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, v.shape[3],
-                   CAUSAL_MODES[causal], seqlens_k, scale, dtype_code(q.dtype), stream)
+    if dropout_p > 0:
+        rc = fa_bwd_kv_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d,
+                               v.shape[3], CAUSAL_MODES[causal], seqlens_k, scale, dropout_p, seed,
+                               offset, dtype_code(q.dtype), stream)
+    else:
+        rc = fa_bwd_kv(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, v.shape[3],
+                       CAUSAL_MODES[causal], seqlens_k, scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_kv")
     return dq, dk, dv
 
 
 def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
-                              max_seqlen_k, causal=None, scale=None, stream=None):
+                              max_seqlen_k, causal=None, scale=None, stream=None, dropout_p=0.0,
+                              seed=0, offset=0):
     """dQ, dK, dV for O, LSE = attention_forward_varlen(q, k, v, cu_seqlens_q,
     cu_seqlens_k, max_seqlen_q, causal) (``fa_bwd_varlen``; token-major
     [total, H, d] tensors, LSE [H, total_q]; max_seqlen_k a host int)."""
@@ -623,9 +699,15 @@ def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k,
     delta = torch.empty((total_q, H), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B, H,
-                       int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, d, v.shape[2],
-                       CAUSAL_MODES[causal], scale, dtype_code(q.dtype), stream)
+    if dropout_p > 0:
+        rc = fa_bwd_varlen_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q,
+                                   cu_seqlens_k, B, H, int(max_seqlen_q), int(max_seqlen_k),
+                                   total_q, total_k, d, v.shape[2], CAUSAL_MODES[causal], scale,
+                                   dropout_p, seed, offset, dtype_code(q.dtype), stream)
+    else:
+        rc = fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k,
+                           B, H, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, d,
+                           v.shape[2], CAUSAL_MODES[causal], scale, dtype_code(q.dtype), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_varlen")
     return dq, dk, dv
@@ -708,44 +790,45 @@ def _autograd():
 
     class _FlashAttentionKv(torch.autograd.Function):
         @staticmethod
-        def forward(ctx, q, k, v, causal, seqlens_k, scale):
+        def forward(ctx, q, k, v, causal, seqlens_k, scale, dropout_p, seed, offset):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-            o, lse = attention_forward_kv(q, k, v, causal=causal, seqlens_k=seqlens_k, scale=scale)
+            o, lse = attention_forward_kv(q, k, v, causal=causal, seqlens_k=seqlens_k, scale=scale,
+                                          dropout_p=dropout_p, seed=seed, offset=offset)
             ctx.save_for_backward(q, k, v, o, lse)
-            ctx.args = (causal, seqlens_k, scale)
+            ctx.args = (causal, seqlens_k, scale, dropout_p, seed, offset)
             ctx.mark_non_differentiable(lse)
             return o, lse
 
         @staticmethod
         def backward(ctx, do, _dlse):
             q, k, v, o, lse = ctx.saved_tensors
-            causal, seqlens_k, scale = ctx.args
-            if v.shape[3] != q.shape[3]:
-                raise NotImplementedError("the backward pass needs the value width equal to d")
+            causal, seqlens_k, scale, dropout_p, seed, offset = ctx.args
             g = attention_backward_kv(q, k, v, o, lse, do.contiguous(), causal=causal,
-                                      seqlens_k=seqlens_k, scale=scale)
-            return g[0], g[1], g[2], None, None, None
+                                      seqlens_k=seqlens_k, scale=scale, dropout_p=dropout_p,
+                                      seed=seed, offset=offset)
+            return g[0], g[1], g[2], None, None, None, None, None, None
 
     class _FlashAttentionVarlen(torch.autograd.Function):
         @staticmethod
-        def forward(ctx, q, k, v, cu_q, cu_k, max_q, max_k, causal, scale):
+        def forward(ctx, q, k, v, cu_q, cu_k, max_q, max_k, causal, scale, dropout_p, seed,
+                    offset):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
             o, lse = attention_forward_varlen(q, k, v, cu_q, cu_k, max_q, causal=causal,
-                                              scale=scale)
+                                              scale=scale, dropout_p=dropout_p, seed=seed,
+                                              offset=offset)
             ctx.save_for_backward(q, k, v, o, lse, cu_q, cu_k)
-            ctx.args = (max_q, max_k, causal, scale)
+            ctx.args = (max_q, max_k, causal, scale, dropout_p, seed, offset)
             ctx.mark_non_differentiable(lse)
             return o, lse
 
         @staticmethod
         def backward(ctx, do, _dlse):
             q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
-            max_q, max_k, causal, scale = ctx.args
-            if v.shape[2] != q.shape[2]:
-                raise NotImplementedError("the backward pass needs the value width equal to d")
+            max_q, max_k, causal, scale, dropout_p, seed, offset = ctx.args
             g = attention_backward_varlen(q, k, v, o, lse, do.contiguous(), cu_q, cu_k, max_q,
-                                          max_k, causal=causal, scale=scale)
-            return g[0], g[1], g[2], None, None, None, None, None, None
+                                          max_k, causal=causal, scale=scale, dropout_p=dropout_p,
+                                          seed=seed, offset=offset)
+            return g[0], g[1], g[2], None, None, None, None, None, None, None, None, None
 
     return _FlashAttention, _FlashAttentionKv, _FlashAttentionVarlen
 
@@ -770,19 +853,23 @@ def flash_attention(q, k, v, causal=False, scale=None, dropout_p=0.0, seed=0, of
                            int(offset))
 
 
-def flash_attention_kv(q, k, v, causal=None, seqlens_k=None, scale=None):
+def flash_attention_kv(q, k, v, causal=None, seqlens_k=None, scale=None, dropout_p=0.0, seed=0,
+                       offset=0):
     """Differentiable O, LSE of queries [B, H, Nq, d] against keys [B, H, Nk, d]
-    (fa_fwd_kv / fa_bwd_kv; the backward needs the value width equal to d)."""
+    and values [B, H, Nk, dv] (fa_fwd_kv / fa_bwd_kv, or their dropout forms
+    when dropout_p > 0)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
-    return _fns()[1].apply(q, k, v, causal, seqlens_k, float(scale))
+    return _fns()[1].apply(q, k, v, causal, seqlens_k, float(scale), float(dropout_p), int(seed),
+                           int(offset))
 
 
 def flash_attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                           causal=None, scale=None):
+                           causal=None, scale=None, dropout_p=0.0, seed=0, offset=0):
     """Differentiable O [total_q, H, dv], LSE [H, total_q] of a packed batch
-    (fa_fwd_varlen / fa_bwd_varlen)."""
+    (fa_fwd_varlen / fa_bwd_varlen, or their dropout forms when dropout_p > 0)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     return _fns()[2].apply(q, k, v, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q),
-                           int(max_seqlen_k), causal, float(scale))
+                           int(max_seqlen_k), causal, float(scale), float(dropout_p), int(seed),
+                           int(offset))

@@ -94,7 +94,10 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   set_dropout(&p, drop_t, seed, drop_off);
   const bool c = causal != 0;
   cudaError_t e;
-  if (kv)
+  if (kv && drop_t < 256)
+    e = (dk_max == 64) ? fa::launch_bwd_kv_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                       : fa::launch_bwd_kv_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  else if (kv)
     e = (dk_max == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
                        : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   else if (drop_t < 256)
@@ -121,11 +124,24 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const 
                   true, seqlens_k, scale, dtype, 256, 0, 0, stream);
 }
 
-int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, float* delta,
-                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
-                  int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
-                  int dv_width, int causal, float scale, int dtype, cudaStream_t stream) {
+int fa_bwd_kv_dropout(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      float* delta, int B, int H, int Nq, int Nk, int d, int dv_width, int causal,
+                      const int* seqlens_k, float scale, float dropout_p, unsigned long long seed,
+                      unsigned int offset, int dtype, cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, Nq, Nk, d, dv_width, causal,
+                  true, seqlens_k, scale, dtype, t, seed, offset, stream);
+}
+
+// fa_bwd_varlen, and fa_bwd_varlen_dropout when drop_t < 256.
+static int backward_varlen(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           float* delta, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                           int H, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                           int d, int dv_width, int causal, float scale, int dtype, int drop_t,
+                           unsigned long long seed, unsigned int drop_off, cudaStream_t stream) {
   if (B < 0 || H < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 ||
       d <= 0 || dv_width <= 0)
     return FA_ERR_SHAPE;
@@ -195,12 +211,40 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
   p.total_q = total_q;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  set_dropout(&p, 256, 0, 0);
+  set_dropout(&p, drop_t, seed, drop_off);
   const bool c = causal != 0;
-  const cudaError_t e = (dk_max == 64)
-                            ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
-                            : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  cudaError_t e;
+  if (drop_t < 256)
+    e = (dk_max == 64) ? fa::launch_bwd_kv_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                       : fa::launch_bwd_kv_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  else
+    e = (dk_max == 64) ? fa::launch_bwd_kv_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                       : fa::launch_bwd_kv_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* delta,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d,
+                  int dv_width, int causal, float scale, int dtype, cudaStream_t stream) {
+  return backward_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B,
+                         H, max_seqlen_q, max_seqlen_k, total_q, total_k, d, dv_width, causal,
+                         scale, dtype, 256, 0, 0, stream);
+}
+
+int fa_bwd_varlen_dropout(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          float* delta, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                          int H, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                          int d, int dv_width, int causal, float scale, float dropout_p,
+                          unsigned long long seed, unsigned int offset, int dtype,
+                          cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return backward_varlen(q, k, v, o, lse, dout, dq, dk, dv, delta, cu_seqlens_q, cu_seqlens_k, B,
+                         H, max_seqlen_q, max_seqlen_k, total_q, total_k, d, dv_width, causal,
+                         scale, dtype, t, seed, offset, stream);
 }
 
 int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -84,6 +84,14 @@ cudaError_t launch_bwd_drop_d64(const BwdParams& p, const void* o, const void* d
                                 bool bf16, bool causal, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_drop_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
                                  bool bf16, bool causal, int sms, cudaStream_t stream);
+// Queries against a key set of another length, or packed batches, with
+// dropout in the forward pass (the kKv, kDrop variants).
+cudaError_t launch_bwd_kv_drop_d64(const BwdParams& p, const void* o, const void* dout,
+                                   float* delta, bool bf16, bool causal, int sms,
+                                   cudaStream_t stream);
+cudaError_t launch_bwd_kv_drop_d128(const BwdParams& p, const void* o, const void* dout,
+                                    float* delta, bool bf16, bool causal, int sms,
+                                    cudaStream_t stream);
 // Queries against a key set of another length (the kKv variants).
 cudaError_t launch_bwd_kv_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
                               bool bf16, bool causal, int sms, cudaStream_t stream);

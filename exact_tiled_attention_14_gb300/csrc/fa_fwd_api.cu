@@ -419,6 +419,16 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
                     0, stream);
 }
 
+int fa_fwd_kv_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, int dv, int causal, const int* seqlens_k,
+                      float scale, float dropout_p, unsigned long long seed, unsigned int offset,
+                      int dtype, cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return forward_kv(q, k, v, o, lse, B, H, Nq, Nk, d, dv, causal, seqlens_k, scale, dtype, t, seed,
+                    offset, stream);
+}
+
 int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int H, int N, int d, int causal, float scale, float dropout_p,
                    unsigned long long seed, unsigned int offset, int dtype,
@@ -431,10 +441,12 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
                     offset, stream);
 }
 
-int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
-                  int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
-                  float scale, int dtype, cudaStream_t stream) {
+// fa_fwd_varlen, and fa_fwd_varlen_dropout when drop_t < 256.
+static int forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                          int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
+                          float scale, int dtype, int drop_t, unsigned long long seed,
+                          unsigned int drop_off, cudaStream_t stream) {
   if (B < 0 || H < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0 || d <= 0 || dv <= 0)
     return FA_ERR_SHAPE;
   if (causal < 0 || causal > 2) return FA_ERR_SHAPE;
@@ -501,12 +513,36 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   p.cu_k = cu_seqlens_k;
   p.varlen = 1;
   p.total_q = total_q;
-  set_dropout(&p, 256, 0, 0);
+  set_dropout(&p, drop_t, seed, drop_off);
   const int grid = p.num_units < info->sms ? p.num_units : info->sms;
   const bool w64 = d == 64 && dv == 64;
-  const cudaError_t e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
-                            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
+  cudaError_t e;
+  if (drop_t < 256)
+    e = w64 ? fa::launch_fwd_drop_d64(p, grid, bf16, causal != 0, stream)
+            : fa::launch_fwd_drop_d128(p, grid, bf16, causal != 0, stream);
+  else
+    e = w64 ? fa::launch_fwd_kv_d64(p, grid, bf16, causal != 0, stream)
+            : fa::launch_fwd_kv_d128(p, grid, bf16, causal != 0, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                  int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
+                  float scale, int dtype, cudaStream_t stream) {
+  return forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, total_q,
+                        total_k, d, dv, causal, scale, dtype, 256, 0, 0, stream);
+}
+
+int fa_fwd_varlen_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                          int max_seqlen_q, int total_q, int total_k, int d, int dv, int causal,
+                          float scale, float dropout_p, unsigned long long seed,
+                          unsigned int offset, int dtype, cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, total_q,
+                        total_k, d, dv, causal, scale, dtype, t, seed, offset, stream);
 }
 
 }  // extern "C"

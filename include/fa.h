@@ -16,9 +16,11 @@
  *    last round balanced through a caller's or the library's scratch),
  *    fa_fwd_kv (queries against a key set of another length, key counts,
  *    causal alignment, value width), fa_fwd_varlen (packed batches),
- *    fa_fwd_dropout (dropout on the attention weights);
- *  - backward: fa_bwd, fa_bwd_kv, fa_bwd_varlen, fa_bwd_dropout, each the
- *    gradient of the forward of the same name;
+ *    fa_fwd_dropout, fa_fwd_kv_dropout, fa_fwd_varlen_dropout (dropout on
+ *    the attention weights);
+ *  - backward: fa_bwd, fa_bwd_kv, fa_bwd_varlen, fa_bwd_dropout,
+ *    fa_bwd_kv_dropout, fa_bwd_varlen_dropout, each the gradient of the
+ *    forward of the same name;
  *  - decoding: fa_decode (a few queries against a long cache, key axis
  *    split across the GPU);
  *  - status and settings: fa_strerror, fa_status, fa_set_watchdog_ns,
@@ -402,6 +404,48 @@ int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
                    float *delta, int B, int H, int N, int d, int causal, float scale,
                    float dropout_p, unsigned long long seed, unsigned int offset, int dtype,
                    cudaStream_t stream);
+
+/*
+ * fa_fwd_kv_dropout, fa_fwd_varlen_dropout — fa_fwd_kv and fa_fwd_varlen with
+ * dropout on the attention weights, the mask drawn on the device from
+ * (seed, offset) as in fa_fwd_dropout ("Why FlashAttention Can Avoid a
+ * Square Attention Array Without Making Attention Linear", section
+ * "Backward can recreate tiles instead of retaining the square": the
+ * generator's state is kept so the backward pass regenerates the mask).
+ * Element (i, j) of a (batch, head) — with packed batches a (sequence,
+ * head) — is drawn by its query row i and key index j within that pair,
+ * whatever the causal alignment: the alignment only decides which keys a
+ * row sees.  dropout_p = 0 gives fa_fwd_kv's (fa_fwd_varlen's) result.
+ * Arguments and errors as those entry points plus dropout_p, seed, offset
+ * and FA_ERR_DROPOUT as in fa_fwd_dropout.
+ *
+ * fa_bwd_kv_dropout, fa_bwd_varlen_dropout — the matching backward passes
+ * (the same dropout_p, seed and offset as the forward call): arguments and
+ * errors as fa_bwd_kv and fa_bwd_varlen plus those three.
+ */
+int fa_fwd_kv_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int H, int Nq, int Nk, int d, int dv, int causal,
+                      const int *seqlens_k, float scale, float dropout_p,
+                      unsigned long long seed, unsigned int offset, int dtype,
+                      cudaStream_t stream);
+int fa_fwd_varlen_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                          const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                          int max_seqlen_q, int total_q, int total_k, int d, int dv,
+                          int causal, float scale, float dropout_p, unsigned long long seed,
+                          unsigned int offset, int dtype, cudaStream_t stream);
+int fa_bwd_kv_dropout(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                      float *delta, int B, int H, int Nq, int Nk, int d, int dv_width,
+                      int causal, const int *seqlens_k, float scale, float dropout_p,
+                      unsigned long long seed, unsigned int offset, int dtype,
+                      cudaStream_t stream);
+int fa_bwd_varlen_dropout(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                          float *delta, const int *cu_seqlens_q, const int *cu_seqlens_k,
+                          int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
+                          int total_k, int d, int dv_width, int causal, float scale,
+                          float dropout_p, unsigned long long seed, unsigned int offset,
+                          int dtype, cudaStream_t stream);
 
 /*
  * fa_decode — attention of a few new queries against a long key/value cache

@@ -126,3 +126,146 @@ def test_dropout_errors():
         fa.attention_forward_dropout(q, q, q, 1.0, 0, 0)
     with pytest.raises(fa.FaError):
         fa.attention_forward_dropout(q, q, q, -0.5, 0, 0)
+
+
+# ---------------------------------------------------------------- kv and packed batches
+
+KV_CASES = [
+    # B, H, Nq, Nk, d, dv, dtype, causal, seqlens, p
+    (2, 1, 200, 700, 64, 64, "bf16", "bottom_right", None, 0.2),      # a chunk after a cache
+    (3, 2, 256, 500, 128, 64, "fp16", None, [500, 130, 0], 0.1),       # padding, an empty batch
+    (1, 1, 300, 128, 64, 128, "bf16", "bottom_right", None, 0.3),     # Nq > Nk: empty rows
+    (2, 1, 333, 777, 128, 128, "fp16", "upper_left", [777, 400], 0.5),
+]
+
+
+def kv_ids(c):
+    return (f"B{c[0]}H{c[1]}q{c[2]}k{c[3]}d{c[4]}dv{c[5]}{c[6]}{c[7] or 'nc'}"
+            f"{'' if c[8] is None else 'pad'}p{c[9]}")
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,dtype,causal,seqlens,p", KV_CASES,
+                         ids=[kv_ids(c) for c in KV_CASES])
+def test_kv_dropout_vs_oracle(B, H, Nq, Nk, d, dv, dtype, causal, seqlens, p):
+    """fa_fwd_kv_dropout / fa_bwd_kv_dropout against the dropout oracle run per
+    (batch, head) on the batch's keys, each query at its row's position (the
+    mask indexed by row and key, the alignment moving only the causal
+    boundary); rows that see no key come back as O = 0, LSE = -inf, keys no
+    query sees as dK = dV = 0."""
+    seed, off = 4242 + Nq, 6
+    q, k, v = seeded_inputs.make_decode(B, H, Nq, Nk, d, dtype, seed=Nq + Nk + dv, dv=dv)
+    dout = seeded_inputs.make_dout(B, H, Nq, dv, dtype, seed=Nq + dv)
+    scale = default_scale(d)
+    dq_, dk_, dv_, do_ = (t.cuda() for t in (q, k, v, dout))
+    sl = None if seqlens is None else torch.tensor(seqlens, dtype=torch.int32, device="cuda")
+    o, lse = fa.attention_forward_kv(dq_, dk_, dv_, causal=causal, seqlens_k=sl, scale=scale,
+                                     dropout_p=p, seed=seed, offset=off)
+    gq, gk, gv = fa.attention_backward_kv(dq_, dk_, dv_, o, lse, do_, causal=causal, seqlens_k=sl,
+                                          scale=scale, dropout_p=p, seed=seed, offset=off)
+    torch.cuda.synchronize()
+    assert fa.fa_status()[0] == fa.FA_OK
+    o, lse, gq, gk, gv = (t.cpu() for t in (o, lse, gq, gk, gv))
+    s = 256.0 / oracle.dropout_threshold(p)
+    tmax, tmean = TOL[dtype]
+    rq, rk, rv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(B):
+        n = Nk if seqlens is None else max(0, min(seqlens[b], Nk))
+        shift = n - Nq if causal == "bottom_right" else 0
+        for h in range(H):
+            args = (q[b, h].double().numpy(), k[b, h, :n].double().numpy(),
+                    v[b, h, :n].double().numpy())
+            o_ref, l_ref = oracle.attention_dropout(*args, b * H + h, seed, off, p,
+                                                    causal=causal is not None, scale=scale,
+                                                    q_offset=shift)
+            ob, lb = o[b, h].double().numpy(), lse[b, h].double().numpy()
+            empty = np.isneginf(l_ref)
+            assert np.all(np.isneginf(lb[empty])) and np.all(ob[empty] == 0.0)
+            err = np.abs(ob[~empty] - o_ref[~empty])
+            if err.size:
+                assert err.max() <= tmax * s and err.mean() <= tmean * s, (b, h, err.max())
+                assert np.abs(lb[~empty] - l_ref[~empty]).max() <= LSE_TOL
+            gq_r, gk_r, gv_r = oracle.attention_dropout_grad(
+                *args, dout[b, h].double().numpy(), b * H + h, seed, off, p,
+                causal=causal is not None, scale=scale, q_offset=shift)
+            rq[b, h], rk[b, h, :n], rv[b, h, :n] = gq_r, gk_r, gv_r
+        assert torch.all(gk[b, :, n:] == 0) and torch.all(gv[b, :, n:] == 0)
+    name = kv_ids((B, H, Nq, Nk, d, dv, dtype, causal, seqlens, p))
+    check_grad(name + " dQ", gq, rq, dtype)
+    check_grad(name + " dK", gk, rk, dtype)
+    check_grad(name + " dV", gv, rv, dtype)
+
+
+VARLEN_CASES = [
+    # name, lens_q, lens_k, H, d, dv, dtype, causal, p
+    ("self_ul", [1, 127, 129, 300, 0, 517], [1, 127, 129, 300, 0, 517], 2, 64, 64, "bf16",
+     "upper_left", 0.2),
+    ("prefill_br", [64, 200, 1], [1000, 250, 3000], 2, 128, 64, "fp16", "bottom_right", 0.1),
+]
+
+
+@pytest.mark.parametrize("name,lens_q,lens_k,H,d,dv,dtype,causal,p", VARLEN_CASES,
+                         ids=[c[0] for c in VARLEN_CASES])
+def test_varlen_dropout_vs_oracle(name, lens_q, lens_k, H, d, dv, dtype, causal, p):
+    """fa_fwd_varlen_dropout / fa_bwd_varlen_dropout against the dropout oracle
+    run per (sequence, head), the mask of sequence b's head h drawn with
+    index b * H + h."""
+    seed, off = 31337, 2
+    q, k, v, cu_q, cu_k = seeded_inputs.make_varlen(lens_q, lens_k, H, d, dtype, seed=len(lens_q) + dv,
+                                                    dv=dv)
+    g = torch.Generator("cpu").manual_seed(len(lens_q) + d)
+    dout = torch.randn((q.shape[0], H, dv), generator=g).to(q.dtype)
+    scale = default_scale(d)
+    dq_, dk_, dv_, do_, cq, ck = (t.cuda() for t in (q, k, v, dout, cu_q, cu_k))
+    mq, mk = max(lens_q + [0]), max(lens_k + [0])
+    o, lse = fa.attention_forward_varlen(dq_, dk_, dv_, cq, ck, mq, causal=causal, scale=scale,
+                                         dropout_p=p, seed=seed, offset=off)
+    gq, gk, gv = fa.attention_backward_varlen(dq_, dk_, dv_, o, lse, do_, cq, ck, mq, mk,
+                                              causal=causal, scale=scale, dropout_p=p, seed=seed,
+                                              offset=off)
+    torch.cuda.synchronize()
+    assert fa.fa_status()[0] == fa.FA_OK
+    o, lse, gq, gk, gv = (t.cpu() for t in (o, lse, gq, gk, gv))
+    s = 256.0 / oracle.dropout_threshold(p)
+    tmax, tmean = TOL[dtype]
+    rq, rk, rv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    cq_l, ck_l = cu_q.tolist(), cu_k.tolist()
+    for b in range(len(lens_q)):
+        q0, q1, k0, k1 = cq_l[b], cq_l[b + 1], ck_l[b], ck_l[b + 1]
+        shift = (k1 - k0) - (q1 - q0) if causal == "bottom_right" else 0
+        for h in range(H):
+            if q1 == q0:
+                continue
+            args = (q[q0:q1, h].double().numpy(), k[k0:k1, h].double().numpy(),
+                    v[k0:k1, h].double().numpy())
+            o_ref, l_ref = oracle.attention_dropout(*args, b * H + h, seed, off, p,
+                                                    causal=causal is not None, scale=scale,
+                                                    q_offset=shift)
+            ob, lb = o[q0:q1, h].double().numpy(), lse[h, q0:q1].double().numpy()
+            empty = np.isneginf(l_ref)
+            assert np.all(np.isneginf(lb[empty])) and np.all(ob[empty] == 0.0)
+            err = np.abs(ob[~empty] - o_ref[~empty])
+            if err.size:
+                assert err.max() <= tmax * s and err.mean() <= tmean * s, (name, b, h, err.max())
+                assert np.abs(lb[~empty] - l_ref[~empty]).max() <= LSE_TOL
+            if k1 > k0:
+                gq_r, gk_r, gv_r = oracle.attention_dropout_grad(
+                    *args, dout[q0:q1, h].double().numpy(), b * H + h, seed, off, p,
+                    causal=causal is not None, scale=scale, q_offset=shift)
+                rq[q0:q1, h], rk[k0:k1, h], rv[k0:k1, h] = gq_r, gk_r, gv_r
+    check_grad(name + " dQ", gq, rq, dtype)
+    check_grad(name + " dK", gk, rk, dtype)
+    check_grad(name + " dV", gv, rv, dtype)
+
+
+def test_kv_dropout_zero_probability_is_fa_fwd_kv():
+    q, k, v = (t.cuda() for t in seeded_inputs.make_decode(2, 2, 200, 600, 64, "bf16", seed=5))
+    o1, l1 = fa.attention_forward_kv(q, k, v, causal="bottom_right")
+    o2, l2 = fa.attention_forward_kv(q, k, v, causal="bottom_right", dropout_p=0.0, seed=3, offset=1)
+    lib = fa.load_library()
+    o3 = torch.empty_like(o1)
+    l3 = torch.empty_like(l1)
+    assert fa.fa_fwd_kv_dropout(q, k, v, o3, l3, 2, 2, 200, 600, 64, 64, 2, None, 0.125, 0.0, 3, 1,
+                                fa.FA_BF16) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(o1, o3) and torch.equal(l1, l3)
+    assert lib is not None
