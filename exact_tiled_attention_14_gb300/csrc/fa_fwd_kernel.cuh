@@ -57,6 +57,14 @@ constexpr int kThreads = 384;         // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kPvWarp = 10;           // second MMA issuer (own-P layout only)
+// Dropout at d = 128 adds a fourth warpgroup (warps 12 .. 15) that draws the
+// mask of each key tile ahead of the softmax; at d = 64 (a shorter key step
+// than the generator's work) the softmax warps draw their own.
+constexpr int kGenWarp0 = 12;
+template <int D, bool kDrop>
+constexpr bool has_gen() { return kDrop && D == 128; }
+template <int D, bool kDrop>
+constexpr int threads_of() { return has_gen<D, kDrop>() ? 512 : kThreads; }
 // Registers per thread after the split: the launch gives every thread 168
 // (64512 per CTA); the issue warpgroup drops to 88 so the two softmax
 // warpgroups can hold a whole 128-column score row plus its packed P.
@@ -64,6 +72,13 @@ constexpr int kPvWarp = 10;           // second MMA issuer (own-P layout only)
 constexpr uint32_t kSoftmaxRegs = 208;
 constexpr uint32_t kIssueRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kIssueRegs <= 168 * kThreads, "register split");
+// With the mask generator, 512 threads launch with 128 registers each (65536
+// per CTA): softmax 200, issue 64, mask generator 48.
+constexpr uint32_t kSoftmaxRegsDrop = 200;
+constexpr uint32_t kIssueRegsDrop = 64;
+constexpr uint32_t kGenRegs = 48;
+static_assert(2 * 128 * kSoftmaxRegsDrop + 128 * kIssueRegsDrop + 128 * kGenRegs <= 128 * 512,
+              "register split with dropout");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTau = 8.0f;          // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.693147180559945309f;
@@ -71,7 +86,8 @@ constexpr float kLn2 = 0.693147180559945309f;
 // Sites recorded in the status word when a wait runs out.
 enum WaitSite : uint32_t {
   kSiteQEmpty = 1, kSiteKvEmpty = 2, kSiteQFull = 3, kSiteKvFull = 4, kSitePFull = 5,
-  kSiteOFree = 6, kSiteSFull = 7, kSiteSFree = 9, kSitePvDone = 10
+  kSiteOFree = 6, kSiteSFull = 7, kSiteSFree = 9, kSitePvDone = 10, kSiteMaskFull = 11,
+  kSiteMaskEmpty = 12
 };
 
 struct FwdParams {
@@ -211,26 +227,36 @@ struct OwnP {
 // Shared-memory plan.  At d = 128 the two output staging tiles would cost two
 // K/V ring stages (the ring then cannot cover L2 latency), so O is written
 // straight from registers; at d = 64 there is room for both, and O goes out
-// through a staging tile and a TMA store.
-template <int D>
+// through a staging tile and a TMA store.  With the dropout mask generator
+// (d = 128), each query tile's keep bits come over in a ring of kMaskStages
+// buffers of kMaskBytes (128 rows x 128 keys, one bit each); they take the
+// room of one K/V stage, and the ring keeps two (a key step with dropout
+// lasts several microseconds, longer than a tile's load).
+template <int D, bool kDrop = false>
 struct Smem {
+  static constexpr bool kGen = has_gen<D, kDrop>();
   static constexpr int kChunks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kTile = kBM * D * 2;          // one 128 x D tile of 16-bit values
   static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 128 bytes
   static constexpr bool kTmaStore = (D == 64);       // epilogue through smem + TMA store
   // K/V ring depth (at d = 128 with P in shared memory the two P tiles take
   // two of the five stages)
-  static constexpr int kStages = (D == 128) ? (OwnP<D>::kSmem ? 3 : 5) : 8;
+  static constexpr int kStages = (D == 128) ? (OwnP<D>::kSmem ? (kGen ? 2 : 3) : 5) : 8;
+  static constexpr int kMaskStages = 2;
+  static constexpr int kMaskBytes = kBM * kBN / 8;
   static constexpr int kQ = 0;                       // two query tiles
   static constexpr int kKV = kQ + 2 * kTile;         // ring of K or V tiles
   static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles (if any)
   static constexpr int kP = kO + (kTmaStore ? 2 * kTile : 0);   // two P tiles (if in smem)
-  static constexpr int kBar = kP + (OwnP<D>::kSmem ? 2 * kBM * kBN * 2 : 0);
-  // barrier indices
+  static constexpr int kMask = kP + (OwnP<D>::kSmem ? 2 * kBM * kBN * 2 : 0);  // mask rings
+  static constexpr int kBar = kMask + (kGen ? 2 * kMaskStages * kMaskBytes : 0);
+  // barrier indices (the mask barriers, [query tile][stage], only with the generator)
   static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
                        bSFull = 2 + 2 * kStages, bPFull = bSFull + 2,
                        bOFree = bPFull + 2, bSFree = bOFree + 2, bPvDone = bSFree + 2,
-                       bFinal = bPvDone + 2, bFinalPv = bFinal + 1, kNumBars = bFinalPv + 1;
+                       bFinal = bPvDone + 2, bFinalPv = bFinal + 1, bMaskFull = bFinalPv + 1,
+                       bMaskEmpty = bMaskFull + 2 * kMaskStages,
+                       kNumBars = kGen ? bMaskEmpty + 2 * kMaskStages : bFinalPv + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;  // tmem base, abort flag, 2 merge flags
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;       // slack to align the base to 1024
@@ -455,9 +481,9 @@ __device__ __forceinline__ size_t lse_at(const FwdParams& p, const Piece& u, int
 // and a causal alignment (see FwdParams); square calls compile none of it.
 // kDrop: dropout on the attention weights (with kKv on square shapes).
 template <int D, bool kBf16, bool kCausal, bool kSplit, bool kKv = false, bool kDrop = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, kDrop>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -492,6 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar(L::bFinal), 1);
     ptx::mbar_init(bar(L::bFinalPv), 1);
+    if constexpr (L::kGen) {
+      for (int i = 0; i < 2 * L::kMaskStages; ++i) {
+        ptx::mbar_init(bar(L::bMaskFull + i), 128);    // every generator thread
+        ptx::mbar_init(bar(L::bMaskEmpty + i), 128);   // every softmax thread of the tile
+      }
+    }
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
     ptx::prefetch_tmap(&p.tm_q);
@@ -507,8 +539,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grid = gridDim.x;
   const int cta = blockIdx.x;
   // Each role's code sits inside the branch that set its register budget.
-  if (warp >= 8) {
-  ptx::setmaxnreg_dec<kIssueRegs>();
+  bool gen_role = false;
+  if constexpr (L::kGen) gen_role = (warp >= kGenWarp0);
+  if (gen_role) {
+    ptx::setmaxnreg_dec<kGenRegs>();
+    if constexpr (L::kGen) {
+      // ============================================================ dropout mask generator
+      // Thread g draws, for every (query tile, key tile) the softmax will
+      // process, the words of lane g % 4 of row quad g / 4 (drop_words) and
+      // stores them at [lane][quad] of the tile's mask buffer; the softmax
+      // thread of row 4 * quad + r reads the quad's four words back.  The
+      // order (key tile, then query tile) is the order the issuers serve
+      // the two query tiles in, so neither softmax waits on masks the
+      // generator holds back for the other.
+      const int g = threadIdx.x - kGenWarp0 * 32;
+      const uint32_t quad = static_cast<uint32_t>(g) >> 2, kq = static_cast<uint32_t>(g) & 3u;
+      uint32_t mc0 = 0, mc1 = 0;    // masks produced for query tile 0 / 1
+      bool alive = true;
+      Cursor cu;
+      cursor_init<kSplit>(p, cta, grid, cu);
+      Piece u;
+      while (next_piece<kCausal, kSplit, kKv>(p, cta, grid, cu, u)) {
+        const int nkv = max(u.n0, u.n1);
+        for (int j = 0; j < nkv; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            if (j >= (w ? u.n1 : u.n0)) continue;
+            uint32_t& mc = w ? mc1 : mc0;
+            const uint32_t use = mc / L::kMaskStages;
+            const int bi = w * L::kMaskStages + static_cast<int>(mc % L::kMaskStages);
+            if (use > 0)
+              alive = ptx::wait_bounded(bar(L::bMaskEmpty + bi), (use - 1) & 1, wd,
+                                        kSiteMaskEmpty) && alive;
+            if (alive) {
+              const uint32_t qrow0 = static_cast<uint32_t>((2 * u.mblk + w) * kBM) + 4u * quad;
+              const uint4 words = drop_words(qrow0, static_cast<uint32_t>((u.kb + j) * kBN), kq,
+                                             u.bh, p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+              *reinterpret_cast<uint4*>(sgen + L::kMask + bi * L::kMaskBytes +
+                                        (kq * 32 + quad) * 16) = words;
+            }
+            ptx::mbar_arrive(bar(L::bMaskFull + bi));
+            ++mc;
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+  ptx::setmaxnreg_dec<L::kGen ? kIssueRegsDrop : kIssueRegs>();
   if (warp == kLoadWarp) {
     // ============================================================ TMA producer
     if (lane == 0) {
@@ -756,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
   } else {
-    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    ptx::setmaxnreg_inc<L::kGen ? kSoftmaxRegsDrop : kSoftmaxRegs>();
     // ============================================================ softmax + epilogue
     const int w = warp >> 2;                 // query tile of the unit
     const int t = threadIdx.x & 127;         // row within the tile = TMEM lane
@@ -768,10 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.scale_log2;
     uint32_t scnt = 0, ucnt = 0;
     uint32_t pvcnt = 0;                       // P.V products of this tile waited for
+    uint32_t mcnt = 0;                        // dropout masks of this tile consumed
     uint32_t tr = 0;                          // trace events recorded (thread t == 0)
     const bool tracer = (t == 0);
     Prof pf;   // FA_PROFILE: 0 s wait, 1 load S, 2 max + rescale, 3 exp/sum/pack, 4 store P + arrive,
-               // 5 o_done wait, 6 epilogue, 7 other, 8 tiles, 9 rescales
+               // 5 o_done wait, 6 epilogue, 7 other, 8 tiles, 9 rescales, 16 P.V-done wait,
+               // 18 dropout mask wait, 19 dropout mask load and apply
 
     Cursor cu;
     cursor_init<kSplit>(p, cta, grid, cu);
@@ -904,9 +982,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (kDrop) {
           // dropout: the weights of dropped keys leave P (l keeps them: the
-          // normalisation is the softmax's); 256 / t is applied with 1 / l
-          drop_row128(pk, static_cast<uint32_t>(row), static_cast<uint32_t>(kj * kBN), u.bh,
-                      p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+          // normalisation is the softmax's); 256 / t is applied with 1 / l.
+          pf.lap(3);
+          if constexpr (L::kGen) {
+            // the keep bits of this tile come from the generator's ring
+            const int bi = w * L::kMaskStages + static_cast<int>(mcnt % L::kMaskStages);
+            ptx::wait_bounded(bar(L::bMaskFull + bi), (mcnt / L::kMaskStages) & 1, wd,
+                              kSiteMaskFull);
+            pf.lap(18);
+            ++mcnt;
+            const uint8_t* mrow = sgen + L::kMask + bi * L::kMaskBytes + (t >> 2) * 16;
+            uint4 yq[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2)
+              yq[k2] = *reinterpret_cast<const uint4*>(mrow + k2 * 512);
+            ptx::mbar_arrive(bar(L::bMaskEmpty + bi));   // the buffer may be refilled
+            drop_apply(pk, yq, static_cast<uint32_t>(t & 3));
+          } else {
+            drop_row128(pk, static_cast<uint32_t>(row), static_cast<uint32_t>(kj * kBN), u.bh,
+                        p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+          }
+          pf.lap(19);
         }
         pf.lap(3);
         // P_w and O_w are still in use by PV_w_{j-1} until it completes.

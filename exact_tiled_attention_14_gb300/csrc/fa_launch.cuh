@@ -20,11 +20,12 @@ cudaError_t launch_variant(const FwdParams& p, int grid, cudaStream_t stream) {
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
     e = cudaFuncSetAttribute(fa_fwd_kernel<D, kBf16, kCausal, kSplit, kKv, kDrop>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kAlloc);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D, kDrop>::kAlloc);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  fa_fwd_kernel<D, kBf16, kCausal, kSplit, kKv, kDrop><<<grid, kThreads, Smem<D>::kAlloc, stream>>>(p);
+  fa_fwd_kernel<D, kBf16, kCausal, kSplit, kKv, kDrop><<<grid, threads_of<D, kDrop>(), Smem<D, kDrop>::kAlloc,
+                                                         stream>>>(p);
   return cudaGetLastError();
 }
 
