@@ -244,15 +244,20 @@ struct Smem {
   static constexpr int kStages = (D == 128) ? (OwnP<D>::kSmem ? (kGen ? 2 : 3) : 5) : 8;
   static constexpr int kMaskStages = 2;
   static constexpr int kMaskBytes = kBM * kBN / 8;
-  static constexpr int kQ = 0;                       // two query tiles
-  static constexpr int kKV = kQ + 2 * kTile;         // ring of K or V tiles
+  // Q buffers (two query tiles each): at d = 64 two, so a unit's Q tiles
+  // load while the previous unit still runs (units of a few key tiles
+  // otherwise waited for them); at d = 128 one (no room).
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;
+  static constexpr int kQ = 0;
+  static constexpr int kKV = kQ + kQBufs * 2 * kTile;   // ring of K or V tiles
   static constexpr int kO = kKV + kStages * kTile;   // two output staging tiles (if any)
   static constexpr int kP = kO + (kTmaStore ? 2 * kTile : 0);   // two P tiles (if in smem)
   static constexpr int kMask = kP + (OwnP<D>::kSmem ? 2 * kBM * kBN * 2 : 0);  // mask rings
   static constexpr int kBar = kMask + (kGen ? 2 * kMaskStages * kMaskBytes : 0);
   // barrier indices (the mask barriers, [query tile][stage], only with the generator)
-  static constexpr int bQFull = 0, bQEmpty = 1, bKvFull = 2, bKvEmpty = 2 + kStages,
-                       bSFull = 2 + 2 * kStages, bPFull = bSFull + 2,
+  static constexpr int bQFull = 0, bQEmpty = kQBufs, bKvFull = 2 * kQBufs,
+                       bKvEmpty = bKvFull + kStages, bSFull = bKvFull + 2 * kStages,
+                       bPFull = bSFull + 2,
                        bOFree = bPFull + 2, bSFree = bOFree + 2, bPvDone = bSFree + 2,
                        bFinal = bPvDone + 2, bFinalPv = bFinal + 1, bMaskFull = bFinalPv + 1,
                        bMaskEmpty = bMaskFull + 2 * kMaskStages,
@@ -503,8 +508,10 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
   }
   if (threadIdx.x == kLoadWarp * 32) {
     *abort_flag = 0;
-    ptx::mbar_init(bar(L::bQFull), 1);
-    ptx::mbar_init(bar(L::bQEmpty), 1);
+    for (int qb = 0; qb < L::kQBufs; ++qb) {
+      ptx::mbar_init(bar(L::bQFull + qb), 1);
+      ptx::mbar_init(bar(L::bQEmpty + qb), 1);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(L::bKvFull + s), 1);
       ptx::mbar_init(bar(L::bKvEmpty + s), 1);
@@ -603,20 +610,22 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
         // piece's last S MMA has read it; the first K tile does not wait for
         // that, so it is requested first.
         auto load_q = [&]() {
-          if (k_units > 0)
-            alive = ptx::wait_bounded(bar(L::bQEmpty), (k_units - 1) & 1, wd, kSiteQEmpty) && alive;
+          const uint32_t qb = k_units % L::kQBufs, quse = k_units / L::kQBufs;
+          if (quse > 0)
+            alive = ptx::wait_bounded(bar(L::bQEmpty + qb), (quse - 1) & 1, wd, kSiteQEmpty) &&
+                    alive;
           if (alive) {
             const int ntile = u.n1 > 0 ? 2 : 1;
             // kKv with d < D: only the chunks of Q's own columns are loaded
             // (the S products never read the others)
             const int qc = kKv ? p.dqk / 64 : L::kChunks;
-            ptx::mbar_arrive_expect_tx(bar(L::bQFull), ntile * qc * L::kChunkBytes);
+            ptx::mbar_arrive_expect_tx(bar(L::bQFull + qb), ntile * qc * L::kChunkBytes);
             for (int w = 0; w < ntile; ++w) {
               int y = (2 * u.mblk + w) * kBM, z = u.bh;      // row, batch*head
               if (kKv && p.varlen) { z = u.q0 + y; y = u.bh % p.H; }   // head, token
               for (int c = 0; c < qc; ++c)
-                ptx::tma_load_3d(sbase + L::kQ + w * L::kTile + c * L::kChunkBytes, &p.tm_q,
-                                 bar(L::bQFull), c * 64, y, z);
+                ptx::tma_load_3d(sbase + L::kQ + (qb * 2 + w) * L::kTile + c * L::kChunkBytes,
+                                 &p.tm_q, bar(L::bQFull + qb), c * 64, y, z);
             }
             q_issued = k_units + 1;
             trace_event(p, 3, tr, kEvLoadQ, k_units);
@@ -656,7 +665,8 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
       const uint32_t first = loads > (uint32_t)L::kStages ? loads - L::kStages : 0;
       for (uint32_t l = first; l < loads; ++l)
         ptx::wait_drain(bar(L::bKvFull + l % L::kStages), (l / L::kStages) & 1, drain);
-      if (q_issued > 0) ptx::wait_drain(bar(L::bQFull), (q_issued - 1) & 1, drain);
+      for (uint32_t q = q_issued > (uint32_t)L::kQBufs ? q_issued - L::kQBufs : 0; q < q_issued; ++q)
+        ptx::wait_drain(bar(L::bQFull + q % L::kQBufs), (q / L::kQBufs) & 1, drain);
     }
     __syncwarp();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -732,6 +742,7 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
       const uint32_t tP1 = OwnP<D>::kSmem ? ptx::desc_lo(sbase + L::kP + kBM * kBN * 2, 16)
                                           : tmem_base + p_col<D>(1);
       uint32_t sc0 = 0, sc1 = 0;     // S issued into S0 / S1 so far
+      uint32_t q_add = 0;            // address-word offset of the current unit's Q buffer
       auto issue_s_own = [&](int w, uint32_t kslot_) {
         uint32_t& sc = w ? sc1 : sc0;
         pf.lap(6);
@@ -740,7 +751,7 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
         pf.lap(16);
         ptx::tc_fence_after();
         if (alive) {
-          issue_s(w ? tS1 : tS0, w ? q_lo1 : q_lo0, k_lo0 + kslot_ * kSlotLo);
+          issue_s(w ? tS1 : tS0, (w ? q_lo1 : q_lo0) + q_add, k_lo0 + kslot_ * kSlotLo);
           ptx::mma_commit(bar(L::bSFull + w));
         }
         ++sc;
@@ -784,7 +795,10 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
           const int nkv = max(u.n0, u.n1);
           if (kKv && nkv == 0) continue;
           pf.lap(6);
-          alive = ptx::wait_bounded(bar(L::bQFull), k_units & 1, wd, kSiteQFull) && alive;
+          const uint32_t qb = k_units % L::kQBufs;
+          alive = ptx::wait_bounded(bar(L::bQFull + qb), (k_units / L::kQBufs) & 1, wd, kSiteQFull) &&
+                  alive;
+          q_add = qb * static_cast<uint32_t>((2 * L::kTile) >> 4);
           pf.lap(2);
           ptx::tc_fence_after();
           for (int j = 0; j < nkv; ++j) {
@@ -793,7 +807,7 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
             if (j < u.n1) issue_s_own(1, kslot);
             if (alive) {
               ptx::mma_commit(bar(L::bKvEmpty + kslot));
-              if (j + 1 == nkv) ptx::mma_commit(bar(L::bQEmpty));  // last use of Q
+              if (j + 1 == nkv) ptx::mma_commit(bar(L::bQEmpty + qb));  // last use of Q
             }
             issued_any = true;
           }
