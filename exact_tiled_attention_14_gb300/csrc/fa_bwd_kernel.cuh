@@ -625,19 +625,35 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         for (int e = 0; e < 64; ++e)
           if (i * kBwdTile + half * 64 + e < key) pf[e] = 0.f;
       }
-      // dropout: keep bits of this key against the thread's 64 queries; the
-      // dV product reads P with the dropped weights zeroed
-      uint64_t zb = ~0ull;
-      if constexpr (kDrop)
-        zb = keep_col_quad64(static_cast<uint32_t>(key),
-                             static_cast<uint32_t>(i * kBwdTile + half * 64),
-                             static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t);
+      // dropout: keep bits of this key against the thread's 64 queries, from
+      // the quad's words (zw[2 k2 + m]: word m of lane k2, blocks 8m + 4h + k2
+      // of 4 queries each); the dV product reads P with the dropped weights
+      // zeroed
+      uint32_t zw[8];
+      const uint32_t csel = 0x4440u + (static_cast<uint32_t>(lane) & 3u);   // this key's byte
+      if constexpr (kDrop) {
+        const uint2 mine = drop_words16<true>(static_cast<uint32_t>(key >> 2),
+                                              static_cast<uint32_t>(i * kBwdTile + half * 64) >> 2,
+                                              static_cast<uint32_t>(lane) & 3u,
+                                              static_cast<uint32_t>(bh), p.drop_off, p.drop_k0,
+                                              p.drop_k1, p.drop_t);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int src = (lane & ~3) | k2;
+          zw[2 * k2] = __shfl_sync(0xffffffffu, mine.x, src);
+          zw[2 * k2 + 1] = __shfl_sync(0xffffffffu, mine.y, src);
+        }
+      }
+      // query bits of block b (queries 4b .. 4b + 3 of the thread's 64)
+      auto zq = [&](int b) -> uint32_t {
+        return col_query_bits(zw[2 * (b & 3) + (b >> 3)], csel, (b >> 2) & 1);
+      };
       {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
-          if constexpr (kDrop) pk[e] &= pair_mask(zb, 2 * e);
+          if constexpr (kDrop) pk[e] &= prmt(zq(e >> 1), 0u, (e & 1) ? 0xBBAAu : 0x9988u);
         }
         ptx::tmem_st16(tS, pk);          // over S^T columns this warp has read
         ptx::tmem_st16(tS + 16, pk + 16);
@@ -660,19 +676,25 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         for (int e = 0; e < 32; e += 4) {
           const float4 dd = dl4[(ch * 32 + e) / 4];
           const int f = ch * 32 + e;
-          // dP^T, with dropout Z dP^T 256 / t
+          // dP^T, with dropout Z dP^T (the 256 / t joins in the subtraction of D)
+          uint32_t zx = 0;
+          if constexpr (kDrop) zx = zq(f >> 2);   // f is a multiple of 4: one block
           auto dpv = [&](int x) -> float {
-            const float v = __uint_as_float(dpr[e + x]);
-            if constexpr (kDrop) return ((zb >> (f + x)) & 1ull) ? v * p.drop_scale : 0.f;
-            return v;
+            if constexpr (kDrop)
+              return __uint_as_float(dpr[e + x] & prmt(zx, 0u, 0x8888u + 0x1111u * x));
+            return __uint_as_float(dpr[e + x]);
+          };
+          auto dmd = [&](float a, float b, float da, float db) -> uint64_t {
+            if constexpr (kDrop)
+              return ptx::ffma2(ptx::f2_pack(a, b), ptx::f2_pack(p.drop_scale, p.drop_scale),
+                                ptx::f2_pack(-da, -db));
+            return ptx::fadd2(ptx::f2_pack(a, b), ptx::f2_pack(-da, -db));
           };
           float d0, d1, d2, d3;
-          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f], pf[f + 1]),
-                                    ptx::fadd2(ptx::f2_pack(dpv(0), dpv(1)),
-                                               ptx::f2_pack(-dd.x, -dd.y))), d0, d1);
+          ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f], pf[f + 1]), dmd(dpv(0), dpv(1), dd.x, dd.y)),
+                         d0, d1);
           ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[f + 2], pf[f + 3]),
-                                    ptx::fadd2(ptx::f2_pack(dpv(2), dpv(3)),
-                                               ptx::f2_pack(-dd.z, -dd.w))), d2, d3);
+                                    dmd(dpv(2), dpv(3), dd.z, dd.w)), d2, d3);
           dk[f / 2] = ptx::pack2<kBf16>(d0, d1);
           dk[f / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
         }
@@ -861,13 +883,22 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       ptx::mbar_arrive(xbar(X::kSFree));     // S and dP may be overwritten now
-      // dropout: keep bits of this query against the thread's 64 keys
-      uint64_t zb = ~0ull;
+      // dropout: keep bits of this query against the thread's 64 keys, from
+      // the quad's words (zw[2 k2 + m]: word m of lane k2, blocks 8m + 4h + k2
+      // of 4 keys each)
+      uint32_t zw[8];
       if constexpr (kDrop) {
-        uint64_t kb[1];
-        keep_row_quad<16>(static_cast<uint32_t>(qrow), static_cast<uint32_t>(j * kBwdTile + half * 64),
-                          static_cast<uint32_t>(bh), p.drop_off, p.drop_k0, p.drop_k1, p.drop_t, kb);
-        zb = kb[0];
+        const uint2 mine = drop_words16<false>(static_cast<uint32_t>(j * kBwdTile + half * 64) >> 2,
+                                               static_cast<uint32_t>(qrow >> 2),
+                                               static_cast<uint32_t>(lane) & 3u,
+                                               static_cast<uint32_t>(bh), p.drop_off, p.drop_k0,
+                                               p.drop_k1, p.drop_t);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int src = (lane & ~3) | k2;
+          zw[2 * k2] = __shfl_sync(0xffffffffu, mine.x, src);
+          zw[2 * k2 + 1] = __shfl_sync(0xffffffffu, mine.y, src);
+        }
       }
       uint32_t dk[32];
 #pragma unroll
@@ -879,13 +910,18 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
         if (kc >= lim) p0 = 0.f;
         if (kc + 1 >= lim) p1 = 0.f;
         float g0 = __uint_as_float(dpr[kc]), g1 = __uint_as_float(dpr[kc + 1]);
-        if constexpr (kDrop) {   // Z dP 256 / t
-          g0 = ((zb >> kc) & 1ull) ? g0 * p.drop_scale : 0.f;
-          g1 = ((zb >> (kc + 1)) & 1ull) ? g1 * p.drop_scale : 0.f;
+        uint64_t gd;
+        if constexpr (kDrop) {   // Z dP 256 / t - D
+          const int b = kc >> 2;                       // block of keys 4b .. 4b + 3
+          const uint32_t y = zw[2 * (b & 3) + (b >> 3)], r = static_cast<uint32_t>(qrow) & 3u;
+          g0 = __uint_as_float(dpr[kc] & row_key_mask(y, r, (b >> 2) & 1, kc & 3));
+          g1 = __uint_as_float(dpr[kc + 1] & row_key_mask(y, r, (b >> 2) & 1, (kc + 1) & 3));
+          gd = ptx::ffma2(ptx::f2_pack(g0, g1), ptx::f2_pack(p.drop_scale, p.drop_scale), ndl2);
+        } else {
+          gd = ptx::fadd2(ptx::f2_pack(g0, g1), ndl2);
         }
         float d0, d1;
-        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1), ptx::fadd2(ptx::f2_pack(g0, g1), ndl2)),
-                       d0, d1);
+        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(p0, p1), gd), d0, d1);
         dk[kc / 2] = ptx::pack2<kBf16>(d0, d1);
       }
       // dS to its TMEM buffer once the tensor core has read what it held

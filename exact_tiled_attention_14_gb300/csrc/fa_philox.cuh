@@ -13,7 +13,7 @@
 // seed.  Element (i, j) takes byte j % 4 of output word i % 4 and is kept
 // when that byte is below t = round((1 - p) * 256); kept weights are scaled
 // by 256 / t.  A quad of lanes shares the calls of a block row (or block
-// column); see keep_row_quad.
+// column); see drop_words and drop_words16.
 #pragma once
 
 #include <cstdint>
@@ -44,68 +44,6 @@ __host__ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, ui
   return c;
 }
 
-// Word `sel` (0..3) of a call's output.
-__device__ __forceinline__ uint32_t philox_word(const uint4& r, uint32_t sel) {
-  return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
-}
-
-// Keep bits of the four bytes of w (bit b for byte b), 1 <= t <= 255, given
-// c4 = (256 - t) in every byte (t = 256 keeps everything and never reaches
-// the kernels that draw a mask): byte < t exactly when byte + (256 - t) does not carry out of
-// the byte.  The low seven bits are added without reaching the next byte;
-// a byte's carry out is then the majority of its top bit, the complement's
-// top bit and the carry into bit 7, and one multiply gathers the four top
-// bits (7, 15, 23, 31 -> 28 .. 31; the other partial products stay below
-// bit 28 and never overlap, so nothing carries into them).
-__host__ __device__ __forceinline__ uint32_t keep_bits4_swar(uint32_t w, uint32_t c4) {
-  const uint32_t lo = (w & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
-  const uint32_t carry = (w & c4) | ((w ^ c4) & lo);
-  const uint32_t keep = ~carry & 0x80808080u;
-  return (keep * 0x00204081u) >> 28;
-}
-
-// Keep bits of a whole 4 x 4 block: bit 4 w + c for row w, column c.
-__device__ __forceinline__ uint32_t keep16(const uint4& r, uint32_t c4) {
-  return keep_bits4_swar(r.x, c4) | (keep_bits4_swar(r.y, c4) << 4) |
-         (keep_bits4_swar(r.z, c4) << 8) | (keep_bits4_swar(r.w, c4) << 12);
-}
-
-// The same masks with the generator work shared by a quad of lanes (lanes
-// 4m .. 4m+3 hold four consecutive rows, or columns, of one block row, or
-// block column): lane k of the quad draws the blocks b = k, k + 4, ...,
-// two blocks' 16 bits per register, and the quad exchanges the registers
-// with broadcast shuffles; every lane then keeps its own row's (column's)
-// bits.  NB blocks (NB / 4 calls per lane).  All 32 lanes must call it.
-//
-// Row walk: bit 4 b + c of `out` (NB = 16 fills one word, 32 two) is key
-// key0 + 4 b + c of query row qrow.
-template <int NB>
-__device__ __forceinline__ void keep_row_quad(uint32_t qrow, uint32_t key0, uint32_t bh,
-                                              uint32_t off, uint32_t k0, uint32_t k1, uint32_t t,
-                                              uint64_t (&out)[NB / 16]) {
-  const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, r = qrow & 3u;
-  const uint32_t c4 = (256u - t) * 0x01010101u;
-  uint32_t v[NB / 8];
-#pragma unroll
-  for (int a = 0; a < NB / 4; ++a) {
-    const uint4 w = philox4x32_10(make_uint4((key0 >> 2) + 4u * a + k, qrow >> 2, bh, off), k0, k1);
-    const uint32_t bits = keep16(w, c4);
-    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
-  }
-#pragma unroll
-  for (int i = 0; i < NB / 16; ++i) out[i] = 0;
-#pragma unroll
-  for (int k2 = 0; k2 < 4; ++k2) {
-#pragma unroll
-    for (int m = 0; m < NB / 8; ++m) {
-      const uint32_t y = __shfl_sync(0xffffffffu, v[m], (lane & ~3u) | k2);
-      const int b0 = 4 * (2 * m) + k2, b1 = b0 + 4;   // blocks of the two halves
-      out[b0 / 16] |= static_cast<uint64_t>((y >> (4 * r)) & 0xFu) << (4 * (b0 % 16));
-      out[b1 / 16] |= static_cast<uint64_t>((y >> (16 + 4 * r)) & 0xFu) << (4 * (b1 % 16));
-    }
-  }
-}
-
 // prmt.b32 in its default mode: each selector nibble picks a byte of
 // {b, a} (low three bits) and, with its top bit set, replicates that byte's
 // sign bit over all eight bits instead of copying it.  The host form spells
@@ -133,9 +71,12 @@ __host__ __device__ __forceinline__ uint32_t sel_bits(uint32_t m, uint32_t a, ui
   return (a & m) | (b & ~m);
 }
 
-// Bit 7 of byte c of the result is set when byte c of w is kept (below t),
-// given c4 = (256 - t) in every byte: the no-carry-out test of
-// keep_bits4_swar, left unmasked (the other bits are not meaningful).
+// Bit 7 of byte c of the result is set when byte c of w is kept (below t,
+// 1 <= t <= 255), given c4 = (256 - t) in every byte: byte < t exactly when
+// byte + (256 - t) does not carry out of the byte.  The low seven bits are
+// added without reaching the next byte, and the carry out of bit 7 is the
+// majority of the byte's top bit, the complement's top bit and the carry
+// into bit 7.  The other bits of the result are not meaningful.
 __host__ __device__ __forceinline__ uint32_t keep_top(uint32_t w, uint32_t c4) {
   const uint32_t lo = (w & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
   return ~((w & c4) | ((w ^ c4) & lo));
@@ -228,42 +169,47 @@ __device__ __forceinline__ void drop_row128(uint32_t (&pk)[64], uint32_t qrow, u
   }
 }
 
-// Column walk over 64 queries: bit 4 b + w of the result is query
-// q0 + 4 b + w against key column `key`.
-__device__ __forceinline__ uint64_t keep_col_quad64(uint32_t key, uint32_t q0, uint32_t bh,
-                                                    uint32_t off, uint32_t k0, uint32_t k1,
-                                                    uint32_t t) {
-  const uint32_t lane = threadIdx.x & 31u, k = lane & 3u, c = key & 3u;
+// The backward pass walks 64 keys of a query row (dQ pass) or 64 queries of
+// a key column (dK/dV pass) per thread and tile, sixteen 4 x 4 blocks.
+// drop_words16: the two words lane k (0 .. 3) of a quad draws for those
+// blocks: blocks k, k + 4, k + 8, k + 12 of the walk, word m holding blocks
+// 8m + k (bits 7 .. 4 of each byte) and 8m + 4 + k (bits 3 .. 0), laid out
+// by key (keep_by_key).  Row walk (kCol = false): block i is (key block
+// kb0 + i, query block qb0) and the quad's lanes are the block row's four
+// queries; column walk (kCol = true): block i is (kb0, qb0 + i) and the
+// quad's lanes are the block column's four keys.
+template <bool kCol>
+__host__ __device__ __forceinline__ uint2 drop_words16(uint32_t kb0, uint32_t qb0, uint32_t k,
+                                                       uint32_t bh, uint32_t off, uint32_t k0,
+                                                       uint32_t k1, uint32_t t) {
   const uint32_t c4 = (256u - t) * 0x01010101u;
-  uint32_t v[2];
+  uint32_t w[2];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const uint4 w = philox4x32_10(make_uint4(key >> 2, (q0 >> 2) + 4u * a + k, bh, off), k0, k1);
-    const uint32_t bits = keep16(w, c4);
-    if (a & 1) v[a >> 1] |= bits << 16; else v[a >> 1] = bits;
+  for (int m = 0; m < 2; ++m) {
+    const uint32_t i0 = 8u * m + k, i1 = i0 + 4u;
+    const uint4 ra = philox4x32_10(kCol ? make_uint4(kb0, qb0 + i0, bh, off)
+                                        : make_uint4(kb0 + i0, qb0, bh, off), k0, k1);
+    const uint4 rb = philox4x32_10(kCol ? make_uint4(kb0, qb0 + i1, bh, off)
+                                        : make_uint4(kb0 + i1, qb0, bh, off), k0, k1);
+    w[m] = sel_bits(0xF0F0F0F0u, keep_by_key(ra, c4), keep_by_key(rb, c4) >> 4);
   }
-  uint64_t out = 0;
-  // column c of a block's 16 bits (bits c, 4 + c, 8 + c, 12 + c) as a nibble
-  auto col = [&](uint32_t h) -> uint32_t {
-    const uint32_t x = (h >> c) & 0x1111u;
-    return (x | (x >> 3) | (x >> 6) | (x >> 9)) & 0xFu;
-  };
-#pragma unroll
-  for (int k2 = 0; k2 < 4; ++k2) {
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const uint32_t y = __shfl_sync(0xffffffffu, v[m], (lane & ~3u) | k2);
-      const int b0 = 4 * (2 * m) + k2, b1 = b0 + 4;
-      out |= static_cast<uint64_t>(col(y & 0xFFFFu)) << (4 * b0);
-      out |= static_cast<uint64_t>(col(y >> 16)) << (4 * b1);
-    }
-  }
-  return out;
+  return make_uint2(w[0], w[1]);
 }
 
-// The 16-bit pair mask of keep bits b0 (low half) and b1 (high half).
-__device__ __forceinline__ uint32_t pair_mask(uint64_t bits, int e) {
-  return (((bits >> e) & 1ull) ? 0x0000FFFFu : 0u) | (((bits >> (e + 1)) & 1ull) ? 0xFFFF0000u : 0u);
+// Row walk: with y the word holding block 8m + 4h + k2 (word m of quad
+// lane k2), the mask (all ones or zero) of key c (0 .. 3) of that block for
+// query row r (0 .. 3) of the quad.
+__host__ __device__ __forceinline__ uint32_t row_key_mask(uint32_t y, uint32_t r, int h, int c) {
+  return prmt(y << (r + 4u * static_cast<uint32_t>(h)), 0u, 0x8888u + 0x1111u * c);
+}
+
+// Column walk: with y as above and csel = 0x4440 + c for key column c of
+// the quad, a word whose byte r has its top bit set when query r of the
+// block is kept (byte c of y moved to byte 0, then one multiply sends bit
+// 7 - r, or 3 - r for the block in the low nibbles, to bit 8r + 7; the
+// partial products fall on distinct bits, so nothing carries).
+__host__ __device__ __forceinline__ uint32_t col_query_bits(uint32_t y, uint32_t csel, int h) {
+  return prmt(y, 0u, csel) * (h ? 0x80402010u : 0x08040201u);
 }
 
 }  // namespace fa
