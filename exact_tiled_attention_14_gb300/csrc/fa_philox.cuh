@@ -124,8 +124,8 @@ __host__ __device__ __forceinline__ uint4 drop_words(uint32_t qrow0, uint32_t ke
 // r (0 .. 3) in it.  One shift brings row r's bit of each key to the top of
 // the key's byte, and two byte permutes with sign replication turn those
 // top bits into the 0x0000FFFF / 0xFFFF0000 halves of pk[2b] and
-// pk[2b + 1] for block b.  The result is the same as applying
-// keep_row_quad<32>'s bits pair by pair.
+// pk[2b + 1] for block b: each 16-bit half of pk is cleared exactly when
+// its key's byte is not below t.
 __host__ __device__ __forceinline__ void drop_apply(uint32_t (&pk)[64], const uint4 (&y)[4], uint32_t r) {
 #pragma unroll
   for (int k2 = 0; k2 < 4; ++k2) {
