@@ -183,6 +183,34 @@ def measured_peaks():
         return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
 
 
+def dtype_peak_check(device):
+    """cuBLAS dense-GEMM rates of fp16 and bf16 at 8192^3 on this GPU (a few
+    timed products each, after a warm-up): fp16 workloads take the measured
+    bf16 peak times the nominal fp16/bf16 ratio of 1, and this probe, run
+    after the timed region, shows that ratio on the box."""
+    import torch
+    out = {}
+    n = 8192
+    for name, dt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        g = torch.Generator(device=device).manual_seed(7)
+        a = torch.randn(n, n, device=device, dtype=dt, generator=g)
+        b = torch.randn(n, n, device=device, dtype=dt, generator=g)
+        for _ in range(3):
+            torch.matmul(a, b)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        s.record()
+        for _ in range(10):
+            torch.matmul(a, b)
+        e.record()
+        torch.cuda.synchronize(device)
+        out[name + "_tflops"] = 10 * 2.0 * n ** 3 / (s.elapsed_time(e) * 1e-3) / 1e12
+        del a, b
+    out["fp16_over_bf16"] = out["fp16_tflops"] / out["bf16_tflops"]
+    out["probe"] = "torch.matmul 8192^3, 10 products after 3 warm-up, cuBLAS, outside the timed region"
+    return out
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -744,6 +772,12 @@ def run_ours(args, w):
     value = world * flops * args.steps * passes / (total_ms * 1e-3) / 1e12
     achieved = flops / (kern_ms_max * 1e-3) / 1e12
     peak, peak_sustained, peak_src = measured_peaks()
+    peak_src = f"{peak_src} bf16 burst"
+    dtype_check = None
+    if w["dtype"] == "fp16":
+        dtype_check = dtype_peak_check(device)
+        peak_src += (" x the nominal fp16/bf16 dense ratio 1 (cuBLAS probe in this run: "
+                     f"{dtype_check['fp16_over_bf16']:.3f})")
     traffic, traffic_note = stored_traffic(w["name"])
     io = io_bytes(w)
     line = {
@@ -764,7 +798,7 @@ def run_ours(args, w):
                           f"{' > L2' if replicas * per_replica > L2_BYTES else ', < L2: launch-bound size'})")
                    if replicas > 1 else "inputs larger than L2"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac": achieved / peak, "peak_source": peak_src, "dtype_peak_check": dtype_check,
                      "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
                      "kernel_ms": kern_ms_max, "flops_per_launch": flops,
                      "traffic": traffic,
