@@ -90,6 +90,13 @@ def test_work_tiles_match_printed_table(lib):
 FAKE = 0x10000  # 16-byte aligned, never dereferenced (errors are returned first)
 
 
+def no_gpu():
+    """Calls that pass every host check reach the device next; with FAKE
+    pointers they are only made where there is no GPU to launch on."""
+    import torch
+    return not torch.cuda.is_available()
+
+
 @pytest.mark.parametrize("args,code", [
     (dict(B=-1), fa.FA_ERR_SHAPE),
     (dict(N=-5), fa.FA_ERR_SHAPE),
@@ -213,8 +220,9 @@ def test_fwd_kv_host_errors(lib):
     for args, code in cases:
         assert fa.fa_fwd_kv(**{**call, **args}) == code, args
     # without keys, k and v may be NULL: the next check is the device's
-    rc = fa.fa_fwd_kv(**{**call, "Nk": 0, "k": None, "v": None})
-    assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
+    if no_gpu():
+        rc = fa.fa_fwd_kv(**{**call, "Nk": 0, "k": None, "v": None})
+        assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
 
 
 def test_fwd_varlen_host_errors(lib):
@@ -235,8 +243,9 @@ def test_fwd_varlen_host_errors(lib):
              (dict(total_q=2 ** 30, H=4), fa.FA_ERR_SHAPE)]
     for args, code in cases:
         assert fa.fa_fwd_varlen(**{**call, **args}) == code, args
-    rc = fa.fa_fwd_varlen(**{**call, "total_k": 0, "k": None, "v": None})
-    assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
+    if no_gpu():
+        rc = fa.fa_fwd_varlen(**{**call, "total_k": 0, "k": None, "v": None})
+        assert rc in (fa.FA_ERR_DEVICE, fa.FA_OK), rc
 
 
 def test_unit_group_setter(lib):
@@ -290,7 +299,8 @@ def test_bwd_kv_host_errors(lib):
     # ones may be NULL: the next check is the device's
     for args in (dict(Nk=0, k=None, v=None, dk=None, dv=None),
                  dict(Nq=0, q=None, o=None, dout=None, dq=None, lse=None, delta=None)):
-        assert fa.fa_bwd_kv(**{**call, **args}) in (fa.FA_ERR_DEVICE, fa.FA_OK), args
+        if no_gpu():
+            assert fa.fa_bwd_kv(**{**call, **args}) in (fa.FA_ERR_DEVICE, fa.FA_OK), args
     # the square entry point keeps its causal contract (0 or 1)
     C = ctypes
     assert lib.fa_bwd(*([FAKE] * 10), 1, 2, 256, 64, 2, C.c_float(0.125), fa.FA_BF16,
@@ -313,7 +323,8 @@ def test_bwd_varlen_host_errors(lib):
              (dict(delta=FAKE + 2), fa.FA_ERR_ALIGN), (dict(k=FAKE + 8), fa.FA_ERR_ALIGN)]
     for args, code in cases:
         assert fa.fa_bwd_varlen(**{**call, **args}) == code, args
-    assert fa.fa_bwd_varlen(**call) in (fa.FA_ERR_DEVICE, fa.FA_OK)
+    if no_gpu():
+        assert fa.fa_bwd_varlen(**call) in (fa.FA_ERR_DEVICE, fa.FA_OK)
 
 
 def test_watchdog_selftest_host_errors(lib):
@@ -322,3 +333,38 @@ def test_watchdog_selftest_host_errors(lib):
     import torch
     if not torch.cuda.is_available():
         assert fa.fa_watchdog_selftest(1000) == fa.FA_ERR_DEVICE
+
+
+def test_kv_varlen_dropout_host_errors(lib):
+    """The dropout forms of the kv and packed-batch entry points check the
+    dropout probability first, then the arguments of their plain forms, and
+    only then reach the device."""
+    kv = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=2, H=4, Nq=300, Nk=5000, d=128, dv=64,
+              causal=2, seqlens_k=None, scale=0.1, dropout_p=0.2, seed=3, offset=1,
+              dtype=fa.FA_BF16)
+    vl = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, B=3,
+              H=4, max_seqlen_q=500, total_q=900, total_k=2000, d=64, dv=128, causal=1, scale=0.1,
+              dropout_p=0.2, seed=3, offset=1, dtype=fa.FA_FP16)
+    bkv = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+               delta=FAKE, B=2, H=3, Nq=300, Nk=900, d=128, dv_width=64, causal=2, seqlens_k=None,
+               scale=0.1, dropout_p=0.2, seed=3, offset=1, dtype=fa.FA_BF16)
+    bvl = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+               delta=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, B=3, H=4, max_seqlen_q=500,
+               max_seqlen_k=2000, total_q=900, total_k=2000, d=64, dv_width=128, causal=1,
+               scale=0.1, dropout_p=0.2, seed=3, offset=1, dtype=fa.FA_FP16)
+    for fn, base, bad_shape in [(fa.fa_fwd_kv_dropout, kv, dict(causal=3)),
+                                (fa.fa_fwd_varlen_dropout, vl, dict(causal=7)),
+                                (fa.fa_bwd_kv_dropout, bkv, dict(causal=3)),
+                                (fa.fa_bwd_varlen_dropout, bvl, dict(causal=7))]:
+        for args, code in [(dict(dropout_p=1.0), fa.FA_ERR_DROPOUT),
+                           (dict(dropout_p=-0.5), fa.FA_ERR_DROPOUT),
+                           (dict(dropout_p=float("nan")), fa.FA_ERR_DROPOUT),
+                           (dict(dropout_p=0.999, d=96), fa.FA_ERR_DROPOUT),
+                           (dict(d=96), fa.FA_ERR_UNSUPPORTED_D), (bad_shape, fa.FA_ERR_SHAPE),
+                           (dict(dtype=9), fa.FA_ERR_DTYPE), (dict(scale=0.0), fa.FA_ERR_SCALE),
+                           (dict(o=None), fa.FA_ERR_NULLPTR), (dict(B=0), fa.FA_OK)]:
+            assert fn(**{**base, **args}) == code, (fn.__name__, args)
+        # p = 0 and p > 0 both pass the host checks; the next check is the device's
+        if no_gpu():
+            for p_ in (0.0, 0.25):
+                assert fn(**{**base, "dropout_p": p_}) in (fa.FA_ERR_DEVICE, fa.FA_OK), fn.__name__
