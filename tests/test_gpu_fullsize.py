@@ -15,8 +15,9 @@ it": the exact float64 reference, at sizes where the result matters).
   512 units;
 * queries against a longer key set: fa_fwd_kv / fa_bwd_kv on the benched
   prefill chunk (B4 H32, 2048 queries after 14336 cached keys, d128 bf16,
-  bottom-right) and the forward on the padded batch (B16 H16, 1024 queries,
-  up to 2048 keys with seeded counts, d64 bf16);
+  bottom-right), also with dropout (fa_fwd_kv_dropout / fa_bwd_kv_dropout,
+  p = 0.1), and the forward on the padded batch (B16 H16, 1024 queries, up
+  to 2048 keys with seeded counts, d64 bf16);
 * packed batches: fa_fwd_varlen / fa_bwd_varlen on the benched batch of 16
   sequences of 256 .. 4096 tokens (H16 d128 bf16, causal).
 
@@ -212,6 +213,45 @@ def test_kv_backward_full_size():
         check_grad(what + " dQ", gq[b, h], rq, w["dtype"])
         check_grad(what + " dK", gk[b, h][keys], rk, w["dtype"])
         check_grad(what + " dV", gv[b, h][keys], rv, w["dtype"])
+
+
+def test_kv_dropout_full_size():
+    """fa_fwd_kv_dropout / fa_bwd_kv_dropout on the benched prefill chunk at
+    p = 0.1 (the d = 128 mask generator warpgroup over 1024 units): O, LSE,
+    dQ, dK and dV of the first and last (batch, head), each query at its
+    position after the cache, the mask drawn by (batch * head, row, key)."""
+    w = seeded_inputs.kv_workload(seeded_inputs.KV_WORKLOADS[0]["name"])
+    B, H, Nq, Nk = w["B"], w["H"], w["Nq"], w["Nk"]
+    q, k, v, seqlens = kv_inputs(w)
+    assert seqlens is None
+    p, seed, off = 0.1, 2024, 7
+    dout = seeded_inputs.make_dout(B, H, Nq, w["d"], w["dtype"], seed=w["seed"] + 1)
+    dq_, dk_, dv_, do_ = (t.cuda() for t in (q, k, v, dout))
+    o, lse = fa.attention_forward_kv(dq_, dk_, dv_, causal=w["causal"], scale=w["scale"],
+                                     dropout_p=p, seed=seed, offset=off)
+    gq, gk, gv = fa.attention_backward_kv(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
+                                          scale=w["scale"], dropout_p=p, seed=seed, offset=off)
+    status_ok()
+    o, lse = o.cpu().double().numpy(), lse.cpu().double().numpy()
+    gq, gk, gv = gq.cpu(), gk.cpu(), gv.cpu()
+    shift = kv_offset(w, Nk)
+    heads = [(0, 0), (B - 1, H - 1)]
+
+    def ref(bh):
+        b, h = bh
+        args = (q[b, h].double().numpy(), k[b, h].double().numpy(), v[b, h].double().numpy())
+        fwd = oracle.attention_dropout(*args, b * H + h, seed, off, p, causal=True,
+                                       scale=w["scale"], q_offset=shift)
+        grad = oracle.attention_dropout_grad(*args, dout[b, h].double().numpy(), b * H + h, seed,
+                                             off, p, causal=True, scale=w["scale"], q_offset=shift)
+        return fwd, grad
+    s = 256.0 / oracle.dropout_threshold(p)
+    for (b, h), ((o_ref, l_ref), (rq, rk, rv)) in zip(heads, pmap(ref, heads)):
+        what = f"{w['name']} p={p} ({b},{h})"
+        check_rows(o[b, h], lse[b, h], o_ref, l_ref, w["dtype"], what, o_scale=s)
+        check_grad(what + " dQ", gq[b, h], rq, w["dtype"])
+        check_grad(what + " dK", gk[b, h], rk, w["dtype"])
+        check_grad(what + " dV", gv[b, h], rv, w["dtype"])
 
 
 # ---------------------------------------------------------------- packed batches
