@@ -49,6 +49,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dro
            "fa_fwd_kv_dropout", "fa_fwd_varlen_dropout", "fa_bwd_kv_dropout",
            "fa_bwd_varlen_dropout",
            "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
+           "fa_bwd_onepass", "fa_bwd_onepass_workspace_size",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
            "fa_version")
@@ -90,6 +91,10 @@ def load_library(path=None):
     lib.fa_fwd_static.restype = i
     lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_onepass.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_onepass.restype = i
+    lib.fa_bwd_onepass_workspace_size.argtypes = [i] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_bwd_onepass_workspace_size.restype = i
     u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
     lib.fa_fwd_dropout.argtypes = [vp] * 5 + [i, i, i, i, i, f, f, u64, u32, i, vp]
     lib.fa_fwd_dropout.restype = i
@@ -291,6 +296,26 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, 
     return lib.fa_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout), _addr(dq),
                       _addr(dk), _addr(dv), _addr(delta), int(B), int(H), int(N), int(d),
                       int(bool(causal)), float(scale), int(dtype), _stream(stream))
+
+
+def fa_bwd_onepass(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, dtype,
+                   workspace, workspace_bytes, stream=None):
+    """Raw C call of the one-pass backward; tensors or integer addresses; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_onepass(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dout),
+                              _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
+                              int(N), int(d), int(bool(causal)), float(scale), int(dtype),
+                              _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_onepass_workspace_size(B, H, N, d):
+    """Bytes of the fp32 dQ sum fa_bwd_onepass needs for this shape."""
+    out = ctypes.c_size_t(0)
+    code = load_library().fa_bwd_onepass_workspace_size(int(B), int(H), int(N), int(d),
+                                                        ctypes.byref(out))
+    if code:
+        raise FaError(code, "fa_bwd_onepass_workspace_size")
+    return out.value
 
 
 def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
@@ -561,6 +586,42 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=N
     rc = fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, code, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def attention_backward_onepass(q, k, v, o, lse, dout, causal=False, scale=None, workspace=None,
+                               stream=None):
+    """The gradients of ``attention_backward`` through ``fa_bwd_onepass``:
+    each (query tile, key tile) pair is visited once and dQ is summed in
+    fp32 through ``workspace`` (a CUDA tensor of at least
+    ``fa_bwd_onepass_workspace_size`` bytes; allocated here when None).  dQ
+    may differ in its last bits from call to call; dK and dV do not."""
+    import torch
+    ts = (q, k, v, o, dout)
+    if any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, o, dout must all be [B, H, N, d] of one shape")
+    if lse.dtype != torch.float32 or lse.shape != q.shape[:3]:
+        raise ValueError("lse must be float32 [B, H, N]")
+    if not all(t.is_cuda and t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    code = dtype_code(q.dtype)
+    need = fa_bwd_onepass_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fa_bwd_onepass(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, code,
+                        workspace, ws_bytes, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_onepass")
     return dq, dk, dv
 
 

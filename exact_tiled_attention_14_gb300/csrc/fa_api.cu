@@ -17,14 +17,23 @@ using namespace fa::host;
 
 extern "C" {
 
-// fa_bwd, fa_bwd_dropout when drop_t < 256, and fa_bwd_kv when kv (Nq
-// queries against Nk keys with per-batch key counts; causal 2 bottom-right;
-// values of width dv_width, which only kv calls may set apart from d).
+// Bytes of the one-pass backward's fp32 dQ accumulator: [B*H, d, N rounded
+// up to whole 128-row tiles].
+static long long onepass_acc_bytes(long long bh, long long n, int d) {
+  const long long pad = (n + fa::kBwdTile - 1) / fa::kBwdTile * fa::kBwdTile;
+  return bh * d * pad * static_cast<long long>(sizeof(float));
+}
+
+// fa_bwd, fa_bwd_dropout when drop_t < 256, fa_bwd_kv when kv (Nq queries
+// against Nk keys with per-batch key counts; causal 2 bottom-right; values
+// of width dv_width, which only kv calls may set apart from d), and
+// fa_bwd_onepass when `one` (square calls; ws holds the dQ accumulator).
 static int backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                     const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
                     int Nq, int Nk, int d, int dv_width, int causal, bool kv,
                     const int* seqlens_k, float scale, int dtype, int drop_t,
-                    unsigned long long seed, unsigned int drop_off, cudaStream_t stream) {
+                    unsigned long long seed, unsigned int drop_off, cudaStream_t stream,
+                    bool one = false, void* ws = nullptr, size_t ws_bytes = 0) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || dv_width <= 0) return FA_ERR_SHAPE;
   if (causal < 0 || causal > (kv ? 2 : 1)) return FA_ERR_SHAPE;
   const long long bh = static_cast<long long>(B) * H;
@@ -45,6 +54,15 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta) |
                        reinterpret_cast<uintptr_t>(seqlens_k);
   if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
+  if (one) {
+    // the dQ conversion runs one block per (batch*head, 32 queries)
+    if (bh * ((static_cast<long long>(Nq) + 31) / 32) > INT_MAX ||
+        n_qtiles * fa::kBwdTile > INT_MAX)
+      return FA_ERR_SHAPE;
+    if (!ws || ws_bytes < static_cast<size_t>(onepass_acc_bytes(bh, Nq, d)))
+      return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 15u) return FA_ERR_ALIGN;
+  }
 
   int dev = 0;
   const DeviceInfo* info = device_info(&dev);
@@ -92,9 +110,14 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   set_dropout(&p, drop_t, seed, drop_off);
+  p.dq_acc = static_cast<float*>(ws);
+  p.dq_pad = static_cast<int>(n_qtiles * fa::kBwdTile);
   const bool c = causal != 0;
   cudaError_t e;
-  if (kv && drop_t < 256)
+  if (one)
+    e = (d == 64) ? fa::launch_bwd_onepass_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+                  : fa::launch_bwd_onepass_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  else if (kv && drop_t < 256)
     e = (dk_max == 64) ? fa::launch_bwd_kv_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
                        : fa::launch_bwd_kv_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   else if (kv)
@@ -114,6 +137,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int d, int causal, float scale, int dtype, cudaStream_t stream) {
   return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
                   nullptr, scale, dtype, 256, 0, 0, stream);
+}
+
+int fa_bwd_onepass_workspace_size(int B, int H, int N, int d, size_t* bytes) {
+  if (!bytes) return FA_ERR_NULLPTR;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  *bytes = static_cast<size_t>(onepass_acc_bytes(static_cast<long long>(B) * H, N, d));
+  return FA_OK;
+}
+
+int fa_bwd_onepass(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int H,
+                   int N, int d, int causal, float scale, int dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
+                  nullptr, scale, dtype, 256, 0, 0, stream, true, workspace, workspace_bytes);
 }
 
 int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -212,6 +251,8 @@ static int backward_varlen(const void* q, const void* k, const void* v, const vo
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   set_dropout(&p, drop_t, seed, drop_off);
+  p.dq_acc = nullptr;
+  p.dq_pad = 0;
   const bool c = causal != 0;
   cudaError_t e;
   if (drop_t < 256)

@@ -71,7 +71,7 @@ constexpr uint32_t kBwdTmemCols = 512;
 enum BwdWaitSite : uint32_t {
   kSiteBwdEmpty = 20, kSiteBwdRes = 21, kSiteBwdFull = 22, kSiteBwdSFull = 23,
   kSiteBwdPFull = 24, kSiteBwdDone = 25, kSiteBwdDpFull = 26, kSiteBwdDsReady = 27,
-  kSiteBwdDsFree = 28, kSiteBwdSFree = 29
+  kSiteBwdDsFree = 28, kSiteBwdSFree = 29, kSiteBwdDqFull = 32, kSiteBwdDqFree = 33
 };
 
 struct BwdParams {
@@ -128,6 +128,14 @@ struct BwdParams {
   const int* cu_k;
   int varlen;
   int total_q;
+  // One-pass kernel (kOne): dQ is accumulated, unscaled, in fp32 in blocks
+  // of 32 queries x 32 columns: block (bh, query tile qt, column block cb,
+  // row quarter rq) holds element (column cc, row rr) at
+  // dq_acc[((((bh * n_tiles + qt) * (width_qk / 32) + cb) * 4 + rq) * 32 + cc) * 32 + rr]
+  // (dq_pad = n_tiles * 128 rows per head).  Zeroed before the launch and
+  // converted to dQ by fa_bwd_dq_convert_kernel afterwards.
+  float* dq_acc;
+  int dq_pad;
 };
 
 // Where head bh's rows sit in a kKv call: its key count len and query
@@ -172,24 +180,30 @@ __device__ __forceinline__ long long bwd_lse_at(const BwdParams& p, bool tok, co
 }
 
 // Shared memory of the two tensor-core kernels: the resident pair of tiles
-// (K_j, V_j or Q_i, dO_i), ring A and ring B of streamed tiles, kVecBytes of
-// per-query vectors (dkdv: -LSE in log2 units and D of the current query
-// tile), the ring barriers and eight kernel-specific barriers.
-template <int D, int kVecBytes>
+// (K_j, V_j or Q_i, dO_i), ring A and ring B of streamed tiles, in the
+// one-pass dK/dV/dQ kernel (kOne) a 128 x 128 tile of dS and a 4 KB dQ
+// staging block per element-wise warp, kVecBytes of per-query vectors
+// (dkdv: -LSE in log2 units and D of the current query tile), the ring
+// barriers and ten kernel-specific barriers.  The dS tile and the staging
+// blocks take the room of ring stages.
+template <int D, int kVecBytes, bool kOne = false>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kBwdTile * D * 2;
   static constexpr int kChunkBytes = kBwdTile * 128;
-  static constexpr int kStagesA = (D == 128) ? 3 : 6;
-  static constexpr int kStagesB = (D == 128) ? 2 : 4;
+  static constexpr int kStagesA = (D == 128) ? (kOne ? 2 : 3) : (kOne ? 4 : 6);
+  static constexpr int kStagesB = (D == 128) ? (kOne ? 1 : 2) : (kOne ? 3 : 4);
   static constexpr int kRes = 0;
   static constexpr int kRingA = kRes + 2 * kTile;
   static constexpr int kRingB = kRingA + kStagesA * kTile;
-  static constexpr int kVec = kRingB + kStagesB * kTile;
+  static constexpr int kDs = kRingB + kStagesB * kTile;   // 1024-aligned like the tiles
+  static constexpr int kStg = kDs + (kOne ? kBwdTile * kBwdTile * 2 : 0);
+  static constexpr int kStgWarpBytes = 32 * 32 * 4;      // one 32 x 32 fp32 block
+  static constexpr int kVec = kStg + (kOne ? 8 * kStgWarpBytes : 0);
   static constexpr int kBar = kVec + kVecBytes;
   static constexpr int bFullA = 0, bEmptyA = kStagesA, bFullB = 2 * kStagesA,
                        bEmptyB = bFullB + kStagesB, bRes = bEmptyB + kStagesB, bX = bRes + 1,
-                       kNumBars = bX + 8;
+                       kNumBars = bX + 10;
   static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -199,6 +213,7 @@ struct BwdSmem {
 // Kernel-specific barriers (offsets from bX).
 struct DkdvBars {
   static constexpr int kSFull = 0, kDpFull = 1, kPReady = 2, kDsReady = 3, kDone = 4;
+  static constexpr int kDqFull = 5, kDqFree = 7;   // one-pass kernel: two each (per dQ buffer)
 };
 struct DqBars {
   static constexpr int kSFull = 0, kSFree = 1, kPFull = 2, kDsFree = 4, kDone = 6;   // PFull, DsFree: 2 each
@@ -243,6 +258,37 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const uint4* __restri
   }
 }
 
+// ---------------------------------------------------------------- dQ = scale * accumulator
+// The one-pass kernel leaves dQ unscaled in fp32 in 32 x 32 blocks, column
+// by column within a block (BwdParams::dq_acc).  Each CTA moves 32 query
+// rows of one head through shared memory and writes them row by row in the
+// storage dtype, scaled.  Blocks: bh * ceil(N / 32) + query block.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                                uint32_t* __restrict__ dq,
+                                                                int N, int W, int pad,
+                                                                float scale) {
+  __shared__ float tile[128][33];
+  const int nqb = (N + 31) / 32;
+  const int bh = blockIdx.x / nqb;
+  const int q0 = (blockIdx.x - bh * nqb) * 32;
+  const int lane = threadIdx.x & 31, row8 = threadIdx.x >> 5;
+  const int n_tiles = pad / kBwdTile, qt = q0 / kBwdTile, rq = (q0 % kBwdTile) / 32;
+  for (int c = row8; c < W; c += 8) {
+    const long long blk =
+        ((static_cast<long long>(bh) * n_tiles + qt) * (W / 32) + c / 32) * 4 + rq;
+    tile[c][lane] = acc[(blk * 32 + c % 32) * 32 + lane];
+  }
+  __syncthreads();
+  const int pairs = W / 2;
+  for (int idx = threadIdx.x; idx < 32 * pairs; idx += 256) {
+    const int r = idx / pairs, cp = idx - r * pairs;
+    if (q0 + r < N)
+      dq[(static_cast<long long>(bh) * N + q0 + r) * pairs + cp] =
+          ptx::pack2<kBf16>(tile[2 * cp][r] * scale, tile[2 * cp + 1][r] * scale);
+  }
+}
+
 // ---------------------------------------------------------------- shared pieces
 // TMEM columns.
 constexpr uint32_t kColS = 0, kColDp = 128, kColAcc = 256;
@@ -274,6 +320,62 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
                 kk > 0 ? 1u : acc);
   }
 }
+
+// Issue A (K-major, shared memory, 128 rows x 128 along K in two 64-column
+// chunks) x B (MN-major tile of 128 rows along K) into d_tmem.
+template <int Chunk>
+__device__ __forceinline__ void issue_smem_a(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t idesc, uint32_t acc) {
+#pragma unroll
+  for (int kk = 0; kk < kBwdTile / 16; ++kk) {
+    const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * Chunk + (kk & 3) * 32) >> 4;
+    ptx::mma_ss(d_tmem, ptx::desc_sw128(a_lo + aoff), ptx::desc_sw128(b_lo + kk * (2048 >> 4)),
+                idesc, kk > 0 ? 1u : acc);
+  }
+}
+
+// Issue A x B with both operands MN-major in shared memory (128 rows along
+// K each, 16 rows = 2 KB per K step) into a fresh accumulator at d_tmem.
+__device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kBwdTile / 16; ++kk)
+    ptx::mma_ss(d_tmem, ptx::desc_sw128(a_lo + kk * (2048 >> 4)),
+                ptx::desc_sw128(b_lo + kk * (2048 >> 4)), idesc, kk > 0 ? 1u : 0u);
+}
+
+// Instruction-descriptor bit that marks A as MN-major (kind::f16).
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+
+// Element-wise fp32 addition of `bytes` (a multiple of 16) of shared memory
+// into global memory by the TMA engine, in this thread's bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(gdst),
+      "r"(ssrc), "r"(bytes)
+      : "memory");
+}
+// Wait until this thread's bulk groups have finished reading shared memory
+// (the source may be overwritten), or have completed entirely.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// One-pass kernel: TMEM column of dQ buffer b.  At d = 128 TMEM holds S^T,
+// dP^T, dV and dK (512 columns), so the single dQ buffer takes the dP^T
+// columns once the element-wise warps have read them; at d = 64 two
+// buffers of 64 columns follow dV and dK.
+template <int D>
+struct DqBuf {
+  static constexpr int kBufs = (D == 128) ? 1 : 2;
+  static __device__ __forceinline__ uint32_t col(int b) {
+    return D == 128 ? kColDp : kColAcc + 2u * D + 64u * b;
+  }
+};
 
 // Write columns [c0, c0 + nc) (nc a multiple of 32) of one row of a TMEM
 // accumulator (fp32), times `mul`, to global memory in the storage dtype, in
@@ -407,11 +509,18 @@ struct DkdvVec {
   static constexpr int kBytes = kBufs * 2 * kBwdTile * 4;
 };
 
-// One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
-template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
+// One CTA of the dK/dV pass: block `blk` of BH * n_tiles.  With kOne it
+// also forms dQ_i = dS K_j for every query tile it visits and adds it, in
+// fp32, into p.dq_acc (five tile products per (i, j) instead of seven): dS
+// goes to a shared-memory tile that serves as A of both dK (K-major: keys
+// x queries) and dQ (MN-major: queries x keys), and a third element-wise
+// phase reads dQ_i from TMEM and adds it to global memory.
+template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv, bool kOne = false>
 __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32_t tmem_base) {
-  using L = BwdSmem<D, DkdvVec<D>::kBytes>;
+  using L = BwdSmem<D, DkdvVec<D>::kBytes, kOne>;
   using X = DkdvBars;
+  using Q = DqBuf<D>;
+  static_assert(!(kOne && kKv), "the one-pass kernel covers square calls");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -466,6 +575,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
     ptx::mbar_init(b(L::bX + X::kPReady), kBwdEwThreads);
     ptx::mbar_init(b(L::bX + X::kDsReady), kBwdEwThreads);
     ptx::mbar_init(b(L::bX + X::kDone), 1);
+    if constexpr (kOne) {
+      for (int q = 0; q < Q::kBufs; ++q) {
+        ptx::mbar_init(b(L::bX + X::kDqFull + q), 1);
+        ptx::mbar_init(b(L::bX + X::kDqFree + q), kBwdEwThreads);
+      }
+    }
   });
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
@@ -491,6 +606,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       const uint32_t do_mn0 = ptx::desc_lo(sbase + L::kRingB, L::kChunkBytes);
       const uint32_t tS = tmem_base + kColS, tDp = tmem_base + kColDp;
       const uint32_t tDv = tmem_base + kColAcc, tDk = tmem_base + kColAcc + D;
+      // one-pass kernel: dS in shared memory as K-major A of dK and MN-major
+      // A of dQ, K_j as MN-major B of dQ
+      const uint32_t ds_k = ptx::desc_lo(sbase + L::kDs, 16);
+      const uint32_t ds_mn = ptx::desc_lo(sbase + L::kDs, L::kChunkBytes);
+      const uint32_t k_mn = ptx::desc_lo(sbase + L::kRes, L::kChunkBytes);
+      const uint32_t idesc_dq = idesc_dk | kIdescAMnMajor;
       auto full_a = [&](int it) {
         return ptx::wait_bounded(bar(L::bFullA + it % L::kStagesA), (it / L::kStagesA) & 1, wd,
                                  kSiteBwdFull);
@@ -535,14 +656,41 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         alive = ptx::wait_bounded(xbar(X::kDsReady), it & 1, wd, kSiteBwdDsReady);
         ptx::tc_fence_after();
         if (!alive) break;
-        // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
-        issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk, it > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
-        if (more) {
-          alive = full_b(it + 1);
-          ptx::tc_fence_after();
-          if (!alive) break;
-          issue_dp(it + 1);  // after dK: dS^T has been read
+        if constexpr (kOne) {
+          // dK_j += dS^T Q_i from the shared-memory dS tile
+          issue_smem_a<L::kChunkBytes>(tDk, ds_k, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk,
+                                       it > 0 ? 1u : 0u);
+          ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
+          // dQ_i = dS K_j into a dQ buffer the element-wise warps have emptied
+          // (with one buffer, the dP^T columns: read before dS was ready)
+          const int b = it % Q::kBufs;
+          if (Q::kBufs > 1 && it >= Q::kBufs) {
+            alive = ptx::wait_bounded(xbar(X::kDqFree + b), ((it / Q::kBufs) - 1) & 1, wd,
+                                      kSiteBwdDqFree);
+            ptx::tc_fence_after();
+            if (!alive) break;
+          }
+          issue_mn_mn(tmem_base + Q::col(b), ds_mn, k_mn, idesc_dq);
+          ptx::mma_commit(xbar(X::kDqFull + b));
+          if (more) {
+            alive = full_b(it + 1);
+            if (Q::kBufs == 1)   // dP^T_{i+1} overwrites dQ_i: wait until it is read
+              alive = alive && ptx::wait_bounded(xbar(X::kDqFree), it & 1, wd, kSiteBwdDqFree);
+            ptx::tc_fence_after();
+            if (!alive) break;
+            issue_dp(it + 1);
+          }
+        } else {
+          // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
+          issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk,
+                             it > 0 ? 1u : 0u);
+          ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
+          if (more) {
+            alive = full_b(it + 1);
+            ptx::tc_fence_after();
+            if (!alive) break;
+            issue_dp(it + 1);  // after dK: dS^T has been read
+          }
         }
       }
       ptx::mma_commit(xbar(X::kDone));
@@ -561,38 +709,55 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
     const long long key = static_cast<long long>(kt) * kBwdTile + t;
     const uint64_t c2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
 
-    // -LSE (log2 units) and D of query row t of tile i, fetched one tile
-    // ahead by the first half of the warps; a query past N gets -LSE = -inf,
-    // so its P is 0.
-    auto fetch = [&](int i, float& nl, float& dd) {
+    // LSE and D of query row t of tile i, fetched one tile ahead by the
+    // first half of the warps.  The loads are unconditional (a row past the
+    // queries reads row 0) and nothing uses their values until the tile is
+    // staged, so the warps do not wait for them; a query past N then gets
+    // -LSE = -inf, so its P is 0, and D = 0.
+    bool in_next = false;
+    auto fetch = [&](int i, float& lse, float& dd) {
       const int qrow = i * kBwdTile + t;
-      const bool in = qrow < q_rows;
-      const long long qi = bwd_lse_at(p, tok, hd, bh, qrow);
-      nl = in ? -p.lse[qi] * 1.4426950408889634f : -INFINITY;
-      dd = in ? p.delta[tok ? bwd_qrow(p, tok, hd, bh, qrow) : qi] : 0.f;
+      in_next = qrow < q_rows;
+      const int qr = in_next ? qrow : 0;
+      const long long qi = bwd_lse_at(p, tok, hd, bh, qr);
+      lse = p.lse[qi];
+      dd = p.delta[tok ? bwd_qrow(p, tok, hd, bh, qr) : qi];
     };
-    float nl_next = 0.f, d_next = 0.f;
-    if (half == 0) fetch(i0, nl_next, d_next);
-    for (int it = 0; it < nq; ++it) {
-      const int i = i0 + it;
-      // vectors of tile i: [0,128) -LSE, [128,256) D
-      float* vec = reinterpret_cast<float*>(sgen + L::kVec) + (it % DkdvVec<D>::kBufs) * 256;
+    float lse_next = 0.f, d_next = 0.f;
+    if (half == 0) fetch(i0, lse_next, d_next);
+    float pf[64];          // P^T of the current tile, from phase 1 to phase 2
+    // dropout: keep bits of this key against the thread's 64 queries, from
+    // the quad's words (zw[2 k2 + m]: word m of lane k2, blocks 8m + 4h + k2
+    // of 4 queries each), from phase 1 to phase 2
+    uint32_t zw[8] = {};
+    const uint32_t csel = 0x4440u + (static_cast<uint32_t>(lane) & 3u);   // this key's byte
+    // query bits of block b (queries 4b .. 4b + 3 of the thread's 64)
+    auto zq = [&](int b) -> uint32_t {
+      return col_query_bits(zw[2 * (b & 3) + (b >> 3)], csel, (b >> 2) & 1);
+    };
+    // vectors of query tile i0 + it: [0,128) -LSE, [128,256) D
+    auto vec_of = [&](int it) {
+      return reinterpret_cast<float*>(sgen + L::kVec) + (it % DkdvVec<D>::kBufs) * 256;
+    };
+    auto stage_vec = [&](int it) {
+      float* vec = vec_of(it);
       // with one buffer, every thread must be done with the previous tile's
       if (DkdvVec<D>::kBufs == 1 && it > 0) ptx::named_bar_sync(1, kBwdEwThreads);
       if (half == 0) {
-        vec[t] = nl_next;
-        vec[128 + t] = d_next;
-        if (it + 1 < nq) fetch(i + 1, nl_next, d_next);
+        vec[t] = in_next ? -lse_next * 1.4426950408889634f : -INFINITY;   // -LSE, log2 units
+        vec[128 + t] = in_next ? d_next : 0.f;
+        if (it + 1 < nq) fetch(i0 + it + 1, lse_next, d_next);
       }
       ptx::named_bar_sync(2, kBwdEwThreads);
-      const float4* nl4 = reinterpret_cast<const float4*>(vec) + half * 16;
-      const float4* dl4 = reinterpret_cast<const float4*>(vec + 128) + half * 16;
+    };
 
-      // ---- phase 1: P^T = 2^(S^T c - LSE) over this thread's 64 queries
+    // ---- phase 1: P^T = 2^(S^T c - LSE) over this thread's 64 queries
+    auto phase1 = [&](int it) {
+      const int i = i0 + it;
+      const float4* nl4 = reinterpret_cast<const float4*>(vec_of(it)) + half * 16;
       ptx::wait_bounded(xbar(X::kSFull), it & 1, wd, kSiteBwdSFull);
       __syncwarp();
       ptx::tc_fence_after();
-      float pf[64];
       {
         uint32_t sr[64];
         ptx::tmem_ld32(tS, sr);
@@ -629,8 +794,6 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       // the quad's words (zw[2 k2 + m]: word m of lane k2, blocks 8m + 4h + k2
       // of 4 queries each); the dV product reads P with the dropped weights
       // zeroed
-      uint32_t zw[8];
-      const uint32_t csel = 0x4440u + (static_cast<uint32_t>(lane) & 3u);   // this key's byte
       if constexpr (kDrop) {
         const uint2 mine = drop_words16<true>(static_cast<uint32_t>(key >> 2),
                                               static_cast<uint32_t>(i * kBwdTile + half * 64) >> 2,
@@ -644,10 +807,6 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
           zw[2 * k2 + 1] = __shfl_sync(0xffffffffu, mine.y, src);
         }
       }
-      // query bits of block b (queries 4b .. 4b + 3 of the thread's 64)
-      auto zq = [&](int b) -> uint32_t {
-        return col_query_bits(zw[2 * (b & 3) + (b >> 3)], csel, (b >> 2) & 1);
-      };
       {
         uint32_t pk[32];
 #pragma unroll
@@ -661,8 +820,11 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(xbar(X::kPReady));
+    };
 
-      // ---- phase 2: dS^T = P^T * (dP^T - D)
+    // ---- phase 2: dS^T = P^T * (dP^T - D)
+    auto phase2 = [&](int it) {
+      const float4* dl4 = reinterpret_cast<const float4*>(vec_of(it) + 128) + half * 16;
       ptx::wait_bounded(xbar(X::kDpFull), it & 1, wd, kSiteBwdDpFull);
       __syncwarp();
       ptx::tc_fence_after();
@@ -699,11 +861,88 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
           dk[f / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
         }
       }
-      ptx::tmem_st16(tDp, dk);           // over dP^T columns this warp has read
-      ptx::tmem_st16(tDp + 16, dk + 16);
-      ptx::tmem_wait_st();
+      if constexpr (kOne) {
+        // row t (key) of the dS tile, this thread's 64 queries: 128 bytes of
+        // query chunk `half` in the 128-byte swizzle (the previous tile's dK
+        // and dQ, which read it, completed before its phase 3 went on)
+        uint8_t* drow = sgen + L::kDs + half * L::kChunkBytes + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(drow + ((c ^ (t & 7)) << 4)) =
+              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(xbar(X::kDsReady));
+      } else {
+        ptx::tmem_st16(tDp, dk);           // over dP^T columns this warp has read
+        ptx::tmem_st16(tDp + 16, dk + 16);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(xbar(X::kDsReady));
+      }
+    };
+
+    // ---- phase 3 (one-pass kernel): dQ_i (queries on the TMEM lanes) added
+    // to p.dq_acc; this thread: query row t of tile i, columns half * D/2 ..
+    auto phase3 = [&](int it) {
+      const int i = i0 + it;
+      const int b = it % Q::kBufs;
+      ptx::wait_bounded(xbar(X::kDqFull + b), (it / Q::kBufs) & 1, wd, kSiteBwdDqFull);
+      __syncwarp();
+      ptx::tc_fence_after();
+      constexpr int kHw = D / 2;   // square calls: width_qk = D
+      const uint32_t tq = tmem_base + lane_off + Q::col(b) + half * kHw;
+      uint32_t r[kHw];
+      ptx::tmem_ld32(tq, r);
+      if constexpr (kHw == 64) ptx::tmem_ld32(tq + 32, r + 32);
+      ptx::tmem_wait_ld();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(xbar(X::kDsReady));
+      ptx::mbar_arrive(xbar(X::kDqFree + b));   // the buffer may be overwritten now
+      // Each 32 x 32 block (this warp's 32 rows, 32 of its columns) goes to
+      // the warp's staging block, column-major, and the TMA engine adds it
+      // into its place in p.dq_acc while the warp goes on.
+      float* stg = reinterpret_cast<float*>(sgen + L::kStg + warp * L::kStgWarpBytes);
+      const uint32_t stg_s = sbase + L::kStg + warp * L::kStgWarpBytes;
+#pragma unroll
+      for (int k = 0; k < kHw / 32; ++k) {
+        if (lane == 0) bulk_wait_read_all();   // the block's previous contents are sent
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) stg[cc * 32 + lane] = __uint_as_float(r[k * 32 + cc]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int cb = half * (kHw / 32) + k;
+          const long long blk =
+              ((static_cast<long long>(bh) * p.n_tiles + i) * (D / 32) + cb) * 4 + quarter;
+          bulk_reduce_add_f32(p.dq_acc + blk * 1024, stg_s, L::kStgWarpBytes);
+        }
+      }
+    };
+
+    if constexpr (kOne) {
+      // phase 1 of the next tile runs while the tensor core forms this
+      // tile's dK and dQ; phase 3 then finds dQ ready
+      stage_vec(0);
+      phase1(0);
+      for (int it = 0; it < nq; ++it) {
+        phase2(it);
+        if (it + 1 < nq) {
+          stage_vec(it + 1);
+          phase1(it + 1);
+        }
+        phase3(it);
+      }
+    } else {
+      for (int it = 0; it < nq; ++it) {
+        stage_vec(it);
+        phase1(it);
+        phase2(it);
+      }
+    }
+    if constexpr (kOne) {
+      if (lane == 0) bulk_wait_all();   // this warp's dQ additions have landed
+      __syncwarp();
     }
     // dV_j rows (warps 0-3) and dK_j = scale * (dS^T Q) rows (warps 4-7)
     ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
@@ -886,7 +1125,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
       // dropout: keep bits of this query against the thread's 64 keys, from
       // the quad's words (zw[2 k2 + m]: word m of lane k2, blocks 8m + 4h + k2
       // of 4 keys each)
-      uint32_t zw[8];
+      uint32_t zw[8] = {};
       if constexpr (kDrop) {
         const uint2 mine = drop_words16<false>(static_cast<uint32_t>(j * kBwdTile + half * 64) >> 2,
                                                static_cast<uint32_t>(qrow >> 2),
@@ -957,7 +1196,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
 // and a CTA that stays resident across items skips the relaunch and the
 // TMEM allocation of every item after its first.  Shared memory is sized
 // for the larger layout.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false, bool kOne = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   __shared__ uint32_t s_tmem_base;
@@ -971,12 +1210,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int per_pass = p.BH * p.n_ktiles;   // dK/dV items, one per key tile
-  const int total = per_pass + p.BH * p.n_tiles;
+  const int total = kOne ? per_pass : per_pass + p.BH * p.n_tiles;
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    if (item < per_pass)
-      bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, item, tmem_base);
-    else
-      bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, item - per_pass, tmem_base);
+    if constexpr (kOne) {
+      bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv, true>(p, item, tmem_base);
+    } else {
+      if (item < per_pass)
+        bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, item, tmem_base);
+      else
+        bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, item - per_pass, tmem_base);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -20,7 +20,8 @@
  *    the attention weights);
  *  - backward: fa_bwd, fa_bwd_kv, fa_bwd_varlen, fa_bwd_dropout,
  *    fa_bwd_kv_dropout, fa_bwd_varlen_dropout, each the gradient of the
- *    forward of the same name;
+ *    forward of the same name; fa_bwd_onepass (fa_bwd in one pass over the
+ *    tiles, dQ summed through a caller's fp32 scratch);
  *  - decoding: fa_decode (a few queries against a long cache, key axis
  *    split across the GPU);
  *  - status and settings: fa_strerror, fa_status, fa_set_watchdog_ns,
@@ -337,6 +338,43 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, float *delta,
            int B, int H, int N, int d, int causal, float scale, int dtype,
            cudaStream_t stream);
+
+/*
+ * fa_bwd_onepass — the gradients fa_bwd computes, with every (query tile,
+ * key tile) pair visited once.  The same passages define them (tiles are
+ * rebuilt from Q, K, V, O and the row statistics, never stored: "Why
+ * FlashAttention Can Avoid a Square Attention Array Without Making
+ * Attention Linear", section "Backward can recreate tiles instead of
+ * retaining the square").  fa_bwd forms S and dP twice, once for dK/dV
+ * (per key tile) and once for dQ (per query tile).  Here the per-key-tile
+ * pass also forms dQ_i = dS K_j and adds it in fp32 into the caller's
+ * scratch; a final kernel writes dQ = scale * sum.  That is five tile
+ * products per pair instead of seven.  The fp32 additions of different key
+ * tiles land in an unspecified order, so dQ can differ from call to call in
+ * its last bits (dK and dV cannot: each of their rows has one writer).
+ *
+ *   q ... dtype, stream : as fa_bwd (d 64 or 128).
+ *   workspace       : device pointer, 16-byte aligned, at least
+ *                     fa_bwd_onepass_workspace_size bytes, owned by the
+ *                     caller; zeroed and overwritten on `stream` by every
+ *                     call.  Must not be in use by other work meanwhile.
+ *   workspace_bytes : its size in bytes.
+ * Errors as fa_bwd, plus FA_ERR_WORKSPACE for a missing or short workspace
+ * and FA_ERR_ALIGN for a misaligned one (checked after the arguments
+ * fa_bwd checks; nothing is launched then).
+ */
+int fa_bwd_onepass(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                   float *delta, int B, int H, int N, int d, int causal, float scale,
+                   int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_bwd_onepass_workspace_size — bytes of the fp32 dQ sum of
+ * fa_bwd_onepass: B * H * d * (N rounded up to a multiple of 128) * 4.
+ * Host-only.  Returns FA_ERR_NULLPTR for a NULL `bytes`, FA_ERR_SHAPE for a
+ * negative B, H or N, FA_ERR_UNSUPPORTED_D for d other than 64 or 128.
+ */
+int fa_bwd_onepass_workspace_size(int B, int H, int N, int d, size_t *bytes);
 
 /*
  * fa_bwd_kv — the backward pass of fa_fwd_kv: dQ, dK, dV of sum(dO * O) for

@@ -204,6 +204,35 @@ def test_decode_host_errors(lib):
     assert lib.fa_decode_workspace_size(1, 1, 4, 0, 64, C.byref(out)) == fa.FA_OK and out.value == 0
 
 
+def test_bwd_onepass_host_errors(lib):
+    """fa_bwd_onepass checks fa_bwd's arguments, then its workspace, and
+    only then reaches the device; its workspace is B*H*d*(N up to 128)*4."""
+    import ctypes as C
+    out = C.c_size_t(7)
+    assert lib.fa_bwd_onepass_workspace_size(1, 1, 256, 64, None) == fa.FA_ERR_NULLPTR
+    assert lib.fa_bwd_onepass_workspace_size(1, -1, 256, 64, C.byref(out)) == fa.FA_ERR_SHAPE
+    assert lib.fa_bwd_onepass_workspace_size(1, 1, 256, 96, C.byref(out)) == fa.FA_ERR_UNSUPPORTED_D
+    assert fa.fa_bwd_onepass_workspace_size(2, 3, 300, 128) == 2 * 3 * 128 * 384 * 4
+    assert fa.fa_bwd_onepass_workspace_size(1, 1, 128, 64) == 64 * 128 * 4
+    assert fa.fa_bwd_onepass_workspace_size(4, 4, 0, 64) == 0
+    need = fa.fa_bwd_onepass_workspace_size(1, 2, 300, 64)
+    call = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                delta=FAKE, B=1, H=2, N=300, d=64, causal=1, scale=0.125, dtype=fa.FA_BF16,
+                workspace=FAKE, workspace_bytes=need)
+    for args, code in [(dict(d=96, workspace=None), fa.FA_ERR_UNSUPPORTED_D),
+                       (dict(scale=0.0), fa.FA_ERR_SCALE),
+                       (dict(dq=None), fa.FA_ERR_NULLPTR),
+                       (dict(dk=FAKE + 4), fa.FA_ERR_ALIGN),
+                       (dict(workspace=None), fa.FA_ERR_WORKSPACE),
+                       (dict(workspace_bytes=need - 1), fa.FA_ERR_WORKSPACE),
+                       (dict(workspace=FAKE + 8), fa.FA_ERR_ALIGN),
+                       (dict(N=0, workspace=None), fa.FA_OK),
+                       (dict(B=0, workspace=None), fa.FA_OK)]:
+        assert fa.fa_bwd_onepass(**{**call, **args}) == code, args
+    if no_gpu():
+        assert fa.fa_bwd_onepass(**call) == fa.FA_ERR_DEVICE
+
+
 def test_fwd_kv_host_errors(lib):
     """fa_fwd_kv checks shapes, the causal mode (0, 1, 2), widths, dtype, scale,
     pointers (k, v may be NULL only without keys) and alignment before the device."""
