@@ -46,7 +46,9 @@ offset per forward step.
 ``--pass bwd`` times the backward pass instead: one step = one ``fa_bwd``
 call (two kernels: the D pass and the dK/dV + dQ grid) with the forward's O
 and LSE and a seeded dO resident on the device; FLOPs are 2.5x the
-forward's (five matmuls against two).
+forward's (five matmuls against two).  ``--onepass`` times
+``fa_bwd_onepass`` instead (the D pass, one grid that also sums dQ through
+an fp32 workspace, and the dQ conversion).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 forward pass has no exchange step); value = all ranks' FLOPs / the slowest
@@ -875,14 +877,24 @@ def run_ours_bwd(args, w):
         delta = torch.empty((B, H, N), dtype=torch.float32, device=device)
         bufs.append((dq_, dk_, dv_, o, lse, do_, gq, gk, gv, delta))
 
+    onepass = args.onepass
+    if onepass and drop > 0:
+        raise SystemExit("--onepass has no dropout form")
+    ws_bytes = fa.fa_bwd_onepass_workspace_size(B, H, N, d) if onepass else 0
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device) if onepass else None
+    entry = "fa_bwd_onepass" if onepass else ("fa_bwd_dropout" if drop > 0 else "fa_bwd")
+
     def step(i):
         if drop > 0:
             rc = fa.fa_bwd_dropout(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], drop,
                                    w["seed"], 0, code, stream)
+        elif onepass:
+            rc = fa.fa_bwd_onepass(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], code,
+                                   ws, ws_bytes, stream)
         else:
             rc = fa.fa_bwd(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], code, stream)
         if rc:
-            raise fa.FaError(rc, "fa_bwd")
+            raise fa.FaError(rc, entry)
 
     t_warm = time.time()
     for i in range(args.warmup):
@@ -913,6 +925,9 @@ def run_ours_bwd(args, w):
             grads = fa.attention_backward_dropout(dq_, dk_, dv_, o, lse, do_, drop, w["seed"], 0,
                                                   causal=w["causal"], scale=w["scale"],
                                                   stream=stream)
+        elif onepass:
+            grads = fa.attention_backward_onepass(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
+                                                  scale=w["scale"], workspace=ws, stream=stream)
         else:
             grads = fa.attention_backward(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
                                           scale=w["scale"], stream=stream)
@@ -947,20 +962,24 @@ def run_ours_bwd(args, w):
         "config": {"workload": w["name"], "pass": "backward", "B": B, "H": H, "N": N, "d": d,
                    "causal": w["causal"], "seed": w["seed"], "scale": w["scale"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "entry": "fa_bwd_dropout" if drop > 0 else "fa_bwd", "dropout": drop,
+                   "entry": entry, "dropout": drop,
                    "l2": (f"{replicas} rotating replicas ({replicas * per_replica / 2**20:.0f} MiB)"
                           if replicas > 1 else "inputs larger than L2")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peak_sustained if peak_sustained else None,
                      "kernel_ms": kern_ms, "flops_per_launch": flops,
-                     "scope": "one fa_bwd call: D, dK/dV and dQ kernels together",
+                     "scope": (f"one {entry} call: D, one-pass and dQ conversion kernels together"
+                               if onepass else
+                               f"one {entry} call: D, dK/dV and dQ kernels together"),
                      "traffic": None, "traffic_note": "no ncu DRAM capture of the backward yet"},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": io["h2d"], "d2h_bytes_per_step": io["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps * passes,   # the D pass and the dK/dV + dQ grid
+        # the D pass and the dK/dV + dQ grid (one-pass: also the dQ conversion;
+        # the workspace clearing is a cudaMemsetAsync)
+        "gpu_launches": (3 if onepass else 2) * args.steps * passes,
         "gpu": torch.cuda.get_device_name(device),
     }
     if not args.no_cpu_baseline:
@@ -1482,6 +1501,8 @@ def main(argv=None):
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability on the attention weights (fa_fwd_dropout, or "
                          "fa_bwd_dropout with --pass bwd); 0 = none")
+    ap.add_argument("--onepass", action="store_true",
+                    help="with --pass bwd: time fa_bwd_onepass instead of fa_bwd")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv", "varlen"], default="fwd",
                     help="time the forward pass (default), the backward pass (fa_bwd), "
                          "split-KV decoding (fa_decode; --workload names a decoding workload) "

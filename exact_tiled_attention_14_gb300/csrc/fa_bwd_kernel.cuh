@@ -25,7 +25,9 @@
 //                        dS, accumulates dQ_i in TMEM.
 // Each gradient row is written by exactly one CTA, so there are no atomics
 // and the result is deterministic; the price is that S and dP are formed
-// twice (seven tile GEMMs per (i, j) instead of five).
+// twice (seven tile GEMMs per (i, j) instead of five).  fa_bwd_onepass.cuh
+// holds the other trade: five tile GEMMs per pair, dQ summed in fp32 by the
+// TMA engine in no fixed order.
 //
 // CTA layout (both tensor-core kernels): warps 0-7 do the element-wise
 // work, warp w on TMEM lanes 32*(w%4) .. +31 (key rows in dkdv, query rows
@@ -128,10 +130,10 @@ struct BwdParams {
   const int* cu_k;
   int varlen;
   int total_q;
-  // One-pass kernel (kOne): dQ is accumulated, unscaled, in fp32 in blocks
-  // of 32 queries x 32 columns: block (bh, query tile qt, column block cb,
-  // row quarter rq) holds element (column cc, row rr) at
-  // dq_acc[((((bh * n_tiles + qt) * (width_qk / 32) + cb) * 4 + rq) * 32 + cc) * 32 + rr]
+  // One-pass kernel: dQ is accumulated, unscaled, in fp32 in blocks of 32
+  // queries x 16 columns: block (bh, query tile qt, column block cb, row
+  // quarter rq) holds element (column cc, row rr) at
+  // dq_acc[((((bh * n_tiles + qt) * (width_qk / 16) + cb) * 4 + rq) * 16 + cc) * 32 + rr]
   // (dq_pad = n_tiles * 128 rows per head).  Zeroed before the launch and
   // converted to dQ by fa_bwd_dq_convert_kernel afterwards.
   float* dq_acc;
@@ -179,13 +181,13 @@ __device__ __forceinline__ long long bwd_lse_at(const BwdParams& p, bool tok, co
              : static_cast<long long>(bh) * p.N + qrow;
 }
 
-// Shared memory of the two tensor-core kernels: the resident pair of tiles
+// Shared memory of the tensor-core kernels: the resident pair of tiles
 // (K_j, V_j or Q_i, dO_i), ring A and ring B of streamed tiles, in the
-// one-pass dK/dV/dQ kernel (kOne) a 128 x 128 tile of dS and a 4 KB dQ
-// staging block per element-wise warp, kVecBytes of per-query vectors
-// (dkdv: -LSE in log2 units and D of the current query tile), the ring
-// barriers and ten kernel-specific barriers.  The dS tile and the staging
-// blocks take the room of ring stages.
+// one-pass kernel (kOne, fa_bwd_onepass.cuh) a 128 x 128 tile of dS and
+// 32 KB of dQ staging blocks, kVecBytes of per-query vectors (dkdv: -LSE in
+// log2 units and D of the current query tile), the ring barriers and ten
+// kernel-specific barriers.  The dS tile and the staging blocks take the
+// room of ring stages.
 template <int D, int kVecBytes, bool kOne = false>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
@@ -198,8 +200,8 @@ struct BwdSmem {
   static constexpr int kRingB = kRingA + kStagesA * kTile;
   static constexpr int kDs = kRingB + kStagesB * kTile;   // 1024-aligned like the tiles
   static constexpr int kStg = kDs + (kOne ? kBwdTile * kBwdTile * 2 : 0);
-  static constexpr int kStgWarpBytes = 32 * 32 * 4;      // one 32 x 32 fp32 block
-  static constexpr int kVec = kStg + (kOne ? 8 * kStgWarpBytes : 0);
+  static constexpr int kStgBytes = 32 * 1024;
+  static constexpr int kVec = kStg + (kOne ? kStgBytes : 0);
   static constexpr int kBar = kVec + kVecBytes;
   static constexpr int bFullA = 0, bEmptyA = kStagesA, bFullB = 2 * kStagesA,
                        bEmptyB = bFullB + kStagesB, bRes = bEmptyB + kStagesB, bX = bRes + 1,
@@ -259,10 +261,11 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const uint4* __restri
 }
 
 // ---------------------------------------------------------------- dQ = scale * accumulator
-// The one-pass kernel leaves dQ unscaled in fp32 in 32 x 32 blocks, column
-// by column within a block (BwdParams::dq_acc).  Each CTA moves 32 query
-// rows of one head through shared memory and writes them row by row in the
-// storage dtype, scaled.  Blocks: bh * ceil(N / 32) + query block.
+// The one-pass kernel leaves dQ unscaled in fp32 in blocks of 32 queries x
+// 16 columns, column by column within a block (BwdParams::dq_acc).  Each
+// CTA moves 32 query rows of one head through shared memory and writes them
+// row by row in the storage dtype, scaled.  Blocks: bh * ceil(N / 32) +
+// query block.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
                                                                 uint32_t* __restrict__ dq,
@@ -276,8 +279,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
   const int n_tiles = pad / kBwdTile, qt = q0 / kBwdTile, rq = (q0 % kBwdTile) / 32;
   for (int c = row8; c < W; c += 8) {
     const long long blk =
-        ((static_cast<long long>(bh) * n_tiles + qt) * (W / 32) + c / 32) * 4 + rq;
-    tile[c][lane] = acc[(blk * 32 + c % 32) * 32 + lane];
+        ((static_cast<long long>(bh) * n_tiles + qt) * (W / 16) + c / 16) * 4 + rq;
+    tile[c][lane] = acc[(blk * 16 + c % 16) * 32 + lane];
   }
   __syncthreads();
   const int pairs = W / 2;
@@ -509,18 +512,11 @@ struct DkdvVec {
   static constexpr int kBytes = kBufs * 2 * kBwdTile * 4;
 };
 
-// One CTA of the dK/dV pass: block `blk` of BH * n_tiles.  With kOne it
-// also forms dQ_i = dS K_j for every query tile it visits and adds it, in
-// fp32, into p.dq_acc (five tile products per (i, j) instead of seven): dS
-// goes to a shared-memory tile that serves as A of both dK (K-major: keys
-// x queries) and dQ (MN-major: queries x keys), and a third element-wise
-// phase reads dQ_i from TMEM and adds it to global memory.
-template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv, bool kOne = false>
+// One CTA of the dK/dV pass: block `blk` of BH * n_tiles.
+template <int D, bool kBf16, bool kCausal, bool kDrop, bool kKv>
 __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32_t tmem_base) {
-  using L = BwdSmem<D, DkdvVec<D>::kBytes, kOne>;
+  using L = BwdSmem<D, DkdvVec<D>::kBytes>;
   using X = DkdvBars;
-  using Q = DqBuf<D>;
-  static_assert(!(kOne && kKv), "the one-pass kernel covers square calls");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -575,12 +571,6 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
     ptx::mbar_init(b(L::bX + X::kPReady), kBwdEwThreads);
     ptx::mbar_init(b(L::bX + X::kDsReady), kBwdEwThreads);
     ptx::mbar_init(b(L::bX + X::kDone), 1);
-    if constexpr (kOne) {
-      for (int q = 0; q < Q::kBufs; ++q) {
-        ptx::mbar_init(b(L::bX + X::kDqFull + q), 1);
-        ptx::mbar_init(b(L::bX + X::kDqFree + q), kBwdEwThreads);
-      }
-    }
   });
   const ptx::Watchdog wd{p.watchdog_cycles, abort_flag, p.status};
 
@@ -606,12 +596,6 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
       const uint32_t do_mn0 = ptx::desc_lo(sbase + L::kRingB, L::kChunkBytes);
       const uint32_t tS = tmem_base + kColS, tDp = tmem_base + kColDp;
       const uint32_t tDv = tmem_base + kColAcc, tDk = tmem_base + kColAcc + D;
-      // one-pass kernel: dS in shared memory as K-major A of dK and MN-major
-      // A of dQ, K_j as MN-major B of dQ
-      const uint32_t ds_k = ptx::desc_lo(sbase + L::kDs, 16);
-      const uint32_t ds_mn = ptx::desc_lo(sbase + L::kDs, L::kChunkBytes);
-      const uint32_t k_mn = ptx::desc_lo(sbase + L::kRes, L::kChunkBytes);
-      const uint32_t idesc_dq = idesc_dk | kIdescAMnMajor;
       auto full_a = [&](int it) {
         return ptx::wait_bounded(bar(L::bFullA + it % L::kStagesA), (it / L::kStagesA) & 1, wd,
                                  kSiteBwdFull);
@@ -656,41 +640,15 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
         alive = ptx::wait_bounded(xbar(X::kDsReady), it & 1, wd, kSiteBwdDsReady);
         ptx::tc_fence_after();
         if (!alive) break;
-        if constexpr (kOne) {
-          // dK_j += dS^T Q_i from the shared-memory dS tile
-          issue_smem_a<L::kChunkBytes>(tDk, ds_k, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk,
-                                       it > 0 ? 1u : 0u);
-          ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
-          // dQ_i = dS K_j into a dQ buffer the element-wise warps have emptied
-          // (with one buffer, the dP^T columns: read before dS was ready)
-          const int b = it % Q::kBufs;
-          if (Q::kBufs > 1 && it >= Q::kBufs) {
-            alive = ptx::wait_bounded(xbar(X::kDqFree + b), ((it / Q::kBufs) - 1) & 1, wd,
-                                      kSiteBwdDqFree);
-            ptx::tc_fence_after();
-            if (!alive) break;
-          }
-          issue_mn_mn(tmem_base + Q::col(b), ds_mn, k_mn, idesc_dq);
-          ptx::mma_commit(xbar(X::kDqFull + b));
-          if (more) {
-            alive = full_b(it + 1);
-            if (Q::kBufs == 1)   // dP^T_{i+1} overwrites dQ_i: wait until it is read
-              alive = alive && ptx::wait_bounded(xbar(X::kDqFree), it & 1, wd, kSiteBwdDqFree);
-            ptx::tc_fence_after();
-            if (!alive) break;
-            issue_dp(it + 1);
-          }
-        } else {
-          // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
-          issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk,
-                             it > 0 ? 1u : 0u);
-          ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
-          if (more) {
-            alive = full_b(it + 1);
-            ptx::tc_fence_after();
-            if (!alive) break;
-            issue_dp(it + 1);  // after dK: dS^T has been read
-          }
+        // dK_j += dS^T Q_i (scale applied at the end); dS^T in columns 128-159 and 192-223
+        issue_tmem_a<true>(tDk, tDp, q_mn0 + (it % L::kStagesA) * kSlotLo, idesc_dk,
+                           it > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(L::bEmptyA + it % L::kStagesA));
+        if (more) {
+          alive = full_b(it + 1);
+          ptx::tc_fence_after();
+          if (!alive) break;
+          issue_dp(it + 1);  // after dK: dS^T has been read
         }
       }
       ptx::mma_commit(xbar(X::kDone));
@@ -861,88 +819,17 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
           dk[f / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
         }
       }
-      if constexpr (kOne) {
-        // row t (key) of the dS tile, this thread's 64 queries: 128 bytes of
-        // query chunk `half` in the 128-byte swizzle (the previous tile's dK
-        // and dQ, which read it, completed before its phase 3 went on)
-        uint8_t* drow = sgen + L::kDs + half * L::kChunkBytes + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(drow + ((c ^ (t & 7)) << 4)) =
-              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-        ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(xbar(X::kDsReady));
-      } else {
-        ptx::tmem_st16(tDp, dk);           // over dP^T columns this warp has read
-        ptx::tmem_st16(tDp + 16, dk + 16);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(xbar(X::kDsReady));
-      }
-    };
-
-    // ---- phase 3 (one-pass kernel): dQ_i (queries on the TMEM lanes) added
-    // to p.dq_acc; this thread: query row t of tile i, columns half * D/2 ..
-    auto phase3 = [&](int it) {
-      const int i = i0 + it;
-      const int b = it % Q::kBufs;
-      ptx::wait_bounded(xbar(X::kDqFull + b), (it / Q::kBufs) & 1, wd, kSiteBwdDqFull);
-      __syncwarp();
-      ptx::tc_fence_after();
-      constexpr int kHw = D / 2;   // square calls: width_qk = D
-      const uint32_t tq = tmem_base + lane_off + Q::col(b) + half * kHw;
-      uint32_t r[kHw];
-      ptx::tmem_ld32(tq, r);
-      if constexpr (kHw == 64) ptx::tmem_ld32(tq + 32, r + 32);
-      ptx::tmem_wait_ld();
+      ptx::tmem_st16(tDp, dk);           // over dP^T columns this warp has read
+      ptx::tmem_st16(tDp + 16, dk + 16);
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(xbar(X::kDqFree + b));   // the buffer may be overwritten now
-      // Each 32 x 32 block (this warp's 32 rows, 32 of its columns) goes to
-      // the warp's staging block, column-major, and the TMA engine adds it
-      // into its place in p.dq_acc while the warp goes on.
-      float* stg = reinterpret_cast<float*>(sgen + L::kStg + warp * L::kStgWarpBytes);
-      const uint32_t stg_s = sbase + L::kStg + warp * L::kStgWarpBytes;
-#pragma unroll
-      for (int k = 0; k < kHw / 32; ++k) {
-        if (lane == 0) bulk_wait_read_all();   // the block's previous contents are sent
-        __syncwarp();
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc) stg[cc * 32 + lane] = __uint_as_float(r[k * 32 + cc]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int cb = half * (kHw / 32) + k;
-          const long long blk =
-              ((static_cast<long long>(bh) * p.n_tiles + i) * (D / 32) + cb) * 4 + quarter;
-          bulk_reduce_add_f32(p.dq_acc + blk * 1024, stg_s, L::kStgWarpBytes);
-        }
-      }
+      ptx::mbar_arrive(xbar(X::kDsReady));
     };
 
-    if constexpr (kOne) {
-      // phase 1 of the next tile runs while the tensor core forms this
-      // tile's dK and dQ; phase 3 then finds dQ ready
-      stage_vec(0);
-      phase1(0);
-      for (int it = 0; it < nq; ++it) {
-        phase2(it);
-        if (it + 1 < nq) {
-          stage_vec(it + 1);
-          phase1(it + 1);
-        }
-        phase3(it);
-      }
-    } else {
-      for (int it = 0; it < nq; ++it) {
-        stage_vec(it);
-        phase1(it);
-        phase2(it);
-      }
-    }
-    if constexpr (kOne) {
-      if (lane == 0) bulk_wait_all();   // this warp's dQ additions have landed
-      __syncwarp();
+    for (int it = 0; it < nq; ++it) {
+      stage_vec(it);
+      phase1(it);
+      phase2(it);
     }
     // dV_j rows (warps 0-3) and dK_j = scale * (dS^T Q) rows (warps 4-7)
     ptx::wait_bounded(xbar(X::kDone), 0, wd, kSiteBwdDone);
@@ -1196,7 +1083,7 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
 // and a CTA that stays resident across items skips the relaunch and the
 // TMEM allocation of every item after its first.  Shared memory is sized
 // for the larger layout.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false, bool kOne = false>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false, bool kKv = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   __shared__ uint32_t s_tmem_base;
@@ -1210,16 +1097,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int per_pass = p.BH * p.n_ktiles;   // dK/dV items, one per key tile
-  const int total = kOne ? per_pass : per_pass + p.BH * p.n_tiles;
+  const int total = per_pass + p.BH * p.n_tiles;
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    if constexpr (kOne) {
-      bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv, true>(p, item, tmem_base);
-    } else {
-      if (item < per_pass)
-        bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, item, tmem_base);
-      else
-        bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, item - per_pass, tmem_base);
-    }
+    if (item < per_pass)
+      bwd_dkdv_cta<D, kBf16, kCausal, kDrop, kKv>(p, item, tmem_base);
+    else
+      bwd_dq_cta<D, kBf16, kCausal, kDrop, kKv>(p, item - per_pass, tmem_base);
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "fa_bwd_kernel.cuh"
+#include "fa_bwd_onepass.cuh"
 
 namespace fa {
 
@@ -52,11 +53,11 @@ cudaError_t launch_bwd_delta(const BwdParams& p, const void* o, const void* dout
 // D pass ends, and wait on the device before reading D.
 template <typename Kernel>
 cudaError_t launch_bwd_grid(Kernel kernel, const BwdParams& p, long long items, int smem, int sms,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int threads = kBwdThreads) {
   const long long grid = items < sms ? items : sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kBwdThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -91,7 +92,7 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
 // ([BH, width_qk, dq_pad]) is zeroed, D formed, one grid of dK/dV CTAs adds
 // every dQ_i = dS K_j into the accumulator, and a last kernel writes
 // dQ = scale * accumulator in the storage dtype, all on `stream`.
-template <int D, bool kBf16, bool kCausal, bool kDrop = false>
+template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_bwd_onepass_variant(const BwdParams& p, const void* o, const void* dout,
                                        float* delta, int sms, cudaStream_t stream) {
   const size_t acc_bytes =
@@ -102,10 +103,11 @@ cudaError_t launch_bwd_onepass_variant(const BwdParams& p, const void* o, const 
   if (e != cudaSuccess) return e;
   static std::atomic<uint64_t> done{0};
   constexpr int kAlloc = BwdSmem<D, DkdvVec<D>::kBytes, true>::kAlloc;
-  auto kernel = fa_bwd_kernel<D, kBf16, kCausal, kDrop, false, true>;
+  auto kernel = fa_bwd_onepass_kernel<D, kBf16, kCausal>;
   e = bwd_smem_attr(kernel, done, kAlloc);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_grid(kernel, p, static_cast<long long>(p.BH) * p.n_ktiles, kAlloc, sms, stream);
+  e = launch_bwd_grid(kernel, p, static_cast<long long>(p.BH) * p.n_ktiles, kAlloc, sms, stream,
+                      kOneThreads);
   if (e != cudaSuccess) return e;
   const long long blocks = static_cast<long long>(p.BH) * ((p.N + 31) / 32);
   fa_bwd_dq_convert_kernel<kBf16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
