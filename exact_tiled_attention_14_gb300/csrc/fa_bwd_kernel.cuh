@@ -138,7 +138,22 @@ struct BwdParams {
   // converted to dQ by fa_bwd_dq_convert_kernel afterwards.
   float* dq_acc;
   int dq_pad;
+  // Work items (key tiles of dK/dV or one-pass CTAs, query tiles of dQ
+  // CTAs) are dealt in groups of item_group heads, tile by tile within a
+  // group, so the CTAs at work share a few heads' streamed tiles in L2.
+  int item_group;
 };
+
+// Tile index and head of work item `blk` among BH * n_tiles items dealt in
+// groups of p.item_group heads (the last group may be smaller).
+__device__ __forceinline__ void bwd_item(const BwdParams& p, int blk, int n_tiles, int& tile,
+                                         int& bh) {
+  const int per_group = p.item_group * n_tiles;
+  const int g = blk / per_group, r = blk - g * per_group;
+  const int gh = min(p.item_group, p.BH - g * p.item_group);
+  tile = r / gh;
+  bh = g * p.item_group + (r - tile * gh);
+}
 
 // Where head bh's rows sit in a kKv call: its key count len and query
 // offset off (query i at position i + off), its query count lenq, and with
@@ -526,10 +541,10 @@ __device__ __forceinline__ void bwd_dkdv_cta(const BwdParams& p, int blk, uint32
   auto xbar = [&](int i) -> uint32_t { return bar(L::bX + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
 
-  // Key tile kt of head bh; for causal runs the first key tiles (the most
-  // query tiles to visit) are dealt first.
-  const int kt = blk / p.BH;
-  const int bh = blk - kt * p.BH;
+  // Key tile kt of head bh; for causal runs the first key tiles of a group
+  // of heads (the most query tiles to visit) are dealt first.
+  int kt, bh;
+  bwd_item(p, blk, p.n_ktiles, kt, bh);
   int i0 = kCausal ? kt : 0;                 // query tiles i >= kt see this key tile
   int len = p.N, off = 0;                    // keys of this head, query offset (kKv)
   int n_q = p.n_tiles;                       // query tiles of this head
@@ -870,8 +885,8 @@ __device__ __forceinline__ void bwd_dq_cta(const BwdParams& p, int blk, uint32_t
 
   // Query tile qt of head bh; for causal runs the last query tiles (the most
   // key tiles to visit) are dealt first.
-  const int r = blk / p.BH;
-  const int bh = blk - r * p.BH;
+  int r, bh;
+  bwd_item(p, blk, p.n_tiles, r, bh);
   const int qt = kCausal ? p.n_tiles - 1 - r : r;
   int nk = kCausal ? qt + 1 : p.n_tiles;   // key tiles j <= qt are visible
   int len = p.N, off = 0;                  // keys of this head, query offset (kKv)

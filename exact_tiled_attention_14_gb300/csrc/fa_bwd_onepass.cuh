@@ -74,10 +74,12 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
   auto xbar = [&](int i) -> uint32_t { return bar(L::bX + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + L::kMisc + 4);
 
-  // Key tile kt of head bh; for causal runs the first key tiles (the most
-  // query tiles to visit) are dealt first.  Query tiles i >= kt see it.
-  const int kt = blk / p.BH;
-  const int bh = blk - kt * p.BH;
+  // Key tile kt of head bh: items come in groups of item_group heads, key
+  // tile by key tile within a group, so for causal runs the first key tiles
+  // of a group (the most query tiles to visit) are dealt first.  Query
+  // tiles i >= kt see key tile kt.
+  int kt, bh;
+  bwd_item(p, blk, p.n_ktiles, kt, bh);
   const int i0 = kCausal ? kt : 0;
   const int nq = p.n_tiles - i0;
 
