@@ -113,9 +113,10 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   p.dq_acc = static_cast<float*>(ws);
   p.dq_pad = static_cast<int>(n_qtiles * fa::kBwdTile);
   // item order: a head at a time (its tiles share the streamed tiles and,
-  // in one pass, the dQ sums in L2) unless causal, where groups of 8 heads
-  // balance the tiles' unequal ranges across the SMs
-  p.item_group = causal ? static_cast<int>(bh < 8 ? bh : 8) : 1;
+  // in one pass, the dQ sums in L2) when every tile of a kind costs the
+  // same; groups of 8 heads when causal masks or key counts make the
+  // tiles' ranges unequal, so the round-robin deal mixes long and short
+  p.item_group = (causal || seqlens_k) ? static_cast<int>(bh < 8 ? bh : 8) : 1;
   const bool c = causal != 0;
   cudaError_t e;
   if (one)
@@ -257,7 +258,7 @@ static int backward_varlen(const void* q, const void* k, const void* v, const vo
   set_dropout(&p, drop_t, seed, drop_off);
   p.dq_acc = nullptr;
   p.dq_pad = 0;
-  p.item_group = causal ? static_cast<int>(bh < 8 ? bh : 8) : 1;
+  p.item_group = static_cast<int>(bh < 8 ? bh : 8);   // sequences of unequal lengths
   const bool c = causal != 0;
   cudaError_t e;
   if (drop_t < 256)
