@@ -878,14 +878,16 @@ def run_ours_bwd(args, w):
         bufs.append((dq_, dk_, dv_, o, lse, do_, gq, gk, gv, delta))
 
     onepass = args.onepass
-    if onepass and drop > 0:
-        raise SystemExit("--onepass has no dropout form")
     ws_bytes = fa.fa_bwd_onepass_workspace_size(B, H, N, d) if onepass else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device) if onepass else None
-    entry = "fa_bwd_onepass" if onepass else ("fa_bwd_dropout" if drop > 0 else "fa_bwd")
+    entry = ("fa_bwd_onepass" if onepass else "fa_bwd") + ("_dropout" if drop > 0 else "")
 
     def step(i):
-        if drop > 0:
+        if drop > 0 and onepass:
+            rc = fa.fa_bwd_onepass_dropout(*bufs[i % replicas], B, H, N, d, w["causal"],
+                                           w["scale"], drop, w["seed"], 0, code, ws, ws_bytes,
+                                           stream)
+        elif drop > 0:
             rc = fa.fa_bwd_dropout(*bufs[i % replicas], B, H, N, d, w["causal"], w["scale"], drop,
                                    w["seed"], 0, code, stream)
         elif onepass:
@@ -921,13 +923,14 @@ def run_ours_bwd(args, w):
     def e2e_step():
         for dst, src in zip((dq_, dk_, dv_, o, lse, do_), hosts + [ho, hl, hdo]):
             dst.copy_(src, non_blocking=True)
-        if drop > 0:
+        if onepass:
+            grads = fa.attention_backward_onepass(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
+                                                  scale=w["scale"], workspace=ws, stream=stream,
+                                                  dropout_p=drop, seed=w["seed"], offset=0)
+        elif drop > 0:
             grads = fa.attention_backward_dropout(dq_, dk_, dv_, o, lse, do_, drop, w["seed"], 0,
                                                   causal=w["causal"], scale=w["scale"],
                                                   stream=stream)
-        elif onepass:
-            grads = fa.attention_backward_onepass(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
-                                                  scale=w["scale"], workspace=ws, stream=stream)
         else:
             grads = fa.attention_backward(dq_, dk_, dv_, o, lse, do_, causal=w["causal"],
                                           scale=w["scale"], stream=stream)
@@ -1502,7 +1505,8 @@ def main(argv=None):
                     help="dropout probability on the attention weights (fa_fwd_dropout, or "
                          "fa_bwd_dropout with --pass bwd); 0 = none")
     ap.add_argument("--onepass", action="store_true",
-                    help="with --pass bwd: time fa_bwd_onepass instead of fa_bwd")
+                    help="with --pass bwd: time fa_bwd_onepass (fa_bwd_onepass_dropout with "
+                         "--dropout) instead of fa_bwd")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "decode", "kv", "varlen"], default="fwd",
                     help="time the forward pass (default), the backward pass (fa_bwd), "
                          "split-KV decoding (fa_decode; --workload names a decoding workload) "

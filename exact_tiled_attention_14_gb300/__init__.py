@@ -49,7 +49,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_kv", "fa_fwd_varlen", "fa_fwd_dropout", "fa_bwd_dro
            "fa_fwd_kv_dropout", "fa_fwd_varlen_dropout", "fa_bwd_kv_dropout",
            "fa_bwd_varlen_dropout",
            "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_static", "fa_bwd",
-           "fa_bwd_onepass", "fa_bwd_onepass_workspace_size",
+           "fa_bwd_onepass", "fa_bwd_onepass_workspace_size", "fa_bwd_onepass_dropout",
            "fa_decode", "fa_decode_workspace_size", "fa_strerror", "fa_status",
            "fa_set_watchdog_ns", "fa_set_unit_group", "fa_watchdog_selftest", "fa_work_tiles",
            "fa_version")
@@ -96,6 +96,9 @@ def load_library(path=None):
     lib.fa_bwd_onepass_workspace_size.argtypes = [i] * 4 + [ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_bwd_onepass_workspace_size.restype = i
     u64, u32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_bwd_onepass_dropout.argtypes = ([vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp,
+                                                         ctypes.c_size_t, vp])
+    lib.fa_bwd_onepass_dropout.restype = i
     lib.fa_fwd_dropout.argtypes = [vp] * 5 + [i, i, i, i, i, f, f, u64, u32, i, vp]
     lib.fa_fwd_dropout.restype = i
     lib.fa_bwd_dropout.argtypes = [vp] * 10 + [i, i, i, i, i, f, f, u64, u32, i, vp]
@@ -306,6 +309,19 @@ def fa_bwd_onepass(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal,
                               _addr(dq), _addr(dk), _addr(dv), _addr(delta), int(B), int(H),
                               int(N), int(d), int(bool(causal)), float(scale), int(dtype),
                               _addr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def fa_bwd_onepass_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale,
+                           dropout_p, seed, offset, dtype, workspace, workspace_bytes,
+                           stream=None):
+    """Raw C call of the one-pass backward with dropout; returns the code."""
+    lib = load_library()
+    return lib.fa_bwd_onepass_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse),
+                                      _addr(dout), _addr(dq), _addr(dk), _addr(dv), _addr(delta),
+                                      int(B), int(H), int(N), int(d), int(bool(causal)),
+                                      float(scale), float(dropout_p), int(seed), int(offset),
+                                      int(dtype), _addr(workspace), int(workspace_bytes),
+                                      _stream(stream))
 
 
 def fa_bwd_onepass_workspace_size(B, H, N, d):
@@ -590,12 +606,14 @@ def attention_backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=N
 
 
 def attention_backward_onepass(q, k, v, o, lse, dout, causal=False, scale=None, workspace=None,
-                               stream=None):
-    """The gradients of ``attention_backward`` through ``fa_bwd_onepass``:
-    each (query tile, key tile) pair is visited once and dQ is summed in
-    fp32 through ``workspace`` (a CUDA tensor of at least
-    ``fa_bwd_onepass_workspace_size`` bytes; allocated here when None).  dQ
-    may differ in its last bits from call to call; dK and dV do not."""
+                               stream=None, dropout_p=0.0, seed=0, offset=0):
+    """The gradients of ``attention_backward`` (or, with dropout_p > 0, of
+    ``attention_backward_dropout``) through ``fa_bwd_onepass`` (or
+    ``fa_bwd_onepass_dropout``): each (query tile, key tile) pair is visited
+    once and dQ is summed in fp32 through ``workspace`` (a CUDA tensor of at
+    least ``fa_bwd_onepass_workspace_size`` bytes; allocated here when
+    None).  dQ may differ in its last bits from call to call; dK and dV do
+    not."""
     import torch
     ts = (q, k, v, o, dout)
     if any(t.dtype != q.dtype for t in ts):
@@ -618,10 +636,15 @@ def attention_backward_onepass(q, k, v, o, lse, dout, causal=False, scale=None, 
     delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fa_bwd_onepass(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale, code,
-                        workspace, ws_bytes, stream)
+    if dropout_p > 0:
+        rc = fa_bwd_onepass_dropout(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal,
+                                    scale, dropout_p, seed, offset, code, workspace, ws_bytes,
+                                    stream)
+    else:
+        rc = fa_bwd_onepass(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, d, causal, scale,
+                            code, workspace, ws_bytes, stream)
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd_onepass")
+        raise FaError(rc, "fa_bwd_onepass_dropout" if dropout_p > 0 else "fa_bwd_onepass")
     return dq, dk, dv
 
 

@@ -119,7 +119,11 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
   p.item_group = (causal || seqlens_k) ? static_cast<int>(bh < 8 ? bh : 8) : 1;
   const bool c = causal != 0;
   cudaError_t e;
-  if (one)
+  if (one && drop_t < 256)
+    e = (d == 64)
+            ? fa::launch_bwd_onepass_drop_d64(p, o, dout, delta, bf16, c, info->sms, stream)
+            : fa::launch_bwd_onepass_drop_d128(p, o, dout, delta, bf16, c, info->sms, stream);
+  else if (one)
     e = (d == 64) ? fa::launch_bwd_onepass_d64(p, o, dout, delta, bf16, c, info->sms, stream)
                   : fa::launch_bwd_onepass_d128(p, o, dout, delta, bf16, c, info->sms, stream);
   else if (kv && drop_t < 256)
@@ -158,6 +162,19 @@ int fa_bwd_onepass(const void* q, const void* k, const void* v, const void* o, c
                    size_t workspace_bytes, cudaStream_t stream) {
   return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
                   nullptr, scale, dtype, 256, 0, 0, stream, true, workspace, workspace_bytes);
+}
+
+int fa_bwd_onepass_dropout(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           float* delta, int B, int H, int N, int d, int causal, float scale,
+                           float dropout_p, unsigned long long seed, unsigned int offset,
+                           int dtype, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  const int t = drop_threshold(dropout_p);
+  if (t < 0) return FA_ERR_DROPOUT;
+  return backward(q, k, v, o, lse, dout, dq, dk, dv, delta, B, H, N, N, d, d, causal, false,
+                  nullptr, scale, dtype, t, seed, offset, stream, true, workspace,
+                  workspace_bytes);
 }
 
 int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -92,7 +92,7 @@ cudaError_t launch_bwd_variant(const BwdParams& p, const void* o, const void* do
 // ([BH, width_qk, dq_pad]) is zeroed, D formed, one grid of dK/dV CTAs adds
 // every dQ_i = dS K_j into the accumulator, and a last kernel writes
 // dQ = scale * accumulator in the storage dtype, all on `stream`.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false>
 cudaError_t launch_bwd_onepass_variant(const BwdParams& p, const void* o, const void* dout,
                                        float* delta, int sms, cudaStream_t stream) {
   const size_t acc_bytes =
@@ -103,7 +103,7 @@ cudaError_t launch_bwd_onepass_variant(const BwdParams& p, const void* o, const 
   if (e != cudaSuccess) return e;
   static std::atomic<uint64_t> done{0};
   constexpr int kAlloc = BwdSmem<D, DkdvVec<D>::kBytes, true>::kAlloc;
-  auto kernel = fa_bwd_onepass_kernel<D, kBf16, kCausal>;
+  auto kernel = fa_bwd_onepass_kernel<D, kBf16, kCausal, kDrop>;
   e = bwd_smem_attr(kernel, done, kAlloc);
   if (e != cudaSuccess) return e;
   e = launch_bwd_grid(kernel, p, static_cast<long long>(p.BH) * p.n_ktiles, kAlloc, sms, stream,
@@ -119,13 +119,20 @@ cudaError_t launch_bwd_d64(const BwdParams& p, const void* o, const void* dout, 
                            bool bf16, bool causal, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdParams& p, const void* o, const void* dout, float* delta,
                             bool bf16, bool causal, int sms, cudaStream_t stream);
-// The one-pass backward (square calls, dQ accumulated in p.dq_acc).
+// The one-pass backward (square calls, dQ accumulated in p.dq_acc), and
+// with dropout in the forward pass.
 cudaError_t launch_bwd_onepass_d64(const BwdParams& p, const void* o, const void* dout,
                                    float* delta, bool bf16, bool causal, int sms,
                                    cudaStream_t stream);
 cudaError_t launch_bwd_onepass_d128(const BwdParams& p, const void* o, const void* dout,
                                     float* delta, bool bf16, bool causal, int sms,
                                     cudaStream_t stream);
+cudaError_t launch_bwd_onepass_drop_d64(const BwdParams& p, const void* o, const void* dout,
+                                        float* delta, bool bf16, bool causal, int sms,
+                                        cudaStream_t stream);
+cudaError_t launch_bwd_onepass_drop_d128(const BwdParams& p, const void* o, const void* dout,
+                                         float* delta, bool bf16, bool causal, int sms,
+                                         cudaStream_t stream);
 // With dropout in the forward pass (the kDrop variants).
 cudaError_t launch_bwd_drop_d64(const BwdParams& p, const void* o, const void* dout, float* delta,
                                 bool bf16, bool causal, int sms, cudaStream_t stream);

@@ -31,9 +31,14 @@
 // tensor core forms dK_j += dS^T Q_i and dQ_i.  The MMA thread issues, per
 // tile: dV (after phase 1), S^T of the next tile, dK and dQ (after phase 2),
 // then dP^T of the next tile (at d = 128 once phase 3 has read dQ).
+//
+// With dropout (kDrop) the mask of the forward pass is drawn once per pair
+// from (seed, offset) exactly as fa_bwd_dropout draws it: dV_j += (P Z)^T dO_i
+// (scaled by 256 / t at the end) and dS = P * (Z dP 256 / t - D).
 #pragma once
 
 #include "fa_bwd_kernel.cuh"
+#include "fa_philox.cuh"
 
 namespace fa {
 
@@ -54,12 +59,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
+// Dropout mask words of a key column against 32 queries (eight 4 x 4 blocks
+// of the column walk of drop_words16): lane k (0 .. 3) of a quad, whose
+// four lanes are the block's four keys, draws blocks k and k + 4, in one
+// word laid out by key (bits 7 .. 4 of each byte: block k; bits 3 .. 0:
+// block k + 4).  kb0 is the key block, qb0 the first query block.
+__device__ __forceinline__ uint32_t drop_words8(uint32_t kb0, uint32_t qb0, uint32_t k, uint32_t bh,
+                                                uint32_t off, uint32_t k0, uint32_t k1,
+                                                uint32_t t) {
+  const uint32_t c4 = (256u - t) * 0x01010101u;
+  const uint4 ra = philox4x32_10(make_uint4(kb0, qb0 + k, bh, off), k0, k1);
+  const uint4 rb = philox4x32_10(make_uint4(kb0, qb0 + k + 4u, bh, off), k0, k1);
+  return sel_bits(0xF0F0F0F0u, keep_by_key(ra, c4), keep_by_key(rb, c4) >> 4);
+}
+
 // One CTA of the one-pass backward: key tile blk / BH of head blk % BH.
 // The fp32 dQ workspace (BwdParams::dq_acc) holds blocks of 32 queries x 16
 // columns: block (bh, query tile qt, column block cb, row quarter rq) keeps
 // element (column cc, row rr) at
 //   dq_acc[((((bh * n_tiles + qt) * (D / 16) + cb) * 4 + rq) * 16 + cc) * 32 + rr].
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop>
 __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uint32_t tmem_base) {
   using L = BwdSmem<D, DkdvVec<D>::kBytes, true>;
   using X = DkdvBars;
@@ -237,6 +256,12 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
     };
 
     float pf[32];   // P^T of the current tile, from phase 1 to phase 2
+    // dropout: the quad's words for this key block against the thread's 32
+    // queries (zw[k2]: the word of quad lane k2), from phase 1 to phase 2;
+    // zq(b) has byte r's top bit set when query 4b + r is kept
+    uint32_t zw[4] = {0u, 0u, 0u, 0u};
+    const uint32_t csel = 0x4440u + (static_cast<uint32_t>(lane) & 3u);   // this key's byte
+    auto zq = [&](int b) -> uint32_t { return col_query_bits(zw[b & 3], csel, b >> 2); };
     auto phase1 = [&](int it) {
       const int i = i0 + it;
       const float4* nl4 = reinterpret_cast<const float4*>(vec_of(it)) + part * 8;
@@ -264,9 +289,22 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
         for (int e = 0; e < 32; ++e)
           if (i * kBwdTile + part * 32 + e < key) pf[e] = 0.f;
       }
+      if constexpr (kDrop) {
+        const uint32_t mine = drop_words8(static_cast<uint32_t>(key >> 2),
+                                          static_cast<uint32_t>(i * kBwdTile + part * 32) >> 2,
+                                          static_cast<uint32_t>(lane) & 3u,
+                                          static_cast<uint32_t>(bh), p.drop_off, p.drop_k0,
+                                          p.drop_k1, p.drop_t);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) zw[k2] = __shfl_sync(0xffffffffu, mine, (lane & ~3) | k2);
+      }
       uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
+      for (int e = 0; e < 16; ++e) {
+        pk[e] = ptx::pack2<kBf16>(pf[2 * e], pf[2 * e + 1]);
+        // the dV product reads P with the dropped weights zeroed
+        if constexpr (kDrop) pk[e] &= prmt(zq(e >> 1), 0u, (e & 1) ? 0xBBAAu : 0x9988u);
+      }
       ptx::tmem_st16(tS, pk);   // over the S^T columns this warp has read
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -285,15 +323,25 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         const float4 dd = dl4[e / 4];
+        // dP^T, with dropout Z dP^T (the 256 / t joins in the subtraction of D)
+        uint32_t zx = 0;
+        if constexpr (kDrop) zx = zq(e >> 2);   // e is a multiple of 4: one block
+        auto dpv = [&](int x) -> float {
+          if constexpr (kDrop)
+            return __uint_as_float(dpr[e + x] & prmt(zx, 0u, 0x8888u + 0x1111u * x));
+          return __uint_as_float(dpr[e + x]);
+        };
+        auto dmd = [&](float a, float b, float da, float db) -> uint64_t {
+          if constexpr (kDrop)
+            return ptx::ffma2(ptx::f2_pack(a, b), ptx::f2_pack(p.drop_scale, p.drop_scale),
+                              ptx::f2_pack(-da, -db));
+          return ptx::fadd2(ptx::f2_pack(a, b), ptx::f2_pack(-da, -db));
+        };
         float d0, d1, d2, d3;
-        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[e], pf[e + 1]),
-                                  ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e]),
-                                                          __uint_as_float(dpr[e + 1])),
-                                             ptx::f2_pack(-dd.x, -dd.y))), d0, d1);
+        ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[e], pf[e + 1]), dmd(dpv(0), dpv(1), dd.x, dd.y)),
+                       d0, d1);
         ptx::f2_unpack(ptx::fmul2(ptx::f2_pack(pf[e + 2], pf[e + 3]),
-                                  ptx::fadd2(ptx::f2_pack(__uint_as_float(dpr[e + 2]),
-                                                          __uint_as_float(dpr[e + 3])),
-                                             ptx::f2_pack(-dd.z, -dd.w))), d2, d3);
+                                  dmd(dpv(2), dpv(3), dd.z, dd.w)), d2, d3);
         ds[e / 2] = ptx::pack2<kBf16>(d0, d1);
         ds[e / 2 + 1] = ptx::pack2<kBf16>(d2, d3);
       }
@@ -373,8 +421,8 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
     const long long row = static_cast<long long>(bh) * p.Nk + key;
     const int c0 = (part & 1) * (D / 2);
     if (part < 2)
-      store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc, c0, D / 2, D, 1.f, p.dv, row,
-                            key < p.Nk);
+      store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc, c0, D / 2, D,
+                            kDrop ? p.drop_scale : 1.f, p.dv, row, key < p.Nk);
     else
       store_acc_cols<kBf16>(tmem_base + lane_off + kColAcc + D, c0, D / 2, D, p.scale, p.dk, row,
                             key < p.Nk);
@@ -384,7 +432,7 @@ __device__ __forceinline__ void bwd_onepass_cta(const BwdParams& p, int blk, uin
 
 // The one-pass backward grid: at most one CTA per SM walking the key tiles
 // (the ones with the most query tiles first); the CTA allocates TMEM once.
-template <int D, bool kBf16, bool kCausal>
+template <int D, bool kBf16, bool kCausal, bool kDrop = false>
 __global__ void __launch_bounds__(kOneThreads, 1)
     fa_bwd_onepass_kernel(const __grid_constant__ BwdParams p) {
   __shared__ uint32_t s_tmem_base;
@@ -399,7 +447,7 @@ __global__ void __launch_bounds__(kOneThreads, 1)
   const uint32_t tmem_base = s_tmem_base;
   const int items = p.BH * p.n_ktiles;
   for (int item = blockIdx.x; item < items; item += gridDim.x)
-    bwd_onepass_cta<D, kBf16, kCausal>(p, item, tmem_base);
+    bwd_onepass_cta<D, kBf16, kCausal, kDrop>(p, item, tmem_base);
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kOneMmaWarp) {

@@ -20,8 +20,9 @@
  *    the attention weights);
  *  - backward: fa_bwd, fa_bwd_kv, fa_bwd_varlen, fa_bwd_dropout,
  *    fa_bwd_kv_dropout, fa_bwd_varlen_dropout, each the gradient of the
- *    forward of the same name; fa_bwd_onepass (fa_bwd in one pass over the
- *    tiles, dQ summed through a caller's fp32 scratch);
+ *    forward of the same name; fa_bwd_onepass, fa_bwd_onepass_dropout
+ *    (fa_bwd and fa_bwd_dropout in one pass over the tiles, dQ summed
+ *    through a caller's fp32 scratch);
  *  - decoding: fa_decode (a few queries against a long cache, key axis
  *    split across the GPU);
  *  - status and settings: fa_strerror, fa_status, fa_set_watchdog_ns,
@@ -369,8 +370,26 @@ int fa_bwd_onepass(const void *q, const void *k, const void *v, const void *o,
                    int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_bwd_onepass_dropout — fa_bwd_dropout computed as fa_bwd_onepass does:
+ * each (query tile, key tile) pair is visited once and the forward's mask is
+ * drawn once for it from the same dropout_p, seed and offset.  dK and dV
+ * equal fa_bwd_dropout's bit for bit; dQ is summed in fp32 through
+ * `workspace` in no fixed order.  Arguments as fa_bwd_dropout plus workspace
+ * and workspace_bytes (as fa_bwd_onepass); errors as fa_bwd_onepass plus
+ * FA_ERR_DROPOUT (checked first) for a dropout_p outside [0, 1) or leaving
+ * t = 0.
+ */
+int fa_bwd_onepass_dropout(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                           float *delta, int B, int H, int N, int d, int causal, float scale,
+                           float dropout_p, unsigned long long seed, unsigned int offset,
+                           int dtype, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
  * fa_bwd_onepass_workspace_size — bytes of the fp32 dQ sum of
- * fa_bwd_onepass: B * H * d * (N rounded up to a multiple of 128) * 4.
+ * fa_bwd_onepass and fa_bwd_onepass_dropout: B * H * d * (N rounded up to a
+ * multiple of 128) * 4.
  * Host-only.  Returns FA_ERR_NULLPTR for a NULL `bytes`, FA_ERR_SHAPE for a
  * negative B, H or N, FA_ERR_UNSUPPORTED_D for d other than 64 or 128.
  */

@@ -231,6 +231,15 @@ def test_bwd_onepass_host_errors(lib):
         assert fa.fa_bwd_onepass(**{**call, **args}) == code, args
     if no_gpu():
         assert fa.fa_bwd_onepass(**call) == fa.FA_ERR_DEVICE
+    # the dropout form checks the probability first, then as fa_bwd_onepass
+    dcall = {k: v for k, v in call.items() if k != "dtype"}
+    dcall.update(dropout_p=0.1, seed=1, offset=2, dtype=fa.FA_BF16)
+    assert fa.fa_bwd_onepass_dropout(**{**dcall, "dropout_p": 1.0, "d": 96}) == fa.FA_ERR_DROPOUT
+    assert fa.fa_bwd_onepass_dropout(**{**dcall, "dropout_p": -0.1}) == fa.FA_ERR_DROPOUT
+    assert fa.fa_bwd_onepass_dropout(**{**dcall, "d": 96}) == fa.FA_ERR_UNSUPPORTED_D
+    assert fa.fa_bwd_onepass_dropout(**{**dcall, "workspace": None}) == fa.FA_ERR_WORKSPACE
+    if no_gpu():
+        assert fa.fa_bwd_onepass_dropout(**dcall) == fa.FA_ERR_DEVICE
 
 
 def test_fwd_kv_host_errors(lib):

@@ -1,4 +1,5 @@
-"""fa_bwd_onepass on the GPU: the float64 gradient oracle, and fa_bwd.
+"""fa_bwd_onepass and fa_bwd_onepass_dropout on the GPU: the float64
+gradient oracles, and fa_bwd / fa_bwd_dropout.
 
 The one-pass kernel visits each (query tile, key tile) pair once and sums
 dQ in fp32 through a workspace (the fp32 additions of different key tiles
@@ -100,6 +101,66 @@ def test_onepass_on_workloads(name):
         check_grad(f"{name} dQ head {b},{h}", gq[b, h], rq, w["dtype"])
         check_grad(f"{name} dK head {b},{h}", gk[b, h][keys], rk, w["dtype"])
         check_grad(f"{name} dV head {b},{h}", gv[b, h][keys], rv, w["dtype"])
+
+
+DROP_CASES = [
+    # B, H, N, d, dtype, causal, p, seed, offset: the dropout backward cases
+    # of tests/test_gpu_dropout.py, a causal d = 128 shape past one ring
+    # cycle, and an unmasked d = 64 shape with several tiles
+    (1, 2, 300, 64, "bf16", True, 0.1, 1234, 0),
+    (2, 1, 257, 128, "fp16", False, 0.5, 7, 3),
+    (1, 1, 129, 128, "bf16", True, 0.3, 2 ** 40 + 3, 11),
+    (1, 2, 640, 64, "fp16", False, 0.2, 99, 2 ** 31 + 5),
+    (1, 1, 1000, 128, "bf16", True, 0.1, 5, 6),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal,p,seed,off", DROP_CASES,
+                         ids=[f"B{c[0]}H{c[1]}N{c[2]}d{c[3]}{c[4]}{'c' if c[5] else ''}p{c[6]}"
+                              for c in DROP_CASES])
+def test_onepass_dropout_vs_oracle(B, H, N, d, dtype, causal, p, seed, off):
+    """fa_bwd_onepass_dropout against the float64 dropout gradient oracle;
+    dK and dV equal fa_bwd_dropout's bit for bit."""
+    q, k, v = seeded_inputs.make_qkv(B, H, N, d, dtype, 1.0, seed=N + d)
+    dout = seeded_inputs.make_dout(B, H, N, d, dtype, seed=N + d)
+    dq_, dk_, dv_, do_ = (t.cuda() for t in (q, k, v, dout))
+    o, lse = fa.attention_forward_dropout(dq_, dk_, dv_, p, seed, off, causal=causal)
+    _, tk, tv = fa.attention_backward_dropout(dq_, dk_, dv_, o, lse, do_, p, seed, off,
+                                              causal=causal)
+    gq, gk, gv = fa.attention_backward_onepass(dq_, dk_, dv_, o, lse, do_, causal=causal,
+                                               dropout_p=p, seed=seed, offset=off)
+    status_ok()
+    scale = default_scale(d)
+    name = f"B{B}H{H}N{N}d{d}{dtype} p={p}"
+    for b in range(B):
+        for h in range(H):
+            rq, rk, rv = oracle.attention_dropout_grad(
+                q[b, h].double().numpy(), k[b, h].double().numpy(), v[b, h].double().numpy(),
+                dout[b, h].double().numpy(), b * H + h, seed, off, p, causal=causal, scale=scale)
+            check_grad(f"{name} ({b},{h}) dQ", gq[b, h].cpu(), rq, dtype)
+            check_grad(f"{name} ({b},{h}) dK", gk[b, h].cpu(), rk, dtype)
+            check_grad(f"{name} ({b},{h}) dV", gv[b, h].cpu(), rv, dtype)
+    assert torch.equal(gk, tk), "dK differs from fa_bwd_dropout"
+    assert torch.equal(gv, tv), "dV differs from fa_bwd_dropout"
+
+
+def test_onepass_dropout_zero_probability_and_errors():
+    """p = 0 gives fa_bwd_onepass's dK and dV; a bad probability is refused
+    before the other checks."""
+    q, k, v = (t.cuda() for t in make(1, 2, 300, 64, "bf16", seed=8))
+    dout = seeded_inputs.make_dout(1, 2, 300, 64, "bf16", seed=8).cuda()
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    a = fa.attention_backward_onepass(q, k, v, o, lse, dout, causal=True)
+    need = fa.fa_bwd_onepass_workspace_size(1, 2, 300, 64)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty(1, 2, 300, dtype=torch.float32, device="cuda")
+    args = (q, k, v, o, lse, dout, dq, dk, dv, delta, 1, 2, 300, 64, 1, 0.125)
+    assert fa.fa_bwd_onepass_dropout(*args, 0.0, 1, 2, fa.FA_BF16, ws, need) == fa.FA_OK
+    status_ok()
+    assert torch.equal(dk, a[1]) and torch.equal(dv, a[2])
+    assert fa.fa_bwd_onepass_dropout(*args, 1.0, 1, 2, fa.FA_BF16, ws, need) == fa.FA_ERR_DROPOUT
+    assert fa.fa_bwd_onepass_dropout(*args, 0.1, 1, 2, fa.FA_BF16, None, 0) == fa.FA_ERR_WORKSPACE
 
 
 def test_onepass_errors():
