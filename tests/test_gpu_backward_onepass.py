@@ -59,6 +59,23 @@ def test_onepass_every_row(B, H, N, d, dtype, causal):
     assert torch.equal(gv, tv), "dV differs from fa_bwd"
 
 
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "fp16")])
+def test_partial_head_group(d, dtype):
+    """Causal calls deal work items in groups of 8 heads; with B*H = 12 the
+    last group holds 4.  Both backward paths against the oracle."""
+    B, H, N = 3, 4, 300
+    q, k, v = make(B, H, N, d, dtype, q_std=1.5, seed=31 + d)
+    dout = seeded_inputs.make_dout(B, H, N, d, dtype, seed=31 + d)
+    scale = default_scale(d)
+    (tq, tk, tv), (gq, gk, gv) = run_both(q, k, v, dout, True, scale)
+    rq, rk, rv = oracle.attention_grad(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                       dout.double().numpy(), causal=True, scale=scale)
+    for name, (a, b, c) in (("fa_bwd", (tq, tk, tv)), ("fa_bwd_onepass", (gq, gk, gv))):
+        check_grad(f"{name} dQ", a, rq, dtype)
+        check_grad(f"{name} dK", b, rk, dtype)
+        check_grad(f"{name} dV", c, rv, dtype)
+
+
 def test_onepass_repeat_and_workspace_reuse():
     """A reused (dirty) workspace gives the same dK, dV and a dQ within
     fp32 summation-order noise; a larger workspace than needed is fine."""

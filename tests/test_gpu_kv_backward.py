@@ -69,6 +69,9 @@ CASES = [
     (3, 1, 129, 700, 64, "bf16", "bottom_right", [700, 64, 1]),
     (2, 2, 260, 900, 64, "fp16", "upper_left", [900, 131]),
     (1, 1, 640, 2000, 128, "bf16", "bottom_right", [1500]),
+    # ten (batch, head) pairs: work items dealt in groups of 8 heads, the
+    # last group of 2
+    (5, 2, 200, 600, 64, "bf16", "bottom_right", [600, 300, 0, 129, 450]),
 ]
 
 
