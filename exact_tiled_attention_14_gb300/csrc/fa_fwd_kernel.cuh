@@ -990,6 +990,27 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
           }
         };
 
+        // P_w and O_w are still in use by PV_w_{j-1} until it completes
+        // (the wait of the early stores below).
+        auto wait_pv = [&]() {
+          if (j > 0) {
+            pf.lap(3);
+            ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
+            ++pvcnt;
+            pf.lap(16);
+            __syncwarp();
+            ptx::tc_fence_after();
+          }
+        };
+        // Without dropout (no mask to apply after the exponentials) the
+        // first half of P is stored as soon as it is packed, once
+        // PV_w_{j-1} has completed, so the store overlaps the second half's
+        // exponentials: into TMEM at d = 64; into shared memory (the first
+        // 64-key chunk) at d = 128 for unmasked calls (measured slower on
+        // the causal workload, which runs power-capped).
+        constexpr bool kEarlyP = !kDrop && OwnP<D>::kTmem;
+        constexpr bool kEarlyS = !kDrop && OwnP<D>::kSmem && !kCausal;
+
         pf.lap(2);
         // P = 2^(s*c - m_ref*c), summed into l, packed to 16 bits into TMEM.
         // The exponent argument and the row sum use two-lane fp32 instructions.
@@ -999,6 +1020,24 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
         uint32_t pk[kBN / 2];
 #pragma unroll
         for (int i = 0; i < kBN / 2; i += 2) {
+          if constexpr (kEarlyS) {
+            if (i == kBN / 4) {   // keys 0 .. 63 (chunk 0) are packed
+              wait_pv();
+              if (rescale) rescale_o();
+              uint8_t* prow0 = sgen + L::kP + w * (kBM * kBN * 2) + t * 128;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(prow0 + (((k & 7) ^ (t & 7)) << 4)) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
+          }
+          if constexpr (kEarlyP) {
+            if (i == kBN / 4) {   // pk[0 .. 31] are packed
+              wait_pv();
+              if (rescale) rescale_o();
+              ptx::tmem_st32(tP, pk);
+            }
+          }
           float x0, x1, x2, x3;
           ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(sv[2 * i + 0], sv[2 * i + 1]), c2, nm2), x0, x1);
           ptx::f2_unpack(ptx::ffma2(ptx::f2_pack(sv[2 * i + 2], sv[2 * i + 3]), c2, nm2), x2, x3);
@@ -1039,26 +1078,28 @@ __global__ void __launch_bounds__(threads_of<D, kDrop>(), 1)
           pf.lap(19);
         }
         pf.lap(3);
-        // P_w and O_w are still in use by PV_w_{j-1} until it completes.
-        if (j > 0) {
-          pf.lap(3);
-          ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
-          ++pvcnt;
-          pf.lap(16);
-          __syncwarp();
-          ptx::tc_fence_after();
+        if constexpr (!kEarlyP && !kEarlyS) {
+          // P_w and O_w are still in use by PV_w_{j-1} until it completes.
+          if (j > 0) {
+            pf.lap(3);
+            ptx::wait_bounded(bar(L::bPvDone + w), pvcnt & 1, wd, kSitePvDone);
+            ++pvcnt;
+            pf.lap(16);
+            __syncwarp();
+            ptx::tc_fence_after();
+          }
+          if (rescale) rescale_o();
         }
-        if (rescale) rescale_o();
         if constexpr (OwnP<D>::kSmem) {
           // row t of the P_w tile: 16 pieces of 8 keys, 128-byte swizzle
           uint8_t* prow = sgen + L::kP + w * (kBM * kBN * 2) + t * 128;
 #pragma unroll
-          for (int k = 0; k < kBN / 8; ++k)
+          for (int k = kEarlyS ? 8 : 0; k < kBN / 8; ++k)
             *reinterpret_cast<uint4*>(prow + (k >> 3) * L::kChunkBytes + (((k & 7) ^ (t & 7)) << 4)) =
                 make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
           ptx::fence_proxy_async_smem();   // visible to the tensor core's reads
         } else {
-          ptx::tmem_st32(tP, pk);
+          if constexpr (!kEarlyP) ptx::tmem_st32(tP, pk);
           ptx::tmem_st32(tP + 32, pk + 32);
         }
         ptx::tmem_wait_st();               // P (in TMEM) and a rescaled O are written
