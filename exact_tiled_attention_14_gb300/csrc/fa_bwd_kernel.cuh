@@ -146,11 +146,12 @@ struct BwdParams {
 
 // Tile index and head of work item `blk` among BH * n_tiles items dealt in
 // groups of p.item_group heads (the last group may be smaller).
-__device__ __forceinline__ void bwd_item(const BwdParams& p, int blk, int n_tiles, int& tile,
-                                         int& bh) {
+__host__ __device__ __forceinline__ void bwd_item(const BwdParams& p, int blk, int n_tiles,
+                                                  int& tile, int& bh) {
   const int per_group = p.item_group * n_tiles;
   const int g = blk / per_group, r = blk - g * per_group;
-  const int gh = min(p.item_group, p.BH - g * p.item_group);
+  const int left = p.BH - g * p.item_group;
+  const int gh = p.item_group < left ? p.item_group : left;
   tile = r / gh;
   bh = g * p.item_group + (r - tile * gh);
 }

@@ -59,20 +59,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-// Dropout mask words of a key column against 32 queries (eight 4 x 4 blocks
-// of the column walk of drop_words16): lane k (0 .. 3) of a quad, whose
-// four lanes are the block's four keys, draws blocks k and k + 4, in one
-// word laid out by key (bits 7 .. 4 of each byte: block k; bits 3 .. 0:
-// block k + 4).  kb0 is the key block, qb0 the first query block.
-__device__ __forceinline__ uint32_t drop_words8(uint32_t kb0, uint32_t qb0, uint32_t k, uint32_t bh,
-                                                uint32_t off, uint32_t k0, uint32_t k1,
-                                                uint32_t t) {
-  const uint32_t c4 = (256u - t) * 0x01010101u;
-  const uint4 ra = philox4x32_10(make_uint4(kb0, qb0 + k, bh, off), k0, k1);
-  const uint4 rb = philox4x32_10(make_uint4(kb0, qb0 + k + 4u, bh, off), k0, k1);
-  return sel_bits(0xF0F0F0F0u, keep_by_key(ra, c4), keep_by_key(rb, c4) >> 4);
-}
-
 // One CTA of the one-pass backward: key tile blk / BH of head blk % BH.
 // The fp32 dQ workspace (BwdParams::dq_acc) holds blocks of 32 queries x 16
 // columns: block (bh, query tile qt, column block cb, row quarter rq) keeps

@@ -196,6 +196,21 @@ __host__ __device__ __forceinline__ uint2 drop_words16(uint32_t kb0, uint32_t qb
   return make_uint2(w[0], w[1]);
 }
 
+// The one-pass backward walks 32 queries of a key column per thread and
+// tile, eight 4 x 4 blocks.  drop_words8: the word lane k (0 .. 3) of a
+// quad, whose four lanes are the block column's four keys, draws for those
+// blocks: blocks k (bits 7 .. 4 of each byte) and k + 4 (bits 3 .. 0) of
+// the walk, laid out by key.  kb0 is the key block, qb0 the first query
+// block; block i is (kb0, qb0 + i), as in drop_words16's column walk.
+__host__ __device__ __forceinline__ uint32_t drop_words8(uint32_t kb0, uint32_t qb0, uint32_t k,
+                                                         uint32_t bh, uint32_t off, uint32_t k0,
+                                                         uint32_t k1, uint32_t t) {
+  const uint32_t c4 = (256u - t) * 0x01010101u;
+  const uint4 ra = philox4x32_10(make_uint4(kb0, qb0 + k, bh, off), k0, k1);
+  const uint4 rb = philox4x32_10(make_uint4(kb0, qb0 + k + 4u, bh, off), k0, k1);
+  return sel_bits(0xF0F0F0F0u, keep_by_key(ra, c4), keep_by_key(rb, c4) >> 4);
+}
+
 // Row walk: with y the word holding block 8m + 4h + k2 (word m of quad
 // lane k2), the mask (all ones or zero) of key c (0 .. 3) of that block for
 // query row r (0 .. 3) of the quad.

@@ -5,7 +5,8 @@ quad's words to the 16-bit masks of a row's packed weights), and the
 backward's drop_words16 with the row walk (row_key_mask, the dQ pass: 64
 keys of a query row) and the column walk (col_query_bits, the dK/dV pass:
 64 queries of a key column, as element masks and as the 16-bit pair masks
-of the packed P^T).
+of the packed P^T), and the one-pass backward's drop_words8 (32 queries of
+a key column).
 
 The mask is what "Why FlashAttention Can Avoid a Square Attention Array
 Without Making Attention Linear", section "Backward can recreate tiles
@@ -73,6 +74,22 @@ int main(int argc, char** argv) {
           }
         }
       }
+  } else if (!std::strcmp(mode, "col32")) {   // one-pass backward: 32 queries from q0
+    for (int key = 0; key < keys; ++key)
+      for (int q0 = 0; q0 < rows; q0 += 32) {
+        uint32_t w[4];
+        for (uint32_t k = 0; k < 4; ++k)
+          w[k] = fa::drop_words8(key >> 2, q0 >> 2, k, bh, off, k0, k1, t);
+        const uint32_t csel = 0x4440u + (key & 3);
+        for (int b = 0; b < 8; ++b) {
+          const uint32_t x = fa::col_query_bits(w[b & 3], csel, b >> 2);
+          for (int r = 0; r < 4; ++r) {
+            const uint32_t mk = fa::prmt(x, 0u, 0x8888u + 0x1111u * r);
+            if (mk != 0u && mk != 0xFFFFFFFFu) return 2;
+            at(q0 + 4 * b + r, key) = mk ? '1' : '0';
+          }
+        }
+      }
   } else {   // dK/dV pass: key column key, 64 queries from q0
     for (int key = 0; key < keys; ++key)
       for (int q0 = 0; q0 < rows; q0 += 64) {
@@ -130,7 +147,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode", ["fwd", "row", "col"])
+@pytest.mark.parametrize("mode", ["fwd", "row", "col", "col32"])
 @pytest.mark.parametrize("bh,seed,off,p,rows,keys", CASES)
 def test_packed_mask_matches_oracle(mask_program, mode, bh, seed, off, p, rows, keys):
     t = oracle.dropout_threshold(p)
