@@ -60,6 +60,21 @@ def test_backward_checks():
         fa.attention_backward_dropout(q, q, q, q, torch.zeros(2, 8), q, 0.1, 0, 0)
 
 
+def test_backward_onepass_checks():
+    q = t(1, 2, 8, 64)
+    lse = torch.zeros(1, 2, 8)
+    with pytest.raises(TypeError):
+        fa.attention_backward_onepass(q, q, q, q, lse, t(1, 2, 8, 64, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        fa.attention_backward_onepass(q, q, q, q, torch.zeros(1, 2, 7), q)   # lse shape
+    with pytest.raises(ValueError):
+        fa.attention_backward_onepass(q, q, q, q, lse.double(), q)           # lse dtype
+    with pytest.raises(ValueError):
+        fa.attention_backward_onepass(q, t(1, 2, 9, 64), q, q, lse, q)       # shapes differ
+    with pytest.raises(ValueError):
+        fa.attention_backward_onepass(q, q, q, q, lse, q, dropout_p=0.1)     # host tensors
+
+
 def test_backward_varlen_checks():
     q, k = t(10, 2, 64), t(20, 2, 64)
     cu = torch.tensor([0, 10], dtype=torch.int32)
