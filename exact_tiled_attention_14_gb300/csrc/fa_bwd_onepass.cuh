@@ -59,8 +59,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-// One CTA of the one-pass backward: key tile blk / BH of head blk % BH.
-// The fp32 dQ workspace (BwdParams::dq_acc) holds blocks of 32 queries x 16
+// One CTA of the one-pass backward: work item blk, one key tile of one head
+// (dealt by bwd_item in groups of heads).  The fp32 dQ workspace (BwdParams::dq_acc) holds blocks of 32 queries x 16
 // columns: block (bh, query tile qt, column block cb, row quarter rq) keeps
 // element (column cc, row rr) at
 //   dq_acc[((((bh * n_tiles + qt) * (D / 16) + cb) * 4 + rq) * 16 + cc) * 32 + rr].
