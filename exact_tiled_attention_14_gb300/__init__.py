@@ -1,11 +1,12 @@
-"""Exact tiled attention forward for GB300 (sm_103a): Python binding.
+"""Exact tiled attention for GB300 (sm_103a): Python binding.
 
 This module only marshals arguments to the C ABI in ``include/fa.h``
-(``fa_fwd``, ``fa_fwd_kv``, ``fa_fwd_varlen``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd_kv``, ``fa_bwd_varlen``, ``fa_fwd_ws``, ``fa_fwd_workspace_size``, ``fa_fwd_static``,
-``fa_bwd``, ``fa_decode``, ``fa_decode_workspace_size``, ``fa_strerror``,
-``fa_status``, ``fa_set_watchdog_ns``, ``fa_set_unit_group``, ``fa_watchdog_selftest``,
-``fa_work_tiles``, ``fa_version``),
-under the same names.  Every step of
+(every name in ``EXPORTS``: the forward entry points ``fa_fwd``,
+``fa_fwd_ws``, ``fa_fwd_static``, ``fa_fwd_kv``, ``fa_fwd_varlen`` and their
+``_dropout`` forms; the backward ``fa_bwd``, ``fa_bwd_kv``, ``fa_bwd_varlen``,
+their ``_dropout`` forms, ``fa_bwd_onepass`` and ``fa_bwd_onepass_dropout``;
+``fa_decode``; the workspace sizes, status and settings), under the same
+names.  Every step of
 the attention computation runs in the CUDA kernels of ``_build/libfa.so``;
 there is no CPU or PyTorch fallback.  When the library has not been built,
 every call raises.
@@ -16,7 +17,8 @@ memory is PyTorch's job here — and calls ``fa_fwd`` or ``fa_fwd_ws`` on the
 current CUDA stream.  ``attention_backward`` does the same for ``fa_bwd``
 (dQ, dK, dV and the D scratch), ``attention_decode`` for ``fa_decode``,
 ``attention_forward_kv`` for ``fa_fwd_kv``, ``attention_forward_varlen`` for
-``fa_fwd_varlen``.  ``flash_attention``, ``flash_attention_kv`` and
+``fa_fwd_varlen``, ``attention_backward_onepass`` for ``fa_bwd_onepass``
+(and ``fa_bwd_onepass_dropout``).  ``flash_attention``, ``flash_attention_kv`` and
 ``flash_attention_varlen`` wrap the forward and backward entry points in
 torch.autograd functions.
 """
