@@ -55,10 +55,9 @@ static int backward(const void* q, const void* k, const void* v, const void* o, 
                        reinterpret_cast<uintptr_t>(seqlens_k);
   if ((a16 & 15u) || (a4 & 3u)) return FA_ERR_ALIGN;
   if (one) {
-    // the dQ conversion runs one block per (batch*head, 32 queries)
-    if (bh * ((static_cast<long long>(Nq) + 31) / 32) > INT_MAX ||
-        n_qtiles * fa::kBwdTile > INT_MAX)
-      return FA_ERR_SHAPE;
+    // the dQ sum keeps every row of the last tile (the conversion runs one
+    // block per (batch*head, query tile), within the grid bound above)
+    if (n_qtiles * fa::kBwdTile > INT_MAX) return FA_ERR_SHAPE;
     if (!ws || ws_bytes < static_cast<size_t>(onepass_acc_bytes(bh, Nq, d)))
       return FA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) & 15u) return FA_ERR_ALIGN;

@@ -278,33 +278,53 @@ __global__ void __launch_bounds__(256) fa_bwd_delta_kernel(const uint4* __restri
 
 // ---------------------------------------------------------------- dQ = scale * accumulator
 // The one-pass kernel leaves dQ unscaled in fp32 in blocks of 32 queries x
-// 16 columns, column by column within a block (BwdParams::dq_acc).  Each
-// CTA moves 32 query rows of one head through shared memory and writes them
-// row by row in the storage dtype, scaled.  Blocks: bh * ceil(N / 32) +
-// query block.
+// 16 columns, column by column within a block (BwdParams::dq_acc); the
+// blocks of one (batch*head, 128-query tile) are contiguous, 128 x W floats.
+// One CTA per (batch*head, query tile) moves them, 64 columns at a time,
+// through a shared-memory tile with 16-byte loads and writes the rows in
+// the storage dtype, scaled, with 16-byte stores.  Blocks: bh * n_tiles +
+// query tile.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
                                                                 uint32_t* __restrict__ dq,
                                                                 int N, int W, int pad,
                                                                 float scale) {
-  __shared__ float tile[128][33];
-  const int nqb = (N + 31) / 32;
-  const int bh = blockIdx.x / nqb;
-  const int q0 = (blockIdx.x - bh * nqb) * 32;
-  const int lane = threadIdx.x & 31, row8 = threadIdx.x >> 5;
-  const int n_tiles = pad / kBwdTile, qt = q0 / kBwdTile, rq = (q0 % kBwdTile) / 32;
-  for (int c = row8; c < W; c += 8) {
-    const long long blk =
-        ((static_cast<long long>(bh) * n_tiles + qt) * (W / 16) + c / 16) * 4 + rq;
-    tile[c][lane] = acc[(blk * 16 + c % 16) * 32 + lane];
-  }
-  __syncthreads();
-  const int pairs = W / 2;
-  for (int idx = threadIdx.x; idx < 32 * pairs; idx += 256) {
-    const int r = idx / pairs, cp = idx - r * pairs;
-    if (q0 + r < N)
-      dq[(static_cast<long long>(bh) * N + q0 + r) * pairs + cp] =
-          ptx::pack2<kBf16>(tile[2 * cp][r] * scale, tile[2 * cp + 1][r] * scale);
+  __shared__ float tile[kBwdTile][65];
+  const int n_tiles = pad / kBwdTile;
+  const int bh = blockIdx.x / n_tiles;
+  const int qt = blockIdx.x - bh * n_tiles;
+  const float4* src = reinterpret_cast<const float4*>(
+      acc + (static_cast<long long>(bh) * n_tiles + qt) * kBwdTile * W);
+  for (int h = 0; h < W / 64; ++h) {
+    // blocks cb = 4h .. 4h + 3 of the tile: 4 x 4 blocks of 512 floats
+    const float4* s4 = src + h * (4 * 4 * 512 / 4);
+    for (int idx = threadIdx.x; idx < 4 * 4 * 512 / 4; idx += 256) {
+      const float4 v = s4[idx];
+      const int e = idx * 4;                          // float index within the half
+      const int blk = e >> 9, in = e & 511;           // block (cb - 4h) * 4 + rq, offset
+      const int cc = in >> 5, rr = in & 31;           // column within the block, row
+      const int row = (blk & 3) * 32 + rr, col = (blk >> 2) * 16 + cc;
+      tile[row][col] = v.x;
+      tile[row + 1][col] = v.y;
+      tile[row + 2][col] = v.z;
+      tile[row + 3][col] = v.w;
+    }
+    __syncthreads();
+    // 128 rows x 8 pieces of 8 columns
+    for (int idx = threadIdx.x; idx < kBwdTile * 8; idx += 256) {
+      const int r = idx >> 3, c8 = (idx & 7) * 8;
+      const int q = qt * kBwdTile + r;
+      if (q < N) {
+        uint4 out;
+        out.x = ptx::pack2<kBf16>(tile[r][c8] * scale, tile[r][c8 + 1] * scale);
+        out.y = ptx::pack2<kBf16>(tile[r][c8 + 2] * scale, tile[r][c8 + 3] * scale);
+        out.z = ptx::pack2<kBf16>(tile[r][c8 + 4] * scale, tile[r][c8 + 5] * scale);
+        out.w = ptx::pack2<kBf16>(tile[r][c8 + 6] * scale, tile[r][c8 + 7] * scale);
+        *reinterpret_cast<uint4*>(dq + (static_cast<long long>(bh) * N + q) * (W / 2) +
+                                  (h * 64 + c8) / 2) = out;
+      }
+    }
+    __syncthreads();
   }
 }
 

@@ -109,7 +109,7 @@ cudaError_t launch_bwd_onepass_variant(const BwdParams& p, const void* o, const 
   e = launch_bwd_grid(kernel, p, static_cast<long long>(p.BH) * p.n_ktiles, kAlloc, sms, stream,
                       kOneThreads);
   if (e != cudaSuccess) return e;
-  const long long blocks = static_cast<long long>(p.BH) * ((p.N + 31) / 32);
+  const long long blocks = static_cast<long long>(p.BH) * p.n_tiles;
   fa_bwd_dq_convert_kernel<kBf16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       p.dq_acc, static_cast<uint32_t*>(p.dq), p.N, p.width_qk, p.dq_pad, p.scale);
   return cudaGetLastError();
